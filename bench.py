@@ -1,0 +1,358 @@
+#!/usr/bin/env python3
+"""Benchmark: paged decode attention over a paged KV cache on GB300.
+
+One step = one decode step of the whole hot path for the batch: host slot
+assignment with copy-on-write (pkv_prepare_append), the step's table/slot
+uploads, the block copy, and for every layer the append of the new token's K/V
+followed by paged decode attention (split-KV, fused combine).
+
+Default workload: 7B shape (32 layers, 32 heads x 128, fp16 KV), block size 16,
+batch 32 with context lengths U[256, 2048], pool 1.3x the blocks needed with
+shuffled block ids. Each layer's KV (~0.5 GB) is far larger than the 129 MB L2,
+so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0). ``value`` is KV GB/s: algorithmic K+V bytes read by
+the attention launches of the timed steps / device time of those steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--config 2|3|4|5] [--layout NHD|HND] [--block-size B]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak); seq·steps/s at 7B shape"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.txt")
+KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_88_gb300", "csrc", "decode_attention.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--layout", default="NHD", choices=["NHD", "HND"])
+    ap.add_argument("--block-size", type=int, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on the current kernel source."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+        vals = dict(l.split(":", 1) for l in text.splitlines() if ":" in l and not l.startswith("#"))
+        src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+        if vals.get("source_sha256", "").strip() != src_hash:
+            return None
+        return float(vals["traffic_bytes_per_full_launch"].strip())
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def make_bench_workload(args, extra_steps: int):
+    import workloads as wl
+    w = wl.make_workload(args.config, decode_steps=extra_steps, layout=args.layout, block_size=args.block_size)
+    return w
+
+
+def cpu_baseline_oracle(w, k_layer, v_layer, tables, lens, seconds: float):
+    """The C oracle (float64, OpenMP over (sequence, head)) on one layer, repeated for ~``seconds``."""
+    import numpy as np
+    from oracle import ref_attn_c as rc
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((w.num_seqs, w.num_heads, w.head_dim)).astype(np.float16)
+    bytes_per = int(np.asarray(lens, dtype=np.int64).sum()) * w.kv_bytes_per_token_layer
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        rc.decode_attention(q, k_layer, v_layer, tables, lens, w.block_size, w.layout)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or passes >= 64:
+            break
+    return {"value": bytes_per * passes / el / 1e9, "unit": "GB/s", "cores": rc.max_threads(), "kind": "oracle",
+            "sample": f"{passes} pass(es) of one layer ({w.num_seqs} seqs x {w.num_heads} heads, "
+                      f"{int(np.sum(lens))} tokens) of the same workload, fp64 C oracle, {el:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle, as it stands, timed on the host cores (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import workloads as wl
+    from oracle import ref_alloc as ra
+    from oracle import ref_attn_c as rc
+    w = make_bench_workload(args, 8)
+    op = ra.RefPool(w.num_blocks, [int(x) for x in w.free_order])
+    tables = np.asarray([ra.admit(op, int(t), w.block_size, w.max_blocks) for t in w.context_lens], dtype=np.int32)
+    lens = np.asarray(w.context_lens, dtype=np.int32)
+    shape = wl.pool_shape(w)[1:]
+    k = wl.normal_fp16(w.seed, (100, 0), shape)
+    v = wl.normal_fp16(w.seed, (101, 0), shape)
+    q = wl.normal_fp16(w.seed, (200, 0), (w.num_seqs, w.num_heads, w.head_dim))
+    bytes_per = int(lens.astype(np.int64).sum()) * w.kv_bytes_per_token_layer
+    for _ in range(args.warmup):
+        rc.decode_attention(q, k, v, tables, lens, w.block_size, w.layout)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        rc.decode_attention(q, k, v, tables, lens, w.block_size, w.layout)
+    el = time.perf_counter() - t0
+    val = bytes_per * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(w.describe(), step="one layer of the workload (bounded sample)"),
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": rc.max_threads(), "kind": "oracle",
+                         "sample": f"each step = one layer of {w.num_seqs} seqs x {w.num_heads} heads, "
+                                   f"{int(lens.sum())} tokens, fp64 C oracle"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_cache_88_gb300.engine import DecodeEngine
+    import paged_kv_cache_88_gb300 as pkv
+
+    e2e_steps = 0 if args.no_e2e else args.steps
+    total_steps = 2 * args.warmup + args.steps + e2e_steps + 2
+    w = make_bench_workload(args, total_steps)
+    if world > 1:                         # weak scaling: each rank serves its own batch
+        import workloads as wl
+        w = wl.make_workload(args.config, decode_steps=total_steps, layout=args.layout,
+                             block_size=args.block_size, seed=1000 + args.config + 7919 * rank)
+    eng = DecodeEngine(w, device=str(dev), fill="torch")
+    eng.run_script(values="torch")
+    torch.cuda.synchronize()
+    L, S, H, D = w.num_layers, w.num_seqs, w.num_heads, w.head_dim
+    q, kn, vn = eng.step_inputs(0, "torch")
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        eng.step(q, kn, vn, out, stream)
+    barrier()
+    if eng.device_status() != 0:
+        raise RuntimeError(f"device status {eng.device_status():#x} after warm-up")
+
+    # ---- timed region: K decode steps, inputs resident in HBM
+    attn_ev = []
+    step_bytes = []
+    launches = 0
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        t_start.record(stream)
+        for _ in range(args.steps):
+            n_slots, n_pairs = eng.prepare_step(stream)
+            step_bytes.append(eng.kv_bytes_per_layer())
+            eng.device_step(q, kn, vn, out, n_slots, n_pairs, stream, attn_events=attn_ev)
+            launches += 2 * L + (1 if n_pairs else 0)
+        t_end.record(stream)
+        barrier()
+    clocks = clk.summary()
+    ms = t_start.elapsed_time(t_end)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    status = eng.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x} in the timed region")
+
+    kv_bytes = sum(step_bytes) * L
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, float(kv_bytes), float(S * args.steps)], dtype=torch.float64, device=dev)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        sm = t.clone()
+        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+        ms_job, bytes_job, seqsteps_job = mx[0].item(), sm[1].item(), sm[2].item()
+    else:
+        ms_job, bytes_job, seqsteps_job = ms, float(kv_bytes), float(S * args.steps)
+    value = bytes_job / (ms_job / 1e3) / 1e9
+    seq_steps = seqsteps_job / (ms_job / 1e3)
+
+    # roofline of the dominant kernel (decode attention): algorithmic bytes / average launch time
+    per_launch_bytes = []
+    tables_bytes = []
+    for b in step_bytes:
+        per_launch_bytes += [b] * L
+    extra = 2 * S * H * D * 2 + S * 4 + int(np.sum(-(-eng.lens // w.block_size))) * 4
+    achieved = (sum(per_launch_bytes) + extra * len(per_launch_bytes)) / (sum(attn_ms) / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = kernel_traffic()
+
+    # ---- end to end through the public API: inputs from pinned host memory, output read back
+    e2e = None
+    if e2e_steps:
+        hq = q.cpu().pin_memory()
+        hk = kn.cpu().pin_memory()
+        hv = vn.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+        e_bytes = 0
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            eng.step(qd, kd, vd, out, stream)
+            e_bytes += eng.kv_bytes_per_layer() * L
+            hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        h2d = 3 * q.numel() * 2 + eng.tables.size * 4 + S * 4 + S * 8
+        e2e = {"value": e_bytes / (e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(out.numel() * 2), "ms_per_step": e_ms / e2e_steps}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        kl = eng.k_pool[0].cpu().numpy()
+        vl = eng.v_pool[0].cpu().numpy()
+        cpu = cpu_baseline_oracle(w, kl, vl, eng.tables.copy(), eng.lens.copy(), args.cpu_seconds)
+
+    info = pkv.decode_launch_info(S, D)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_job / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic",
+            "config": dict(w.describe(), l2="inputs larger than L2 (each layer's KV >> 129 MB), no flush",
+                           parallelism="replicas" if world > 1 else "single"),
+            "seq_steps_per_s": seq_steps,
+            "frac_of_hbm_peak": value / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                         "kernel": "decode_attention_kernel<128>", "launches": len(attn_ms),
+                         "mean_launch_us": 1e3 * sum(attn_ms) / max(len(attn_ms), 1),
+                         "grid_ctas": info["grid_ctas"], "ctas_per_sm": info["ctas_per_sm"]},
+            "clocks": clocks,
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

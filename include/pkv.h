@@ -1,0 +1,242 @@
+/*
+ * pkv.h -- C ABI of libpkv: a paged KV cache and decode attention over it,
+ * hand-written for NVIDIA GB300 (sm_103a).
+ *
+ * The method: K and V of every token live in a pool of fixed-size physical
+ * blocks carved once at start-up; each sequence owns a block table mapping its
+ * logical blocks to physical ones; blocks are shared between sequences with a
+ * refcount and copied on write; the decode step appends one token per
+ * sequence and attends its query over the whole cached history through the
+ * table. Sources, by page address and the page's own section numbers:
+ *   hnwysp.cn/news/103996    sections 1.2, 3.1-3.4, 4.1-4.4
+ *   icman.com.cn/news/78786  sections 1.1, 2.1-2.4, 3.4, 4.1, 6.3
+ *   m.lqnn.cn/news/240480    sections 3.1-3.3, 5.2
+ *
+ * Conventions (all entry points):
+ *   - Every call returns a pkv_status; nothing throws across the ABI.
+ *     pkv_last_error() gives a thread-local message for the last failure.
+ *   - A call that fails leaves all state (pool, tables, lengths) unchanged.
+ *   - Device memory (the K/V pools, q, out, tables, lengths, workspaces) is
+ *     owned by the caller; the library never allocates or frees it. A pool
+ *     handle owns only host metadata.
+ *   - Device entry points only enqueue work on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream): no host synchronisation, no
+ *     allocation. They are asynchronous; their errors found on the host are
+ *     returned, errors found on the device are OR-ed into a caller-provided
+ *     device status word (PKV_DEV_* bits) that the caller reads when it wants.
+ *   - Kernels never trap: an out-of-range index is skipped (or clamped) and
+ *     flagged in the status word; every wait in a kernel has a time limit.
+ *   - A pool handle is not thread-safe: the caller serialises calls that
+ *     mutate it. Distinct pools are independent.
+ *   - Element type: IEEE binary16 (fp16) for K, V, q and out.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* a size, pointer or shape is outside what the call accepts */
+    PKV_ERR_OUT_OF_BLOCKS = 2, /* the free queue cannot satisfy the request (nothing allocated) */
+    PKV_ERR_BAD_BLOCK = 3,     /* a block id outside [0, num_blocks) */
+    PKV_ERR_REFCOUNT = 4,      /* free/incref of a block whose refcount does not allow it */
+    PKV_ERR_CUDA = 5,          /* a CUDA runtime call failed (message in pkv_last_error) */
+    PKV_ERR_UNSUPPORTED = 6    /* a shape the kernels are not built for (e.g. head_dim 96) */
+} pkv_status;
+
+/* Block layouts within one layer's pool of N blocks (both put B*H*D contiguous
+ * elements per block, so a block is one contiguous byte range):
+ *   PKV_LAYOUT_NHD: [N][B][H][D] -- the order m.lqnn.cn/news/240480 §3.3 prints,
+ *                   [page, slot, head, dim];
+ *   PKV_LAYOUT_HND: [N][H][B][D] -- one head's tokens of a block contiguous. */
+enum { PKV_LAYOUT_NHD = 0, PKV_LAYOUT_HND = 1 };
+
+/* Bits of the device status word (uint32_t) that device entry points OR into. */
+#define PKV_DEV_BAD_BLOCK 0x1u   /* a block-table entry outside [0, num_blocks): clamped to 0 */
+#define PKV_DEV_BAD_LENGTH 0x2u  /* a context length < 0 or > max_blocks * block_size: clamped */
+#define PKV_DEV_TIMEOUT 0x4u     /* a pipeline wait hit its time limit; outputs are garbage */
+#define PKV_DEV_BAD_SLOT 0x8u    /* a slot >= num_blocks * block_size: that token not written */
+#define PKV_DEV_BAD_PAIR 0x10u   /* a copy pair with an id outside [0, num_blocks): skipped */
+
+typedef struct pkv_pool_desc {
+    int32_t num_layers; /* L >= 1 */
+    int32_t num_blocks; /* N >= 1 physical blocks per layer */
+    int32_t block_size; /* B tokens per block: 8, 16, 32, 64, 128 or 256 */
+    int32_t num_heads;  /* H KV heads (query heads = KV heads) */
+    int32_t head_dim;   /* D: 64, 128 or 256 */
+    int32_t layout;     /* PKV_LAYOUT_NHD or PKV_LAYOUT_HND */
+} pkv_pool_desc;
+
+typedef struct pkv_stats {
+    int32_t free_blocks;   /* blocks in the free queue */
+    int32_t used_blocks;   /* blocks with refcount >= 1 */
+    int32_t shared_blocks; /* blocks with refcount >= 2 */
+    int32_t max_refcount;
+    int64_t cow_copies;    /* copy-on-write copies issued by pkv_prepare_append so far */
+} pkv_stats;
+
+typedef struct pkv_pool pkv_pool; /* opaque host metadata */
+
+/* Thread-local text of the last failure of this thread ("" if none). */
+const char *pkv_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t pkv_version(void);
+
+/* ------------------------------------------------------------------ host: pool
+ * Carve the pool: hnwysp.cn/news/103996 §3.2, §4.1 (reserve once, thread every
+ * block onto the free list); icman.com.cn/news/78786 §2.3.
+ *
+ * k_pool, v_pool: device pointers to L * N * B * H * D fp16 elements each, laid
+ *   out [L][N][block] with the block as `layout` says; 16-byte aligned. They may
+ *   be NULL for a host-only pool (allocator use without a GPU); device entry
+ *   points then refuse the pool. The caller keeps ownership.
+ * initial_free_order: host array of N distinct ids 0..N-1 giving the free queue
+ *   from head to tail, or NULL for 0, 1, ..., N-1. Copied.
+ * out: receives the handle. Errors: INVALID_ARG (bad sizes, order not a
+ *   permutation, N*B or L*N*B*H*D too large). Touches no CUDA state. */
+pkv_status pkv_pool_create(const pkv_pool_desc *desc, void *k_pool, void *v_pool,
+                           const int32_t *initial_free_order, pkv_pool **out);
+
+/* Free the host metadata. Does not free the device pools. NULL is accepted. */
+pkv_status pkv_pool_destroy(pkv_pool *pool);
+
+/* Read back the descriptor and the device pointers given at creation. */
+pkv_status pkv_pool_info(const pkv_pool *pool, pkv_pool_desc *desc, void **k_pool, void **v_pool);
+
+/* Take n blocks from the head of the free queue, each with refcount 1, and
+ * write their ids to out_ids (host, n entries) in queue order.
+ * hnwysp.cn/news/103996 §3.4, §4.4 (take from the head of the free queue).
+ * All-or-nothing: OUT_OF_BLOCKS if fewer than n are free, nothing taken. */
+pkv_status pkv_alloc(pkv_pool *pool, int32_t n, int32_t *out_ids);
+
+/* One more reference to each listed block (host array, n ids; repeats count
+ * twice): sharing a prefix or forking a sequence, icman.com.cn/news/78786 §3.4.
+ * BAD_BLOCK for an id out of range, REFCOUNT for a free block; all-or-nothing. */
+pkv_status pkv_incref(pkv_pool *pool, const int32_t *ids, int32_t n);
+
+/* Drop one reference per listed block (host array, n ids; repeats count).
+ * A block reaching 0 is pushed to the tail of the free queue, in list order:
+ * hnwysp.cn/news/103996 §3.3, §3.4, §4.4; icman.com.cn/news/78786 §6.3.
+ * BAD_BLOCK / REFCOUNT (a count would go below 0); all-or-nothing. */
+pkv_status pkv_free(pkv_pool *pool, const int32_t *ids, int32_t n);
+
+/* Refcount of block id (0 = free). BAD_BLOCK if out of range. */
+pkv_status pkv_refcount(const pkv_pool *pool, int32_t id, int32_t *out);
+
+/* Pool counters (icman.com.cn/news/78786 §6.5 lists pool use as the first
+ * figure to watch). */
+pkv_status pkv_get_stats(const pkv_pool *pool, pkv_stats *out);
+
+/* Copy the free queue, head first, into out (capacity entries); *count gets
+ * its length. INVALID_ARG if capacity is too small. */
+pkv_status pkv_free_queue(const pkv_pool *pool, int32_t *out, int32_t capacity, int32_t *count);
+
+/* Check the bookkeeping: the free queue holds every block with refcount 0 once
+ * and nothing else. REFCOUNT if not (never expected; a test hook). */
+pkv_status pkv_validate(const pkv_pool *pool);
+
+/* Give slots to the next tokens of a batch of sequences; the host half of the
+ * decode step (m.lqnn.cn/news/240480 §3.2 step 3; hnwysp.cn/news/103996 §3.3).
+ *
+ * For s = 0..num_seqs-1 in order, and for each of its num_new[s] tokens in
+ * order (num_new NULL = one token each), with p = context_lens[s]:
+ *   - if p % B == 0: a block is taken from the free queue into
+ *     block_tables[s][p / B];
+ *   - else, if the block block_tables[s][p / B] has refcount > 1: a block dst
+ *     is taken, the pair (that block, dst) is emitted, the old block loses one
+ *     reference and dst replaces it in the table (copy-on-write);
+ *   - the token's slot is block_tables[s][p / B] * B + p % B, and p grows by 1.
+ * block_tables: host int32 [num_seqs][max_blocks], updated in place (entries
+ *   past the sequence's blocks are not read). context_lens: host int32
+ *   [num_seqs], updated in place. slot_mapping: host int64, capacity
+ *   slot_capacity; *num_slots = tokens given slots, in (sequence, token) order.
+ * copy_pairs: host int32 [pair_capacity][2] (src, dst); *num_pairs = pairs.
+ *   The caller must run pkv_copy_blocks on these pairs before pkv_append
+ *   writes the new tokens.
+ * Errors (all-or-nothing, nothing changed): OUT_OF_BLOCKS; INVALID_ARG (a table
+ *   too short for the new length, capacities too small, negative counts);
+ *   BAD_BLOCK (a table entry that is out of range or not allocated). */
+pkv_status pkv_prepare_append(pkv_pool *pool, int32_t num_seqs, int32_t *block_tables,
+                              int32_t max_blocks, int32_t *context_lens, const int32_t *num_new,
+                              int64_t *slot_mapping, int32_t slot_capacity, int32_t *num_slots,
+                              int32_t *copy_pairs, int32_t pair_capacity, int32_t *num_pairs);
+
+/* ---------------------------------------------------------------- device ops */
+
+/* Write num_tokens new tokens' K and V of layer `layer` into their slots
+ * ("reshape and cache"; m.lqnn.cn/news/240480 §3.2 step 3, §3.3).
+ * k_new, v_new: device fp16 [num_tokens][H][D], 16-byte aligned.
+ * slot_mapping: device int64 [num_tokens]; slot < 0 means "skip this token";
+ *   slot >= N * B is skipped and flagged PKV_DEV_BAD_SLOT. Slots must be
+ *   distinct (two tokens to one slot race).
+ * status: device uint32 status word (may be NULL). Bit copy, no arithmetic.
+ * Host errors: INVALID_ARG (layer out of range, host-only pool, misaligned). */
+pkv_status pkv_append(const pkv_pool *pool, int32_t layer, const void *k_new, const void *v_new,
+                      const int64_t *slot_mapping, int32_t num_tokens, uint32_t *status,
+                      void *stream);
+
+/* Copy-on-write data move (hnwysp.cn/news/103996 §3.3): for each pair
+ * (src, dst) of the device int32 array pairs[num_pairs][2], block dst <- block
+ * src in every layer, K and V (B * H * D elements each). A pair with an id out
+ * of range is skipped and flagged PKV_DEV_BAD_PAIR. dst blocks must be distinct
+ * and must not appear as a src. num_pairs = 0 enqueues nothing. */
+pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *pairs, int32_t num_pairs,
+                           uint32_t *status, void *stream);
+
+/* Paged decode attention for one layer: for every sequence s and head h,
+ *   out[s][h] = softmax_t(scale * q[s][h] . K_s[t]) V_s[t],  t = 0..T_s-1,
+ * where token t of sequence s is read from physical block
+ * block_tables[s][t / B] at slot t % B (m.lqnn.cn/news/240480 §3.3;
+ * icman.com.cn/news/78786 §2.4). Products and sums in fp32, out in fp16
+ * (round to nearest even). T_s = 0 gives out[s][h] = 0.
+ *
+ * q: device fp16 [num_seqs][H][D]. k_cache, v_cache: device pointers to one
+ *   layer's pool (N blocks in `layout`), 16-byte aligned.
+ * block_tables: device int32 [num_seqs][max_blocks]. context_lens: device int32
+ *   [num_seqs] (the lengths after this step's append).
+ * scale: softmax scale; pass 0 or a negative value for 1/sqrt(D).
+ * out: device fp16 [num_seqs][H][D].
+ * workspace: device scratch of at least pkv_decode_workspace_bytes(...) bytes,
+ *   16-byte aligned, ZERO-FILLED before its first use; each call leaves its
+ *   counter area zero again, so one workspace serves every later call on the
+ *   same stream (calls that overlap on the GPU must use distinct workspaces).
+ *   Its first 4 bytes are the device status word of the call (PKV_DEV_* bits,
+ *   sticky: clear it to reset).
+ * Errors: INVALID_ARG (sizes, alignment, workspace too small), UNSUPPORTED
+ *   (head_dim or block_size not built), CUDA (launch failure). */
+pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                int32_t num_blocks, int32_t block_size, int32_t num_heads,
+                                int32_t head_dim, int32_t layout, const int32_t *block_tables,
+                                int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs,
+                                float scale, void *out, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/* Bytes of workspace pkv_decode_attention needs for these sizes on the
+ * current CUDA device (0 and a pkv_last_error message on bad arguments). */
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim);
+
+/* The same attention on a pool handle's layer (pointers and shape from the
+ * pool). */
+pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const void *q,
+                                     const int32_t *block_tables, int32_t max_blocks,
+                                     const int32_t *context_lens, int32_t num_seqs, float scale,
+                                     void *out, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/* Launch geometry of pkv_decode_attention on the current device, for
+ * reporting: CTAs per launch, CTAs per SM, and the SM count. */
+pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t *grid_ctas,
+                                  int32_t *ctas_per_sm, int32_t *num_sms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,92 @@
+"""Oracle replay of a workload: the allocator oracle plus float64 attention (test infrastructure only).
+
+Mirrors a decode step of the product path with the oracle's own pieces:
+``RefPool.prepare_append`` (slots, COW pairs), ``copy_blocks``, ``append_kv`` and
+``decode_attention`` over NumPy pools. Shares nothing with the CUDA library; it
+reads the same seeded inputs from ``workloads``.
+"""
+from __future__ import annotations
+
+from typing import Callable, List, Optional
+
+import numpy as np
+
+import workloads as wl
+
+from . import ref_alloc as ra
+from . import ref_attn as rf
+
+
+class OracleEngine:
+    def __init__(self, w: wl.Workload, k_pool: np.ndarray, v_pool: np.ndarray):
+        """``k_pool``/``v_pool``: the initial pools, shape ``workloads.pool_shape(w)`` (copied)."""
+        self.w = w
+        self.k_pool = np.array(k_pool, dtype=np.float16, copy=True)
+        self.v_pool = np.array(v_pool, dtype=np.float16, copy=True)
+        self.pool = ra.RefPool(w.num_blocks, [int(x) for x in w.free_order])
+        self.tables: List[List[int]] = [[-1] * w.max_blocks for _ in range(w.num_seqs)]
+        self.lens: List[int] = [0] * w.num_seqs
+        self.dummies = {}
+        self.last_slots: list = []
+        self.last_pairs: list = []
+
+    def tables_array(self) -> np.ndarray:
+        return np.asarray(self.tables, dtype=np.int32)
+
+    def run_script(self, values: Optional[Callable] = None):
+        """Replay the set-up script. ``values(op_index, layer, which, n)`` gives written K/V (default: workloads)."""
+        w, B = self.w, self.w.block_size
+        values = values or (lambda oi, l, wh, n: wl.write_values(w, oi, l, wh, n))
+        for op_index, op in enumerate(w.script):
+            kind = op[0]
+            if kind == "admit":
+                _, s, T = op
+                self.tables[s] = ra.admit(self.pool, T, B, w.max_blocks)
+                self.lens[s] = T
+            elif kind == "fork":
+                _, src, dst = op
+                self.tables[dst] = ra.fork(self.pool, self.tables[src], self.lens[src], B)
+                self.lens[dst] = self.lens[src]
+            elif kind == "dummy_alloc":
+                _, d, n = op
+                self.dummies[d] = self.pool.alloc(n)
+            elif kind == "dummy_free":
+                _, d = op
+                self.pool.free(self.dummies.pop(d))
+            elif kind == "write":
+                counts = [int(x) for x in op[1]]
+                total = sum(counts)
+                slots, pairs = self.pool.prepare_append(self.tables, self.lens, counts, B, w.max_blocks)
+                rf.copy_blocks(self.k_pool, self.v_pool, pairs)
+                for layer in range(w.num_layers):
+                    rf.append_kv(self.k_pool[layer], self.v_pool[layer], values(op_index, layer, 0, total),
+                                 values(op_index, layer, 1, total), slots, B, w.layout)
+                self.last_slots, self.last_pairs = slots, pairs
+            else:
+                raise ValueError(kind)
+
+    def step(self, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, scale: Optional[float] = None,
+             layers: Optional[list] = None, pairs_only: Optional[list] = None) -> np.ndarray:
+        """One decode step: a3 (slots, COW), a4 copy, a5 append, a6/a7 attention. Returns float64 [L, S, H, D]."""
+        w = self.w
+        slots, pairs = self.pool.prepare_append(self.tables, self.lens, [1] * w.num_seqs, w.block_size,
+                                                w.max_blocks)
+        rf.copy_blocks(self.k_pool, self.v_pool, pairs)
+        out = np.zeros((w.num_layers, w.num_seqs, w.num_heads, w.head_dim))
+        tab = self.tables_array()
+        for layer in range(w.num_layers):
+            rf.append_kv(self.k_pool[layer], self.v_pool[layer], k_new[layer], v_new[layer], slots, w.block_size,
+                         w.layout)
+            if layers is not None and layer not in layers:
+                continue
+            out[layer] = rf.decode_attention(q[layer], self.k_pool[layer], self.v_pool[layer], tab, self.lens,
+                                             w.block_size, w.layout, scale, pairs=pairs_only)
+        self.last_slots, self.last_pairs = slots, pairs
+        return out
+
+    def step_inputs(self, step: int):
+        w = self.w
+        q = np.stack([wl.query_values(w, step, l) for l in range(w.num_layers)])
+        k = np.stack([wl.new_token_values(w, step, l, 0) for l in range(w.num_layers)])
+        v = np.stack([wl.new_token_values(w, step, l, 1) for l in range(w.num_layers)])
+        return q, k, v

@@ -1,0 +1,302 @@
+"""ctypes binding of libpkv (include/pkv.h): argument marshalling only.
+
+Every function here forwards to the C ABI with the same name (minus the
+``pkv_`` prefix); all work happens in the library's CUDA kernels or its host
+allocator. Tensors are passed as raw pointers (``tensor.data_ptr()``), the
+stream as ``torch.cuda.current_stream().cuda_stream`` unless one is given.
+If ``libpkv.so`` is missing the import fails loudly: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_BLOCKS", 3: "BAD_BLOCK", 4: "REFCOUNT", 5: "CUDA",
+                6: "UNSUPPORTED"}
+LAYOUTS = {"NHD": 0, "HND": 1}
+DEV_BAD_BLOCK, DEV_BAD_LENGTH, DEV_TIMEOUT, DEV_BAD_SLOT, DEV_BAD_PAIR = 0x1, 0x2, 0x4, 0x8, 0x10
+
+EXPORTED = [
+    "pkv_last_error", "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_info", "pkv_alloc",
+    "pkv_incref", "pkv_free", "pkv_refcount", "pkv_get_stats", "pkv_free_queue", "pkv_validate",
+    "pkv_prepare_append", "pkv_append", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_workspace_bytes",
+    "pkv_pool_decode_attention", "pkv_decode_launch_info",
+]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.code = STATUS_NAMES.get(status, str(status))
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("layout", ctypes.c_int32)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("free_blocks", ctypes.c_int32), ("used_blocks", ctypes.c_int32), ("shared_blocks", ctypes.c_int32),
+                ("max_refcount", ctypes.c_int32), ("cow_copies", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lib = None
+vp, i32, i64, u64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run paged_kv_cache_88_gb300.build.build() "
+                              "(the CUDA library is required, there is no fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "pkv_last_error": (ctypes.c_char_p, []),
+            "pkv_version": (i32, []),
+            "pkv_pool_create": (i32, [ctypes.POINTER(PoolDesc), vp, vp, vp, ctypes.POINTER(vp)]),
+            "pkv_pool_destroy": (i32, [vp]),
+            "pkv_pool_info": (i32, [vp, ctypes.POINTER(PoolDesc), ctypes.POINTER(vp), ctypes.POINTER(vp)]),
+            "pkv_alloc": (i32, [vp, i32, vp]),
+            "pkv_incref": (i32, [vp, vp, i32]),
+            "pkv_free": (i32, [vp, vp, i32]),
+            "pkv_refcount": (i32, [vp, i32, ctypes.POINTER(i32)]),
+            "pkv_get_stats": (i32, [vp, ctypes.POINTER(Stats)]),
+            "pkv_free_queue": (i32, [vp, vp, i32, ctypes.POINTER(i32)]),
+            "pkv_validate": (i32, [vp]),
+            "pkv_prepare_append": (i32, [vp, i32, vp, i32, vp, vp, vp, i32, ctypes.POINTER(i32), vp, i32,
+                                         ctypes.POINTER(i32)]),
+            "pkv_append": (i32, [vp, i32, vp, vp, vp, i32, vp, vp]),
+            "pkv_copy_blocks": (i32, [vp, vp, i32, vp, vp]),
+            "pkv_decode_attention": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
+                                           vp]),
+            "pkv_decode_workspace_bytes": (sz, [i32, i32, i32]),
+            "pkv_pool_decode_attention": (i32, [vp, i32, vp, vp, i32, vp, i32, f32, vp, vp, sz, vp]),
+            "pkv_decode_launch_info": (i32, [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                             ctypes.POINTER(i32)]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().pkv_last_error().decode()
+
+
+def check(status: int) -> None:
+    if status != OK:
+        raise PkvError(status, last_error())
+
+
+def _ptr(a) -> Optional[int]:
+    """Address of a numpy array or torch tensor (None stays None)."""
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        return a.ctypes.data
+    return a.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _require(t, dtype_name: str, what: str):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA tensor")
+    if str(t.dtype) != f"torch.{dtype_name}":
+        raise ValueError(f"{what} must be {dtype_name}, got {t.dtype}")
+
+
+class Pool:
+    """A block pool (host metadata in libpkv) over caller-owned K/V pool tensors.
+
+    ``k_pool``/``v_pool``: CUDA fp16 tensors of L*N*B*H*D elements laid out as
+    [L, N, B, H, D] (NHD) or [L, N, H, B, D] (HND), or None for a host-only pool.
+    """
+
+    def __init__(self, num_layers: int, num_blocks: int, block_size: int, num_heads: int, head_dim: int,
+                 layout: str = "NHD", k_pool=None, v_pool=None, initial_free_order: Optional[Sequence[int]] = None):
+        self.desc = PoolDesc(num_layers, num_blocks, block_size, num_heads, head_dim, LAYOUTS[layout])
+        self.layout = layout
+        self.k_pool, self.v_pool = k_pool, v_pool
+        if k_pool is not None:
+            _require(k_pool, "float16", "k_pool")
+            _require(v_pool, "float16", "v_pool")
+            want = num_layers * num_blocks * block_size * num_heads * head_dim
+            if k_pool.numel() != want or v_pool.numel() != want:
+                raise ValueError(f"pool tensors must hold {want} elements")
+        order = None
+        if initial_free_order is not None:
+            order = np.ascontiguousarray(initial_free_order, dtype=np.int32)
+            if order.shape != (num_blocks,):
+                raise ValueError("initial_free_order must have num_blocks entries")
+        h = vp()
+        check(lib().pkv_pool_create(ctypes.byref(self.desc), _ptr(k_pool), _ptr(v_pool), _ptr(order),
+                                    ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().pkv_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    # -- host allocator ---------------------------------------------------------------
+    def alloc(self, n: int) -> list:
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        check(lib().pkv_alloc(self._h, n, _ptr(out)))
+        return out[:n].tolist()
+
+    def incref(self, ids: Sequence[int]) -> None:
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        check(lib().pkv_incref(self._h, _ptr(a), a.size))
+
+    def free(self, ids: Sequence[int]) -> None:
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        check(lib().pkv_free(self._h, _ptr(a), a.size))
+
+    def refcount(self, block: int) -> int:
+        r = i32()
+        check(lib().pkv_refcount(self._h, block, ctypes.byref(r)))
+        return r.value
+
+    def stats(self) -> dict:
+        s = Stats()
+        check(lib().pkv_get_stats(self._h, ctypes.byref(s)))
+        return s.as_dict()
+
+    def free_queue(self) -> list:
+        n = i32()
+        out = np.zeros(self.desc.num_blocks, dtype=np.int32)
+        check(lib().pkv_free_queue(self._h, _ptr(out), out.size, ctypes.byref(n)))
+        return out[: n.value].tolist()
+
+    def validate(self) -> None:
+        check(lib().pkv_validate(self._h))
+
+    def prepare_append(self, block_tables: np.ndarray, context_lens: np.ndarray,
+                       num_new: Optional[Sequence[int]] = None,
+                       slot_out: Optional[np.ndarray] = None, pair_out: Optional[np.ndarray] = None
+                       ) -> Tuple[np.ndarray, np.ndarray]:
+        """Host step a3; ``block_tables`` (int32 [S, maxb]) and ``context_lens`` (int32 [S]) change in place.
+
+        Returns (slot_mapping int64 [n_tokens], copy_pairs int32 [n_pairs, 2]); with
+        ``slot_out``/``pair_out`` given (e.g. pinned buffers) they are filled and views returned.
+        """
+        assert block_tables.dtype == np.int32 and block_tables.flags.c_contiguous
+        assert context_lens.dtype == np.int32 and context_lens.flags.c_contiguous
+        S, maxb = block_tables.shape
+        nn = None if num_new is None else np.ascontiguousarray(num_new, dtype=np.int32)
+        total = S if nn is None else int(nn.sum())
+        slots = slot_out if slot_out is not None else np.zeros(max(total, 1), dtype=np.int64)
+        pairs = pair_out if pair_out is not None else np.zeros((max(total, 1), 2), dtype=np.int32)
+        ns, npair = i32(), i32()
+        check(lib().pkv_prepare_append(self._h, S, _ptr(block_tables), maxb, _ptr(context_lens), _ptr(nn),
+                                       _ptr(slots), slots.shape[0], ctypes.byref(ns), _ptr(pairs), pairs.shape[0],
+                                       ctypes.byref(npair)))
+        return slots[: ns.value], pairs[: npair.value]
+
+    # -- device ops ---------------------------------------------------------------------
+    def append(self, layer: int, k_new, v_new, slot_mapping, num_tokens: Optional[int] = None, status=None,
+               stream=None) -> None:
+        _require(k_new, "float16", "k_new")
+        _require(v_new, "float16", "v_new")
+        _require(slot_mapping, "int64", "slot_mapping")
+        n = slot_mapping.numel() if num_tokens is None else num_tokens
+        check(lib().pkv_append(self._h, layer, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), n, _ptr(status),
+                               _stream(stream)))
+
+    def copy_blocks(self, pairs, num_pairs: Optional[int] = None, status=None, stream=None) -> None:
+        _require(pairs, "int32", "pairs")
+        n = pairs.numel() // 2 if num_pairs is None else num_pairs
+        check(lib().pkv_copy_blocks(self._h, _ptr(pairs), n, _ptr(status), _stream(stream)))
+
+    def decode_attention(self, layer: int, q, block_tables, context_lens, out, workspace, scale: float = 0.0,
+                         stream=None) -> None:
+        _require(q, "float16", "q")
+        _require(out, "float16", "out")
+        _require(block_tables, "int32", "block_tables")
+        _require(context_lens, "int32", "context_lens")
+        S = q.shape[0]
+        check(lib().pkv_pool_decode_attention(self._h, layer, _ptr(q), _ptr(block_tables), block_tables.shape[1],
+                                              _ptr(context_lens), S, float(scale), _ptr(out), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+    def layer_view(self, which: str, layer: int):
+        t = self.k_pool if which == "k" else self.v_pool
+        d = self.desc
+        return t.view(d.num_layers, -1)[layer]
+
+
+def decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int) -> int:
+    n = lib().pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim)
+    if n == 0:
+        raise PkvError(1, last_error())
+    return int(n)
+
+
+def new_workspace(num_seqs: int, num_heads: int, head_dim: int, device="cuda"):
+    """A zero-filled workspace tensor (uint8) for :func:`decode_attention`; its first 4 bytes are the status word."""
+    import torch
+    return torch.zeros(decode_workspace_bytes(num_seqs, num_heads, head_dim), dtype=torch.uint8, device=device)
+
+
+def workspace_status(workspace) -> int:
+    """Read the device status word (first 4 bytes) of a workspace (synchronises)."""
+    return int(workspace[:4].view(dtype=__import__("torch").int32).item()) & 0xFFFFFFFF
+
+
+def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, num_blocks: int, block_size: int,
+                     layout: str = "NHD", scale: float = 0.0, out=None, workspace=None, stream=None):
+    """Paged decode attention on one layer's caches (pkv_decode_attention); returns ``out``."""
+    import torch
+    _require(q, "float16", "q")
+    _require(k_cache, "float16", "k_cache")
+    _require(v_cache, "float16", "v_cache")
+    _require(block_tables, "int32", "block_tables")
+    _require(context_lens, "int32", "context_lens")
+    S, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = new_workspace(S, H, D, q.device)
+    check(lib().pkv_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, block_size, H, D,
+                                     LAYOUTS[layout], _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                     S, float(scale), _ptr(out), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def decode_launch_info(num_seqs: int, head_dim: int) -> dict:
+    g, per, sms = i32(), i32(), i32()
+    check(lib().pkv_decode_launch_info(num_seqs, head_dim, ctypes.byref(g), ctypes.byref(per), ctypes.byref(sms)))
+    return {"grid_ctas": g.value, "ctas_per_sm": per.value, "num_sms": sms.value}

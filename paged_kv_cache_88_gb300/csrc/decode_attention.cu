@@ -1,0 +1,743 @@
+// Paged decode attention for sm_103a (GB300).
+//
+// What it computes (per layer): for every sequence s and head h,
+//   out[s][h] = softmax_t(scale * q[s][h] . K_s[t]) V_s[t],   t = 0..T_s-1,
+// with token t of sequence s read from physical block table[s][t / B], slot
+// t % B (m.lqnn.cn/news/240480 §3.3 remaps [batch, head, pos, dim] to
+// [page, slot, head, dim] through the page table; icman.com.cn/news/78786 §2.4
+// walks the block table and loads each block's K/V). Single-query decode is a
+// GEMV over the cache: about 0.5 FMA per byte, so the kernel is bound by HBM
+// bandwidth and uses no tensor cores.
+//
+// Design (GB300-first; the pages' A100 kernel advice -- table in shared memory,
+// vectorised loads, many heads per launch -- is prior art, not the blueprint):
+//
+// * Work unit = one tile of 32 tokens of one (sequence, head). All tiles of the
+//   batch are numbered (s, h, t) and the launch's CTAs take equal contiguous
+//   ranges of that list (a persistent grid of SMs x resident CTAs). Mixed
+//   context lengths therefore cost no tail imbalance: every CTA streams the same
+//   number of tiles (+-1).
+// * A producer warp walks the CTA's range and issues TMA tensor loads of each
+//   tile's K and V rows (one box per block, or a 32-row box inside a large
+//   block) into a multi-stage shared-memory ring guarded by mbarriers; it keeps a
+//   window of 32 block-table entries of the current sequence in registers (one
+//   coalesced load serves every head of the sequence). The query row of a new
+//   (s, h) rides along in the same stage as a 1-D bulk copy.
+// * Four consumer warps split each tile into 16 groups of 8 lanes; a group owns
+//   two tokens, a lane 8 or 16 elements of the head dim. q.K is an fp32 dot
+//   product finished with three xor-shuffles; each group keeps its own online
+//   softmax state (running max m, sum l, unnormalised o), so no block-wide
+//   synchronisation happens per tile.
+// * When an (s, h) ends inside the CTA, the 16 group states are merged through
+//   shared memory. A (s, h) that lies wholly in the CTA is written straight to
+//   out; one split across CTAs writes its piece (m, l, o) to the workspace and
+//   the last CTA to arrive (an atomic counter, no waiting) merges the pieces and
+//   writes out -- split-KV with the combine fused into the same launch.
+// * Every mbarrier wait has a time limit; on expiry the CTA flags
+//   PKV_DEV_TIMEOUT, stops waiting and runs to the end (no trap, no hang).
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+using namespace pkv;
+
+constexpr int kTile = 32;            // tokens per pipeline stage
+constexpr int kConsumerWarps = 4;    // warps that compute
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kGroups = kConsumerWarps * 4;      // 8-lane groups
+constexpr int kStages = 4;
+constexpr int kMaxSeqs = 4096;
+constexpr int kMaxCtasPerSm = 8;     // bound used to size the workspace
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr int kStatusBytes = 256;
+
+struct Params {
+    const __half *q;
+    __half *out;
+    const int32_t *tables;
+    const int32_t *lens;
+    float *pieces;       // [grid][2][D + 4]
+    int32_t *counters;   // [S * H]
+    uint32_t *status;
+    int32_t S, H, max_blocks, B, N, layout;
+    float scale_log2;    // scale * log2(e)
+};
+
+__host__ __device__ constexpr int stage_bytes(int D) {
+    // K tile + V tile + the query row, rounded to 128 bytes
+    return ((2 * kTile * D * 2 + D * 2) + 127) / 128 * 128;
+}
+
+__host__ __device__ constexpr int piece_stride(int D) { return D + 4; }
+
+// Shared memory: [stages][reduction][seq arrays][barriers + flags]
+__host__ size_t smem_bytes(int D, int S) {
+    size_t b = (size_t)kStages * stage_bytes(D);
+    b += (size_t)kGroups * (D + 2) * sizeof(float);
+    b += (size_t)(2 * S + 2) * sizeof(int32_t);
+    b = (b + 15) / 16 * 16;
+    b += 2 * kStages * sizeof(uint64_t) + 16;
+    return b + 128;  // slack to align the base to 128 bytes (TMA destination)
+}
+
+struct Smem {
+    unsigned char *stage;  // kStages * stage_bytes(D)
+    float *red_o;          // [kGroups][D]
+    float *red_m;          // [kGroups]
+    float *red_l;          // [kGroups]
+    int32_t *len;          // [S]
+    int32_t *base;         // [S + 1] exclusive prefix of H * ntiles
+    uint64_t *full;        // [kStages]
+    uint64_t *empty;       // [kStages]
+    volatile int32_t *flags;  // [0] = timed out, [1] = last-arriver flag
+};
+
+template <int D>
+__device__ __forceinline__ Smem carve(unsigned char *raw, int S) {
+    Smem m;
+    uintptr_t p = (reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127);
+    m.stage = reinterpret_cast<unsigned char *>(p);
+    p += (size_t)kStages * stage_bytes(D);
+    m.red_o = reinterpret_cast<float *>(p);
+    p += (size_t)kGroups * D * sizeof(float);
+    m.red_m = reinterpret_cast<float *>(p);
+    p += kGroups * sizeof(float);
+    m.red_l = reinterpret_cast<float *>(p);
+    p += kGroups * sizeof(float);
+    m.len = reinterpret_cast<int32_t *>(p);
+    p += (size_t)S * sizeof(int32_t);
+    m.base = reinterpret_cast<int32_t *>(p);
+    p += (size_t)(S + 1) * sizeof(int32_t);
+    p = (p + 15) & ~uintptr_t(15);
+    m.full = reinterpret_cast<uint64_t *>(p);
+    m.empty = m.full + kStages;
+    m.flags = reinterpret_cast<volatile int32_t *>(m.empty + kStages);
+    return m;
+}
+
+// Position in the CTA's tile range: sequence, head, tile of the (s, h).
+struct Cursor {
+    int32_t s, h, t, nt;
+};
+
+__device__ __forceinline__ int32_t ntiles_of(int32_t T) { return (T + kTile - 1) / kTile; }
+
+__device__ __forceinline__ Cursor locate(const Smem &sm, int32_t S, int32_t H, int32_t g) {
+    // largest s with base[s] <= g (g < total, so that s has tiles)
+    int32_t lo = 0, hi = S - 1;
+    while (lo < hi) {
+        int32_t mid = (lo + hi + 1) >> 1;
+        if (sm.base[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    Cursor c;
+    c.s = lo;
+    c.nt = ntiles_of(sm.len[lo]);
+    int32_t r = g - sm.base[lo];
+    c.h = r / c.nt;
+    c.t = r - c.h * c.nt;
+    return c;
+}
+
+__device__ __forceinline__ void advance(Cursor &c, const Smem &sm, int32_t S, int32_t H) {
+    if (++c.t < c.nt) return;
+    c.t = 0;
+    if (++c.h < H) return;
+    c.h = 0;
+    do {
+        ++c.s;
+    } while (c.s < S && sm.len[c.s] == 0);
+    if (c.s < S) c.nt = ntiles_of(sm.len[c.s]);
+}
+
+// First tile index of CTA c among `total` tiles split over `grid` CTAs.
+__device__ __forceinline__ int32_t range_start(int64_t total, int32_t grid, int32_t c) {
+    return static_cast<int32_t>((total * c) / grid);
+}
+
+// The CTA whose range holds tile g.
+__device__ __forceinline__ int32_t cta_of(int64_t total, int32_t grid, int32_t g) {
+    return static_cast<int32_t>(((int64_t)(g + 1) * grid - 1) / total);
+}
+
+// Bounded wait: false (and PKV_DEV_TIMEOUT) if the phase does not complete
+// within the limit; after one timeout in the CTA every later wait returns at once.
+__device__ __forceinline__ bool wait_phase(const Smem &sm, uint32_t bar, uint32_t parity, uint32_t *status) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (sm.flags[0]) return false;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (sm.flags[0]) return false;
+        if (ptx::global_timer_ns() - t0 > kWaitLimitNs) {
+            sm.flags[0] = 1;
+            atomicOr(status, PKV_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const Params p) {
+    constexpr int NCH = D / 64;  // 16-byte chunks per lane per row
+    constexpr int SB = stage_bytes(D);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const Smem sm = carve<D>(smem_raw, p.S);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int32_t S = p.S, H = p.H;
+    const int32_t cap = p.max_blocks * p.B;
+
+    // ---- set-up: lengths, tile prefix over sequences, barriers
+    for (int32_t s = tid; s < S; s += kThreads) {
+        int32_t T = p.lens[s];
+        if (T < 0 || T > cap) {
+            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            T = T < 0 ? 0 : cap;
+        }
+        sm.len[s] = T;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            ptx::mbar_init(ptx::smem_addr(&sm.full[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sm.empty[i]), kConsumerWarps);
+        }
+        sm.flags[0] = 0;
+        sm.flags[1] = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int32_t running = 0;
+        for (int32_t s0 = 0; s0 < S; s0 += 32) {
+            const int32_t s = s0 + lane;
+            const int32_t v = s < S ? H * ntiles_of(sm.len[s]) : 0;
+            int32_t incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            if (s < S) sm.base[s] = running + incl - v;
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) sm.base[S] = running;
+    }
+    __syncthreads();
+
+    const int32_t total = sm.base[S];
+    const int32_t grid = gridDim.x;
+    const int32_t cta = blockIdx.x;
+
+    // Empty contexts: out = 0 (softmax over no tokens contributes nothing).
+    if (warp < kConsumerWarps) {
+        for (int32_t i = cta; i < S * H; i += grid) {
+            if (sm.len[i / H] != 0) continue;
+            if (tid < D / 8)
+                reinterpret_cast<uint4 *>(p.out + (size_t)i * D)[tid] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (total == 0) return;
+    const int32_t g0 = range_start(total, grid, cta);
+    const int32_t g1 = range_start(total, grid, cta + 1);
+    const int32_t n = g1 - g0;
+    if (n <= 0) return;
+
+    const uint32_t stage0 = ptx::smem_addr(sm.stage);
+    const uint32_t full0 = ptx::smem_addr(sm.full);
+    const uint32_t empty0 = ptx::smem_addr(sm.empty);
+
+    if (warp == kConsumerWarps) {
+        // ================= producer warp
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&kmap);
+            ptx::prefetch_tensormap(&vmap);
+        }
+        const int32_t B = p.B;
+        const int32_t rows = B < kTile ? B : kTile;           // rows per TMA box
+        const uint32_t box_bytes = (uint32_t)rows * D * 2;
+        Cursor c = locate(sm, S, H, g0);
+        int32_t win_s = -1, win_lb0 = 0, win_val = 0;
+        for (int32_t k = 0; k < n; ++k) {
+            const int32_t stage = k % kStages;
+            if (k >= kStages) {
+                const uint32_t parity = ((k / kStages) - 1) & 1;
+                wait_phase(sm, empty0 + 8 * stage, parity, p.status);
+            }
+            const int32_t T = sm.len[c.s];
+            const int32_t t0 = c.t * kTile;
+            const int32_t ntok = min(kTile, T - t0);
+            const int32_t lb = t0 / B;                         // first logical block of the tile
+            const int32_t nbox = B < kTile ? (ntok + B - 1) / B : 1;
+            const int32_t r0 = B < kTile ? 0 : t0 % B;         // first row inside the block
+            if (c.s != win_s || lb < win_lb0 || lb + nbox > win_lb0 + 32) {
+                win_s = c.s;
+                win_lb0 = lb;
+                const int32_t e = lb + lane;
+                win_val = e < p.max_blocks ? __ldg(p.tables + (size_t)c.s * p.max_blocks + e) : 0;
+            }
+            const bool first = (k == 0) || (c.t == 0);
+            const uint32_t bytes = (uint32_t)nbox * box_bytes * 2 + (first ? D * 2 : 0);
+            const uint32_t dst = stage0 + stage * SB;
+            const uint32_t bar = full0 + 8 * stage;
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar, bytes);
+            for (int32_t i = 0; i < nbox; ++i) {
+                int32_t blk = __shfl_sync(0xffffffffu, win_val, lb + i - win_lb0);
+                if (lane == 0) {
+                    if (blk < 0 || blk >= p.N) {
+                        atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                        blk = 0;
+                    }
+                    int32_t x, y;
+                    if (p.layout == PKV_LAYOUT_NHD) {
+                        x = c.h * D;
+                        y = blk * B + r0;
+                    } else {
+                        x = 0;
+                        y = (blk * H + c.h) * B + r0;
+                    }
+                    ptx::tma_load_2d(dst + i * box_bytes, &kmap, x, y, bar);
+                    ptx::tma_load_2d(dst + kTile * D * 2 + i * box_bytes, &vmap, x, y, bar);
+                }
+            }
+            if (lane == 0 && first)
+                ptx::bulk_load(dst + 2 * kTile * D * 2, p.q + ((size_t)c.s * H + c.h) * D, D * 2, bar);
+            __syncwarp();
+            advance(c, sm, S, H);
+        }
+        return;
+    }
+
+    // ================= consumer warps
+    const int grp = warp * 4 + (lane >> 3);  // 0..15
+    const int j = lane & 7;
+    float qf[NCH * 8];
+    float o[NCH * 8];
+    float m = -INFINITY, l = 0.f;
+    Cursor c = locate(sm, S, H, g0);
+    int32_t seg_g0 = g0;  // first tile of the current (s, h) inside this CTA
+
+    for (int32_t k = 0; k < n; ++k) {
+        const int32_t stage = k % kStages;
+        const unsigned char *st = sm.stage + stage * SB;
+        wait_phase(sm, full0 + 8 * stage, (k / kStages) & 1, p.status);
+        const bool first = (k == 0) || (c.t == 0);
+        const int32_t T = sm.len[c.s];
+        const int32_t ntok = min(kTile, T - c.t * kTile);
+        if (first) {
+            const __half *qs = reinterpret_cast<const __half *>(st + 2 * kTile * D * 2);
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(qs + ch * 64 + j * 8);
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    qf[ch * 8 + 2 * e] = f.x * p.scale_log2;
+                    qf[ch * 8 + 2 * e + 1] = f.y * p.scale_log2;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < NCH * 8; ++e) o[e] = 0.f;
+            m = -INFINITY;
+            l = 0.f;
+            seg_g0 = g0 + k;
+        }
+        const __half *ks = reinterpret_cast<const __half *>(st);
+        const __half *vs = reinterpret_cast<const __half *>(st + kTile * D * 2);
+        float x[2];
+        bool valid[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int tok = grp + 16 * u;
+            valid[u] = tok < ntok;
+            float dot = 0.f;
+            if (valid[u]) {
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(ks + tok * D + ch * 64 + j * 8);
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(h2[e]);
+                        dot = fmaf(qf[ch * 8 + 2 * e], f.x, dot);
+                        dot = fmaf(qf[ch * 8 + 2 * e + 1], f.y, dot);
+                    }
+                }
+            }
+            dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+            x[u] = valid[u] ? dot : -INFINITY;
+        }
+        const float mx = fmaxf(x[0], x[1]);
+        if (mx > m) {
+            const float alpha = ptx::ex2(m - mx);
+#pragma unroll
+            for (int e = 0; e < NCH * 8; ++e) o[e] *= alpha;
+            l *= alpha;
+            m = mx;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!valid[u]) continue;
+            const int tok = grp + 16 * u;
+            const float pw = ptx::ex2(x[u] - m);
+            l += pw;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(vs + tok * D + ch * 64 + j * 8);
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    o[ch * 8 + 2 * e] = fmaf(pw, f.x, o[ch * 8 + 2 * e]);
+                    o[ch * 8 + 2 * e + 1] = fmaf(pw, f.y, o[ch * 8 + 2 * e + 1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty0 + 8 * stage);
+
+        const bool last = (k == n - 1) || (c.t == c.nt - 1);
+        if (last) {
+            // ---- merge the 16 group states of this (s, h)
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sm.red_o[grp * D + ch * 64 + j * 8 + e] = o[ch * 8 + e];
+            if (j == 0) {
+                sm.red_m[grp] = m;
+                sm.red_l[grp] = l;
+            }
+            ptx::named_barrier(1, kConsumerThreads);
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kGroups; ++i) M = fmaxf(M, sm.red_m[i]);
+            float w[kGroups];
+            float L = 0.f;
+#pragma unroll
+            for (int i = 0; i < kGroups; ++i) {
+                w[i] = ptx::ex2(sm.red_m[i] - M);
+                L = fmaf(w[i], sm.red_l[i], L);
+            }
+            constexpr int DPT = (D + kConsumerThreads - 1) / kConsumerThreads;  // dims per thread
+            float O[DPT];
+#pragma unroll
+            for (int r = 0; r < DPT; ++r) {
+                const int d = tid + r * kConsumerThreads;
+                float acc = 0.f;
+                if (d < D) {
+#pragma unroll
+                    for (int i = 0; i < kGroups; ++i) acc = fmaf(w[i], sm.red_o[i * D + d], acc);
+                }
+                O[r] = acc;
+            }
+            const int32_t seg_lo = sm.base[c.s] + c.h * c.nt;   // (s, h) tiles: [seg_lo, seg_lo + nt)
+            const int32_t seg_hi = seg_lo + c.nt - 1;
+            const int32_t ca = cta_of(total, grid, seg_lo);
+            const int32_t cb = cta_of(total, grid, seg_hi);
+            __half *dst_out = p.out + ((size_t)c.s * H + c.h) * D;
+            if (ca == cb) {
+                const float inv = 1.f / L;
+#pragma unroll
+                for (int r = 0; r < DPT; ++r) {
+                    const int d = tid + r * kConsumerThreads;
+                    if (d < D) dst_out[d] = __float2half_rn(O[r] * inv);
+                }
+            } else {
+                const int slot = seg_g0 == g0 ? 0 : 1;  // 0: the CTA's first (s, h); 1: its last
+                float *piece = p.pieces + ((size_t)cta * 2 + slot) * piece_stride(D);
+#pragma unroll
+                for (int r = 0; r < DPT; ++r) {
+                    const int d = tid + r * kConsumerThreads;
+                    if (d < D) piece[d] = O[r];
+                }
+                if (tid == 0) {
+                    piece[D] = M;
+                    piece[D + 1] = L;
+                }
+                __threadfence();
+                ptx::named_barrier(1, kConsumerThreads);
+                if (tid == 0) {
+                    const int32_t prev = atomicAdd(p.counters + (size_t)c.s * H + c.h, 1);
+                    sm.flags[1] = (prev == cb - ca) ? 1 : 0;
+                }
+                ptx::named_barrier(1, kConsumerThreads);
+                if (sm.flags[1]) {
+                    __threadfence();
+                    const int32_t start_a = range_start(total, grid, ca);
+                    float Mg = -INFINITY;
+                    for (int32_t cc = ca; cc <= cb; ++cc) {
+                        const int sl = (cc > ca || start_a == seg_lo) ? 0 : 1;
+                        const float *pc = p.pieces + ((size_t)cc * 2 + sl) * piece_stride(D);
+                        Mg = fmaxf(Mg, __ldcg(pc + D));
+                    }
+                    float Lg = 0.f;
+                    float Og[DPT];
+#pragma unroll
+                    for (int r = 0; r < DPT; ++r) Og[r] = 0.f;
+                    for (int32_t cc = ca; cc <= cb; ++cc) {
+                        const int sl = (cc > ca || start_a == seg_lo) ? 0 : 1;
+                        const float *pc = p.pieces + ((size_t)cc * 2 + sl) * piece_stride(D);
+                        const float wc = ptx::ex2(__ldcg(pc + D) - Mg);
+                        Lg = fmaf(wc, __ldcg(pc + D + 1), Lg);
+#pragma unroll
+                        for (int r = 0; r < DPT; ++r) {
+                            const int d = tid + r * kConsumerThreads;
+                            if (d < D) Og[r] = fmaf(wc, __ldcg(pc + d), Og[r]);
+                        }
+                    }
+                    const float inv = 1.f / Lg;
+#pragma unroll
+                    for (int r = 0; r < DPT; ++r) {
+                        const int d = tid + r * kConsumerThreads;
+                        if (d < D) dst_out[d] = __float2half_rn(Og[r] * inv);
+                    }
+                    if (tid == 0) p.counters[(size_t)c.s * H + c.h] = 0;
+                }
+            }
+            ptx::named_barrier(1, kConsumerThreads);
+        }
+        advance(c, sm, S, H);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+struct DeviceInfo {
+    int num_sms = 0;
+    int ctas_per_sm[3] = {0, 0, 0};  // per head_dim 64/128/256, at the smem size last queried
+    size_t smem_for[3] = {0, 0, 0};
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int dim_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : 2); }
+
+template <int D>
+const void *kernel_ptr() {
+    return reinterpret_cast<const void *>(&decode_attention_kernel<D>);
+}
+
+const void *kernel_for(int D) {
+    switch (D) {
+        case 64: return kernel_ptr<64>();
+        case 128: return kernel_ptr<128>();
+        default: return kernel_ptr<256>();
+    }
+}
+
+// SMs and resident CTAs per SM for head_dim D with S sequences on `dev`.
+pkv_status launch_shape(int dev, int D, int S, int *grid, int *per_sm, int *sms, size_t *smem) {
+    if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_CUDA, "device index %d", dev);
+    const size_t bytes = smem_bytes(D, S);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo &di = g_dev[dev];
+    if (di.num_sms == 0) {
+        if (cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return fail(PKV_ERR_CUDA, "cudaDeviceGetAttribute failed");
+    }
+    const int di_ix = dim_index(D);
+    if (di.smem_for[di_ix] != bytes) {
+        cudaError_t e = cudaFuncSetAttribute(kernel_for(D), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)std::max<size_t>(bytes, 48 * 1024));
+        if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel_for(D), kThreads, bytes);
+        if (e != cudaSuccess || occ < 1)
+            return fail(PKV_ERR_CUDA, "occupancy query failed (%s, %d)", cudaGetErrorString(e), occ);
+        di.ctas_per_sm[di_ix] = std::min(occ, kMaxCtasPerSm);
+        di.smem_for[di_ix] = bytes;
+    }
+    *per_sm = di.ctas_per_sm[di_ix];
+    *sms = di.num_sms;
+    *grid = di.num_sms * di.ctas_per_sm[di_ix];
+    *smem = bytes;
+    return PKV_OK;
+}
+
+size_t counters_offset() { return kStatusBytes; }
+
+size_t pieces_offset(int S, int H) {
+    return counters_offset() + ((size_t)S * H * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+size_t workspace_bytes_for(int S, int H, int D, int num_sms) {
+    return pieces_offset(S, H) + (size_t)num_sms * kMaxCtasPerSm * 2 * piece_stride(D) * sizeof(float);
+}
+
+pkv_status encode_map(CUtensorMap *map, const void *base, int N, int B, int H, int D, int layout) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2], strides[1];
+    if (layout == PKV_LAYOUT_NHD) {
+        dims[0] = (cuuint64_t)H * D;
+        dims[1] = (cuuint64_t)N * B;
+        strides[0] = (cuuint64_t)H * D * 2;
+    } else {
+        dims[0] = (cuuint64_t)D;
+        dims[1] = (cuuint64_t)N * H * B;
+        strides[0] = (cuuint64_t)D * 2;
+    }
+    const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)std::min(B, kTile)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim) {
+    if (num_seqs < 0 || num_seqs > kMaxSeqs || num_heads < 1 || !supported_head_dim(head_dim)) {
+        fail(PKV_ERR_INVALID_ARG, "bad sizes for the workspace");
+        return 0;
+    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        fail(PKV_ERR_CUDA, "no CUDA device");
+        return 0;
+    }
+    return workspace_bytes_for(num_seqs, num_heads, head_dim, sms);
+}
+
+pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t *grid_ctas, int32_t *ctas_per_sm,
+                                  int32_t *num_sms) {
+    if (!supported_head_dim(head_dim) || num_seqs < 0 || num_seqs > kMaxSeqs)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(PKV_ERR_CUDA, "no CUDA device");
+    int g = 0, per = 0, sms = 0;
+    size_t smem = 0;
+    pkv_status st = launch_shape(dev, head_dim, num_seqs, &g, &per, &sms, &smem);
+    if (st != PKV_OK) return st;
+    if (grid_ctas) *grid_ctas = g;
+    if (ctas_per_sm) *ctas_per_sm = per;
+    if (num_sms) *num_sms = sms;
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *v_cache, int32_t num_blocks,
+                                int32_t block_size, int32_t num_heads, int32_t head_dim, int32_t layout,
+                                const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
+                                int32_t num_seqs, float scale, void *out, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    if (num_seqs < 0 || num_seqs > kMaxSeqs)
+        return fail(PKV_ERR_INVALID_ARG, "num_seqs %d outside [0, %d]", num_seqs, kMaxSeqs);
+    if (num_seqs == 0) return PKV_OK;
+    if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d", head_dim);
+    if (!supported_block_size(block_size)) return fail(PKV_ERR_UNSUPPORTED, "block_size %d", block_size);
+    if (layout != PKV_LAYOUT_NHD && layout != PKV_LAYOUT_HND) return fail(PKV_ERR_INVALID_ARG, "layout %d", layout);
+    if (num_heads < 1 || num_blocks < 1 || max_blocks < 1) return fail(PKV_ERR_INVALID_ARG, "sizes must be >= 1");
+    if ((int64_t)num_blocks * block_size * num_heads >= ((int64_t)1 << 31))
+        return fail(PKV_ERR_INVALID_ARG, "num_blocks * block_size * num_heads must be < 2^31");
+    const int64_t tiles_bound = (int64_t)num_seqs * num_heads * (((int64_t)max_blocks * block_size + kTile - 1) / kTile);
+    if (tiles_bound >= ((int64_t)1 << 31) - 1)
+        return fail(PKV_ERR_INVALID_ARG, "num_seqs * num_heads * max_context / 32 must be < 2^31");
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+        return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return fail(PKV_ERR_INVALID_ARG, "misaligned pointer (q, caches, out, workspace: 16 B; tables, lens: 4 B)");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(PKV_ERR_CUDA, "no CUDA device");
+    int grid = 0, per = 0, sms = 0;
+    size_t smem = 0;
+    pkv_status st = launch_shape(dev, head_dim, num_seqs, &grid, &per, &sms, &smem);
+    if (st != PKV_OK) return st;
+    const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, sms);
+    if (workspace_bytes < need)
+        return fail(PKV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+
+    CUtensorMap kmap, vmap;
+    st = encode_map(&kmap, k_cache, num_blocks, block_size, num_heads, head_dim, layout);
+    if (st != PKV_OK) return st;
+    st = encode_map(&vmap, v_cache, num_blocks, block_size, num_heads, head_dim, layout);
+    if (st != PKV_OK) return st;
+
+    Params prm;
+    prm.q = static_cast<const __half *>(q);
+    prm.out = static_cast<__half *>(out);
+    prm.tables = block_tables;
+    prm.lens = context_lens;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    prm.status = reinterpret_cast<uint32_t *>(ws);
+    prm.counters = reinterpret_cast<int32_t *>(ws + counters_offset());
+    prm.pieces = reinterpret_cast<float *>(ws + pieces_offset(num_seqs, num_heads));
+    prm.S = num_seqs;
+    prm.H = num_heads;
+    prm.max_blocks = max_blocks;
+    prm.B = block_size;
+    prm.N = num_blocks;
+    prm.layout = layout;
+    const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)head_dim);
+    prm.scale_log2 = (float)(sc * 1.4426950408889634);  // log2(e)
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (head_dim) {
+        case 64: decode_attention_kernel<64><<<grid, kThreads, smem, s>>>(kmap, vmap, prm); break;
+        case 128: decode_attention_kernel<128><<<grid, kThreads, smem, s>>>(kmap, vmap, prm); break;
+        default: decode_attention_kernel<256><<<grid, kThreads, smem, s>>>(kmap, vmap, prm); break;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "decode attention launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const void *q, const int32_t *block_tables,
+                                     int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs, float scale,
+                                     void *out, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    const pkv_pool_desc &d = pool->desc;
+    if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
+    if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+    const size_t off = (size_t)layer * layer_elems(d) * 2;
+    return pkv_decode_attention(q, static_cast<const char *>(pool->k_pool) + off,
+                                static_cast<const char *>(pool->v_pool) + off, d.num_blocks, d.block_size,
+                                d.num_heads, d.head_dim, d.layout, block_tables, max_blocks, context_lens, num_seqs,
+                                scale, out, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

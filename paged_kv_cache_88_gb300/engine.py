@@ -1,0 +1,208 @@
+"""Decode-step driver over libpkv: pool tensors, block tables and one decode step.
+
+One decode step over a batch (all through the C ABI):
+
+1. host, ``pkv_prepare_append``: one slot per sequence, new blocks at block
+   boundaries, copy-on-write pairs for shared blocks;
+2. the step's tables, lengths, slots and pairs go host -> device from pinned
+   double-buffered staging (the host can prepare step k+1 while step k runs);
+3. ``pkv_copy_blocks`` once for the step, across all layers;
+4. per layer: ``pkv_append`` of the new token's K/V, then
+   ``pkv_pool_decode_attention`` over the cache including it.
+
+The driver also replays a workload's set-up script (admissions, forks, dummy
+churn, multi-token writes). It holds no arithmetic of the method: slots,
+copies, tables and attention all come from the library.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+import workloads as wl
+
+from . import binding as bd
+
+
+class DecodeEngine:
+    def __init__(self, w: wl.Workload, device: str = "cuda", fill: str = "torch", max_new_per_step: int = 1):
+        self.w = w
+        self.device = torch.device(device)
+        shape = wl.pool_shape(w)
+        if fill == "numpy":
+            self.k_pool = torch.from_numpy(wl.pool_values(w, 0)).to(self.device)
+            self.v_pool = torch.from_numpy(wl.pool_values(w, 1)).to(self.device)
+        elif fill == "torch":
+            self.k_pool = wl.torch_normal_fp16(w.seed, (100,), shape, self.device)
+            self.v_pool = wl.torch_normal_fp16(w.seed, (101,), shape, self.device)
+        else:
+            raise ValueError(fill)
+        self.pool = bd.Pool(w.num_layers, w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.layout,
+                            self.k_pool, self.v_pool, w.free_order)
+        S, maxb = w.num_seqs, w.max_blocks
+        self.tables = np.full((S, maxb), -1, dtype=np.int32)
+        self.lens = np.zeros(S, dtype=np.int32)
+        self.dummies = {}
+        self.tables_d = torch.full((S, maxb), -1, dtype=torch.int32, device=self.device)
+        self.lens_d = torch.zeros(S, dtype=torch.int32, device=self.device)
+        self.status = torch.zeros(4, dtype=torch.int32, device=self.device)
+        self.workspace = bd.new_workspace(S, w.num_heads, w.head_dim, self.device)
+        self._cap_slots = S * max_new_per_step
+        self.slots_d = torch.zeros(max(self._cap_slots, 1), dtype=torch.int64, device=self.device)
+        self.pairs_d = torch.zeros((max(self._cap_slots, 1), 2), dtype=torch.int32, device=self.device)
+        # pinned, double-buffered host staging for the per-step H2D copies
+        self._stage = []
+        for _ in range(2):
+            self._stage.append({
+                "tables": torch.empty((S, maxb), dtype=torch.int32).pin_memory(),
+                "lens": torch.empty(S, dtype=torch.int32).pin_memory(),
+                "slots": torch.empty(max(self._cap_slots, 1), dtype=torch.int64).pin_memory(),
+                "pairs": torch.empty((max(self._cap_slots, 1), 2), dtype=torch.int32).pin_memory(),
+                "event": None,
+            })
+        self._buf = 0
+        self.last_pairs = np.zeros((0, 2), dtype=np.int32)
+        self.last_slots = np.zeros(0, dtype=np.int64)
+
+    # ------------------------------------------------------------------ set-up script
+    def run_script(self, values: str = "numpy", stream=None):
+        """Replay the workload's host operations; ``write`` ops append generated K/V through the kernels."""
+        w, B = self.w, self.w.block_size
+        for op_index, op in enumerate(w.script):
+            kind = op[0]
+            if kind == "admit":
+                _, s, T = op
+                nb = -(-T // B)
+                ids = self.pool.alloc(nb)
+                self.tables[s, :nb] = ids
+                self.lens[s] = T
+            elif kind == "fork":
+                _, src, dst = op
+                nb = -(-int(self.lens[src]) // B)
+                self.pool.incref(self.tables[src, :nb])
+                self.tables[dst] = self.tables[src]
+                self.lens[dst] = self.lens[src]
+            elif kind == "dummy_alloc":
+                _, d, n = op
+                self.dummies[d] = self.pool.alloc(n)
+            elif kind == "dummy_free":
+                _, d = op
+                self.pool.free(self.dummies.pop(d))
+            elif kind == "write":
+                counts = np.asarray(op[1], dtype=np.int32)
+                self.write_tokens(op_index, counts, values, stream)
+            else:
+                raise ValueError(kind)
+        self.upload_tables()
+
+    def write_tokens(self, op_index: int, counts: np.ndarray, values: str = "numpy", stream=None):
+        """Append counts[s] tokens to each sequence (a multi-token write through a3..a5)."""
+        w = self.w
+        total = int(counts.sum())
+        slots, pairs = self.pool.prepare_append(self.tables, self.lens, counts)
+        slots_d = torch.from_numpy(slots.copy()).to(self.device)
+        if len(pairs):
+            self.pool.copy_blocks(torch.from_numpy(pairs.copy()).to(self.device), status=self.status, stream=stream)
+        for layer in range(w.num_layers):
+            if values == "numpy":
+                kn = torch.from_numpy(wl.write_values(w, op_index, layer, 0, total)).to(self.device)
+                vn = torch.from_numpy(wl.write_values(w, op_index, layer, 1, total)).to(self.device)
+            else:
+                kn = wl.torch_normal_fp16(w.seed, (400, op_index, layer), (total, w.num_heads, w.head_dim), self.device)
+                vn = wl.torch_normal_fp16(w.seed, (401, op_index, layer), (total, w.num_heads, w.head_dim), self.device)
+            self.pool.append(layer, kn, vn, slots_d, status=self.status, stream=stream)
+        self.last_pairs, self.last_slots = pairs.copy(), slots.copy()
+        return slots, pairs
+
+    def upload_tables(self):
+        self.tables_d.copy_(torch.from_numpy(self.tables))
+        self.lens_d.copy_(torch.from_numpy(self.lens))
+
+    # ------------------------------------------------------------------ decode step
+    def prepare_step(self, stream=None):
+        """Host half of a decode step plus its H2D copies (enqueued on ``stream``)."""
+        st = self._stage[self._buf]
+        if st["event"] is not None:
+            st["event"].synchronize()       # staging buffer no longer read by an older step
+        slots, pairs = self.pool.prepare_append(self.tables, self.lens, None,
+                                                slot_out=st["slots"].numpy(), pair_out=st["pairs"].numpy())
+        st["tables"].numpy()[...] = self.tables
+        st["lens"].numpy()[...] = self.lens
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            self.tables_d.copy_(st["tables"], non_blocking=True)
+            self.lens_d.copy_(st["lens"], non_blocking=True)
+            self.slots_d[: len(slots)].copy_(st["slots"][: len(slots)], non_blocking=True)
+            if len(pairs):
+                self.pairs_d[: len(pairs)].copy_(st["pairs"][: len(pairs)], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s)
+        st["event"] = ev
+        self._buf ^= 1
+        self.last_pairs, self.last_slots = pairs.copy(), slots.copy()
+        return len(slots), len(pairs)
+
+    def device_step(self, q, k_new, v_new, out, n_slots: int, n_pairs: int, stream=None,
+                    attn_events: Optional[list] = None, scale: float = 0.0):
+        """Device half of a decode step: COW copies, then per layer append + attention.
+
+        q, k_new, v_new, out: contiguous fp16 [L, S, H, D] on the device.
+        ``attn_events`` (optional) gets (start, end) CUDA events around each
+        layer's attention launch. Arguments are marshalled once per step; each
+        launch is one C call.
+        """
+        w = self.w
+        L = bd.lib()
+        s = stream if stream is not None else torch.cuda.current_stream()
+        sp = s.cuda_stream
+        for t in (q, k_new, v_new, out):
+            if t.dtype != torch.float16 or not t.is_contiguous() or t.shape[0] != w.num_layers:
+                raise ValueError("step tensors must be contiguous fp16 [L, S, H, D]")
+        h = self.pool.handle
+        status = self.status.data_ptr()
+        if n_pairs:
+            bd.check(L.pkv_copy_blocks(h, self.pairs_d.data_ptr(), n_pairs, status, sp))
+        row = w.num_seqs * w.num_heads * w.head_dim * 2
+        qp, kp, vp, op = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), out.data_ptr()
+        tp, lp, slp = self.tables_d.data_ptr(), self.lens_d.data_ptr(), self.slots_d.data_ptr()
+        wsp, wsb = self.workspace.data_ptr(), self.workspace.numel()
+        maxb, S = w.max_blocks, w.num_seqs
+        sc = float(scale)
+        for layer in range(w.num_layers):
+            off = layer * row
+            bd.check(L.pkv_append(h, layer, kp + off, vp + off, slp, n_slots, status, sp))
+            if attn_events is not None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+            bd.check(L.pkv_pool_decode_attention(h, layer, qp + off, tp, maxb, lp, S, sc, op + off, wsp, wsb, sp))
+            if attn_events is not None:
+                e1.record(s)
+                attn_events.append((e0, e1))
+
+    def step(self, q, k_new, v_new, out, stream=None, attn_events=None, scale: float = 0.0):
+        n_slots, n_pairs = self.prepare_step(stream)
+        self.device_step(q, k_new, v_new, out, n_slots, n_pairs, stream, attn_events, scale)
+        return n_slots, n_pairs
+
+    # ------------------------------------------------------------------ inputs and checks
+    def step_inputs(self, step: int, values: str = "numpy"):
+        """q, k_new, v_new for every layer of ``step``: fp16 [L, S, H, D] on the device."""
+        w = self.w
+        if values == "numpy":
+            q = np.stack([wl.query_values(w, step, l) for l in range(w.num_layers)])
+            k = np.stack([wl.new_token_values(w, step, l, 0) for l in range(w.num_layers)])
+            v = np.stack([wl.new_token_values(w, step, l, 1) for l in range(w.num_layers)])
+            return tuple(torch.from_numpy(a).to(self.device) for a in (q, k, v))
+        shp = (w.num_layers, w.num_seqs, w.num_heads, w.head_dim)
+        return tuple(wl.torch_normal_fp16(w.seed, (tag, step), shp, self.device) for tag in (200, 300, 301))
+
+    def device_status(self) -> int:
+        a = int(self.status[0].item()) & 0xFFFFFFFF
+        b = bd.workspace_status(self.workspace)
+        return a | b
+
+    def kv_bytes_per_layer(self) -> int:
+        """Algorithmic K+V bytes one attention launch reads (current lengths)."""
+        return int(self.lens.astype(np.int64).sum()) * self.w.kv_bytes_per_token_layer

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, element by element.
+
+Bar: block tables, slots, COW pairs and every pool byte after append / copy are
+bit-exact; attention outputs satisfy |gpu - ref| <= 2e-3 + 1e-2 |ref| against the
+float64 oracle (fp16 K/V with fp32 accumulation, fp16 output).
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import paged_kv_cache_88_gb300 as pkv  # noqa: E402
+from paged_kv_cache_88_gb300.engine import DecodeEngine  # noqa: E402
+from oracle import ref_attn as rf  # noqa: E402
+from oracle import ref_attn_c as rc  # noqa: E402
+from oracle.driver import OracleEngine  # noqa: E402
+import workloads as wl  # noqa: E402
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def assert_close(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
+    gpu = gpu.astype(np.float64)
+    err = np.abs(gpu - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err - bound, -np.inf)), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst at {i}: "
+                             f"gpu {gpu[i]} ref {ref[i]} err {err[i]:.3e}")
+
+
+def u16(t):
+    return t.detach().cpu().numpy().view(np.uint16)
+
+
+def run_parity(w, steps: int):
+    eng = DecodeEngine(w, fill="numpy")
+    ora = OracleEngine(w, wl.pool_values(w, 0), wl.pool_values(w, 1))
+    eng.run_script(values="numpy")
+    ora.run_script()
+    torch.cuda.synchronize()
+    assert eng.tables.tolist() == ora.tables and eng.lens.tolist() == ora.lens
+    assert np.array_equal(u16(eng.k_pool), ora.k_pool.view(np.uint16))
+    assert np.array_equal(u16(eng.v_pool), ora.v_pool.view(np.uint16))
+    for step in range(steps):
+        q, k, v = ora.step_inputs(step)
+        qd, kd, vd = eng.step_inputs(step, "numpy")
+        out = torch.empty_like(qd)
+        eng.step(qd, kd, vd, out)
+        torch.cuda.synchronize()
+        ref = ora.step(q, k, v)
+        assert eng.last_slots.tolist() == ora.last_slots
+        assert [tuple(p) for p in eng.last_pairs.tolist()] == ora.last_pairs
+        assert eng.tables.tolist() == ora.tables and eng.lens.tolist() == ora.lens
+        assert np.array_equal(u16(eng.k_pool), ora.k_pool.view(np.uint16)), f"K pool differs after step {step}"
+        assert np.array_equal(u16(eng.v_pool), ora.v_pool.view(np.uint16)), f"V pool differs after step {step}"
+        assert_close(out.cpu().numpy(), ref, f"{w.name} step {step}")
+        assert eng.device_status() == 0
+    eng.pool.validate()
+    return eng, ora
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_tiny_config(layout):
+    w = wl.make_workload(1, layout=layout, decode_steps=3)
+    eng, _ = run_parity(w, 3)
+    # 64 -> 65 -> 66 -> 67 tokens: the block boundary at 64 took a fresh block
+    assert eng.lens.tolist() == [20, 36, 53, 67]
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_7b_shape_reduced(layout):
+    w = wl.make_workload(2, num_layers=2, num_seqs=8, len_scale=0.3, decode_steps=3, layout=layout)
+    run_parity(w, 3)
+
+
+def test_prefix_sharing_cow_reduced():
+    w = wl.make_workload(3, num_layers=2, num_seqs=8, len_scale=0.25, decode_steps=3)
+    eng, ora = run_parity(w, 3)
+    st = eng.pool.stats()
+    assert st["cow_copies"] == w.num_seqs - 1
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_13b_shape_churned_pool_reduced(layout):
+    w = wl.make_workload(4, num_layers=2, num_seqs=24, len_scale=0.5, decode_steps=2, layout=layout)
+    run_parity(w, 2)
+
+
+@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 256])
+def test_long_context_block_sweep_reduced(block_size):
+    w = wl.make_workload(5, num_layers=1, num_seqs=3, len_scale=0.12, decode_steps=2, block_size=block_size)
+    run_parity(w, 2)
+
+
+# ----------------------------------------------------------------------------- raw-call edge cases
+
+def _raw_case(lens, H=3, D=128, B=16, N=None, seed=0, layout="NHD", canary_nan=True):
+    rng = np.random.default_rng(seed)
+    S = len(lens)
+    nb = [-(-t // B) for t in lens]
+    N = N or sum(nb) + 5
+    perm = rng.permutation(N)
+    maxb = max(nb + [1])
+    tables = np.zeros((S, maxb), dtype=np.int32)
+    i = 0
+    for s in range(S):
+        for j in range(nb[s]):
+            tables[s, j] = perm[i]
+            i += 1
+    shape = (N, B, H, D) if layout == "NHD" else (N, H, B, D)
+    if canary_nan:
+        kp = np.full(shape, np.uint16(0x7E00), dtype=np.uint16).view(np.float16)   # NaN everywhere ...
+        vp = kp.copy()
+        for s, t in enumerate(lens):                                               # ... but valid tokens
+            for tok in range(t):
+                blk, off = tables[s, tok // B], tok % B
+                idx = (blk, off) if layout == "NHD" else (blk, slice(None), off)
+                kp[idx] = rng.standard_normal((H, D)).astype(np.float16)
+                vp[idx] = rng.standard_normal((H, D)).astype(np.float16)
+    else:
+        kp = rng.standard_normal(shape).astype(np.float16)
+        vp = rng.standard_normal(shape).astype(np.float16)
+    q = rng.standard_normal((S, H, D)).astype(np.float16)
+    return q, kp, vp, tables, np.asarray(lens, dtype=np.int32), B, N
+
+
+def _gpu_attn(q, kp, vp, tables, lens, B, N, layout="NHD", scale=0.0, ws=None):
+    dev = "cuda"
+    qd = torch.from_numpy(q).to(dev)
+    kd = torch.from_numpy(kp).to(dev)
+    vd = torch.from_numpy(vp).to(dev)
+    td = torch.from_numpy(tables).to(dev)
+    ld = torch.from_numpy(lens).to(dev)
+    if ws is None:
+        ws = pkv.new_workspace(q.shape[0], q.shape[1], q.shape[2], dev)
+    out = pkv.decode_attention(qd, kd, vd, td, ld, num_blocks=N, block_size=B, layout=layout, scale=scale,
+                               workspace=ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), pkv.workspace_status(ws), ws
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_edge_lengths_with_nan_canary(layout):
+    lens = [0, 1, 15, 16, 17, 31, 32, 33, 64, 100, 257]
+    q, kp, vp, tab, ln, B, N = _raw_case(lens, layout=layout)
+    out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N, layout)
+    assert st == 0
+    assert np.isfinite(out).all()
+    assert np.all(out[0] == 0)          # empty context
+    ref = rf.decode_attention(q, kp, vp, tab, ln, B, layout)
+    assert_close(out, ref, "edge lengths")
+    # T = 1: out is V[0] rounded to fp16
+    blk = tab[1, 0]
+    v0 = vp[blk, 0] if layout == "NHD" else vp[blk, :, 0]
+    assert np.array_equal(out[1].astype(np.float16).view(np.uint16), v0.view(np.uint16))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_head_dims(D):
+    q, kp, vp, tab, ln, B, N = _raw_case([5, 77, 300, 129], H=2, D=D, canary_nan=False, seed=D)
+    out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N)
+    assert st == 0
+    assert_close(out, rc.decode_attention(q, kp, vp, tab, ln, B), f"D={D}")
+
+
+def test_explicit_scale():
+    q, kp, vp, tab, ln, B, N = _raw_case([40, 90], H=2, canary_nan=False, seed=3)
+    out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N, scale=0.05)
+    assert st == 0
+    assert_close(out, rf.decode_attention(q, kp, vp, tab, ln, B, scale=0.05), "scale 0.05")
+
+
+def test_one_long_sequence_spans_every_cta():
+    """One (s, h) split over all CTAs of the launch: the fused combine merges hundreds of pieces."""
+    q, kp, vp, tab, ln, B, N = _raw_case([40000], H=1, B=256, canary_nan=False, seed=5)
+    out, st, ws = _gpu_attn(q, kp, vp, tab, ln, B, N)
+    assert st == 0
+    assert_close(out, rc.decode_attention(q, kp, vp, tab, ln, B), "long")
+    out2, st2, _ = _gpu_attn(q, kp, vp, tab, ln, B, N, ws=ws)   # counters were reset: same result
+    assert st2 == 0 and np.array_equal(out, out2)
+
+
+def test_many_short_sequences():
+    rng = np.random.default_rng(11)
+    lens = rng.integers(1, 70, size=700).tolist()
+    q, kp, vp, tab, ln, B, N = _raw_case(lens, H=4, D=64, B=8, canary_nan=False, seed=6)
+    out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N)
+    assert st == 0
+    assert_close(out, rc.decode_attention(q, kp, vp, tab, ln, B), "many short")
+
+
+def test_bad_block_id_is_flagged_not_faulted():
+    q, kp, vp, tab, ln, B, N = _raw_case([40, 20], H=2, canary_nan=False, seed=7)
+    tab[0, 1] = N + 5            # out of range: the kernel clamps it and flags it
+    out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N)
+    assert st & pkv.DEV_BAD_BLOCK
+    tab[0, 1] = -3
+    _, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N)
+    assert st & pkv.DEV_BAD_BLOCK
+    # the context is fine afterwards
+    q, kp, vp, tab, ln, B, N = _raw_case([40, 20], H=2, canary_nan=False, seed=7)
+    out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N)
+    assert st == 0
+    assert_close(out, rf.decode_attention(q, kp, vp, tab, ln, B), "after bad block")
+
+
+def test_bad_length_is_flagged():
+    q, kp, vp, tab, ln, B, N = _raw_case([40, 20], H=2, canary_nan=False, seed=8)
+    ln[1] = tab.shape[1] * B + 7
+    _, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N)
+    assert st & pkv.DEV_BAD_LENGTH
+
+
+def test_bad_slot_and_pair_are_flagged():
+    w = wl.make_workload(1)
+    eng = DecodeEngine(w, fill="numpy")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    k0 = eng.k_pool.clone()
+    kn = torch.zeros((2, w.num_heads, w.head_dim), dtype=torch.float16, device="cuda")
+    slots = torch.tensor([-1, w.num_blocks * w.block_size], dtype=torch.int64, device="cuda")
+    eng.pool.append(0, kn, kn, slots, status=status)
+    pairs = torch.tensor([[0, w.num_blocks]], dtype=torch.int32, device="cuda")
+    eng.pool.copy_blocks(pairs, status=status)
+    torch.cuda.synchronize()
+    st = int(status[0].item())
+    assert st & pkv.DEV_BAD_SLOT and st & pkv.DEV_BAD_PAIR
+    assert torch.equal(eng.k_pool, k0)          # nothing was written
+
+
+def test_host_argument_errors():
+    dev = "cuda"
+    q = torch.zeros((2, 2, 96), dtype=torch.float16, device=dev)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.decode_attention(q, q, q, torch.zeros((2, 1), dtype=torch.int32, device=dev),
+                             torch.zeros(2, dtype=torch.int32, device=dev), num_blocks=1, block_size=16,
+                             workspace=torch.zeros(1 << 20, dtype=torch.uint8, device=dev))
+    assert e.value.code in ("UNSUPPORTED", "INVALID_ARG")
+    q = torch.zeros((2, 2, 128), dtype=torch.float16, device=dev)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.decode_attention(q, q, q, torch.zeros((2, 1), dtype=torch.int32, device=dev),
+                             torch.zeros(2, dtype=torch.int32, device=dev), num_blocks=1, block_size=16,
+                             workspace=torch.zeros(64, dtype=torch.uint8, device=dev))
+    assert e.value.code == "INVALID_ARG" and "workspace" in pkv.last_error()
+
+
+# ----------------------------------------------------------------------------- full size
+
+def test_7b_full_size_bench_launch_sampled():
+    """The 7B-shape batch-32 workload at full size, 32 layers, in the benchmark's launch configuration.
+
+    The oracle allocator replays the same script (tables bit-exact); for two
+    layers the pre-step pools are read back and the float64 C oracle computes
+    every (sequence, head) of the step.
+    """
+    w = wl.make_workload(2)
+    eng = DecodeEngine(w, fill="torch")
+    eng.run_script()
+    from oracle import ref_alloc as ra
+    op = ra.RefPool(w.num_blocks, [int(x) for x in w.free_order])
+    tabs = [ra.admit(op, int(t), w.block_size, w.max_blocks) for t in w.context_lens]
+    lens = [int(t) for t in w.context_lens]
+    assert eng.tables.tolist() == tabs
+    qd, kd, vd = eng.step_inputs(0, "torch")
+    check_layers = [0, w.num_layers - 1]
+    before = {l: (eng.k_pool[l].cpu().numpy(), eng.v_pool[l].cpu().numpy()) for l in check_layers}
+    out = torch.empty_like(qd)
+    eng.step(qd, kd, vd, out)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+    slots, pairs = op.prepare_append(tabs, lens, [1] * w.num_seqs, w.block_size, w.max_blocks)
+    assert eng.last_slots.tolist() == slots and pairs == []
+    assert eng.tables.tolist() == tabs
+    tab = np.asarray(tabs, dtype=np.int32)
+    for l in check_layers:
+        kp, vp = before[l]
+        rf.append_kv(kp, vp, kd[l].cpu().numpy(), vd[l].cpu().numpy(), slots, w.block_size, w.layout)
+        assert np.array_equal(kp.view(np.uint16), u16(eng.k_pool[l]))
+        ref = rc.decode_attention(qd[l].cpu().numpy(), kp, vp, tab, np.asarray(lens, dtype=np.int32),
+                                  w.block_size, w.layout)
+        assert_close(out[l].cpu().numpy(), ref, f"7b full layer {l}")
