@@ -1,6 +1,7 @@
 """Build libpkv.so in-tree: nvcc for sm_103a, one -gencode, translation units in parallel.
 
-Usage: ``python -m paged_kv_cache_88_gb300.build`` (or ``build()`` from Python).
+Usage: ``python paged_kv_cache_88_gb300/build.py`` (or ``build()`` from Python; the
+package itself cannot be imported before the library exists).
 The library lands next to this file; nothing is installed.
 """
 from __future__ import annotations
