@@ -239,18 +239,20 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     __syncthreads();
 
     const int32_t total = sm.base[S];
-    const int32_t grid = gridDim.x;
     const int32_t cta = blockIdx.x;
 
     // Empty contexts: out = 0 (softmax over no tokens contributes nothing).
     if (warp < kConsumerWarps) {
-        for (int32_t i = cta; i < S * H; i += grid) {
+        for (int32_t i = cta; i < S * H; i += gridDim.x) {
             if (sm.len[i / H] != 0) continue;
             if (tid < D / 8)
                 reinterpret_cast<uint4 *>(p.out + (size_t)i * D)[tid] = make_uint4(0, 0, 0, 0);
         }
     }
-    if (total == 0) return;
+    // The tile list is split over min(CTAs, tiles) CTAs so that every working CTA
+    // owns at least one tile (the piece count of a split (s, h) relies on it).
+    const int32_t grid = min((int32_t)gridDim.x, total);
+    if (cta >= grid) return;
     const int32_t g0 = range_start(total, grid, cta);
     const int32_t g1 = range_start(total, grid, cta + 1);
     const int32_t n = g1 - g0;

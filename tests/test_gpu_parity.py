@@ -57,6 +57,7 @@ def run_parity(w, steps: int):
         eng.step(qd, kd, vd, out)
         torch.cuda.synchronize()
         ref = ora.step(q, k, v)
+        assert eng.device_status() == 0
         assert eng.last_slots.tolist() == ora.last_slots
         assert [tuple(p) for p in eng.last_pairs.tolist()] == ora.last_pairs
         assert eng.tables.tolist() == ora.tables and eng.lens.tolist() == ora.lens
