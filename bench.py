@@ -48,6 +48,7 @@ def parse_args():
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
     ap.add_argument("--layout", default="NHD", choices=["NHD", "HND"])
     ap.add_argument("--block-size", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling captures only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -135,7 +136,8 @@ class ClockSampler:
 
 def make_bench_workload(args, extra_steps: int):
     import workloads as wl
-    w = wl.make_workload(args.config, decode_steps=extra_steps, layout=args.layout, block_size=args.block_size)
+    w = wl.make_workload(args.config, decode_steps=extra_steps, layout=args.layout, block_size=args.block_size,
+                         num_layers=args.layers)
     return w
 
 
@@ -217,7 +219,7 @@ def run_ours(args):
     if world > 1:                         # weak scaling: each rank serves its own batch
         import workloads as wl
         w = wl.make_workload(args.config, decode_steps=total_steps, layout=args.layout,
-                             block_size=args.block_size, seed=1000 + args.config + 7919 * rank)
+                             block_size=args.block_size, num_layers=args.layers, seed=1000 + args.config + 7919 * rank)
     eng = DecodeEngine(w, device=str(dev), fill="torch")
     eng.run_script(values="torch")
     torch.cuda.synchronize()
