@@ -131,11 +131,12 @@ class Pool:
     """A block pool (host metadata in libpkv) over caller-owned K/V pool tensors.
 
     ``k_pool``/``v_pool``: CUDA fp16 tensors of L*N*B*H*D elements laid out as
-    [L, N, B, H, D] (NHD) or [L, N, H, B, D] (HND), or None for a host-only pool.
+    [L, N, H, B, D] (HND, the default) or [L, N, B, H, D] (NHD), or None for a
+    host-only pool.
     """
 
     def __init__(self, num_layers: int, num_blocks: int, block_size: int, num_heads: int, head_dim: int,
-                 layout: str = "NHD", k_pool=None, v_pool=None, initial_free_order: Optional[Sequence[int]] = None):
+                 layout: str = "HND", k_pool=None, v_pool=None, initial_free_order: Optional[Sequence[int]] = None):
         self.desc = PoolDesc(num_layers, num_blocks, block_size, num_heads, head_dim, LAYOUTS[layout])
         self.layout = layout
         self.k_pool, self.v_pool = k_pool, v_pool
@@ -276,7 +277,7 @@ def workspace_status(workspace) -> int:
 
 
 def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, num_blocks: int, block_size: int,
-                     layout: str = "NHD", scale: float = 0.0, out=None, workspace=None, stream=None):
+                     layout: str = "HND", scale: float = 0.0, out=None, workspace=None, stream=None):
     """Paged decode attention on one layer's caches (pkv_decode_attention); returns ``out``."""
     import torch
     _require(q, "float16", "q")

@@ -24,10 +24,13 @@
 //   coalesced load serves every head of the sequence). The query row of a new
 //   (s, h) rides along in the same stage as a 1-D bulk copy.
 // * Four consumer warps split each tile into 16 groups of 8 lanes; a group owns
-//   two tokens, a lane 8 or 16 elements of the head dim. q.K is an fp32 dot
-//   product finished with three xor-shuffles; each group keeps its own online
-//   softmax state (running max m, sum l, unnormalised o), so no block-wide
-//   synchronisation happens per tile.
+//   two rows (tokens) of the tile, a lane 8 x (D / 64) elements of the head dim.
+//   Rows are read from shared memory as 16-byte words, a group covering 128
+//   contiguous bytes per load (no bank conflicts). q.K accumulates fp16 x fp16
+//   products in fp32 (mixed-precision FMA; the products are exact) and finishes
+//   with three xor-shuffles; p.V runs as packed fp32 pair FMAs. Each group keeps
+//   its own online-softmax state (running max m, sum l, unnormalised o), so no
+//   block-wide synchronisation happens per tile.
 // * When an (s, h) ends inside the CTA, the 16 group states are merged through
 //   shared memory. A (s, h) that lies wholly in the CTA is written straight to
 //   out; one split across CTAs writes its piece (m, l, o) to the workspace and
@@ -50,12 +53,24 @@ namespace {
 
 using namespace pkv;
 
-constexpr int kTile = 32;            // tokens per pipeline stage
-constexpr int kConsumerWarps = 4;    // warps that compute
+#ifndef PKV_ATTN_TILE
+#define PKV_ATTN_TILE 32
+#endif
+#ifndef PKV_ATTN_WARPS
+#define PKV_ATTN_WARPS 4
+#endif
+#ifndef PKV_ATTN_STAGES
+#define PKV_ATTN_STAGES 3
+#endif
+
+constexpr int kTile = PKV_ATTN_TILE;              // tokens per pipeline stage
+constexpr int kConsumerWarps = PKV_ATTN_WARPS;    // warps that compute
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kGroups = kConsumerWarps * 4;      // 8-lane groups
-constexpr int kStages = 4;
+constexpr int kThreads = kConsumerThreads + 32;   // + one producer warp
+constexpr int kGroups = kConsumerWarps * 4;       // 8-lane groups
+constexpr int kTokPerGroup = kTile / kGroups;     // rows of a tile one group owns
+constexpr int kStages = PKV_ATTN_STAGES;
+static_assert(kTile % kGroups == 0 && kTokPerGroup >= 1 && kTokPerGroup <= 4, "tile / group split");
 constexpr int kMaxSeqs = 4096;
 constexpr int kMaxCtasPerSm = 8;     // bound used to size the workspace
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
@@ -83,7 +98,7 @@ __host__ __device__ constexpr int piece_stride(int D) { return D + 4; }
 // Shared memory: [stages][reduction][seq arrays][barriers + flags]
 __host__ size_t smem_bytes(int D, int S) {
     size_t b = (size_t)kStages * stage_bytes(D);
-    b += (size_t)kGroups * (D + 2) * sizeof(float);
+    b += (size_t)kConsumerWarps * (D + 2) * sizeof(float);
     b += (size_t)(2 * S + 2) * sizeof(int32_t);
     b = (b + 15) / 16 * 16;
     b += 2 * kStages * sizeof(uint64_t) + 16;
@@ -92,9 +107,9 @@ __host__ size_t smem_bytes(int D, int S) {
 
 struct Smem {
     unsigned char *stage;  // kStages * stage_bytes(D)
-    float *red_o;          // [kGroups][D]
-    float *red_m;          // [kGroups]
-    float *red_l;          // [kGroups]
+    float *red_o;          // [kConsumerWarps][D]
+    float *red_m;          // [kConsumerWarps]
+    float *red_l;          // [kConsumerWarps]
     int32_t *len;          // [S]
     int32_t *base;         // [S + 1] exclusive prefix of H * ntiles
     uint64_t *full;        // [kStages]
@@ -109,11 +124,11 @@ __device__ __forceinline__ Smem carve(unsigned char *raw, int S) {
     m.stage = reinterpret_cast<unsigned char *>(p);
     p += (size_t)kStages * stage_bytes(D);
     m.red_o = reinterpret_cast<float *>(p);
-    p += (size_t)kGroups * D * sizeof(float);
+    p += (size_t)kConsumerWarps * D * sizeof(float);
     m.red_m = reinterpret_cast<float *>(p);
-    p += kGroups * sizeof(float);
+    p += kConsumerWarps * sizeof(float);
     m.red_l = reinterpret_cast<float *>(p);
-    p += kGroups * sizeof(float);
+    p += kConsumerWarps * sizeof(float);
     m.len = reinterpret_cast<int32_t *>(p);
     p += (size_t)S * sizeof(int32_t);
     m.base = reinterpret_cast<int32_t *>(p);
@@ -201,15 +216,9 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     const int32_t S = p.S, H = p.H;
     const int32_t cap = p.max_blocks * p.B;
 
-    // ---- set-up: lengths, tile prefix over sequences, barriers
-    for (int32_t s = tid; s < S; s += kThreads) {
-        int32_t T = p.lens[s];
-        if (T < 0 || T > cap) {
-            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
-            T = T < 0 ? 0 : cap;
-        }
-        sm.len[s] = T;
-    }
+    // ---- set-up: barriers (before the grid dependency resolves), then lengths
+    // and the tile prefix over sequences
+    ptx::launch_dependents();
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sm.full[i]), 1);
@@ -218,6 +227,19 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         sm.flags[0] = 0;
         sm.flags[1] = 0;
         ptx::fence_barrier_init();
+    }
+    if (warp == kConsumerWarps && lane == 0) {
+        ptx::prefetch_tensormap(&kmap);
+        ptx::prefetch_tensormap(&vmap);
+    }
+    ptx::grid_dependency_wait();
+    for (int32_t s = tid; s < S; s += kThreads) {
+        int32_t T = p.lens[s];
+        if (T < 0 || T > cap) {
+            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            T = T < 0 ? 0 : cap;
+        }
+        sm.len[s] = T;
     }
     __syncthreads();
     if (warp == 0) {
@@ -264,10 +286,6 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
 
     if (warp == kConsumerWarps) {
         // ================= producer warp
-        if (lane == 0) {
-            ptx::prefetch_tensormap(&kmap);
-            ptx::prefetch_tensormap(&vmap);
-        }
         const int32_t B = p.B;
         const int32_t rows = B < kTile ? B : kTile;           // rows per TMA box
         const uint32_t box_bytes = (uint32_t)rows * D * 2;
@@ -326,88 +344,110 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     // ================= consumer warps
     const int grp = warp * 4 + (lane >> 3);  // 0..15
     const int j = lane & 7;
-    float qf[NCH * 8];
-    float o[NCH * 8];
-    float m = -INFINITY, l = 0.f;
+    // q of the current (s, h): this lane's 8 x NCH elements as fp16 halves
+    uint16_t qlo[NCH * 4], qhi[NCH * 4];
+    float2 o[NCH * 4];                        // unnormalised output, this lane's elements
+    float m = -INFINITY, l = 0.f;             // running max (log2 units) and sum
     Cursor c = locate(sm, S, H, g0);
-    int32_t seg_g0 = g0;  // first tile of the current (s, h) inside this CTA
+    int32_t seg_g0 = g0;                      // first tile of the current (s, h) inside this CTA
+    const uint32_t lane_off = (uint32_t)j * 16;  // byte offset of this lane's 16 B inside a 128 B chunk
 
     for (int32_t k = 0; k < n; ++k) {
         const int32_t stage = k % kStages;
-        const unsigned char *st = sm.stage + stage * SB;
+        const uint32_t kb = stage0 + stage * SB;             // K tile (shared address)
+        const uint32_t vb = kb + kTile * D * 2;              // V tile
         wait_phase(sm, full0 + 8 * stage, (k / kStages) & 1, p.status);
         const bool first = (k == 0) || (c.t == 0);
-        const int32_t T = sm.len[c.s];
-        const int32_t ntok = min(kTile, T - c.t * kTile);
+        const int32_t ntok = min(kTile, sm.len[c.s] - c.t * kTile);
         if (first) {
-            const __half *qs = reinterpret_cast<const __half *>(st + 2 * kTile * D * 2);
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(qs + ch * 64 + j * 8);
-                const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+                const uint4 raw = ptx::lds128(vb + kTile * D * 2 + ch * 128 + lane_off);
+                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(h2[e]);
-                    qf[ch * 8 + 2 * e] = f.x * p.scale_log2;
-                    qf[ch * 8 + 2 * e + 1] = f.y * p.scale_log2;
-                }
+                for (int e = 0; e < 4; ++e) ptx::split_half2(wv[e], qlo[ch * 4 + e], qhi[ch * 4 + e]);
             }
 #pragma unroll
-            for (int e = 0; e < NCH * 8; ++e) o[e] = 0.f;
+            for (int e = 0; e < NCH * 4; ++e) o[e] = make_float2(0.f, 0.f);
             m = -INFINITY;
             l = 0.f;
             seg_g0 = g0 + k;
         }
-        const __half *ks = reinterpret_cast<const __half *>(st);
-        const __half *vs = reinterpret_cast<const __half *>(st + kTile * D * 2);
-        float x[2];
-        bool valid[2];
+        // this group's rows of the tile: grp, grp + kGroups, ...
+        const bool full = ntok == kTile;
+        bool vld[kTokPerGroup];
+        uint4 kr[kTokPerGroup][NCH], vr[kTokPerGroup][NCH];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int tok = grp + 16 * u;
-            valid[u] = tok < ntok;
-            float dot = 0.f;
-            if (valid[u]) {
+        for (int u = 0; u < kTokPerGroup; ++u) {
+            vld[u] = full || grp + kGroups * u < ntok;
 #pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(ks + tok * D + ch * 64 + j * 8);
-                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+            for (int ch = 0; ch < NCH; ++ch)
+                kr[u][ch] = ptx::lds128(kb + (grp + kGroups * u) * D * 2 + ch * 128 + lane_off);
+        }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(h2[e]);
-                        dot = fmaf(qf[ch * 8 + 2 * e], f.x, dot);
-                        dot = fmaf(qf[ch * 8 + 2 * e + 1], f.y, dot);
-                    }
+        for (int u = 0; u < kTokPerGroup; ++u)
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+                vr[u][ch] = ptx::lds128(vb + (grp + kGroups * u) * D * 2 + ch * 128 + lane_off);
+        float x[kTokPerGroup];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kTokPerGroup; ++u) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                const uint32_t wk[4] = {kr[u][ch].x, kr[u][ch].y, kr[u][ch].z, kr[u][ch].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint16_t klo, khi;
+                    ptx::split_half2(wk[e], klo, khi);
+                    a0 = ptx::fma_f16_f32(qlo[ch * 4 + e], klo, a0);
+                    a1 = ptx::fma_f16_f32(qhi[ch * 4 + e], khi, a1);
                 }
             }
+            float dot = a0 + a1;
             dot += __shfl_xor_sync(0xffffffffu, dot, 4);
             dot += __shfl_xor_sync(0xffffffffu, dot, 2);
             dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-            x[u] = valid[u] ? dot : -INFINITY;
+            x[u] = vld[u] ? dot * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, x[u]);
         }
-        const float mx = fmaxf(x[0], x[1]);
-        if (mx > m) {
+        if (mx > m) {                          // new running max: rescale (group-uniform branch)
             const float alpha = ptx::ex2(m - mx);
 #pragma unroll
-            for (int e = 0; e < NCH * 8; ++e) o[e] *= alpha;
+            for (int e = 0; e < NCH * 4; ++e) o[e] = make_float2(o[e].x * alpha, o[e].y * alpha);
             l *= alpha;
             m = mx;
         }
+        // rows past the context may hold any bits (NaN included): weight 0 and V skipped
+        float pw[kTokPerGroup];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (!valid[u]) continue;
-            const int tok = grp + 16 * u;
-            const float pw = ptx::ex2(x[u] - m);
-            l += pw;
+        for (int u = 0; u < kTokPerGroup; ++u) {
+            pw[u] = vld[u] ? ptx::ex2(x[u] - m) : 0.f;
+            l += pw[u];
+        }
+        if (full) {
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(vs + tok * D + ch * 64 + j * 8);
-                const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+            for (int u = 0; u < kTokPerGroup; ++u)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(h2[e]);
-                    o[ch * 8 + 2 * e] = fmaf(pw, f.x, o[ch * 8 + 2 * e]);
-                    o[ch * 8 + 2 * e + 1] = fmaf(pw, f.y, o[ch * 8 + 2 * e + 1]);
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const uint32_t wv[4] = {vr[u][ch].x, vr[u][ch].y, vr[u][ch].z, vr[u][ch].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(wv[e]),
+                                                   o[ch * 4 + e]);
+                }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kTokPerGroup; ++u) {
+                if (!vld[u]) continue;
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const uint32_t wv[4] = {vr[u][ch].x, vr[u][ch].y, vr[u][ch].z, vr[u][ch].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(wv[e]),
+                                                   o[ch * 4 + e]);
                 }
             }
         }
@@ -416,23 +456,43 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
 
         const bool last = (k == n - 1) || (c.t == c.nt - 1);
         if (last) {
-            // ---- merge the 16 group states of this (s, h)
+            // ---- merge the group states of this (s, h): the 4 groups of a warp
+            // by xor-shuffles, then the warps through shared memory
+            float mw = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
+            const float sc = mw == -INFINITY ? 0.f : ptx::ex2(m - mw);   // a warp with no row at all: 0
+            float lw = l * sc;
+            lw += __shfl_xor_sync(0xffffffffu, lw, 8);
+            lw += __shfl_xor_sync(0xffffffffu, lw, 16);
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch)
+            for (int e = 0; e < NCH * 4; ++e) {
+                float2 v = make_float2(o[e].x * sc, o[e].y * sc);
+                v.x += __shfl_xor_sync(0xffffffffu, v.x, 8);
+                v.y += __shfl_xor_sync(0xffffffffu, v.y, 8);
+                v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
+                v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
+                o[e] = v;
+            }
+            if (lane < 8) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sm.red_o[grp * D + ch * 64 + j * 8 + e] = o[ch * 8 + e];
-            if (j == 0) {
-                sm.red_m[grp] = m;
-                sm.red_l[grp] = l;
+                for (int ch = 0; ch < NCH; ++ch) {
+                    float4 *dst = reinterpret_cast<float4 *>(sm.red_o + warp * D + ch * 64 + j * 8);
+                    dst[0] = make_float4(o[ch * 4 + 0].x, o[ch * 4 + 0].y, o[ch * 4 + 1].x, o[ch * 4 + 1].y);
+                    dst[1] = make_float4(o[ch * 4 + 2].x, o[ch * 4 + 2].y, o[ch * 4 + 3].x, o[ch * 4 + 3].y);
+                }
+                if (lane == 0) {
+                    sm.red_m[warp] = mw;
+                    sm.red_l[warp] = lw;
+                }
             }
             ptx::named_barrier(1, kConsumerThreads);
             float M = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < kGroups; ++i) M = fmaxf(M, sm.red_m[i]);
-            float w[kGroups];
+            for (int i = 0; i < kConsumerWarps; ++i) M = fmaxf(M, sm.red_m[i]);
+            float w[kConsumerWarps];
             float L = 0.f;
 #pragma unroll
-            for (int i = 0; i < kGroups; ++i) {
+            for (int i = 0; i < kConsumerWarps; ++i) {
                 w[i] = ptx::ex2(sm.red_m[i] - M);
                 L = fmaf(w[i], sm.red_l[i], L);
             }
@@ -444,7 +504,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 float acc = 0.f;
                 if (d < D) {
 #pragma unroll
-                    for (int i = 0; i < kGroups; ++i) acc = fmaf(w[i], sm.red_o[i * D + d], acc);
+                    for (int i = 0; i < kConsumerWarps; ++i) acc = fmaf(w[i], sm.red_o[i * D + d], acc);
                 }
                 O[r] = acc;
             }
@@ -472,15 +532,17 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                     piece[D] = M;
                     piece[D + 1] = L;
                 }
-                __threadfence();
+                // piece stores -> barrier -> one fence + counter bump (release); the
+                // last arriver fences again before reading the pieces (acquire)
                 ptx::named_barrier(1, kConsumerThreads);
                 if (tid == 0) {
+                    __threadfence();
                     const int32_t prev = atomicAdd(p.counters + (size_t)c.s * H + c.h, 1);
+                    __threadfence();
                     sm.flags[1] = (prev == cb - ca) ? 1 : 0;
                 }
                 ptx::named_barrier(1, kConsumerThreads);
                 if (sm.flags[1]) {
-                    __threadfence();
                     const int32_t start_a = range_start(total, grid, ca);
                     float Mg = -INFINITY;
                     for (int32_t cc = ca; cc <= cb; ++cc) {
@@ -718,12 +780,13 @@ pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *
     prm.scale_log2 = (float)(sc * 1.4426950408889634);  // log2(e)
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
     switch (head_dim) {
-        case 64: decode_attention_kernel<64><<<grid, kThreads, smem, s>>>(kmap, vmap, prm); break;
-        case 128: decode_attention_kernel<128><<<grid, kThreads, smem, s>>>(kmap, vmap, prm); break;
-        default: decode_attention_kernel<256><<<grid, kThreads, smem, s>>>(kmap, vmap, prm); break;
+        case 64: e = launch_pdl(decode_attention_kernel<64>, grid, kThreads, smem, s, kmap, vmap, prm); break;
+        case 128: e = launch_pdl(decode_attention_kernel<128>, grid, kThreads, smem, s, kmap, vmap, prm); break;
+        default: e = launch_pdl(decode_attention_kernel<256>, grid, kThreads, smem, s, kmap, vmap, prm); break;
     }
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "decode attention launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }

@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include "pkv_internal.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -25,6 +26,8 @@ __global__ void __launch_bounds__(kAppendThreads)
 append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, const int64_t *__restrict__ slots,
               int32_t num_tokens, uint4 *__restrict__ k_layer, uint4 *__restrict__ v_layer, int64_t num_slots,
               int32_t B, int32_t H, int32_t words_per_row, int32_t layout, uint32_t *status) {
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
     const int64_t words_per_token = (int64_t)H * words_per_row;
     const int64_t total = (int64_t)num_tokens * words_per_token;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -52,6 +55,8 @@ append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, 
 __global__ void __launch_bounds__(kCopyThreads)
 copy_blocks_kernel(const int32_t *__restrict__ pairs, int32_t num_pairs, uint4 *k_pool, uint4 *v_pool,
                    int32_t num_layers, int32_t num_blocks, int64_t block_words, uint32_t *status) {
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
     const int64_t jobs = (int64_t)num_pairs * num_layers;
     for (int64_t y = blockIdx.y; y < jobs; y += gridDim.y) {
         const int32_t pr = (int32_t)(y / num_layers);
@@ -109,12 +114,12 @@ pkv_status pkv_append(const pkv_pool *pool, int32_t layer, const void *k_new, co
     const int64_t want = (total + kAppendThreads - 1) / kAppendThreads;
     const int grid = (int)(want < 65535 * 16 ? want : 65535 * 16);
     const size_t off = (size_t)layer * layer_elems(d) * 2;
-    append_kernel<<<grid, kAppendThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
-        reinterpret_cast<uint4 *>(static_cast<char *>(pool->k_pool) + off),
-        reinterpret_cast<uint4 *>(static_cast<char *>(pool->v_pool) + off), (int64_t)d.num_blocks * d.block_size,
-        d.block_size, d.num_heads, wpr, d.layout, status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(append_kernel, dim3(grid), dim3(kAppendThreads), 0, static_cast<cudaStream_t>(stream),
+                               static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
+                               num_tokens, reinterpret_cast<uint4 *>(static_cast<char *>(pool->k_pool) + off),
+                               reinterpret_cast<uint4 *>(static_cast<char *>(pool->v_pool) + off),
+                               (int64_t)d.num_blocks * d.block_size, d.block_size, d.num_heads, wpr, d.layout, status);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }
@@ -133,10 +138,11 @@ pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *pairs, int32_t n
     if (gx < 1) gx = 1;
     const int64_t jobs = (int64_t)num_pairs * d.num_layers;
     const int gy = (int)(jobs < 65535 ? jobs : 65535);
-    copy_blocks_kernel<<<dim3(gx, gy), kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        pairs, num_pairs, static_cast<uint4 *>(pool->k_pool), static_cast<uint4 *>(pool->v_pool), d.num_layers,
-        d.num_blocks, block_words, status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(copy_blocks_kernel, dim3(gx, gy), dim3(kCopyThreads), 0,
+                               static_cast<cudaStream_t>(stream), pairs, num_pairs,
+                               static_cast<uint4 *>(pool->k_pool), static_cast<uint4 *>(pool->v_pool), d.num_layers,
+                               d.num_blocks, block_words, status);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "copy launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }

@@ -2,7 +2,12 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <vector>
+
+#ifdef __CUDACC__
+#include <cuda_runtime.h>
+#endif
 
 #include "pkv.h"
 
@@ -34,5 +39,27 @@ inline bool supported_head_dim(int32_t d) { return d == 64 || d == 128 || d == 2
 inline bool supported_block_size(int32_t b) {
     return b == 8 || b == 16 || b == 32 || b == 64 || b == 128 || b == 256;
 }
+
+// Launch `kernel` on `stream` with programmatic stream serialisation: its CTAs
+// may start while the previous kernel of the stream drains; every kernel of
+// libpkv calls griddepcontrol.wait before its first global-memory access, so
+// stream order of memory effects is unchanged.
+#ifdef __CUDACC__
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#endif
 
 }  // namespace pkv

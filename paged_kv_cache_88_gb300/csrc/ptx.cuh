@@ -2,7 +2,10 @@
 // bulk) loads into shared memory, named barriers and the global timer.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include <cstdint>
+#include <cstring>
 
 namespace pkv {
 namespace ptx {
@@ -75,13 +78,55 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// 16-byte shared-memory load by 32-bit shared address. Volatile (with a
+// "memory" clobber) so it is never hoisted above the mbarrier wait that
+// publishes the data.
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
+
+// The two fp16 halves of a 32-bit word (low half = element 0).
+__device__ __forceinline__ void split_half2(uint32_t w, uint16_t &lo, uint16_t &hi) {
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
+}
+
+// a * b + c with fp16 a, b and fp32 c: the product of two fp16 values is exact
+// in fp32, so this is an fp32 accumulation of fp16 products (one rounding).
+__device__ __forceinline__ float fma_f16_f32(uint16_t a, uint16_t b, float c) {
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+
+// Packed fp32 pair FMA: d = a * b + c element-wise, round to nearest even.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t w) {
+    __half2 h;
+    memcpy(&h, &w, 4);
+    return __half22float2(h);
+}
+
+// Programmatic dependent launch. launch_dependents lets the next kernel of the
+// stream start launching its CTAs; grid_dependency_wait blocks until every
+// prerequisite grid has completed and its memory is visible (a no-op when the
+// kernel was launched without the programmatic-serialization attribute).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // 2^x with the SFU (max relative error about 2^-22); 2^-inf = +0.
 __device__ __forceinline__ float ex2(float x) {

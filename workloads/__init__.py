@@ -63,7 +63,7 @@ class Workload:
     script: list
     decode_steps: int
     seed: int
-    layout: str = "NHD"
+    layout: str = "HND"
     description: str = ""
 
     @property
@@ -101,7 +101,7 @@ def _finish(index, name, L, H, D, B, lens, script, steps, seed, N, layout, desc,
 
 def make_workload(index: int, *, num_layers: Optional[int] = None, num_seqs: Optional[int] = None,
                   block_size: Optional[int] = None, decode_steps: Optional[int] = None,
-                  layout: str = "NHD", seed: Optional[int] = None,
+                  layout: str = "HND", seed: Optional[int] = None,
                   len_scale: float = 1.0) -> Workload:
     """The seeded workload ``index`` (1..5); keyword overrides shrink it for tests.
 
