@@ -42,7 +42,7 @@ KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_88_gb300", "csrc", "decode_atten
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
@@ -214,7 +214,7 @@ def run_ours(args):
     import paged_kv_cache_88_gb300 as pkv
 
     e2e_steps = 0 if args.no_e2e else args.steps
-    total_steps = 2 * args.warmup + args.steps + max(2, args.steps // 4) + e2e_steps + 2
+    total_steps = 3 * args.warmup + args.steps + e2e_steps + 4
     w = make_bench_workload(args, total_steps)
     if world > 1:                         # weak scaling: each rank serves its own batch
         import workloads as wl
@@ -234,9 +234,13 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- warm-up
+    # ---- warm-up (eager), then the step is captured once as a CUDA graph
     for _ in range(args.warmup):
         eng.step(q, kn, vn, out, stream)
+    barrier()
+    eng.capture(q, kn, vn, out)
+    for _ in range(args.warmup):
+        eng.step_graph(stream)
     barrier()
     if eng.device_status() != 0:
         raise RuntimeError(f"device status {eng.device_status():#x} after warm-up")
@@ -249,26 +253,29 @@ def run_ours(args):
         t_end = torch.cuda.Event(enable_timing=True)
         barrier()
         t_start.record(stream)
+        h0 = time.perf_counter()
         for _ in range(args.steps):
-            n_slots, n_pairs = eng.prepare_step(stream)
+            n_slots, n_pairs = eng.step_graph(stream)
             step_bytes.append(eng.kv_bytes_per_layer())
-            eng.device_step(q, kn, vn, out, n_slots, n_pairs, stream)
             launches += 2 * L + (1 if n_pairs else 0)
+        host_ms = (time.perf_counter() - h0) * 1e3 / args.steps
         t_end.record(stream)
         barrier()
-        # roofline pass: the same steps again with CUDA events around every
-        # attention launch (events between kernels stop launch overlap, so this
-        # pass is kept out of the step time above)
-        attn_ev = []
-        attn_bytes = []
-        for _ in range(max(2, args.steps // 4)):
-            n_slots, n_pairs = eng.prepare_step(stream)
-            attn_bytes.append(eng.kv_bytes_per_layer())
-            eng.device_step(q, kn, vn, out, n_slots, n_pairs, stream, attn_events=attn_ev)
+        # roofline pass: the dominant kernel alone, back to back over the
+        # step's layers (same launches as in a step, without the appends), CUDA
+        # events on the launching stream at both ends
+        n_attn = max(2, args.steps // 2) * L
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for i in range(n_attn):
+            eng.attention(i % L, q, out, stream)
+        a1.record(stream)
         barrier()
     clocks = clk.summary()
     ms = t_start.elapsed_time(t_end)
-    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    attn_ms_total = a0.elapsed_time(a1)
+    attn_launch_bytes = eng.kv_bytes_per_layer()
     status = eng.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status:#x} in the timed region")
@@ -288,11 +295,9 @@ def run_ours(args):
     seq_steps = seqsteps_job / (ms_job / 1e3)
 
     # roofline of the dominant kernel (decode attention): algorithmic bytes / average launch time
-    per_launch_bytes = []
-    for b in attn_bytes:
-        per_launch_bytes += [b] * L
     extra = 2 * S * H * D * 2 + S * 4 + int(np.sum(-(-eng.lens // w.block_size))) * 4
-    achieved = (sum(per_launch_bytes) + extra * len(per_launch_bytes)) / (sum(attn_ms) / 1e3) / 1e9
+    mean_launch_ms = attn_ms_total / n_attn
+    achieved = (attn_launch_bytes + extra) / (mean_launch_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
     traffic = kernel_traffic()
 
@@ -303,17 +308,16 @@ def run_ours(args):
         hk = kn.cpu().pin_memory()
         hv = vn.cpu().pin_memory()
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        qd, kd, vd = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
         e_bytes = 0
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
-            qd.copy_(hq, non_blocking=True)
-            kd.copy_(hk, non_blocking=True)
-            vd.copy_(hv, non_blocking=True)
-            eng.step(qd, kd, vd, out, stream)
+            q.copy_(hq, non_blocking=True)
+            kn.copy_(hk, non_blocking=True)
+            vn.copy_(hv, non_blocking=True)
+            eng.step_graph(stream)
             e_bytes += eng.kv_bytes_per_layer() * L
             hout.copy_(out, non_blocking=True)
         e1.record(stream)
@@ -334,7 +338,8 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_job / args.steps, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": ms_job / args.steps, "host_ms_per_step": host_ms,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic",
             "config": dict(w.describe(), l2="inputs larger than L2 (each layer's KV >> 129 MB), no flush",
                            parallelism="replicas" if world > 1 else "single"),
@@ -342,8 +347,8 @@ def run_ours(args):
             "frac_of_hbm_peak": value / peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                         "kernel": "decode_attention_kernel<128>", "launches": len(attn_ms),
-                         "mean_launch_us": 1e3 * sum(attn_ms) / max(len(attn_ms), 1),
+                         "kernel": "decode_attention_kernel<128>", "launches": n_attn,
+                         "mean_launch_us": 1e3 * mean_launch_ms, "bytes_per_launch": attn_launch_bytes + extra,
                          "grid_ctas": info["grid_ctas"], "ctas_per_sm": info["ctas_per_sm"]},
             "clocks": clocks,
             "gpu_launches": launches,

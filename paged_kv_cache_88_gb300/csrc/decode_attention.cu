@@ -60,7 +60,10 @@ using namespace pkv;
 #define PKV_ATTN_WARPS 4
 #endif
 #ifndef PKV_ATTN_STAGES
-#define PKV_ATTN_STAGES 3
+#define PKV_ATTN_STAGES 2
+#endif
+#ifndef PKV_ATTN_MIN_CTAS
+#define PKV_ATTN_MIN_CTAS 4
 #endif
 
 constexpr int kTile = PKV_ATTN_TILE;              // tokens per pipeline stage
@@ -203,7 +206,7 @@ __device__ __forceinline__ bool wait_phase(const Smem &sm, uint32_t bar, uint32_
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, D >= 256 ? 1 : PKV_ATTN_MIN_CTAS)
 decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const Params p) {
     constexpr int NCH = D / 64;  // 16-byte chunks per lane per row

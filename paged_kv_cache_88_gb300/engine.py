@@ -181,6 +181,52 @@ class DecodeEngine:
                 e1.record(s)
                 attn_events.append((e0, e1))
 
+    def capture(self, q, k_new, v_new, out, scale: float = 0.0):
+        """Capture the device half of a decode step without COW copies into a CUDA graph.
+
+        The graph holds, per layer, the append and the attention launches on the
+        fixed device buffers (tables, lengths, slots, q, k_new, v_new, out);
+        :meth:`step_graph` refreshes those buffers and replays it.
+        """
+        w = self.w
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            # first launches (attribute and occupancy queries) happen outside capture
+            self.device_step(q, k_new, v_new, out, w.num_seqs, 0, side, scale=scale)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            self.device_step(q, k_new, v_new, out, w.num_seqs, 0, None, scale=scale)
+        torch.cuda.synchronize()
+        self._graph = g
+        self._graph_tensors = (q, k_new, v_new, out)
+        return g
+
+    def step_graph(self, stream=None):
+        """A decode step replaying the captured graph (COW copies, if any, run first)."""
+        n_slots, n_pairs = self.prepare_step(stream)
+        if n_slots != self.w.num_seqs:
+            raise RuntimeError("the captured step appends one token per sequence")
+        s = stream if stream is not None else torch.cuda.current_stream()
+        if n_pairs:
+            bd.check(bd.lib().pkv_copy_blocks(self.pool.handle, self.pairs_d.data_ptr(), n_pairs,
+                                              self.status.data_ptr(), s.cuda_stream))
+        with torch.cuda.stream(s):
+            self._graph.replay()
+        return n_slots, n_pairs
+
+    def attention(self, layer: int, q, out, stream=None, scale: float = 0.0):
+        """One layer's decode attention over the current tables (q, out: fp16 [L, S, H, D])."""
+        w = self.w
+        s = stream if stream is not None else torch.cuda.current_stream()
+        off = layer * w.num_seqs * w.num_heads * w.head_dim * 2
+        bd.check(bd.lib().pkv_pool_decode_attention(
+            self.pool.handle, layer, q.data_ptr() + off, self.tables_d.data_ptr(), w.max_blocks,
+            self.lens_d.data_ptr(), w.num_seqs, float(scale), out.data_ptr() + off, self.workspace.data_ptr(),
+            self.workspace.numel(), s.cuda_stream))
+
     def step(self, q, k_new, v_new, out, stream=None, attn_events=None, scale: float = 0.0):
         n_slots, n_pairs = self.prepare_step(stream)
         self.device_step(q, k_new, v_new, out, n_slots, n_pairs, stream, attn_events, scale)
