@@ -218,6 +218,24 @@ pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *
                                 float scale, void *out, void *workspace, size_t workspace_bytes,
                                 void *stream);
 
+/* The decode step of one layer in one launch: exactly pkv_append(pool, layer,
+ * k_new, v_new, slot_mapping, num_seqs) followed by pkv_pool_decode_attention
+ * over the same layer, for ONE new token per sequence (m.lqnn.cn/news/240480
+ * §3.2 step 3 then §3.3). Token s is sequence s's newest token: slot_mapping[s]
+ * must be the slot of position context_lens[s] - 1 (what pkv_prepare_append
+ * returns), and context_lens already counts it. The CTA that reads the tile
+ * holding that position stores the token's K/V row (all heads handled by their
+ * own CTAs) right before loading the tile, so no separate append launch runs.
+ * slot_mapping[s] < 0: nothing is stored for s (the pool row is used as it is);
+ * >= N * B: skipped and flagged PKV_DEV_BAD_SLOT.
+ * k_new, v_new: device fp16 [num_seqs][H][D], 16-byte aligned; other arguments
+ * as pkv_pool_decode_attention. */
+pkv_status pkv_decode_append_attention(const pkv_pool *pool, int32_t layer, const void *q, const void *k_new,
+                                       const void *v_new, const int64_t *slot_mapping,
+                                       const int32_t *block_tables, int32_t max_blocks,
+                                       const int32_t *context_lens, int32_t num_seqs, float scale, void *out,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of workspace pkv_decode_attention needs for these sizes on the
  * current CUDA device (0 and a pkv_last_error message on bad arguments). */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim);

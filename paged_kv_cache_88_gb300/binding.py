@@ -27,7 +27,7 @@ EXPORTED = [
     "pkv_last_error", "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_info", "pkv_alloc",
     "pkv_incref", "pkv_free", "pkv_refcount", "pkv_get_stats", "pkv_free_queue", "pkv_validate",
     "pkv_prepare_append", "pkv_append", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_workspace_bytes",
-    "pkv_pool_decode_attention", "pkv_decode_launch_info",
+    "pkv_pool_decode_attention", "pkv_decode_launch_info", "pkv_decode_append_attention",
 ]
 
 
@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
             "pkv_pool_decode_attention": (i32, [vp, i32, vp, vp, i32, vp, i32, f32, vp, vp, sz, vp]),
             "pkv_decode_launch_info": (i32, [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                              ctypes.POINTER(i32)]),
+            "pkv_decode_append_attention": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, f32, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -251,6 +252,18 @@ class Pool:
         check(lib().pkv_pool_decode_attention(self._h, layer, _ptr(q), _ptr(block_tables), block_tables.shape[1],
                                               _ptr(context_lens), S, float(scale), _ptr(out), _ptr(workspace),
                                               workspace.numel() * workspace.element_size(), _stream(stream)))
+
+    def decode_append_attention(self, layer: int, q, k_new, v_new, slot_mapping, block_tables, context_lens, out,
+                                workspace, scale: float = 0.0, stream=None) -> None:
+        """Append one token per sequence and attend, in one launch (pkv_decode_append_attention)."""
+        for t, dt, name in ((q, "float16", "q"), (k_new, "float16", "k_new"), (v_new, "float16", "v_new"),
+                            (out, "float16", "out"), (slot_mapping, "int64", "slot_mapping"),
+                            (block_tables, "int32", "block_tables"), (context_lens, "int32", "context_lens")):
+            _require(t, dt, name)
+        check(lib().pkv_decode_append_attention(
+            self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(block_tables),
+            block_tables.shape[1], _ptr(context_lens), q.shape[0], float(scale), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream)))
 
     def layer_view(self, which: str, layer: int):
         t = self.k_pool if which == "k" else self.v_pool

@@ -87,6 +87,13 @@ struct Params {
     float *pieces;       // [grid][2][D + 4]
     int32_t *counters;   // [S * H]
     uint32_t *status;
+    // fused append (decode step): token s's K/V row (all heads) goes to slot
+    // slots[s] of the layer before the tile holding it is read; null = no append
+    const uint4 *k_new;  // [S][H][D] fp16 as 16-byte words
+    const uint4 *v_new;
+    const int64_t *slots;  // [S]
+    uint4 *k_layer;      // this layer's pools, as 16-byte words
+    uint4 *v_layer;
     int32_t S, H, max_blocks, B, N, layout;
     float scale_log2;    // scale * log2(e)
 };
@@ -292,13 +299,53 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         const int32_t B = p.B;
         const int32_t rows = B < kTile ? B : kTile;           // rows per TMA box
         const uint32_t box_bytes = (uint32_t)rows * D * 2;
+        constexpr int W = D / 8;                              // 16-byte words per row
+        constexpr int NW = (2 * W + 31) / 32;                 // words of the new K+V rows per lane
         Cursor c = locate(sm, S, H, g0);
         int32_t win_s = -1, win_lb0 = 0, win_val = 0;
+        uint4 nw[NW];                                         // the new token's K/V row words
+        int64_t new_slot = -1;                                // pending append of the current (s, h)
         for (int32_t k = 0; k < n; ++k) {
             const int32_t stage = k % kStages;
+            if (p.k_new != nullptr && ((k == 0) || (c.t == 0))) {
+                // a new (s, h): if its last tile is ours, fetch the appended token's rows now
+                const int32_t seg_last = sm.base[c.s] + c.h * c.nt + c.nt - 1;
+                new_slot = -1;
+                if (seg_last < g1) {
+                    new_slot = p.slots[c.s];
+                    const size_t rw = ((size_t)c.s * H + c.h) * W;
+#pragma unroll
+                    for (int i = 0; i < NW; ++i) {
+                        const int wi = lane + 32 * i;
+                        if (wi < 2 * W) nw[i] = wi < W ? p.k_new[rw + wi] : p.v_new[rw + wi - W];
+                    }
+                }
+            }
             if (k >= kStages) {
                 const uint32_t parity = ((k / kStages) - 1) & 1;
                 wait_phase(sm, empty0 + 8 * stage, parity, p.status);
+            }
+            if (new_slot >= 0 && c.t == c.nt - 1) {
+                // the tile holding the new token: store its rows, then order the
+                // generic-proxy stores before the tile's TMA (async-proxy) read
+                if (new_slot < (int64_t)p.N * p.B) {
+                    const int64_t blk = new_slot / p.B, off = new_slot - blk * p.B;
+                    const int64_t row = p.layout == PKV_LAYOUT_NHD ? (blk * p.B + off) * H + c.h
+                                                                   : (blk * H + c.h) * p.B + off;
+#pragma unroll
+                    for (int i = 0; i < NW; ++i) {
+                        const int wi = lane + 32 * i;
+                        if (wi < 2 * W) {
+                            if (wi < W) p.k_layer[row * W + wi] = nw[i];
+                            else p.v_layer[row * W + wi - W] = nw[i];
+                        }
+                    }
+                    ptx::fence_proxy_async_global();
+                } else if (lane == 0) {
+                    atomicOr(p.status, PKV_DEV_BAD_SLOT);
+                }
+                new_slot = -1;
+                __syncwarp();
             }
             const int32_t T = sm.len[c.s];
             const int32_t t0 = c.t * kTile;
@@ -726,11 +773,17 @@ pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t *g
     return PKV_OK;
 }
 
-pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *v_cache, int32_t num_blocks,
-                                int32_t block_size, int32_t num_heads, int32_t head_dim, int32_t layout,
-                                const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
-                                int32_t num_seqs, float scale, void *out, void *workspace, size_t workspace_bytes,
-                                void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared implementation of the attention entry points; k_new / v_new / slots
+// non-null = fused append of one token per sequence (decode step).
+pkv_status decode_attention_impl(const void *q, const void *k_cache, const void *v_cache, int32_t num_blocks,
+                                 int32_t block_size, int32_t num_heads, int32_t head_dim, int32_t layout,
+                                 const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
+                                 int32_t num_seqs, float scale, void *out, void *workspace, size_t workspace_bytes,
+                                 void *stream, const void *k_new, const void *v_new, const int64_t *slots) {
     if (num_seqs < 0 || num_seqs > kMaxSeqs)
         return fail(PKV_ERR_INVALID_ARG, "num_seqs %d outside [0, %d]", num_seqs, kMaxSeqs);
     if (num_seqs == 0) return PKV_OK;
@@ -781,6 +834,11 @@ pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *
     prm.layout = layout;
     const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)head_dim);
     prm.scale_log2 = (float)(sc * 1.4426950408889634);  // log2(e)
+    prm.k_new = static_cast<const uint4 *>(k_new);
+    prm.v_new = static_cast<const uint4 *>(v_new);
+    prm.slots = slots;
+    prm.k_layer = static_cast<uint4 *>(const_cast<void *>(k_cache));
+    prm.v_layer = static_cast<uint4 *>(const_cast<void *>(v_cache));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -792,6 +850,40 @@ pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "decode attention launch: %s", cudaGetErrorString(e));
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *v_cache, int32_t num_blocks,
+                                int32_t block_size, int32_t num_heads, int32_t head_dim, int32_t layout,
+                                const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
+                                int32_t num_seqs, float scale, void *out, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    return decode_attention_impl(q, k_cache, v_cache, num_blocks, block_size, num_heads, head_dim, layout,
+                                 block_tables, max_blocks, context_lens, num_seqs, scale, out, workspace,
+                                 workspace_bytes, stream, nullptr, nullptr, nullptr);
+}
+
+pkv_status pkv_decode_append_attention(const pkv_pool *pool, int32_t layer, const void *q, const void *k_new,
+                                       const void *v_new, const int64_t *slot_mapping, const int32_t *block_tables,
+                                       int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs,
+                                       float scale, void *out, void *workspace, size_t workspace_bytes,
+                                       void *stream) {
+    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    const pkv_pool_desc &d = pool->desc;
+    if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
+    if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping))
+        return fail(PKV_ERR_INVALID_ARG, "NULL k_new, v_new or slot_mapping");
+    if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return fail(PKV_ERR_INVALID_ARG, "k_new/v_new must be 16-byte aligned, slot_mapping 8-byte aligned");
+    const size_t off = (size_t)layer * layer_elems(d) * 2;
+    return decode_attention_impl(q, static_cast<const char *>(pool->k_pool) + off,
+                                 static_cast<const char *>(pool->v_pool) + off, d.num_blocks, d.block_size,
+                                 d.num_heads, d.head_dim, d.layout, block_tables, max_blocks, context_lens, num_seqs,
+                                 scale, out, workspace, workspace_bytes, stream, k_new, v_new, slot_mapping);
 }
 
 pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const void *q, const int32_t *block_tables,

@@ -7,8 +7,9 @@ One decode step over a batch (all through the C ABI):
 2. the step's tables, lengths, slots and pairs go host -> device from pinned
    double-buffered staging (the host can prepare step k+1 while step k runs);
 3. ``pkv_copy_blocks`` once for the step, across all layers;
-4. per layer: ``pkv_append`` of the new token's K/V, then
-   ``pkv_pool_decode_attention`` over the cache including it.
+4. per layer: the new token's K/V appended and attention over the cache
+   including it -- one ``pkv_decode_append_attention`` launch (default), or
+   ``pkv_append`` then ``pkv_pool_decode_attention``.
 
 The driver also replays a workload's set-up script (admissions, forks, dummy
 churn, multi-token writes). It holds no arithmetic of the method: slots,
@@ -27,8 +28,10 @@ from . import binding as bd
 
 
 class DecodeEngine:
-    def __init__(self, w: wl.Workload, device: str = "cuda", fill: str = "torch", max_new_per_step: int = 1):
+    def __init__(self, w: wl.Workload, device: str = "cuda", fill: str = "torch", max_new_per_step: int = 1,
+                 fused: bool = True):
         self.w = w
+        self.fused = fused      # append inside the attention launch (pkv_decode_append_attention)
         self.device = torch.device(device)
         shape = wl.pool_shape(w)
         if fill == "numpy":
@@ -170,13 +173,19 @@ class DecodeEngine:
         wsp, wsb = self.workspace.data_ptr(), self.workspace.numel()
         maxb, S = w.max_blocks, w.num_seqs
         sc = float(scale)
+        fused = self.fused and n_slots == S
         for layer in range(w.num_layers):
             off = layer * row
-            bd.check(L.pkv_append(h, layer, kp + off, vp + off, slp, n_slots, status, sp))
             if attn_events is not None:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(s)
-            bd.check(L.pkv_pool_decode_attention(h, layer, qp + off, tp, maxb, lp, S, sc, op + off, wsp, wsb, sp))
+            if fused:
+                bd.check(L.pkv_decode_append_attention(h, layer, qp + off, kp + off, vp + off, slp, tp, maxb, lp, S,
+                                                       sc, op + off, wsp, wsb, sp))
+            else:
+                bd.check(L.pkv_append(h, layer, kp + off, vp + off, slp, n_slots, status, sp))
+                bd.check(L.pkv_pool_decode_attention(h, layer, qp + off, tp, maxb, lp, S, sc, op + off, wsp, wsb,
+                                                     sp))
             if attn_events is not None:
                 e1.record(s)
                 attn_events.append((e0, e1))

@@ -41,8 +41,8 @@ def u16(t):
     return t.detach().cpu().numpy().view(np.uint16)
 
 
-def run_parity(w, steps: int):
-    eng = DecodeEngine(w, fill="numpy")
+def run_parity(w, steps: int, fused: bool = True):
+    eng = DecodeEngine(w, fill="numpy", fused=fused)
     ora = OracleEngine(w, wl.pool_values(w, 0), wl.pool_values(w, 1))
     eng.run_script(values="numpy")
     ora.run_script()
@@ -78,9 +78,11 @@ def test_tiny_config(layout):
 
 
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
-def test_7b_shape_reduced(layout):
+@pytest.mark.parametrize("fused", [True, False])
+def test_7b_shape_reduced(layout, fused):
+    """The decode step with the append fused into the attention launch, and with two launches."""
     w = wl.make_workload(2, num_layers=2, num_seqs=8, len_scale=0.3, decode_steps=3, layout=layout)
-    run_parity(w, 3)
+    run_parity(w, 3, fused=fused)
 
 
 def test_prefix_sharing_cow_reduced():
@@ -235,6 +237,36 @@ def test_bad_slot_and_pair_are_flagged():
     st = int(status[0].item())
     assert st & pkv.DEV_BAD_SLOT and st & pkv.DEV_BAD_PAIR
     assert torch.equal(eng.k_pool, k0)          # nothing was written
+
+
+def test_fused_append_skip_and_bad_slot():
+    """Slot -1: nothing stored, the pool row is used as it is; slot >= N*B: flagged, not stored."""
+    w = wl.make_workload(1, decode_steps=2)
+    eng = DecodeEngine(w, fill="numpy")
+    ora = OracleEngine(w, wl.pool_values(w, 0), wl.pool_values(w, 1))
+    eng.run_script()
+    ora.run_script()
+    q, k, v = ora.step_inputs(0)
+    qd, kd, vd = eng.step_inputs(0)
+    n_slots, n_pairs = eng.prepare_step()
+    slots = eng.slots_d.clone()
+    eng.slots_d[1] = -1
+    eng.slots_d[2] = w.num_blocks * w.block_size + 3
+    out = torch.empty_like(qd)
+    eng.device_step(qd, kd, vd, out, n_slots, n_pairs)
+    torch.cuda.synchronize()
+    assert pkv.workspace_status(eng.workspace) & pkv.DEV_BAD_SLOT
+    eng.workspace.zero_()
+    # oracle: the same step with sequences 1 and 2 not written
+    slots_o, pairs_o = ora.pool.prepare_append(ora.tables, ora.lens, [1] * w.num_seqs, w.block_size, w.max_blocks)
+    assert slots_o == slots.tolist()
+    slots_o[1] = -1
+    slots_o[2] = -1
+    rf.append_kv(ora.k_pool[0], ora.v_pool[0], k[0], v[0], slots_o, w.block_size, w.layout)
+    ref = rf.decode_attention(q[0], ora.k_pool[0], ora.v_pool[0], ora.tables_array(), ora.lens, w.block_size,
+                              w.layout)
+    assert np.array_equal(u16(eng.k_pool), ora.k_pool.view(np.uint16))
+    assert_close(out[0].cpu().numpy(), ref, "fused skip / bad slot")
 
 
 def test_host_argument_errors():
