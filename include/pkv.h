@@ -236,6 +236,31 @@ pkv_status pkv_decode_append_attention(const pkv_pool *pool, int32_t layer, cons
                                        const int32_t *context_lens, int32_t num_seqs, float scale, void *out,
                                        void *workspace, size_t workspace_bytes, void *stream);
 
+/* pkv_decode_attention without a caller workspace: the scratch comes from a
+ * 4 MiB array compiled into the library. The method's pages have no
+ * counterpart for this call; it is here for callers that cannot allocate
+ * device memory -- e.g. a host framework that owns every device byte and gives
+ * a plugin no workspace, or a serving loop that forbids allocation once it runs
+ * because cudaMalloc can synchronise the device and stall other streams.
+ *
+ * Arguments and result as pkv_decode_attention, minus the workspace; status
+ * (device uint32, may be NULL) receives the call's PKV_DEV_* bits OR-ed in.
+ * Limit: the sizes must need at most 4 MiB of scratch (what
+ * pkv_decode_workspace_bytes reports for them); larger ones return
+ * PKV_ERR_INVALID_ARG with the sizes in pkv_last_error and launch nothing.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * Every GPU that loads the library holds the 4 MiB until the process exits.
+ * The first call on a device, made with that device current, looks the
+ * array's device address up once (cudaGetSymbolAddress); make that first call
+ * before any stream capture. All calls share the one array and each clears its
+ * counters on `stream` first, so calls that overlap on the GPU (other streams,
+ * other threads) race: serialise them. */
+pkv_status pkv_decode_attention_static(const void *q, const void *k_cache, const void *v_cache,
+                                       int32_t num_blocks, int32_t block_size, int32_t num_heads,
+                                       int32_t head_dim, int32_t layout, const int32_t *block_tables,
+                                       int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs,
+                                       float scale, void *out, uint32_t *status, void *stream);
+
 /* Bytes of workspace pkv_decode_attention needs for these sizes on the
  * current CUDA device (0 and a pkv_last_error message on bad arguments). */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim);

@@ -28,6 +28,7 @@ EXPORTED = [
     "pkv_incref", "pkv_free", "pkv_refcount", "pkv_get_stats", "pkv_free_queue", "pkv_validate",
     "pkv_prepare_append", "pkv_append", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_workspace_bytes",
     "pkv_pool_decode_attention", "pkv_decode_launch_info", "pkv_decode_append_attention",
+    "pkv_decode_attention_static",
 ]
 
 
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
             "pkv_decode_launch_info": (i32, [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                              ctypes.POINTER(i32)]),
             "pkv_decode_append_attention": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, f32, vp, vp, sz, vp]),
+            "pkv_decode_attention_static": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32, vp,
+                                                  vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

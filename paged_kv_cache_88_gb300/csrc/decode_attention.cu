@@ -783,7 +783,8 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
                                  int32_t block_size, int32_t num_heads, int32_t head_dim, int32_t layout,
                                  const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
                                  int32_t num_seqs, float scale, void *out, void *workspace, size_t workspace_bytes,
-                                 void *stream, const void *k_new, const void *v_new, const int64_t *slots) {
+                                 void *stream, const void *k_new, const void *v_new, const int64_t *slots,
+                                 uint32_t *status_override = nullptr) {
     if (num_seqs < 0 || num_seqs > kMaxSeqs)
         return fail(PKV_ERR_INVALID_ARG, "num_seqs %d outside [0, %d]", num_seqs, kMaxSeqs);
     if (num_seqs == 0) return PKV_OK;
@@ -823,7 +824,7 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     prm.tables = block_tables;
     prm.lens = context_lens;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    prm.status = reinterpret_cast<uint32_t *>(ws);
+    prm.status = status_override ? status_override : reinterpret_cast<uint32_t *>(ws);
     prm.counters = reinterpret_cast<int32_t *>(ws + counters_offset());
     prm.pieces = reinterpret_cast<float *>(ws + pieces_offset(num_seqs, num_heads));
     prm.S = num_seqs;
@@ -898,6 +899,80 @@ pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const 
                                 static_cast<const char *>(pool->v_pool) + off, d.num_blocks, d.block_size,
                                 d.num_heads, d.head_dim, d.layout, block_tables, max_blocks, context_lens, num_seqs,
                                 scale, out, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free entry point
+//
+// pkv_decode_attention_static runs the same kernel as pkv_decode_attention but
+// takes its scratch (last-arriver counters and split pieces) from a fixed array
+// compiled into the library instead of a caller-provided workspace. It exists
+// for callers that cannot allocate device memory: a host framework that owns
+// every device byte and offers a plugin no workspace hook, or a serving loop
+// that forbids allocation once it is running (cudaMalloc may synchronise the
+// device and stall every other stream). Such a caller still passes its own
+// inputs and outputs; only the scratch moves into the library.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)4 << 20;  // 4 MiB, held by every GPU that loads libpkv
+
+// The scratch itself. In host code this name is only a host-side stand-in for
+// the symbol; its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+void *g_static_scratch_addr[kMaxDevices] = {};
+std::mutex g_static_scratch_mu;
+
+// Device address of the scratch on `dev` (the current device): looked up once
+// per device, on the first call made with that device current.
+pkv_status static_scratch(int dev, void **out) {
+    if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_CUDA, "device index %d", dev);
+    std::lock_guard<std::mutex> lk(g_static_scratch_mu);
+    if (!g_static_scratch_addr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(PKV_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
+        g_static_scratch_addr[dev] = p;
+    }
+    *out = g_static_scratch_addr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_decode_attention_static(const void *q, const void *k_cache, const void *v_cache, int32_t num_blocks,
+                                       int32_t block_size, int32_t num_heads, int32_t head_dim, int32_t layout,
+                                       const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
+                                       int32_t num_seqs, float scale, void *out, uint32_t *status, void *stream) {
+    if (num_seqs < 0 || num_seqs > kMaxSeqs)
+        return fail(PKV_ERR_INVALID_ARG, "num_seqs %d outside [0, %d]", num_seqs, kMaxSeqs);
+    if (num_seqs == 0) return PKV_OK;
+    if (num_heads < 1 || !supported_head_dim(head_dim))
+        return fail(PKV_ERR_INVALID_ARG, "bad num_heads or head_dim");
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "no CUDA device");
+    const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, sms);
+    if (need > kStaticScratchBytes)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "%d sequences x %d heads (head_dim %d) need %zu bytes of scratch; the static scratch holds %zu",
+                    num_seqs, num_heads, head_dim, need, kStaticScratchBytes);
+    void *scratch = nullptr;
+    pkv_status st = static_scratch(dev, &scratch);
+    if (st != PKV_OK) return st;
+    // The array keeps the previous call's contents: the status word and the
+    // last-arriver counters must start at zero, so clear them on the stream.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, pieces_offset(num_seqs, num_heads), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "clearing the static scratch: %s", cudaGetErrorString(e));
+    return decode_attention_impl(q, k_cache, v_cache, num_blocks, block_size, num_heads, head_dim, layout,
+                                 block_tables, max_blocks, context_lens, num_seqs, scale, out, scratch,
+                                 kStaticScratchBytes, stream, nullptr, nullptr, nullptr, status);
 }
 
 }  // extern "C"
