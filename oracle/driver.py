@@ -66,8 +66,12 @@ class OracleEngine:
                 raise ValueError(kind)
 
     def step(self, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, scale: Optional[float] = None,
-             layers: Optional[list] = None, pairs_only: Optional[list] = None) -> np.ndarray:
-        """One decode step: a3 (slots, COW), a4 copy, a5 append, a6/a7 attention. Returns float64 [L, S, H, D]."""
+             layers: Optional[list] = None, pairs_only: Optional[list] = None, impl: str = "numpy") -> np.ndarray:
+        """One decode step: a3 (slots, COW), a4 copy, a5 append, a6/a7 attention. Returns float64 [L, S, H, D].
+
+        ``impl="c"`` computes the attention with the C oracle (same definition,
+        for full-size cases).
+        """
         w = self.w
         slots, pairs = self.pool.prepare_append(self.tables, self.lens, [1] * w.num_seqs, w.block_size,
                                                 w.max_blocks)
@@ -79,8 +83,14 @@ class OracleEngine:
                          w.layout)
             if layers is not None and layer not in layers:
                 continue
-            out[layer] = rf.decode_attention(q[layer], self.k_pool[layer], self.v_pool[layer], tab, self.lens,
-                                             w.block_size, w.layout, scale, pairs=pairs_only)
+            if impl == "c":
+                from . import ref_attn_c as rc
+                out[layer] = rc.decode_attention(q[layer], self.k_pool[layer], self.v_pool[layer], tab,
+                                                 np.asarray(self.lens, dtype=np.int32), w.block_size, w.layout,
+                                                 scale, pairs=pairs_only)
+            else:
+                out[layer] = rf.decode_attention(q[layer], self.k_pool[layer], self.v_pool[layer], tab, self.lens,
+                                                 w.block_size, w.layout, scale, pairs=pairs_only)
         self.last_slots, self.last_pairs = slots, pairs
         return out
 

@@ -287,7 +287,15 @@ def test_host_argument_errors():
 
 # ----------------------------------------------------------------------------- full size
 
-def test_7b_full_size_bench_launch_sampled():
+@pytest.fixture
+def free_gpu_memory():
+    yield
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_7b_full_size_bench_launch_sampled(free_gpu_memory):
     """The 7B-shape batch-32 workload at full size, 32 layers, in the benchmark's launch configuration.
 
     The oracle allocator replays the same script (tables bit-exact); for two
@@ -320,3 +328,69 @@ def test_7b_full_size_bench_launch_sampled():
         ref = rc.decode_attention(qd[l].cpu().numpy(), kp, vp, tab, np.asarray(lens, dtype=np.int32),
                                   w.block_size, w.layout)
         assert_close(out[l].cpu().numpy(), ref, f"7b full layer {l}")
+
+
+def _full_size(w, check_layers, steps: int = 2):
+    """Full-size workload through the engine (torch-made pools); oracle on the listed layers.
+
+    The oracle replays the same host script with its own allocator (tables,
+    slots and COW pairs bit-exact), starts from the pools read back before any
+    write, applies its own copies and appends, and computes every (sequence,
+    head) of each step with the float64 C oracle.
+    """
+    import dataclasses
+    eng = DecodeEngine(w, fill="torch")
+    snap_k = np.stack([eng.k_pool[l].cpu().numpy() for l in check_layers])
+    snap_v = np.stack([eng.v_pool[l].cpu().numpy() for l in check_layers])
+    eng.run_script(values="torch")
+    sub = dataclasses.replace(w, num_layers=len(check_layers))
+    ora = OracleEngine(sub, snap_k, snap_v)
+    del snap_k, snap_v
+
+    def values(op_index, i, which, n):
+        layer = check_layers[i]
+        return wl.torch_normal_fp16(w.seed, (400 + which, op_index, layer), (n, w.num_heads, w.head_dim),
+                                    "cuda").cpu().numpy()
+
+    ora.run_script(values)
+    torch.cuda.synchronize()
+    assert eng.tables.tolist() == ora.tables and eng.lens.tolist() == ora.lens
+    for i, l in enumerate(check_layers):
+        assert np.array_equal(u16(eng.k_pool[l]), ora.k_pool[i].view(np.uint16)), f"K layer {l} after set-up"
+        assert np.array_equal(u16(eng.v_pool[l]), ora.v_pool[i].view(np.uint16)), f"V layer {l} after set-up"
+    for step in range(steps):
+        qd, kd, vd = eng.step_inputs(step, "torch")
+        out = torch.empty_like(qd)
+        eng.step(qd, kd, vd, out)
+        torch.cuda.synchronize()
+        assert eng.device_status() == 0
+        sel = lambda t: t[check_layers].cpu().numpy()
+        ref = ora.step(sel(qd), sel(kd), sel(vd), impl="c")
+        assert eng.last_slots.tolist() == ora.last_slots
+        assert [tuple(p) for p in eng.last_pairs.tolist()] == ora.last_pairs
+        assert eng.tables.tolist() == ora.tables
+        for i, l in enumerate(check_layers):
+            assert np.array_equal(u16(eng.k_pool[l]), ora.k_pool[i].view(np.uint16)), f"K layer {l} step {step}"
+            assert_close(out[l].cpu().numpy(), ref[i], f"{w.name} full size, layer {l}, step {step}")
+    eng.pool.validate()
+    return eng
+
+
+
+def test_prefix_full_size_sampled(free_gpu_memory):
+    """64 sequences on one 520-token prompt at full size: 63 COW copies in every layer, then decode steps."""
+    w = wl.make_workload(3, decode_steps=4)
+    eng = _full_size(w, [0, 17, w.num_layers - 1], steps=2)
+    assert eng.pool.stats()["cow_copies"] == w.num_seqs - 1
+
+
+def test_13b_full_size_sampled(free_gpu_memory):
+    """13B shape, batch 128, block 32, pool 90 % occupied after churn, full size (40 layers)."""
+    w = wl.make_workload(4, decode_steps=4)
+    _full_size(w, [0, w.num_layers - 1], steps=2)
+
+
+def test_long_context_full_size_sampled(free_gpu_memory):
+    """16 sequences of 4k-16k tokens in 4 MiB pages, full size (32 layers)."""
+    w = wl.make_workload(5, decode_steps=4)
+    _full_size(w, [0, w.num_layers - 1], steps=2)
