@@ -152,6 +152,29 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def aggregate_ranks(ms: float, kv_bytes: float, seq_steps: float, device=None):
+    """Whole-job figures over the ranks: the slowest rank's time, the sum of the work.
+
+    Ranks are independent replicas (each its own pool and batch): the only
+    communication is this reduction of the measurements.
+    """
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms, kv_bytes, seq_steps
+    t = torch.tensor([ms, kv_bytes, seq_steps], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    sm = t.clone()
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return mx[0].item(), sm[1].item(), sm[2].item()
+
+
+def rank_seed(config: int, rank: int) -> int:
+    """Seed of rank ``rank``'s batch (rank 0 runs the single-GPU workload)."""
+    return 1000 + config + 7919 * rank
+
+
 def make_bench_workload(args, extra_steps: int):
     import workloads as wl
     w = wl.make_workload(args.config, decode_steps=extra_steps, layout=args.layout, block_size=args.block_size,
@@ -237,7 +260,7 @@ def run_ours(args):
     if world > 1:                         # weak scaling: each rank serves its own batch
         import workloads as wl
         w = wl.make_workload(args.config, decode_steps=total_steps, layout=args.layout,
-                             block_size=args.block_size, num_layers=args.layers, seed=1000 + args.config + 7919 * rank)
+                             block_size=args.block_size, num_layers=args.layers, seed=rank_seed(args.config, rank))
     eng = DecodeEngine(w, device=str(dev), fill="torch")
     eng.run_script(values="torch")
     torch.cuda.synchronize()
@@ -299,16 +322,7 @@ def run_ours(args):
         raise RuntimeError(f"device status {status:#x} in the timed region")
 
     kv_bytes = sum(step_bytes) * L
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, float(kv_bytes), float(S * args.steps)], dtype=torch.float64, device=dev)
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        sm = t.clone()
-        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
-        ms_job, bytes_job, seqsteps_job = mx[0].item(), sm[1].item(), sm[2].item()
-    else:
-        ms_job, bytes_job, seqsteps_job = ms, float(kv_bytes), float(S * args.steps)
+    ms_job, bytes_job, seqsteps_job = aggregate_ranks(ms, float(kv_bytes), float(S * args.steps), dev)
     value = bytes_job / (ms_job / 1e3) / 1e9
     seq_steps = seqsteps_job / (ms_job / 1e3)
 
