@@ -74,11 +74,16 @@ typedef struct pkv_pool_desc {
 } pkv_pool_desc;
 
 typedef struct pkv_stats {
-    int32_t free_blocks;   /* blocks in the free queue */
-    int32_t used_blocks;   /* blocks with refcount >= 1 */
-    int32_t shared_blocks; /* blocks with refcount >= 2 */
+    int32_t free_blocks;        /* blocks in the free queue */
+    int32_t used_blocks;        /* blocks with refcount >= 1 */
+    int32_t shared_blocks;      /* blocks with refcount >= 2 */
     int32_t max_refcount;
-    int64_t cow_copies;    /* copy-on-write copies issued by pkv_prepare_append so far */
+    int64_t cow_copies;         /* copy-on-write copies issued by pkv_prepare_append so far */
+    int32_t cached_blocks;      /* blocks registered in the prefix cache (in use or free) */
+    int32_t cached_free_blocks; /* of those, blocks in the free queue (revived by a hit) */
+    int64_t prefix_hits;        /* blocks found by pkv_prefix_lookup so far */
+    int64_t prefix_misses;      /* blocks looked up and not found */
+    int64_t evictions;          /* cached blocks whose hash was dropped when reused */
 } pkv_stats;
 
 typedef struct pkv_pool pkv_pool; /* opaque host metadata */
@@ -141,6 +146,33 @@ pkv_status pkv_free_queue(const pkv_pool *pool, int32_t *out, int32_t capacity, 
 /* Check the bookkeeping: the free queue holds every block with refcount 0 once
  * and nothing else. REFCOUNT if not (never expected; a test hook). */
 pkv_status pkv_validate(const pkv_pool *pool);
+
+/* ------------------------------------------------------------- prefix cache
+ * Requests that start with the same tokens share the KV blocks of those tokens
+ * (icman.com.cn/news/78786 §3.2-§3.4; hnwysp.cn/news/103996 §4.3): each FULL block of
+ * a prompt is keyed by a hash chained from the start of the sequence, a hit
+ * takes one more reference to the cached block and writes no KV. A block whose
+ * refcount drops to 0 keeps its hash while it waits in the free queue, so the
+ * queue doubles as the LRU of cached blocks: a later hit takes it back out,
+ * and taking it from the head for reuse drops (evicts) its hash. */
+
+/* Hash of one block: 64-bit FNV-1a over `parent` (the previous block's hash, 0
+ * for the first block; 8 bytes little-endian) followed by the n token ids (4
+ * bytes little-endian each). */
+uint64_t pkv_block_hash(uint64_t parent, const int32_t *token_ids, int32_t n);
+
+/* For i = 0, 1, ... look hashes[i] up; stop at the first miss. Each hit gets
+ * one more reference (a cached block in the free queue is taken out of it and
+ * gets refcount 1) and its id goes to out_ids[i]. *num_hits = the hits.
+ * Chained hashes make a later block meaningless after a miss, hence the stop. */
+pkv_status pkv_prefix_lookup(pkv_pool *pool, const uint64_t *hashes, int32_t n, int32_t *out_ids,
+                             int32_t *num_hits);
+
+/* Register full blocks whose KV has been written: hashes[i] -> ids[i] (blocks in
+ * use). A hash already held by another block keeps that block; a block
+ * re-registered under a new hash drops the old one. BAD_BLOCK / REFCOUNT (a
+ * free block) refuse the whole call. */
+pkv_status pkv_prefix_register(pkv_pool *pool, const uint64_t *hashes, const int32_t *ids, int32_t n);
 
 /* Give slots to the next tokens of a batch of sequences; the host half of the
  * decode step (m.lqnn.cn/news/240480 §3.2 step 3; hnwysp.cn/news/103996 §3.3).

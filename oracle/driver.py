@@ -62,6 +62,23 @@ class OracleEngine:
                     rf.append_kv(self.k_pool[layer], self.v_pool[layer], values(op_index, layer, 0, total),
                                  values(op_index, layer, 1, total), slots, B, w.layout)
                 self.last_slots, self.last_pairs = slots, pairs
+            elif kind == "prompt":
+                _, s, tokens = op
+                hashes = ra.prompt_block_hashes(tokens, B)
+                hit = self.pool.prefix_lookup(hashes)
+                self.tables[s] = hit + [-1] * (w.max_blocks - len(hit))
+                self.lens[s] = len(hit) * B
+                counts = [0] * w.num_seqs
+                counts[s] = len(tokens) - len(hit) * B
+                total = counts[s]
+                slots, pairs = self.pool.prepare_append(self.tables, self.lens, counts, B, w.max_blocks)
+                rf.copy_blocks(self.k_pool, self.v_pool, pairs)
+                for layer in range(w.num_layers):
+                    rf.append_kv(self.k_pool[layer], self.v_pool[layer], values(op_index, layer, 0, total),
+                                 values(op_index, layer, 1, total), slots, B, w.layout)
+                if len(hashes) > len(hit):
+                    self.pool.prefix_register(hashes[len(hit):], self.tables[s][len(hit):len(hashes)])
+                self.last_slots, self.last_pairs = slots, pairs
             else:
                 raise ValueError(kind)
 

@@ -22,12 +22,24 @@ What it follows:
   block at the fork point is copied (hnwysp.cn/news/103996 §3.3;
   icman.com.cn/news/78786 §3.4).
 
+* Prefix caching: each full block of a prompt is keyed by a hash of its tokens
+  chained from the start of the sequence; a request whose leading blocks hash
+  to cached blocks shares them (one more reference, no KV written); cached
+  blocks with no reference stay evictable in LRU order and a later hit revives
+  them (icman.com.cn/news/78786 §3.1-§3.4; hnwysp.cn/news/103996 §4.3).
+
 Readings taken where the pages are silent (each is listed in the design doc):
 
 * Allocation is all-or-nothing and a failed call changes nothing.
 * COW fires iff the refcount of the block being written is > 1 at the moment of
   the write; sequences are processed in ascending index, tokens in order.
 * A slot is ``physical_block * B + offset``; -1 in a table means "no block".
+* The block hash is 64-bit FNV-1a (the pages name SHA256 or xxHash; any fixed
+  hash serves) over the parent hash's 8 little-endian bytes and the block's
+  token ids, 4 little-endian bytes each; the first block's parent is 0.
+* The free queue is the LRU of cached blocks: a freed block keeps its hash at
+  the tail; a hit takes it back out; reusing it from the head drops its hash.
+  Lookup stops at the first miss (a chained hash past a miss cannot be used).
 """
 from __future__ import annotations
 
@@ -51,6 +63,35 @@ REFCOUNT = "refcount"
 INVALID_ARG = "invalid_arg"
 
 
+FNV64_OFFSET = 0xCBF29CE484222325
+FNV64_PRIME = 0x100000001B3
+MASK64 = (1 << 64) - 1
+
+
+def fnv1a64(data: bytes) -> int:
+    """64-bit FNV-1a: xor each byte into the state, then multiply by the FNV prime."""
+    h = FNV64_OFFSET
+    for byte in data:
+        h = ((h ^ byte) * FNV64_PRIME) & MASK64
+    return h
+
+
+def block_hash(parent: int, token_ids: Sequence[int]) -> int:
+    """Hash of one block chained on its parent's hash (0 for the first block)."""
+    data = int(parent).to_bytes(8, "little") + b"".join(int(t).to_bytes(4, "little", signed=True)
+                                                       for t in token_ids)
+    return fnv1a64(data)
+
+
+def prompt_block_hashes(token_ids: Sequence[int], block_size: int) -> List[int]:
+    """Chained hashes of the full blocks of a prompt."""
+    out, parent = [], 0
+    for i in range(len(token_ids) // block_size):
+        parent = block_hash(parent, token_ids[i * block_size:(i + 1) * block_size])
+        out.append(parent)
+    return out
+
+
 @dataclass
 class PoolStats:
     free_blocks: int
@@ -58,6 +99,11 @@ class PoolStats:
     shared_blocks: int
     max_refcount: int
     cow_copies: int
+    cached_blocks: int = 0
+    cached_free_blocks: int = 0
+    prefix_hits: int = 0
+    prefix_misses: int = 0
+    evictions: int = 0
 
 
 class RefPool:
@@ -73,6 +119,21 @@ class RefPool:
         self.free_queue: deque = deque(order)
         self.refcount: List[int] = [0] * num_blocks
         self.cow_copies = 0
+        self.hash_of: dict = {}     # block -> registered hash
+        self.by_hash: dict = {}     # hash -> block
+        self.prefix_hits = 0
+        self.prefix_misses = 0
+        self.evictions = 0
+
+    def _take(self) -> int:
+        """Pop the head of the free queue; a cached block loses its hash (eviction)."""
+        b = self.free_queue.popleft()
+        if b in self.hash_of:
+            h = self.hash_of.pop(b)
+            if self.by_hash.get(h) == b:
+                del self.by_hash[h]
+            self.evictions += 1
+        return b
 
     # -- a2: alloc / incref / free ------------------------------------------------
     def alloc(self, n: int) -> List[int]:
@@ -81,7 +142,7 @@ class RefPool:
             raise PoolError(INVALID_ARG, "negative count")
         if n > len(self.free_queue):
             raise PoolError(OUT_OF_BLOCKS, f"want {n}, have {len(self.free_queue)}")
-        ids = [self.free_queue.popleft() for _ in range(n)]
+        ids = [self._take() for _ in range(n)]
         for b in ids:
             self.refcount[b] = 1
         return ids
@@ -128,7 +189,8 @@ class RefPool:
         """
         if block_size <= 0 or max_blocks <= 0 or len(tables) != len(lens) or len(num_new) != len(lens):
             raise PoolError(INVALID_ARG, "bad shapes")
-        saved = (copy.deepcopy(tables), list(lens), deque(self.free_queue), list(self.refcount), self.cow_copies)
+        saved = (copy.deepcopy(tables), list(lens), deque(self.free_queue), list(self.refcount), self.cow_copies,
+                 dict(self.hash_of), dict(self.by_hash), self.evictions)
         try:
             slots: List[int] = []
             pairs: List[tuple] = []
@@ -161,7 +223,43 @@ class RefPool:
             self.free_queue = saved[2]
             self.refcount = saved[3]
             self.cow_copies = saved[4]
+            self.hash_of, self.by_hash, self.evictions = saved[5], saved[6], saved[7]
             raise
+
+    # -- prefix cache ---------------------------------------------------------------
+    def prefix_lookup(self, hashes: Sequence[int]) -> List[int]:
+        """Blocks of the leading run of cached hashes; each gets one more reference."""
+        ids: List[int] = []
+        for h in hashes:
+            b = self.by_hash.get(int(h))
+            if b is None:
+                break
+            if self.refcount[b] == 0:
+                self.free_queue.remove(b)      # a cached free block is revived
+            self.refcount[b] += 1
+            ids.append(b)
+        self.prefix_hits += len(ids)
+        self.prefix_misses += len(hashes) - len(ids)
+        return ids
+
+    def prefix_register(self, hashes: Sequence[int], ids: Sequence[int]) -> None:
+        """Record full, written blocks under their hashes (first holder of a hash keeps it)."""
+        ids = [int(b) for b in ids]
+        self._check_ids(ids)
+        for b in ids:
+            if self.refcount[b] == 0:
+                raise PoolError(REFCOUNT, f"block {b} is free")
+        for h, b in zip((int(x) for x in hashes), ids):
+            if b in self.hash_of:
+                if self.hash_of[b] == h:
+                    continue
+                old = self.hash_of.pop(b)
+                if self.by_hash.get(old) == b:
+                    del self.by_hash[old]
+            if h in self.by_hash:
+                continue
+            self.by_hash[h] = b
+            self.hash_of[b] = h
 
     # -- bookkeeping ------------------------------------------------------------------
     def stats(self) -> PoolStats:
@@ -172,6 +270,11 @@ class RefPool:
             shared_blocks=sum(1 for r in self.refcount if r > 1),
             max_refcount=max(self.refcount) if self.refcount else 0,
             cow_copies=self.cow_copies,
+            cached_blocks=len(self.hash_of),
+            cached_free_blocks=sum(1 for b in self.hash_of if self.refcount[b] == 0),
+            prefix_hits=self.prefix_hits,
+            prefix_misses=self.prefix_misses,
+            evictions=self.evictions,
         )
 
     def validate(self) -> None:
@@ -184,6 +287,12 @@ class RefPool:
             raise PoolError(REFCOUNT, "free queue and zero refcounts disagree")
         if any(r < 0 for r in self.refcount):
             raise PoolError(REFCOUNT, "negative refcount")
+        for b, h in self.hash_of.items():
+            if self.by_hash.get(h) != b:
+                raise PoolError(REFCOUNT, f"cached block {b} missing from the map")
+        for h, b in self.by_hash.items():
+            if self.hash_of.get(b) != h:
+                raise PoolError(REFCOUNT, f"map entry {h:#x} without its block")
 
 
 def admit(pool: RefPool, num_tokens: int, block_size: int, max_blocks: int) -> List[int]:

@@ -28,7 +28,7 @@ EXPORTED = [
     "pkv_incref", "pkv_free", "pkv_refcount", "pkv_get_stats", "pkv_free_queue", "pkv_validate",
     "pkv_prepare_append", "pkv_append", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_workspace_bytes",
     "pkv_pool_decode_attention", "pkv_decode_launch_info", "pkv_decode_append_attention",
-    "pkv_decode_attention_static",
+    "pkv_decode_attention_static", "pkv_block_hash", "pkv_prefix_lookup", "pkv_prefix_register",
 ]
 
 
@@ -46,7 +46,9 @@ class PoolDesc(ctypes.Structure):
 
 class Stats(ctypes.Structure):
     _fields_ = [("free_blocks", ctypes.c_int32), ("used_blocks", ctypes.c_int32), ("shared_blocks", ctypes.c_int32),
-                ("max_refcount", ctypes.c_int32), ("cow_copies", ctypes.c_int64)]
+                ("max_refcount", ctypes.c_int32), ("cow_copies", ctypes.c_int64), ("cached_blocks", ctypes.c_int32),
+                ("cached_free_blocks", ctypes.c_int32), ("prefix_hits", ctypes.c_int64),
+                ("prefix_misses", ctypes.c_int64), ("evictions", ctypes.c_int64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -89,6 +91,9 @@ def lib() -> ctypes.CDLL:
             "pkv_decode_append_attention": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, f32, vp, vp, sz, vp]),
             "pkv_decode_attention_static": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32, vp,
                                                   vp, vp]),
+            "pkv_block_hash": (u64, [u64, vp, i32]),
+            "pkv_prefix_lookup": (i32, [vp, vp, i32, vp, ctypes.POINTER(i32)]),
+            "pkv_prefix_register": (i32, [vp, vp, vp, i32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -189,6 +194,21 @@ class Pool:
         a = np.ascontiguousarray(ids, dtype=np.int32)
         check(lib().pkv_free(self._h, _ptr(a), a.size))
 
+    def prefix_lookup(self, hashes: Sequence[int]) -> list:
+        """Blocks of the longest cached run of ``hashes`` (each gets one more reference)."""
+        h = np.ascontiguousarray(hashes, dtype=np.uint64)
+        out = np.zeros(max(h.size, 1), dtype=np.int32)
+        nh = i32()
+        check(lib().pkv_prefix_lookup(self._h, _ptr(h), h.size, _ptr(out), ctypes.byref(nh)))
+        return out[: nh.value].tolist()
+
+    def prefix_register(self, hashes: Sequence[int], ids: Sequence[int]) -> None:
+        h = np.ascontiguousarray(hashes, dtype=np.uint64)
+        b = np.ascontiguousarray(ids, dtype=np.int32)
+        if h.size != b.size:
+            raise ValueError("one id per hash")
+        check(lib().pkv_prefix_register(self._h, _ptr(h), _ptr(b), h.size))
+
     def refcount(self, block: int) -> int:
         r = i32()
         check(lib().pkv_refcount(self._h, block, ctypes.byref(r)))
@@ -272,6 +292,21 @@ class Pool:
         t = self.k_pool if which == "k" else self.v_pool
         d = self.desc
         return t.view(d.num_layers, -1)[layer]
+
+
+def block_hash(parent: int, token_ids: Sequence[int]) -> int:
+    """pkv_block_hash: chained hash of one block's token ids."""
+    t = np.ascontiguousarray(token_ids, dtype=np.int32)
+    return int(lib().pkv_block_hash(parent, _ptr(t), t.size))
+
+
+def prompt_block_hashes(token_ids: Sequence[int], block_size: int) -> list:
+    """Chained hashes of the full blocks of a prompt (pkv_block_hash per block)."""
+    hs, parent = [], 0
+    for i in range(len(token_ids) // block_size):
+        parent = block_hash(parent, token_ids[i * block_size:(i + 1) * block_size])
+        hs.append(parent)
+    return hs
 
 
 def decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int) -> int:

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <unordered_map>
 #include <utility>
 #include <vector>
 
@@ -16,12 +17,18 @@ struct pkv_pool {
     pkv_pool_desc desc;
     void *k_pool;
     void *v_pool;
-    // FIFO free queue as a ring buffer of capacity N: head index + count.
-    std::vector<int32_t> ring;
-    int32_t head;
-    int32_t count;
+    // FIFO free queue as a doubly linked list over block ids (-1 = none): O(1)
+    // take from the head, return to the tail, and removal of a cached block
+    // that a prefix lookup revives.
+    std::vector<int32_t> next, prev;
+    int32_t head, tail, count;
     std::vector<int32_t> refcount;
     int64_t cow_copies;
+    // prefix cache: full blocks registered under the chained hash of their tokens
+    std::vector<uint64_t> hash_of;
+    std::vector<uint8_t> has_hash;
+    std::unordered_map<uint64_t, int32_t> by_hash;
+    int64_t prefix_hits, prefix_misses, evictions;
 };
 
 namespace pkv {

@@ -43,22 +43,52 @@ using pkv::fail;
 
 namespace {
 
-inline int32_t ring_pop_front(pkv_pool *p) {
-    int32_t id = p->ring[p->head];
-    p->head = (p->head + 1) % p->desc.num_blocks;
+// ---- free queue (doubly linked list over block ids) --------------------------
+
+inline void q_push_back(pkv_pool *p, int32_t b) {
+    p->next[b] = -1;
+    p->prev[b] = p->tail;
+    if (p->tail >= 0) p->next[p->tail] = b; else p->head = b;
+    p->tail = b;
+    p->count += 1;
+}
+
+inline void q_push_front(pkv_pool *p, int32_t b) {
+    p->prev[b] = -1;
+    p->next[b] = p->head;
+    if (p->head >= 0) p->prev[p->head] = b; else p->tail = b;
+    p->head = b;
+    p->count += 1;
+}
+
+inline void q_remove(pkv_pool *p, int32_t b) {
+    if (p->prev[b] >= 0) p->next[p->prev[b]] = p->next[b]; else p->head = p->next[b];
+    if (p->next[b] >= 0) p->prev[p->next[b]] = p->prev[b]; else p->tail = p->prev[b];
+    p->next[b] = p->prev[b] = -1;
     p->count -= 1;
-    return id;
 }
 
-inline void ring_push_back(pkv_pool *p, int32_t id) {
-    p->ring[(p->head + p->count) % p->desc.num_blocks] = id;
-    p->count += 1;
+// A block leaving the free queue for reuse loses its cached prefix hash (LRU
+// eviction: the queue holds freed blocks in the order they were freed).
+struct Evicted {
+    int32_t block;
+    uint64_t hash;
+};
+
+inline void drop_hash(pkv_pool *p, int32_t b, std::vector<Evicted> *log) {
+    if (!p->has_hash[b]) return;
+    auto it = p->by_hash.find(p->hash_of[b]);
+    if (it != p->by_hash.end() && it->second == b) p->by_hash.erase(it);
+    if (log) log->push_back({b, p->hash_of[b]});
+    p->has_hash[b] = 0;
+    p->evictions += 1;
 }
 
-inline void ring_push_front(pkv_pool *p, int32_t id) {
-    p->head = (p->head + p->desc.num_blocks - 1) % p->desc.num_blocks;
-    p->ring[p->head] = id;
-    p->count += 1;
+inline int32_t q_pop_front(pkv_pool *p, std::vector<Evicted> *log = nullptr) {
+    const int32_t b = p->head;
+    q_remove(p, b);
+    drop_hash(p, b, log);
+    return b;
 }
 
 pkv_status check_desc(const pkv_pool_desc *d) {
@@ -114,11 +144,16 @@ pkv_status pkv_pool_create(const pkv_pool_desc *desc, void *k_pool, void *v_pool
     p->desc = *desc;
     p->k_pool = k_pool;
     p->v_pool = v_pool;
-    p->ring = std::move(order);
-    p->head = 0;
-    p->count = N;
+    p->next.assign(N, -1);
+    p->prev.assign(N, -1);
+    p->head = p->tail = -1;
+    p->count = 0;
+    for (int32_t i = 0; i < N; ++i) q_push_back(p, order[i]);
     p->refcount.assign(N, 0);
     p->cow_copies = 0;
+    p->hash_of.assign(N, 0);
+    p->has_hash.assign(N, 0);
+    p->prefix_hits = p->prefix_misses = p->evictions = 0;
     *out = p;
     return PKV_OK;
 }
@@ -142,7 +177,7 @@ pkv_status pkv_alloc(pkv_pool *pool, int32_t n, int32_t *out_ids) {
     if (n > pool->count)
         return fail(PKV_ERR_OUT_OF_BLOCKS, "want %d blocks, %d free", n, pool->count);
     for (int32_t i = 0; i < n; ++i) {
-        int32_t id = ring_pop_front(pool);
+        int32_t id = q_pop_front(pool);
         pool->refcount[id] = 1;
         out_ids[i] = id;
     }
@@ -183,7 +218,7 @@ pkv_status pkv_free(pkv_pool *pool, const int32_t *ids, int32_t n) {
     for (int32_t j = 0; j < n; ++j) rc[ids[j]] += 1;
     for (int32_t j = 0; j < n; ++j) {
         rc[ids[j]] -= 1;
-        if (rc[ids[j]] == 0) ring_push_back(pool, ids[j]);
+        if (rc[ids[j]] == 0) q_push_back(pool, ids[j]);
     }
     return PKV_OK;
 }
@@ -199,13 +234,83 @@ pkv_status pkv_get_stats(const pkv_pool *pool, pkv_stats *out) {
     if (!pool || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
     pkv_stats s{};
     s.free_blocks = pool->count;
-    for (int32_t r : pool->refcount) {
+    for (size_t b = 0; b < pool->refcount.size(); ++b) {
+        const int32_t r = pool->refcount[b];
         if (r > 0) s.used_blocks += 1;
         if (r > 1) s.shared_blocks += 1;
         if (r > s.max_refcount) s.max_refcount = r;
+        if (pool->has_hash[b]) {
+            s.cached_blocks += 1;
+            if (r == 0) s.cached_free_blocks += 1;
+        }
     }
     s.cow_copies = pool->cow_copies;
+    s.prefix_hits = pool->prefix_hits;
+    s.prefix_misses = pool->prefix_misses;
+    s.evictions = pool->evictions;
     *out = s;
+    return PKV_OK;
+}
+
+// ---- prefix cache (icman.com.cn/news/78786 §3.2-§3.4; hnwysp.cn/news/103996 §4.3)
+
+uint64_t pkv_block_hash(uint64_t parent, const int32_t *token_ids, int32_t n) {
+    // 64-bit FNV-1a over the parent hash (8 bytes, little-endian) and then each
+    // token id (4 bytes, little-endian, two's complement).
+    uint64_t h = 0xcbf29ce484222325ull;
+    auto mix = [&h](uint8_t byte) {
+        h ^= byte;
+        h *= 0x100000001b3ull;
+    };
+    for (int i = 0; i < 8; ++i) mix(static_cast<uint8_t>(parent >> (8 * i)));
+    for (int32_t t = 0; t < n; ++t) {
+        const uint32_t v = static_cast<uint32_t>(token_ids[t]);
+        for (int i = 0; i < 4; ++i) mix(static_cast<uint8_t>(v >> (8 * i)));
+    }
+    return h;
+}
+
+pkv_status pkv_prefix_lookup(pkv_pool *pool, const uint64_t *hashes, int32_t n, int32_t *out_ids,
+                             int32_t *num_hits) {
+    if (!pool || !num_hits) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+    if (n < 0 || (n > 0 && (!hashes || !out_ids))) return fail(PKV_ERR_INVALID_ARG, "bad count or arrays");
+    int32_t i = 0;
+    for (; i < n; ++i) {
+        auto it = pool->by_hash.find(hashes[i]);
+        if (it == pool->by_hash.end()) break;
+        const int32_t b = it->second;
+        if (pool->refcount[b] == 0) q_remove(pool, b);  // a cached free block comes back into use
+        pool->refcount[b] += 1;
+        out_ids[i] = b;
+    }
+    *num_hits = i;
+    pool->prefix_hits += i;
+    pool->prefix_misses += n - i;
+    return PKV_OK;
+}
+
+pkv_status pkv_prefix_register(pkv_pool *pool, const uint64_t *hashes, const int32_t *ids, int32_t n) {
+    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (n < 0 || (n > 0 && (!hashes || !ids))) return fail(PKV_ERR_INVALID_ARG, "bad count or arrays");
+    const int32_t N = pool->desc.num_blocks;
+    for (int32_t i = 0; i < n; ++i)
+        if (ids[i] < 0 || ids[i] >= N) return fail(PKV_ERR_BAD_BLOCK, "block %d out of range", ids[i]);
+    for (int32_t i = 0; i < n; ++i)
+        if (pool->refcount[ids[i]] == 0) return fail(PKV_ERR_REFCOUNT, "block %d is free", ids[i]);
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t b = ids[i];
+        const uint64_t h = hashes[i];
+        if (pool->has_hash[b]) {
+            if (pool->hash_of[b] == h) continue;
+            auto old = pool->by_hash.find(pool->hash_of[b]);
+            if (old != pool->by_hash.end() && old->second == b) pool->by_hash.erase(old);
+            pool->has_hash[b] = 0;
+        }
+        if (pool->by_hash.count(h)) continue;  // another block already holds these tokens
+        pool->by_hash[h] = b;
+        pool->hash_of[b] = h;
+        pool->has_hash[b] = 1;
+    }
     return PKV_OK;
 }
 
@@ -214,7 +319,8 @@ pkv_status pkv_free_queue(const pkv_pool *pool, int32_t *out, int32_t capacity, 
     *count = pool->count;
     if (capacity < pool->count || (pool->count > 0 && !out))
         return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d", capacity, pool->count);
-    for (int32_t i = 0; i < pool->count; ++i) out[i] = pool->ring[(pool->head + i) % pool->desc.num_blocks];
+    int32_t i = 0;
+    for (int32_t b = pool->head; b >= 0; b = pool->next[b]) out[i++] = b;
     return PKV_OK;
 }
 
@@ -222,17 +328,29 @@ pkv_status pkv_validate(const pkv_pool *pool) {
     if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
     const int32_t N = pool->desc.num_blocks;
     std::vector<char> inq(N, 0);
-    for (int32_t i = 0; i < pool->count; ++i) {
-        int32_t b = pool->ring[(pool->head + i) % N];
-        if (b < 0 || b >= N || inq[b]) return fail(PKV_ERR_REFCOUNT, "free queue corrupt at %d", i);
+    int32_t seen = 0, last = -1;
+    for (int32_t b = pool->head; b >= 0; b = pool->next[b]) {
+        if (b >= N || inq[b] || seen >= N || pool->prev[b] != last)
+            return fail(PKV_ERR_REFCOUNT, "free queue corrupt at position %d", seen);
         inq[b] = 1;
+        last = b;
+        seen += 1;
     }
+    if (seen != pool->count || last != pool->tail) return fail(PKV_ERR_REFCOUNT, "free queue count/tail wrong");
     for (int32_t b = 0; b < N; ++b) {
         if (pool->refcount[b] < 0) return fail(PKV_ERR_REFCOUNT, "block %d refcount < 0", b);
         if ((pool->refcount[b] == 0) != (inq[b] != 0))
             return fail(PKV_ERR_REFCOUNT, "block %d: refcount %d but %s the free queue", b,
                         pool->refcount[b], inq[b] ? "in" : "not in");
+        if (pool->has_hash[b]) {
+            auto it = pool->by_hash.find(pool->hash_of[b]);
+            if (it == pool->by_hash.end() || it->second != b)
+                return fail(PKV_ERR_REFCOUNT, "block %d: cached hash not in the map", b);
+        }
     }
+    for (const auto &kv : pool->by_hash)
+        if (kv.second < 0 || kv.second >= N || !pool->has_hash[kv.second] || pool->hash_of[kv.second] != kv.first)
+            return fail(PKV_ERR_REFCOUNT, "prefix map entry without its block");
     return PKV_OK;
 }
 
@@ -260,6 +378,8 @@ pkv_status pkv_prepare_append(pkv_pool *pool, int32_t num_seqs, int32_t *block_t
     // Undo log: every change is recorded so that a failure restores the state.
     struct TableEdit { int64_t at; int32_t old; };
     std::vector<int32_t> allocated;  // in pop order
+    std::vector<Evicted> evicted;    // cached hashes dropped by those pops
+    const int64_t evictions0 = pool->evictions;
     std::vector<int32_t> decrefs;
     std::vector<TableEdit> edits;
     std::vector<int32_t> lens0(context_lens, context_lens + num_seqs);
@@ -272,7 +392,7 @@ pkv_status pkv_prepare_append(pkv_pool *pool, int32_t num_seqs, int32_t *block_t
             st = fail(PKV_ERR_OUT_OF_BLOCKS, "free queue empty");
             return false;
         }
-        *id = ring_pop_front(pool);
+        *id = q_pop_front(pool, &evicted);
         pool->refcount[*id] = 1;
         allocated.push_back(*id);
         return true;
@@ -326,8 +446,14 @@ pkv_status pkv_prepare_append(pkv_pool *pool, int32_t num_seqs, int32_t *block_t
         for (int32_t r : decrefs) pool->refcount[r] += 1;
         for (size_t j = allocated.size(); j-- > 0;) {
             pool->refcount[allocated[j]] = 0;
-            ring_push_front(pool, allocated[j]);
+            q_push_front(pool, allocated[j]);
         }
+        for (const Evicted &e : evicted) {
+            pool->hash_of[e.block] = e.hash;
+            pool->has_hash[e.block] = 1;
+            pool->by_hash[e.hash] = e.block;
+        }
+        pool->evictions = evictions0;
         for (int32_t s = 0; s < num_seqs; ++s) context_lens[s] = lens0[s];
         pool->cow_copies = cow0;
         *num_slots = 0;

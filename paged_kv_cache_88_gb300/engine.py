@@ -96,6 +96,9 @@ class DecodeEngine:
             elif kind == "write":
                 counts = np.asarray(op[1], dtype=np.int32)
                 self.write_tokens(op_index, counts, values, stream)
+            elif kind == "prompt":
+                _, s, tokens = op
+                self.admit_prompt(op_index, s, tokens, values, stream)
             else:
                 raise ValueError(kind)
         self.upload_tables()
@@ -118,6 +121,23 @@ class DecodeEngine:
             self.pool.append(layer, kn, vn, slots_d, status=self.status, stream=stream)
         self.last_pairs, self.last_slots = pairs.copy(), slots.copy()
         return slots, pairs
+
+    def admit_prompt(self, op_index: int, s: int, tokens, values: str = "numpy", stream=None):
+        """Sequence s arrives with prompt ``tokens``: cached leading blocks are shared
+        (pkv_prefix_lookup), the remaining tokens are written through the append
+        path, and the prompt's full blocks are registered (pkv_prefix_register)."""
+        w, B = self.w, self.w.block_size
+        hashes = bd.prompt_block_hashes(tokens, B)
+        hit = self.pool.prefix_lookup(hashes)
+        self.tables[s, :len(hit)] = hit
+        self.lens[s] = len(hit) * B
+        n_new = len(tokens) - len(hit) * B
+        counts = np.zeros(w.num_seqs, dtype=np.int32)
+        counts[s] = n_new
+        self.write_tokens(op_index, counts, values, stream)
+        full = len(hashes)
+        if full > len(hit):
+            self.pool.prefix_register(hashes[len(hit):], self.tables[s, len(hit):full])
 
     def upload_tables(self):
         self.tables_d.copy_(torch.from_numpy(self.tables))

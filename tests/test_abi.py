@@ -150,10 +150,12 @@ def test_allocator_matches_oracle_random_ops(seed):
         _same(c, o)
 
 
-@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
-def test_workload_setup_tables_match_oracle(index):
-    """Every workload's set-up script (admit / fork / churn / COW writes) gives identical tables."""
-    w = wl.make_workload(index, num_layers=1)
+@pytest.mark.parametrize("index,mode", [(1, "fork"), (2, "fork"), (3, "fork"), (3, "hash"), (4, "fork"),
+                                        (5, "fork")])
+def test_workload_setup_tables_match_oracle(index, mode):
+    """Every workload's set-up script (admit / fork / churn / COW writes / prefix-cache prompts) gives
+    identical tables."""
+    w = wl.make_workload(index, num_layers=1, prefix_mode=mode)
     c = bd.Pool(1, w.num_blocks, w.block_size, w.num_heads, w.head_dim, initial_free_order=w.free_order)
     o = ra.RefPool(w.num_blocks, [int(x) for x in w.free_order])
     B = w.block_size
@@ -188,6 +190,23 @@ def test_workload_setup_tables_match_oracle(index):
             sc, pc = c.prepare_append(tc, lc, op[1])
             so, po = o.prepare_append(to, lo, op[1], B, w.max_blocks)
             assert sc.tolist() == so and [tuple(p) for p in pc.tolist()] == po
+        elif op[0] == "prompt":
+            _, s, tokens = op
+            hc_, ho_ = bd.prompt_block_hashes(tokens, B), ra.prompt_block_hashes(tokens, B)
+            assert hc_ == ho_
+            hit_c, hit_o = c.prefix_lookup(hc_), o.prefix_lookup(ho_)
+            assert hit_c == hit_o
+            tc[s, :len(hit_c)] = hit_c
+            lc[s] = len(hit_c) * B
+            to[s] = hit_o + [-1] * (w.max_blocks - len(hit_o))
+            lo[s] = len(hit_o) * B
+            counts = [0] * w.num_seqs
+            counts[s] = len(tokens) - len(hit_o) * B
+            sc, pc = c.prepare_append(tc, lc, counts)
+            so, po = o.prepare_append(to, lo, counts, B, w.max_blocks)
+            assert sc.tolist() == so
+            c.prefix_register(hc_[len(hit_c):], tc[s, len(hit_c):len(hc_)])
+            o.prefix_register(ho_[len(hit_o):], to[s][len(hit_o):len(ho_)])
         assert tc.tolist() == to and lc.tolist() == lo
     # a few decode steps
     for _ in range(3):
@@ -222,3 +241,69 @@ def test_device_ops_refuse_host_only_pool():
     assert rc == 1 and "device memory" in pkv.last_error()
     rc = pkv.lib().pkv_copy_blocks(c.handle, None, 1, None, None)
     assert rc == 1
+
+
+# ------------------------------------------------------------------ prefix cache: library vs oracle
+
+def test_block_hash_matches_oracle():
+    rng = random.Random(5)
+    for _ in range(200):
+        parent = rng.randrange(1 << 64)
+        toks = [rng.randrange(-2**31, 2**31) for _ in range(rng.randrange(0, 40))]
+        assert bd.block_hash(parent, toks) == ra.block_hash(parent, toks)
+    toks = [rng.randrange(32000) for _ in range(100)]
+    assert bd.prompt_block_hashes(toks, 16) == ra.prompt_block_hashes(toks, 16)
+
+
+def _same_prefix_state(c, o):
+    _same(c, o)
+    st, so = c.stats(), o.stats()
+    assert (st["cached_blocks"], st["cached_free_blocks"], st["prefix_hits"], st["prefix_misses"],
+            st["evictions"]) == (so.cached_blocks, so.cached_free_blocks, so.prefix_hits, so.prefix_misses,
+                                 so.evictions)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_prefix_cache_matches_oracle(seed):
+    rng = random.Random(100 + seed)
+    B, N, maxb = 8, 20, 8
+    order = rng.sample(range(N), N)
+    c = bd.Pool(1, N, B, 1, 64, initial_free_order=order)
+    o = ra.RefPool(N, order)
+    prefixes = [[rng.randrange(40) for _ in range(24)] for _ in range(3)]
+    live = {}
+    for step in range(160):
+        r = rng.random()
+        if live and r < 0.3:
+            k = rng.choice(sorted(live))
+            ids = live.pop(k)
+            _both(lambda: c.free(ids), lambda: o.free(ids))
+        elif r < 0.4:
+            ids = [rng.randrange(-1, N + 1) for _ in range(2)]
+            hs = [rng.randrange(1 << 64) for _ in range(2)]
+            _both(lambda: c.prefix_register(hs, ids), lambda: o.prefix_register(hs, ids))
+        else:
+            toks = rng.choice(prefixes)[: rng.randrange(8, 25)] + [rng.randrange(40) for _ in range(rng.randrange(9))]
+            hs = ra.prompt_block_hashes(toks, B)
+            hc, ho = _both(lambda: c.prefix_lookup(hs), lambda: o.prefix_lookup(hs))
+            assert hc == ho
+            need = -(-len(toks) // B) - len(ho)
+            nc, no = _both(lambda: c.alloc(need), lambda: o.alloc(need))
+            if no is None:
+                _both(lambda: c.free(ho), lambda: o.free(ho))
+            else:
+                assert nc == no
+                ids = ho + no
+                _both(lambda: c.prefix_register(hs[len(ho):], ids[len(ho):len(hs)]),
+                      lambda: o.prefix_register(hs[len(ho):], ids[len(ho):len(hs)]))
+                live[step] = ids
+        _same_prefix_state(c, o)
+    # appends that take cached free blocks evict them in both, and roll back alike on failure
+    tables_c = np.full((1, maxb), -1, dtype=np.int32)
+    lens_c = np.zeros(1, dtype=np.int32)
+    tables_o, lens_o = [[-1] * maxb], [0]
+    for n in (3, 20, 200):
+        rc, ro = _both(lambda: c.prepare_append(tables_c, lens_c, [n]),
+                       lambda: o.prepare_append(tables_o, lens_o, [n], B, maxb))
+        assert tables_c.tolist() == tables_o and lens_c.tolist() == lens_o
+        _same_prefix_state(c, o)

@@ -92,6 +92,19 @@ def test_prefix_sharing_cow_reduced():
     assert st["cow_copies"] == w.num_seqs - 1
 
 
+def test_prefix_found_by_block_hash_reduced():
+    """Requests arriving with the same prompt tokens share its full blocks through the prefix cache."""
+    w = wl.make_workload(3, num_layers=2, num_seqs=8, len_scale=0.25, decode_steps=3, prefix_mode="hash")
+    eng, ora = run_parity(w, 3)
+    st = eng.pool.stats()
+    shared_full = 130 // w.block_size                  # 0.25 x 520 prompt tokens -> 8 full blocks
+    assert st["prefix_hits"] == (w.num_seqs - 1) * shared_full
+    assert st["cow_copies"] == 0
+    so = ora.pool.stats()
+    assert (st["prefix_hits"], st["prefix_misses"], st["cached_blocks"]) == \
+        (so.prefix_hits, so.prefix_misses, so.cached_blocks)
+
+
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
 def test_13b_shape_churned_pool_reduced(layout):
     w = wl.make_workload(4, num_layers=2, num_seqs=24, len_scale=0.5, decode_steps=2, layout=layout)

@@ -34,7 +34,17 @@ A workload's ``script`` is a list of host operations, each a tuple:
 * ``("dummy_alloc", d, n)``  an unrelated request d takes n blocks;
 * ``("dummy_free", d)``      request d releases its blocks;
 * ``("write", counts)``      counts[s] new tokens of sequence s are appended
-                              (data from :func:`write_values`).
+                              (data from :func:`write_values`);
+* ``("prompt", s, tokens)``  sequence s arrives with prompt token ids ``tokens``:
+                              its leading full blocks are looked up in the prefix
+                              cache, the rest is written (data from
+                              :func:`write_values`) and its full blocks registered.
+
+Workload 3 comes in two forms: ``prefix_mode="fork"`` (the shared prompt is
+forked to every request, the first suffix token copies the shared partial
+block) and ``prefix_mode="hash"`` (every request arrives with the same 520
+prompt tokens plus its own suffix tokens and finds the shared blocks through
+the prefix cache).
 """
 from __future__ import annotations
 
@@ -102,7 +112,7 @@ def _finish(index, name, L, H, D, B, lens, script, steps, seed, N, layout, desc,
 def make_workload(index: int, *, num_layers: Optional[int] = None, num_seqs: Optional[int] = None,
                   block_size: Optional[int] = None, decode_steps: Optional[int] = None,
                   layout: str = "HND", seed: Optional[int] = None,
-                  len_scale: float = 1.0) -> Workload:
+                  len_scale: float = 1.0, prefix_mode: str = "fork") -> Workload:
     """The seeded workload ``index`` (1..5); keyword overrides shrink it for tests.
 
     ``len_scale`` multiplies sampled context lengths (tests use it to keep the
@@ -141,14 +151,24 @@ def make_workload(index: int, *, num_layers: Optional[int] = None, num_seqs: Opt
         suffix = np.maximum(1, np.round(suffix * len_scale)).astype(np.int64)
         B = block_size or B
         steps = 64 if decode_steps is None else decode_steps
-        script = [("admit", 0, prefix)] + [("fork", 0, s) for s in range(1, S)]
-        script.append(("write", [int(x) for x in suffix]))
+        if prefix_mode == "fork":
+            script = [("admit", 0, prefix)] + [("fork", 0, s) for s in range(1, S)]
+            script.append(("write", [int(x) for x in suffix]))
+        elif prefix_mode == "hash":
+            tr = _rng(seed, 5)
+            shared = [int(t) for t in tr.integers(0, 32000, size=prefix)]
+            script = [("prompt", s, shared + [int(t) for t in tr.integers(0, 32000, size=int(suffix[s]))])
+                      for s in range(S)]
+        else:
+            raise ValueError(prefix_mode)
         lens = prefix + suffix
         shared = _ceil_div(prefix, B)
         need = shared + S + sum(_ceil_div(int(t) + steps, B) - shared for t in lens)
         N = int(math.ceil(1.3 * need))
-        return _finish(3, "prefix", num_layers or L, H, D, B, lens, script, steps, seed, N, layout,
-                       "7B shape, B=16, 64 seqs share a 520-token prefix, suffix U[64,512], COW")
+        return _finish(3, "prefix" if prefix_mode == "fork" else "prefix-hash", num_layers or L, H, D, B, lens,
+                       script, steps, seed, N, layout,
+                       "7B shape, B=16, 64 seqs share a 520-token prefix, suffix U[64,512], "
+                       + ("COW" if prefix_mode == "fork" else "found by block hash"))
     if index == 4:
         L, H, D, B = 40, 40, 128, 32
         S = 128 if num_seqs is None else num_seqs
