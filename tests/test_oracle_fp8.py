@@ -1,0 +1,98 @@
+"""Pins of the FP8 E4M3 quantisation oracle (oracle/fp8.py)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import fp8
+from oracle import ref_attn as rf
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "e4m3.json")))
+
+
+def test_decode_matches_spec_values():
+    for v in GOLD["values"]:
+        got = fp8.DECODE[int(v["code"], 16)]
+        if v["value"] == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == v["value"], v
+    finite = fp8.DECODE[~np.isnan(fp8.DECODE)]
+    assert finite.max() == 448.0 and finite.min() == -448.0 and len(finite) == 254
+
+
+def test_encode_round_trip_all_codes():
+    for code in range(256):
+        v = fp8.DECODE[code]
+        if np.isnan(v):
+            continue
+        assert fp8.e4m3_encode(np.array([v]))[0] == code
+
+
+def test_encode_ties_to_even_and_saturation():
+    # 1.0625 lies halfway between 1.0 (0x38, even) and 1.125 (0x39): ties go to even
+    assert fp8.e4m3_encode(np.array([1.0625]))[0] == 0x38
+    assert fp8.e4m3_encode(np.array([1.1875]))[0] == 0x3A     # halfway 1.125 / 1.25 -> 1.25 (even)
+    assert fp8.e4m3_encode(np.array([1000.0, -1000.0])).tolist() == [0x7E, 0xFE]
+    assert fp8.e4m3_encode(np.array([2.0 ** -10]))[0] == 0x00   # halfway 0 / 2^-9 -> 0 (even)
+
+
+def test_encode_matches_torch_float8():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    for sc in (1e-3, 1.0, 300.0):
+        x = np.clip(rng.standard_normal(100000).astype(np.float32) * sc, -448, 448)
+        t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(fp8.e4m3_encode(x), t)
+
+
+def test_quantize_rows_properties():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((50, 3, 128)).astype(np.float16)
+    codes, scales = fp8.quantize_rows(x)
+    assert codes.dtype == np.uint8 and scales.dtype == np.float32 and scales.shape == (50, 3)
+    # the row maximum maps to +-448 exactly
+    assert np.all(np.max(np.abs(fp8.DECODE[codes]), axis=-1) == 448.0)
+    deq = fp8.dequantize(codes, scales)
+    xf = x.astype(np.float64)
+    # relative error of a normal E4M3 value is at most 2^-4 (half of the 3-bit mantissa step)
+    big = np.abs(xf) >= scales[..., None].astype(np.float64) * 2.0 ** -6
+    assert np.all(np.abs(deq - xf)[big] <= 2.0 ** -4 * np.abs(xf)[big] + 1e-12)
+    z, zs = fp8.quantize_rows(np.zeros((2, 128), dtype=np.float16))
+    assert np.all(z == 0) and np.all(zs == 1.0)
+
+
+def test_attention_over_dequantised_values():
+    rng = np.random.default_rng(5)
+    N, H, B, D = 6, 2, 8, 64
+    kc = rng.integers(0, 0x7E, size=(N, H, B, D)).astype(np.uint8)
+    vc = rng.integers(0, 0x7E, size=(N, H, B, D)).astype(np.uint8) | (rng.integers(0, 2, size=(N, H, B, D)) << 7).astype(np.uint8)
+    ks = rng.uniform(1e-3, 1e-2, size=(N, H, B)).astype(np.float32)
+    vs = rng.uniform(1e-3, 1e-2, size=(N, H, B)).astype(np.float32)
+    q = rng.standard_normal((2, H, D)).astype(np.float16)
+    tables = np.array([[3, 1, 4], [0, 5, 2]], dtype=np.int32)
+    lens = np.array([19, 9], dtype=np.int32)
+    got = fp8.decode_attention(q, kc, vc, ks, vs, tables, lens, B)
+    kd = fp8.dequantize(kc, ks)
+    vd = fp8.dequantize(vc, vs)
+    want = rf.decode_attention(q, kd, vd, tables, lens, B, layout="HND")
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+def test_append_and_copy_quantised():
+    rng = np.random.default_rng(6)
+    N, H, B, D = 4, 2, 8, 64
+    kc = np.zeros((1, N, H, B, D), dtype=np.uint8)
+    vc = kc.copy()
+    ks = np.zeros((1, N, H, B), dtype=np.float32)
+    vs = ks.copy()
+    kn = rng.standard_normal((2, H, D)).astype(np.float16)
+    vn = rng.standard_normal((2, H, D)).astype(np.float16)
+    fp8.append_kv(kc[0], vc[0], ks[0], vs[0], kn, vn, [9, -1], B)
+    q, s = fp8.quantize_rows(kn[0])
+    assert np.array_equal(kc[0, 1, :, 1], q) and np.array_equal(ks[0, 1, :, 1], s)
+    assert np.count_nonzero(kc) == np.count_nonzero(q)
+    fp8.copy_blocks(kc, vc, ks, vs, [(1, 3)])
+    assert np.array_equal(kc[:, 3], kc[:, 1]) and np.array_equal(vs[:, 3], vs[:, 1])
