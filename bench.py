@@ -49,6 +49,7 @@ def parse_args():
     ap.add_argument("--layout", default="HND", choices=["NHD", "HND"])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling captures only)")
+    ap.add_argument("--kv-dtype", default="f16", choices=["f16", "e4m3"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -178,14 +179,30 @@ def rank_seed(config: int, rank: int) -> int:
 def make_bench_workload(args, extra_steps: int):
     import workloads as wl
     w = wl.make_workload(args.config, decode_steps=extra_steps, layout=args.layout, block_size=args.block_size,
-                         num_layers=args.layers)
+                         num_layers=args.layers, kv_dtype=args.kv_dtype)
     return w
 
 
-def cpu_baseline_oracle(w, k_layer, v_layer, tables, lens, seconds: float):
-    """The C oracle (float64, OpenMP over (sequence, head)) on one layer, repeated for ~``seconds``."""
+def cpu_baseline_oracle(w, k_layer, v_layer, tables, lens, seconds: float, k_scale=None, v_scale=None):
+    """The oracle on one layer, repeated for ~``seconds``: the C float64 oracle (OpenMP over
+    (sequence, head)) for an fp16 cache; the NumPy E4M3 oracle on one sequence for a quantised one."""
     import numpy as np
     from oracle import ref_attn_c as rc
+    if w.kv_dtype == "e4m3":
+        from oracle import fp8
+        q = np.random.default_rng(0).standard_normal((1, w.num_heads, w.head_dim)).astype(np.float16)
+        t0 = time.perf_counter()
+        passes = 0
+        while True:
+            s = passes % w.num_seqs
+            fp8.decode_attention(q, k_layer, v_layer, k_scale, v_scale, tables[s:s + 1], lens[s:s + 1], w.block_size)
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        nbytes = sum(int(lens[i % w.num_seqs]) for i in range(passes)) * w.kv_bytes_per_token_layer
+        return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{passes} sequence(s) of one layer, NumPy E4M3 oracle (dequantise, float64), {el:.1f} s"}
     rng = np.random.default_rng(0)
     q = rng.standard_normal((w.num_seqs, w.num_heads, w.head_dim)).astype(np.float16)
     bytes_per = int(np.asarray(lens, dtype=np.int64).sum()) * w.kv_bytes_per_token_layer
@@ -260,7 +277,8 @@ def run_ours(args):
     if world > 1:                         # weak scaling: each rank serves its own batch
         import workloads as wl
         w = wl.make_workload(args.config, decode_steps=total_steps, layout=args.layout,
-                             block_size=args.block_size, num_layers=args.layers, seed=rank_seed(args.config, rank))
+                             block_size=args.block_size, num_layers=args.layers, seed=rank_seed(args.config, rank),
+                             kv_dtype=args.kv_dtype)
     eng = DecodeEngine(w, device=str(dev), fill="torch")
     eng.run_script(values="torch")
     torch.cuda.synchronize()
@@ -364,7 +382,9 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         kl = eng.k_pool[0].cpu().numpy()
         vl = eng.v_pool[0].cpu().numpy()
-        cpu = cpu_baseline_oracle(w, kl, vl, eng.tables.copy(), eng.lens.copy(), args.cpu_seconds)
+        ks = eng.k_scale[0].cpu().numpy() if eng.k_scale is not None else None
+        vs = eng.v_scale[0].cpu().numpy() if eng.v_scale is not None else None
+        cpu = cpu_baseline_oracle(w, kl, vl, eng.tables.copy(), eng.lens.copy(), args.cpu_seconds, ks, vs)
 
     info = pkv.decode_launch_info(S, D)
     if rank == 0:
@@ -372,7 +392,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_job / args.steps, "host_ms_per_step": host_ms,
             "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if w.kv_dtype == "f16" else "e4m3",
+            "accumulate": "f32", "data": "synthetic",
             "config": dict(w.describe(), l2="inputs larger than L2 (each layer's KV >> 129 MB), no flush",
                            parallelism="replicas" if world > 1 else "single",
                            mean_context_timed=float(np.mean(step_bytes)) / w.kv_bytes_per_token_layer / S,

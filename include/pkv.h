@@ -57,6 +57,16 @@ typedef enum pkv_status {
  *   PKV_LAYOUT_HND: [N][H][B][D] -- one head's tokens of a block contiguous. */
 enum { PKV_LAYOUT_NHD = 0, PKV_LAYOUT_HND = 1 };
 
+/* Element type of the K/V pools:
+ *   PKV_KV_F16:  IEEE binary16;
+ *   PKV_KV_E4M3: FP8 E4M3 codes (1 byte) with one fp32 scale per (token, head)
+ *                row, value = code * scale, scale = amax(row) / 448 (1 for an
+ *                all-zero row), codes rounded to nearest even and saturated.
+ *                Quantised KV halves the bytes per token (m.lqnn.cn/news/240480
+ *                §6.2; hnwysp.cn/news/103996 §5.4). HND layout, head_dim 64 or 128;
+ *                the scale pools are [L][N][H][B] fp32 (pkv_pool_set_scales). */
+enum { PKV_KV_F16 = 0, PKV_KV_E4M3 = 1 };
+
 /* Bits of the device status word (uint32_t) that device entry points OR into. */
 #define PKV_DEV_BAD_BLOCK 0x1u   /* a block-table entry outside [0, num_blocks): clamped to 0 */
 #define PKV_DEV_BAD_LENGTH 0x2u  /* a context length < 0 or > max_blocks * block_size: clamped */
@@ -71,6 +81,7 @@ typedef struct pkv_pool_desc {
     int32_t num_heads;  /* H KV heads (query heads = KV heads) */
     int32_t head_dim;   /* D: 64, 128 or 256 */
     int32_t layout;     /* PKV_LAYOUT_NHD or PKV_LAYOUT_HND */
+    int32_t kv_dtype;   /* PKV_KV_F16 (0) or PKV_KV_E4M3 */
 } pkv_pool_desc;
 
 typedef struct pkv_stats {
@@ -108,6 +119,11 @@ int32_t pkv_version(void);
  *   permutation, N*B or L*N*B*H*D too large). Touches no CUDA state. */
 pkv_status pkv_pool_create(const pkv_pool_desc *desc, void *k_pool, void *v_pool,
                            const int32_t *initial_free_order, pkv_pool **out);
+
+/* E4M3 pools: attach the caller-owned scale pools (device fp32 [L][N][H][B]
+ * each, 16-byte aligned) that pair with k_pool / v_pool. INVALID_ARG for an
+ * fp16 pool. Device entry points refuse an E4M3 pool without them. */
+pkv_status pkv_pool_set_scales(pkv_pool *pool, void *k_scale, void *v_scale);
 
 /* Free the host metadata. Does not free the device pools. NULL is accepted. */
 pkv_status pkv_pool_destroy(pkv_pool *pool);

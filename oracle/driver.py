@@ -13,16 +13,22 @@ import numpy as np
 
 import workloads as wl
 
+from . import fp8
 from . import ref_alloc as ra
 from . import ref_attn as rf
 
 
 class OracleEngine:
-    def __init__(self, w: wl.Workload, k_pool: np.ndarray, v_pool: np.ndarray):
-        """``k_pool``/``v_pool``: the initial pools, shape ``workloads.pool_shape(w)`` (copied)."""
+    def __init__(self, w: wl.Workload, k_pool: np.ndarray, v_pool: np.ndarray, k_scale=None, v_scale=None):
+        """``k_pool``/``v_pool``: the initial pools, shape ``workloads.pool_shape(w)`` (copied); for an E4M3
+        cache they are the codes and ``k_scale``/``v_scale`` the per-(token, head) scales."""
         self.w = w
-        self.k_pool = np.array(k_pool, dtype=np.float16, copy=True)
-        self.v_pool = np.array(v_pool, dtype=np.float16, copy=True)
+        self.q8 = w.kv_dtype == "e4m3"
+        dt = np.uint8 if self.q8 else np.float16
+        self.k_pool = np.array(k_pool, dtype=dt, copy=True)
+        self.v_pool = np.array(v_pool, dtype=dt, copy=True)
+        self.k_scale = np.array(k_scale, dtype=np.float32, copy=True) if self.q8 else None
+        self.v_scale = np.array(v_scale, dtype=np.float32, copy=True) if self.q8 else None
         self.pool = ra.RefPool(w.num_blocks, [int(x) for x in w.free_order])
         self.tables: List[List[int]] = [[-1] * w.max_blocks for _ in range(w.num_seqs)]
         self.lens: List[int] = [0] * w.num_seqs
@@ -32,6 +38,20 @@ class OracleEngine:
 
     def tables_array(self) -> np.ndarray:
         return np.asarray(self.tables, dtype=np.int32)
+
+    def _copy(self, pairs):
+        if self.q8:
+            fp8.copy_blocks(self.k_pool, self.v_pool, self.k_scale, self.v_scale, pairs)
+        else:
+            rf.copy_blocks(self.k_pool, self.v_pool, pairs)
+
+    def _append(self, layer, k_new, v_new, slots):
+        if self.q8:
+            fp8.append_kv(self.k_pool[layer], self.v_pool[layer], self.k_scale[layer], self.v_scale[layer], k_new,
+                          v_new, slots, self.w.block_size)
+        else:
+            rf.append_kv(self.k_pool[layer], self.v_pool[layer], k_new, v_new, slots, self.w.block_size,
+                         self.w.layout)
 
     def run_script(self, values: Optional[Callable] = None):
         """Replay the set-up script. ``values(op_index, layer, which, n)`` gives written K/V (default: workloads)."""
@@ -57,10 +77,9 @@ class OracleEngine:
                 counts = [int(x) for x in op[1]]
                 total = sum(counts)
                 slots, pairs = self.pool.prepare_append(self.tables, self.lens, counts, B, w.max_blocks)
-                rf.copy_blocks(self.k_pool, self.v_pool, pairs)
+                self._copy(pairs)
                 for layer in range(w.num_layers):
-                    rf.append_kv(self.k_pool[layer], self.v_pool[layer], values(op_index, layer, 0, total),
-                                 values(op_index, layer, 1, total), slots, B, w.layout)
+                    self._append(layer, values(op_index, layer, 0, total), values(op_index, layer, 1, total), slots)
                 self.last_slots, self.last_pairs = slots, pairs
             elif kind == "prompt":
                 _, s, tokens = op
@@ -72,10 +91,9 @@ class OracleEngine:
                 counts[s] = len(tokens) - len(hit) * B
                 total = counts[s]
                 slots, pairs = self.pool.prepare_append(self.tables, self.lens, counts, B, w.max_blocks)
-                rf.copy_blocks(self.k_pool, self.v_pool, pairs)
+                self._copy(pairs)
                 for layer in range(w.num_layers):
-                    rf.append_kv(self.k_pool[layer], self.v_pool[layer], values(op_index, layer, 0, total),
-                                 values(op_index, layer, 1, total), slots, B, w.layout)
+                    self._append(layer, values(op_index, layer, 0, total), values(op_index, layer, 1, total), slots)
                 if len(hashes) > len(hit):
                     self.pool.prefix_register(hashes[len(hit):], self.tables[s][len(hit):len(hashes)])
                 self.last_slots, self.last_pairs = slots, pairs
@@ -92,15 +110,18 @@ class OracleEngine:
         w = self.w
         slots, pairs = self.pool.prepare_append(self.tables, self.lens, [1] * w.num_seqs, w.block_size,
                                                 w.max_blocks)
-        rf.copy_blocks(self.k_pool, self.v_pool, pairs)
+        self._copy(pairs)
         out = np.zeros((w.num_layers, w.num_seqs, w.num_heads, w.head_dim))
         tab = self.tables_array()
         for layer in range(w.num_layers):
-            rf.append_kv(self.k_pool[layer], self.v_pool[layer], k_new[layer], v_new[layer], slots, w.block_size,
-                         w.layout)
+            self._append(layer, k_new[layer], v_new[layer], slots)
             if layers is not None and layer not in layers:
                 continue
-            if impl == "c":
+            if self.q8:
+                out[layer] = fp8.decode_attention(q[layer], self.k_pool[layer], self.v_pool[layer],
+                                                  self.k_scale[layer], self.v_scale[layer], tab, self.lens,
+                                                  w.block_size, scale)
+            elif impl == "c":
                 from . import ref_attn_c as rc
                 out[layer] = rc.decode_attention(q[layer], self.k_pool[layer], self.v_pool[layer], tab,
                                                  np.asarray(self.lens, dtype=np.int32), w.block_size, w.layout,

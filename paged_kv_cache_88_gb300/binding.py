@@ -21,6 +21,7 @@ OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_BLOCKS", 3: "BAD_BLOCK", 4: "REFCOUNT", 5: "CUDA",
                 6: "UNSUPPORTED"}
 LAYOUTS = {"NHD": 0, "HND": 1}
+KV_DTYPES = {"f16": 0, "e4m3": 1}
 DEV_BAD_BLOCK, DEV_BAD_LENGTH, DEV_TIMEOUT, DEV_BAD_SLOT, DEV_BAD_PAIR = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTED = [
@@ -29,6 +30,7 @@ EXPORTED = [
     "pkv_prepare_append", "pkv_append", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_workspace_bytes",
     "pkv_pool_decode_attention", "pkv_decode_launch_info", "pkv_decode_append_attention",
     "pkv_decode_attention_static", "pkv_block_hash", "pkv_prefix_lookup", "pkv_prefix_register",
+    "pkv_pool_set_scales",
 ]
 
 
@@ -41,7 +43,8 @@ class PkvError(RuntimeError):
 
 class PoolDesc(ctypes.Structure):
     _fields_ = [("num_layers", ctypes.c_int32), ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("layout", ctypes.c_int32)]
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("layout", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
 
 
 class Stats(ctypes.Structure):
@@ -94,6 +97,7 @@ def lib() -> ctypes.CDLL:
             "pkv_block_hash": (u64, [u64, vp, i32]),
             "pkv_prefix_lookup": (i32, [vp, vp, i32, vp, ctypes.POINTER(i32)]),
             "pkv_prefix_register": (i32, [vp, vp, vp, i32]),
+            "pkv_pool_set_scales": (i32, [vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -145,13 +149,18 @@ class Pool:
     """
 
     def __init__(self, num_layers: int, num_blocks: int, block_size: int, num_heads: int, head_dim: int,
-                 layout: str = "HND", k_pool=None, v_pool=None, initial_free_order: Optional[Sequence[int]] = None):
-        self.desc = PoolDesc(num_layers, num_blocks, block_size, num_heads, head_dim, LAYOUTS[layout])
+                 layout: str = "HND", k_pool=None, v_pool=None, initial_free_order: Optional[Sequence[int]] = None,
+                 kv_dtype: str = "f16", k_scale=None, v_scale=None):
+        self.desc = PoolDesc(num_layers, num_blocks, block_size, num_heads, head_dim, LAYOUTS[layout],
+                             KV_DTYPES[kv_dtype])
         self.layout = layout
+        self.kv_dtype = kv_dtype
         self.k_pool, self.v_pool = k_pool, v_pool
+        self.k_scale, self.v_scale = k_scale, v_scale
         if k_pool is not None:
-            _require(k_pool, "float16", "k_pool")
-            _require(v_pool, "float16", "v_pool")
+            el = "float16" if kv_dtype == "f16" else "uint8"
+            _require(k_pool, el, "k_pool")
+            _require(v_pool, el, "v_pool")
             want = num_layers * num_blocks * block_size * num_heads * head_dim
             if k_pool.numel() != want or v_pool.numel() != want:
                 raise ValueError(f"pool tensors must hold {want} elements")
@@ -164,6 +173,13 @@ class Pool:
         check(lib().pkv_pool_create(ctypes.byref(self.desc), _ptr(k_pool), _ptr(v_pool), _ptr(order),
                                     ctypes.byref(h)))
         self._h = h
+        if k_scale is not None:
+            _require(k_scale, "float32", "k_scale")
+            _require(v_scale, "float32", "v_scale")
+            want = num_layers * num_blocks * num_heads * block_size
+            if k_scale.numel() != want or v_scale.numel() != want:
+                raise ValueError(f"scale pools must hold {want} elements")
+            check(lib().pkv_pool_set_scales(self._h, _ptr(k_scale), _ptr(v_scale)))
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

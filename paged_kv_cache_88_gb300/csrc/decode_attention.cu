@@ -48,6 +48,7 @@
 
 #include "pkv_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace {
 
@@ -72,7 +73,11 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;   // + one producer warp
 constexpr int kGroups = kConsumerWarps * 4;       // 8-lane groups
 constexpr int kTokPerGroup = kTile / kGroups;     // rows of a tile one group owns
-constexpr int kStages = PKV_ATTN_STAGES;
+constexpr int kStagesF16 = PKV_ATTN_STAGES;
+#ifndef PKV_ATTN_STAGES_Q8
+#define PKV_ATTN_STAGES_Q8 4
+#endif
+constexpr int kStagesQ8 = PKV_ATTN_STAGES_Q8;
 static_assert(kTile % kGroups == 0 && kTokPerGroup >= 1 && kTokPerGroup <= 4, "tile / group split");
 constexpr int kMaxSeqs = 4096;
 constexpr int kMaxCtasPerSm = 8;     // bound used to size the workspace
@@ -92,31 +97,39 @@ struct Params {
     const uint4 *k_new;  // [S][H][D] fp16 as 16-byte words
     const uint4 *v_new;
     const int64_t *slots;  // [S]
-    uint4 *k_layer;      // this layer's pools, as 16-byte words
-    uint4 *v_layer;
+    unsigned char *k_layer;  // this layer's pools (fp16 elements or E4M3 codes)
+    unsigned char *v_layer;
+    float *k_scale;      // quantised cache: this layer's per-(token, head) scales, [N][H][B]
+    float *v_scale;
     int32_t S, H, max_blocks, B, N, layout;
     float scale_log2;    // scale * log2(e)
 };
 
-__host__ __device__ constexpr int stage_bytes(int D) {
-    // K tile + V tile + the query row, rounded to 128 bytes
-    return ((2 * kTile * D * 2 + D * 2) + 127) / 128 * 128;
-}
+// Shape of one pipeline stage: [K tile][V tile][q row][K scales][V scales].
+// Q8 = the cache holds E4M3 codes with a scale per (token, head) row.
+template <int D, bool Q8>
+struct Stage {
+    static constexpr int kElem = Q8 ? 1 : 2;          // bytes per K/V element
+    static constexpr int kRow = D * kElem;            // bytes per token row
+    static constexpr int kTileBytes = kTile * kRow;   // one K (or V) tile
+    static constexpr int kQ = 2 * kTileBytes;         // offset of the query row (fp16)
+    static constexpr int kScales = kQ + D * 2;        // offset of the K scales, then the V scales
+    static constexpr int kBytes = ((kScales + (Q8 ? 2 * kTile * 4 : 0)) + 127) / 128 * 128;
+    static constexpr int kStages = Q8 ? kStagesQ8 : kStagesF16;
+};
 
 __host__ __device__ constexpr int piece_stride(int D) { return D + 4; }
 
 // Shared memory: [stages][reduction][seq arrays][barriers + flags]
-__host__ size_t smem_bytes(int D, int S) {
-    size_t b = (size_t)kStages * stage_bytes(D);
-    b += (size_t)kConsumerWarps * (D + 2) * sizeof(float);
-    b += (size_t)(2 * S + 2) * sizeof(int32_t);
-    b = (b + 15) / 16 * 16;
-    b += 2 * kStages * sizeof(uint64_t) + 16;
-    return b + 128;  // slack to align the base to 128 bytes (TMA destination)
+template <int D, bool Q8>
+__host__ __device__ constexpr size_t smem_bytes_t(int S) {
+    return ((size_t)Stage<D, Q8>::kStages * Stage<D, Q8>::kBytes + (size_t)kConsumerWarps * (D + 2) * sizeof(float) +
+            (size_t)(2 * S + 2) * sizeof(int32_t) + 15) / 16 * 16 +
+           2 * Stage<D, Q8>::kStages * sizeof(uint64_t) + 16 + 128;  // + slack to align the base to 128 bytes
 }
 
 struct Smem {
-    unsigned char *stage;  // kStages * stage_bytes(D)
+    unsigned char *stage;  // kStages * stage bytes
     float *red_o;          // [kConsumerWarps][D]
     float *red_m;          // [kConsumerWarps]
     float *red_l;          // [kConsumerWarps]
@@ -127,12 +140,13 @@ struct Smem {
     volatile int32_t *flags;  // [0] = timed out, [1] = last-arriver flag
 };
 
-template <int D>
+template <int D, bool Q8>
 __device__ __forceinline__ Smem carve(unsigned char *raw, int S) {
+    constexpr int NS = Stage<D, Q8>::kStages;
     Smem m;
     uintptr_t p = (reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127);
     m.stage = reinterpret_cast<unsigned char *>(p);
-    p += (size_t)kStages * stage_bytes(D);
+    p += (size_t)NS * Stage<D, Q8>::kBytes;
     m.red_o = reinterpret_cast<float *>(p);
     p += (size_t)kConsumerWarps * D * sizeof(float);
     m.red_m = reinterpret_cast<float *>(p);
@@ -145,9 +159,17 @@ __device__ __forceinline__ Smem carve(unsigned char *raw, int S) {
     p += (size_t)(S + 1) * sizeof(int32_t);
     p = (p + 15) & ~uintptr_t(15);
     m.full = reinterpret_cast<uint64_t *>(p);
-    m.empty = m.full + kStages;
-    m.flags = reinterpret_cast<volatile int32_t *>(m.empty + kStages);
+    m.empty = m.full + NS;
+    m.flags = reinterpret_cast<volatile int32_t *>(m.empty + NS);
     return m;
+}
+
+// Element index of chunk ch (8 consecutive elements) of the row owned by lane j
+// of a group. fp16 rows: the 8 lanes read 128 contiguous bytes per chunk; E4M3
+// rows (half as many bytes): lane j owns D/8 contiguous elements, one load.
+template <int D, bool Q8>
+__device__ __forceinline__ int chunk_elem(int j, int ch) {
+    return Q8 ? j * (D / 8) + ch * 8 : ch * 64 + j * 8;
 }
 
 // Position in the CTA's tile range: sequence, head, tile of the (s, h).
@@ -212,14 +234,16 @@ __device__ __forceinline__ bool wait_phase(const Smem &sm, uint32_t bar, uint32_
     }
 }
 
-template <int D>
+template <int D, bool Q8>
 __global__ void __launch_bounds__(kThreads, D >= 256 ? 1 : PKV_ATTN_MIN_CTAS)
 decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const Params p) {
-    constexpr int NCH = D / 64;  // 16-byte chunks per lane per row
-    constexpr int SB = stage_bytes(D);
+    using St = Stage<D, Q8>;
+    constexpr int NCH = D / 64;      // chunks of 8 elements per lane per row
+    constexpr int SB = St::kBytes;
+    constexpr int NS = St::kStages;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const Smem sm = carve<D>(smem_raw, p.S);
+    const Smem sm = carve<D, Q8>(smem_raw, p.S);
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -230,7 +254,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     // and the tile prefix over sequences
     ptx::launch_dependents();
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < NS; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sm.full[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&sm.empty[i]), kConsumerWarps);
         }
@@ -298,15 +322,16 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         // ================= producer warp
         const int32_t B = p.B;
         const int32_t rows = B < kTile ? B : kTile;           // rows per TMA box
-        const uint32_t box_bytes = (uint32_t)rows * D * 2;
-        constexpr int W = D / 8;                              // 16-byte words per row
+        const uint32_t box_bytes = (uint32_t)rows * St::kRow;
+        const uint32_t scale_bytes = (uint32_t)rows * 4;
+        constexpr int W = D / 8;                              // 16-byte fp16 words per new row
         constexpr int NW = (2 * W + 31) / 32;                 // words of the new K+V rows per lane
         Cursor c = locate(sm, S, H, g0);
         int32_t win_s = -1, win_lb0 = 0, win_val = 0;
         uint4 nw[NW];                                         // the new token's K/V row words
         int64_t new_slot = -1;                                // pending append of the current (s, h)
         for (int32_t k = 0; k < n; ++k) {
-            const int32_t stage = k % kStages;
+            const int32_t stage = k % NS;
             if (p.k_new != nullptr && ((k == 0) || (c.t == 0))) {
                 // a new (s, h): if its last tile is ours, fetch the appended token's rows now
                 const int32_t seg_last = sm.base[c.s] + c.h * c.nt + c.nt - 1;
@@ -321,23 +346,39 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                     }
                 }
             }
-            if (k >= kStages) {
-                const uint32_t parity = ((k / kStages) - 1) & 1;
+            if (k >= NS) {
+                const uint32_t parity = ((k / NS) - 1) & 1;
                 wait_phase(sm, empty0 + 8 * stage, parity, p.status);
             }
             if (new_slot >= 0 && c.t == c.nt - 1) {
-                // the tile holding the new token: store its rows, then order the
-                // generic-proxy stores before the tile's TMA (async-proxy) read
+                // the tile holding the new token: store its rows (quantised for an
+                // E4M3 cache), then order the generic-proxy stores before the
+                // tile's TMA (async-proxy) read
                 if (new_slot < (int64_t)p.N * p.B) {
                     const int64_t blk = new_slot / p.B, off = new_slot - blk * p.B;
                     const int64_t row = p.layout == PKV_LAYOUT_NHD ? (blk * p.B + off) * H + c.h
                                                                    : (blk * H + c.h) * p.B + off;
+                    if constexpr (Q8) {
+                        // one lane per 8 elements; the W lanes of a row reduce its amax
+                        const int wi = lane;                   // NW == 1 for D <= 128
+                        float mm = q8::amax_word(nw[0]);
 #pragma unroll
-                    for (int i = 0; i < NW; ++i) {
-                        const int wi = lane + 32 * i;
+                        for (int o = 1; o < W; o <<= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+                        const float scale = q8::row_scale(mm);
                         if (wi < 2 * W) {
-                            if (wi < W) p.k_layer[row * W + wi] = nw[i];
-                            else p.v_layer[row * W + wi - W] = nw[i];
+                            const uint2 codes = q8::quantize_word(nw[0], scale);
+                            unsigned char *base = wi < W ? p.k_layer : p.v_layer;
+                            reinterpret_cast<uint2 *>(base + row * D)[wi % W] = codes;
+                            if (wi % W == 0) (wi < W ? p.k_scale : p.v_scale)[row] = scale;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < NW; ++i) {
+                            const int wi = lane + 32 * i;
+                            if (wi < 2 * W) {
+                                unsigned char *base = wi < W ? p.k_layer : p.v_layer;
+                                reinterpret_cast<uint4 *>(base + row * D * 2)[wi % W] = nw[i];
+                            }
                         }
                     }
                     ptx::fence_proxy_async_global();
@@ -360,7 +401,8 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 win_val = e < p.max_blocks ? __ldg(p.tables + (size_t)c.s * p.max_blocks + e) : 0;
             }
             const bool first = (k == 0) || (c.t == 0);
-            const uint32_t bytes = (uint32_t)nbox * box_bytes * 2 + (first ? D * 2 : 0);
+            const uint32_t bytes =
+                (uint32_t)nbox * (box_bytes * 2 + (Q8 ? scale_bytes * 2 : 0)) + (first ? D * 2 : 0);
             const uint32_t dst = stage0 + stage * SB;
             const uint32_t bar = full0 + 8 * stage;
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar, bytes);
@@ -380,11 +422,16 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                         y = (blk * H + c.h) * B + r0;
                     }
                     ptx::tma_load_2d(dst + i * box_bytes, &kmap, x, y, bar);
-                    ptx::tma_load_2d(dst + kTile * D * 2 + i * box_bytes, &vmap, x, y, bar);
+                    ptx::tma_load_2d(dst + St::kTileBytes + i * box_bytes, &vmap, x, y, bar);
+                    if constexpr (Q8) {   // the rows' scales ([N][H][B] layout: rows contiguous)
+                        ptx::bulk_load(dst + St::kScales + i * scale_bytes, p.k_scale + y, scale_bytes, bar);
+                        ptx::bulk_load(dst + St::kScales + kTile * 4 + i * scale_bytes, p.v_scale + y, scale_bytes,
+                                       bar);
+                    }
                 }
             }
             if (lane == 0 && first)
-                ptx::bulk_load(dst + 2 * kTile * D * 2, p.q + ((size_t)c.s * H + c.h) * D, D * 2, bar);
+                ptx::bulk_load(dst + St::kQ, p.q + ((size_t)c.s * H + c.h) * D, D * 2, bar);
             __syncwarp();
             advance(c, sm, S, H);
         }
@@ -400,19 +447,18 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     float m = -INFINITY, l = 0.f;             // running max (log2 units) and sum
     Cursor c = locate(sm, S, H, g0);
     int32_t seg_g0 = g0;                      // first tile of the current (s, h) inside this CTA
-    const uint32_t lane_off = (uint32_t)j * 16;  // byte offset of this lane's 16 B inside a 128 B chunk
 
     for (int32_t k = 0; k < n; ++k) {
-        const int32_t stage = k % kStages;
+        const int32_t stage = k % NS;
         const uint32_t kb = stage0 + stage * SB;             // K tile (shared address)
-        const uint32_t vb = kb + kTile * D * 2;              // V tile
-        wait_phase(sm, full0 + 8 * stage, (k / kStages) & 1, p.status);
+        const uint32_t vb = kb + St::kTileBytes;             // V tile
+        wait_phase(sm, full0 + 8 * stage, (k / NS) & 1, p.status);
         const bool first = (k == 0) || (c.t == 0);
         const int32_t ntok = min(kTile, sm.len[c.s] - c.t * kTile);
         if (first) {
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
-                const uint4 raw = ptx::lds128(vb + kTile * D * 2 + ch * 128 + lane_off);
+                const uint4 raw = ptx::lds128(kb + St::kQ + chunk_elem<D, Q8>(j, ch) * 2);
                 const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) ptx::split_half2(wv[e], qlo[ch * 4 + e], qhi[ch * 4 + e]);
@@ -423,22 +469,51 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             l = 0.f;
             seg_g0 = g0 + k;
         }
-        // this group's rows of the tile: grp, grp + kGroups, ...
+        // this group's rows of the tile: grp, grp + kGroups, ...; kr/vr hold each
+        // chunk's 8 elements as four fp16 pairs
         const bool full = ntok == kTile;
         bool vld[kTokPerGroup];
-        uint4 kr[kTokPerGroup][NCH], vr[kTokPerGroup][NCH];
+        uint32_t kr[kTokPerGroup][NCH][4], vr[kTokPerGroup][NCH][4];
+        float ksc[kTokPerGroup], vsc[kTokPerGroup];
 #pragma unroll
         for (int u = 0; u < kTokPerGroup; ++u) {
-            vld[u] = full || grp + kGroups * u < ntok;
+            const int row = grp + kGroups * u;
+            vld[u] = full || row < ntok;
+            if constexpr (Q8) {
+                uint32_t kc[NCH * 2], vc[NCH * 2];   // 4 codes per word
+                if constexpr (NCH == 2) {
+                    const uint4 a = ptx::lds128(kb + row * St::kRow + j * 16);
+                    const uint4 b = ptx::lds128(vb + row * St::kRow + j * 16);
+                    kc[0] = a.x; kc[1] = a.y; kc[2] = a.z; kc[3] = a.w;
+                    vc[0] = b.x; vc[1] = b.y; vc[2] = b.z; vc[3] = b.w;
+                } else {
+                    const uint2 a = ptx::lds64(kb + row * St::kRow + j * 8);
+                    const uint2 b = ptx::lds64(vb + row * St::kRow + j * 8);
+                    kc[0] = a.x; kc[1] = a.y;
+                    vc[0] = b.x; vc[1] = b.y;
+                }
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch)
-                kr[u][ch] = ptx::lds128(kb + (grp + kGroups * u) * D * 2 + ch * 128 + lane_off);
+                for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int w = ch * 2 + (e >> 1), sh = 16 * (e & 1);
+                        kr[u][ch][e] = q8::e4m3x2_to_half2(kc[w] >> sh);
+                        vr[u][ch][e] = q8::e4m3x2_to_half2(vc[w] >> sh);
+                    }
+                ksc[u] = ptx::ldsf(kb + St::kScales + row * 4);
+                vsc[u] = ptx::ldsf(kb + St::kScales + kTile * 4 + row * 4);
+            } else {
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const uint4 a = ptx::lds128(kb + row * St::kRow + chunk_elem<D, Q8>(j, ch) * 2);
+                    const uint4 b = ptx::lds128(vb + row * St::kRow + chunk_elem<D, Q8>(j, ch) * 2);
+                    kr[u][ch][0] = a.x; kr[u][ch][1] = a.y; kr[u][ch][2] = a.z; kr[u][ch][3] = a.w;
+                    vr[u][ch][0] = b.x; vr[u][ch][1] = b.y; vr[u][ch][2] = b.z; vr[u][ch][3] = b.w;
+                }
+                ksc[u] = 1.f;
+                vsc[u] = 1.f;
+            }
         }
-#pragma unroll
-        for (int u = 0; u < kTokPerGroup; ++u)
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch)
-                vr[u][ch] = ptx::lds128(vb + (grp + kGroups * u) * D * 2 + ch * 128 + lane_off);
         float x[kTokPerGroup];
         float mx = -INFINITY;
 #pragma unroll
@@ -446,11 +521,10 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
-                const uint32_t wk[4] = {kr[u][ch].x, kr[u][ch].y, kr[u][ch].z, kr[u][ch].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     uint16_t klo, khi;
-                    ptx::split_half2(wk[e], klo, khi);
+                    ptx::split_half2(kr[u][ch][e], klo, khi);
                     a0 = ptx::fma_f16_f32(qlo[ch * 4 + e], klo, a0);
                     a1 = ptx::fma_f16_f32(qhi[ch * 4 + e], khi, a1);
                 }
@@ -459,6 +533,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             dot += __shfl_xor_sync(0xffffffffu, dot, 4);
             dot += __shfl_xor_sync(0xffffffffu, dot, 2);
             dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+            if constexpr (Q8) dot *= ksc[u];
             x[u] = vld[u] ? dot * p.scale_log2 : -INFINITY;
             mx = fmaxf(mx, x[u]);
         }
@@ -475,30 +550,27 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         for (int u = 0; u < kTokPerGroup; ++u) {
             pw[u] = vld[u] ? ptx::ex2(x[u] - m) : 0.f;
             l += pw[u];
+            if constexpr (Q8) pw[u] *= vsc[u];   // the V row's scale folds into its weight
         }
         if (full) {
 #pragma unroll
             for (int u = 0; u < kTokPerGroup; ++u)
 #pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    const uint32_t wv[4] = {vr[u][ch].x, vr[u][ch].y, vr[u][ch].z, vr[u][ch].w};
+                for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(wv[e]),
+                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(vr[u][ch][e]),
                                                    o[ch * 4 + e]);
-                }
         } else {
 #pragma unroll
             for (int u = 0; u < kTokPerGroup; ++u) {
                 if (!vld[u]) continue;
 #pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    const uint32_t wv[4] = {vr[u][ch].x, vr[u][ch].y, vr[u][ch].z, vr[u][ch].w};
+                for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(wv[e]),
+                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(vr[u][ch][e]),
                                                    o[ch * 4 + e]);
-                }
             }
         }
         __syncwarp();
@@ -526,7 +598,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             if (lane < 8) {
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch) {
-                    float4 *dst = reinterpret_cast<float4 *>(sm.red_o + warp * D + ch * 64 + j * 8);
+                    float4 *dst = reinterpret_cast<float4 *>(sm.red_o + warp * D + chunk_elem<D, Q8>(j, ch));
                     dst[0] = make_float4(o[ch * 4 + 0].x, o[ch * 4 + 0].y, o[ch * 4 + 1].x, o[ch * 4 + 1].y);
                     dst[1] = make_float4(o[ch * 4 + 2].x, o[ch * 4 + 2].y, o[ch * 4 + 3].x, o[ch * 4 + 3].y);
                 }
@@ -653,54 +725,62 @@ EncodeTiledFn encode_fn() {
 
 struct DeviceInfo {
     int num_sms = 0;
-    int ctas_per_sm[3] = {0, 0, 0};  // per head_dim 64/128/256, at the smem size last queried
-    size_t smem_for[3] = {0, 0, 0};
+    int ctas_per_sm[6] = {0, 0, 0, 0, 0, 0};  // per (head_dim 64/128/256, fp16/E4M3), at the smem size last queried
+    size_t smem_for[6] = {0, 0, 0, 0, 0, 0};
 };
 
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-int dim_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : 2); }
+int variant_index(int D, bool q8) { return (D == 64 ? 0 : (D == 128 ? 1 : 2)) * 2 + (q8 ? 1 : 0); }
 
-template <int D>
-const void *kernel_ptr() {
-    return reinterpret_cast<const void *>(&decode_attention_kernel<D>);
-}
+bool variant_built(int D, bool q8) { return supported_head_dim(D) && (!q8 || D <= 128); }
 
-const void *kernel_for(int D) {
+const void *kernel_for(int D, bool q8) {
+    if (q8) return D == 64 ? reinterpret_cast<const void *>(&decode_attention_kernel<64, true>)
+                           : reinterpret_cast<const void *>(&decode_attention_kernel<128, true>);
     switch (D) {
-        case 64: return kernel_ptr<64>();
-        case 128: return kernel_ptr<128>();
-        default: return kernel_ptr<256>();
+        case 64: return reinterpret_cast<const void *>(&decode_attention_kernel<64, false>);
+        case 128: return reinterpret_cast<const void *>(&decode_attention_kernel<128, false>);
+        default: return reinterpret_cast<const void *>(&decode_attention_kernel<256, false>);
     }
 }
 
-// SMs and resident CTAs per SM for head_dim D with S sequences on `dev`.
-pkv_status launch_shape(int dev, int D, int S, int *grid, int *per_sm, int *sms, size_t *smem) {
+size_t smem_bytes(int D, bool q8, int S) {
+    if (q8) return D == 64 ? smem_bytes_t<64, true>(S) : smem_bytes_t<128, true>(S);
+    switch (D) {
+        case 64: return smem_bytes_t<64, false>(S);
+        case 128: return smem_bytes_t<128, false>(S);
+        default: return smem_bytes_t<256, false>(S);
+    }
+}
+
+// SMs and resident CTAs per SM for head_dim D (fp16 or E4M3 cache) with S sequences on `dev`.
+pkv_status launch_shape(int dev, int D, bool q8, int S, int *grid, int *per_sm, int *sms, size_t *smem) {
     if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_CUDA, "device index %d", dev);
-    const size_t bytes = smem_bytes(D, S);
+    const size_t bytes = smem_bytes(D, q8, S);
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo &di = g_dev[dev];
     if (di.num_sms == 0) {
         if (cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return fail(PKV_ERR_CUDA, "cudaDeviceGetAttribute failed");
     }
-    const int di_ix = dim_index(D);
-    if (di.smem_for[di_ix] != bytes) {
-        cudaError_t e = cudaFuncSetAttribute(kernel_for(D), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int vi = variant_index(D, q8);
+    if (di.smem_for[vi] != bytes) {
+        cudaError_t e = cudaFuncSetAttribute(kernel_for(D, q8), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)std::max<size_t>(bytes, 48 * 1024));
         if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel_for(D), kThreads, bytes);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel_for(D, q8), kThreads, bytes);
         if (e != cudaSuccess || occ < 1)
             return fail(PKV_ERR_CUDA, "occupancy query failed (%s, %d)", cudaGetErrorString(e), occ);
-        di.ctas_per_sm[di_ix] = std::min(occ, kMaxCtasPerSm);
-        di.smem_for[di_ix] = bytes;
+        di.ctas_per_sm[vi] = std::min(occ, kMaxCtasPerSm);
+        di.smem_for[vi] = bytes;
     }
-    *per_sm = di.ctas_per_sm[di_ix];
+    *per_sm = di.ctas_per_sm[vi];
     *sms = di.num_sms;
-    *grid = di.num_sms * di.ctas_per_sm[di_ix];
+    *grid = di.num_sms * di.ctas_per_sm[vi];
     *smem = bytes;
     return PKV_OK;
 }
@@ -715,22 +795,24 @@ size_t workspace_bytes_for(int S, int H, int D, int num_sms) {
     return pieces_offset(S, H) + (size_t)num_sms * kMaxCtasPerSm * 2 * piece_stride(D) * sizeof(float);
 }
 
-pkv_status encode_map(CUtensorMap *map, const void *base, int N, int B, int H, int D, int layout) {
+pkv_status encode_map(CUtensorMap *map, const void *base, int N, int B, int H, int D, int layout, bool q8) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t elem = q8 ? 1 : 2;
     cuuint64_t dims[2], strides[1];
     if (layout == PKV_LAYOUT_NHD) {
         dims[0] = (cuuint64_t)H * D;
         dims[1] = (cuuint64_t)N * B;
-        strides[0] = (cuuint64_t)H * D * 2;
+        strides[0] = (cuuint64_t)H * D * elem;
     } else {
         dims[0] = (cuuint64_t)D;
         dims[1] = (cuuint64_t)N * H * B;
-        strides[0] = (cuuint64_t)D * 2;
+        strides[0] = (cuuint64_t)D * elem;
     }
     const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)std::min(B, kTile)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = fn(map, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -765,7 +847,7 @@ pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t *g
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(PKV_ERR_CUDA, "no CUDA device");
     int g = 0, per = 0, sms = 0;
     size_t smem = 0;
-    pkv_status st = launch_shape(dev, head_dim, num_seqs, &g, &per, &sms, &smem);
+    pkv_status st = launch_shape(dev, head_dim, false, num_seqs, &g, &per, &sms, &smem);
     if (st != PKV_OK) return st;
     if (grid_ctas) *grid_ctas = g;
     if (ctas_per_sm) *ctas_per_sm = per;
@@ -784,11 +866,16 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
                                  const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
                                  int32_t num_seqs, float scale, void *out, void *workspace, size_t workspace_bytes,
                                  void *stream, const void *k_new, const void *v_new, const int64_t *slots,
-                                 uint32_t *status_override = nullptr) {
+                                 uint32_t *status_override = nullptr, const float *k_scale = nullptr,
+                                 const float *v_scale = nullptr) {
+    const bool q8 = k_scale != nullptr;
     if (num_seqs < 0 || num_seqs > kMaxSeqs)
         return fail(PKV_ERR_INVALID_ARG, "num_seqs %d outside [0, %d]", num_seqs, kMaxSeqs);
     if (num_seqs == 0) return PKV_OK;
-    if (!supported_head_dim(head_dim)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d", head_dim);
+    if (!variant_built(head_dim, q8))
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d%s", head_dim, q8 ? " with an E4M3 cache" : "");
+    if (q8 && (layout != PKV_LAYOUT_HND || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+        return fail(PKV_ERR_INVALID_ARG, "an E4M3 cache needs the HND layout and 16-byte aligned scale pools");
     if (!supported_block_size(block_size)) return fail(PKV_ERR_UNSUPPORTED, "block_size %d", block_size);
     if (layout != PKV_LAYOUT_NHD && layout != PKV_LAYOUT_HND) return fail(PKV_ERR_INVALID_ARG, "layout %d", layout);
     if (num_heads < 1 || num_blocks < 1 || max_blocks < 1) return fail(PKV_ERR_INVALID_ARG, "sizes must be >= 1");
@@ -806,16 +893,16 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(PKV_ERR_CUDA, "no CUDA device");
     int grid = 0, per = 0, sms = 0;
     size_t smem = 0;
-    pkv_status st = launch_shape(dev, head_dim, num_seqs, &grid, &per, &sms, &smem);
+    pkv_status st = launch_shape(dev, head_dim, q8, num_seqs, &grid, &per, &sms, &smem);
     if (st != PKV_OK) return st;
     const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, sms);
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", workspace_bytes, need);
 
     CUtensorMap kmap, vmap;
-    st = encode_map(&kmap, k_cache, num_blocks, block_size, num_heads, head_dim, layout);
+    st = encode_map(&kmap, k_cache, num_blocks, block_size, num_heads, head_dim, layout, q8);
     if (st != PKV_OK) return st;
-    st = encode_map(&vmap, v_cache, num_blocks, block_size, num_heads, head_dim, layout);
+    st = encode_map(&vmap, v_cache, num_blocks, block_size, num_heads, head_dim, layout, q8);
     if (st != PKV_OK) return st;
 
     Params prm;
@@ -838,15 +925,26 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     prm.k_new = static_cast<const uint4 *>(k_new);
     prm.v_new = static_cast<const uint4 *>(v_new);
     prm.slots = slots;
-    prm.k_layer = static_cast<uint4 *>(const_cast<void *>(k_cache));
-    prm.v_layer = static_cast<uint4 *>(const_cast<void *>(v_cache));
+    prm.k_layer = static_cast<unsigned char *>(const_cast<void *>(k_cache));
+    prm.v_layer = static_cast<unsigned char *>(const_cast<void *>(v_cache));
+    prm.k_scale = const_cast<float *>(k_scale);
+    prm.v_scale = const_cast<float *>(v_scale);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    switch (head_dim) {
-        case 64: e = launch_pdl(decode_attention_kernel<64>, grid, kThreads, smem, s, kmap, vmap, prm); break;
-        case 128: e = launch_pdl(decode_attention_kernel<128>, grid, kThreads, smem, s, kmap, vmap, prm); break;
-        default: e = launch_pdl(decode_attention_kernel<256>, grid, kThreads, smem, s, kmap, vmap, prm); break;
+    if (q8) {
+        e = head_dim == 64 ? launch_pdl(decode_attention_kernel<64, true>, grid, kThreads, smem, s, kmap, vmap, prm)
+                           : launch_pdl(decode_attention_kernel<128, true>, grid, kThreads, smem, s, kmap, vmap, prm);
+    } else {
+        switch (head_dim) {
+            case 64: e = launch_pdl(decode_attention_kernel<64, false>, grid, kThreads, smem, s, kmap, vmap, prm); break;
+            case 128:
+                e = launch_pdl(decode_attention_kernel<128, false>, grid, kThreads, smem, s, kmap, vmap, prm);
+                break;
+            default:
+                e = launch_pdl(decode_attention_kernel<256, false>, grid, kThreads, smem, s, kmap, vmap, prm);
+                break;
+        }
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "decode attention launch: %s", cudaGetErrorString(e));
@@ -880,11 +978,13 @@ pkv_status pkv_decode_append_attention(const pkv_pool *pool, int32_t layer, cons
         return fail(PKV_ERR_INVALID_ARG, "NULL k_new, v_new or slot_mapping");
     if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
         return fail(PKV_ERR_INVALID_ARG, "k_new/v_new must be 16-byte aligned, slot_mapping 8-byte aligned");
-    const size_t off = (size_t)layer * layer_elems(d) * 2;
-    return decode_attention_impl(q, static_cast<const char *>(pool->k_pool) + off,
-                                 static_cast<const char *>(pool->v_pool) + off, d.num_blocks, d.block_size,
-                                 d.num_heads, d.head_dim, d.layout, block_tables, max_blocks, context_lens, num_seqs,
-                                 scale, out, workspace, workspace_bytes, stream, k_new, v_new, slot_mapping);
+    const PoolLayer pl = pool_layer(pool, layer);
+    if (pool->desc.kv_dtype == PKV_KV_E4M3 && !pl.k_scale)
+        return fail(PKV_ERR_INVALID_ARG, "E4M3 pool without scale pools (pkv_pool_set_scales)");
+    return decode_attention_impl(q, pl.k, pl.v, d.num_blocks, d.block_size, d.num_heads, d.head_dim, d.layout,
+                                 block_tables, max_blocks, context_lens, num_seqs, scale, out, workspace,
+                                 workspace_bytes, stream, k_new, v_new, slot_mapping, nullptr, pl.k_scale,
+                                 pl.v_scale);
 }
 
 pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const void *q, const int32_t *block_tables,
@@ -894,11 +994,12 @@ pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const 
     const pkv_pool_desc &d = pool->desc;
     if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
     if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
-    const size_t off = (size_t)layer * layer_elems(d) * 2;
-    return pkv_decode_attention(q, static_cast<const char *>(pool->k_pool) + off,
-                                static_cast<const char *>(pool->v_pool) + off, d.num_blocks, d.block_size,
-                                d.num_heads, d.head_dim, d.layout, block_tables, max_blocks, context_lens, num_seqs,
-                                scale, out, workspace, workspace_bytes, stream);
+    const PoolLayer pl = pool_layer(pool, layer);
+    if (pool->desc.kv_dtype == PKV_KV_E4M3 && !pl.k_scale)
+        return fail(PKV_ERR_INVALID_ARG, "E4M3 pool without scale pools (pkv_pool_set_scales)");
+    return decode_attention_impl(q, pl.k, pl.v, d.num_blocks, d.block_size, d.num_heads, d.head_dim, d.layout,
+                                 block_tables, max_blocks, context_lens, num_seqs, scale, out, workspace,
+                                 workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr, pl.k_scale, pl.v_scale);
 }
 
 }  // extern "C"

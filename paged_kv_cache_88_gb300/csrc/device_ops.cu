@@ -9,6 +9,7 @@
 
 #include "pkv_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace {
 
@@ -50,11 +51,52 @@ append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, 
     }
 }
 
+// E4M3 cache: one warp per (token, head). Lanes 0..W-1 hold the K row's
+// 16-byte fp16 words, lanes W..2W-1 the V row's (W = D/8 <= 16); each row's
+// amax is reduced over its W lanes, then each lane stores its 8 codes and the
+// first lane of a row the row's scale.
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads)
+append_q8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, const int64_t *__restrict__ slots,
+                 int32_t num_tokens, unsigned char *__restrict__ k_layer, unsigned char *__restrict__ v_layer,
+                 float *__restrict__ k_scale, float *__restrict__ v_scale, int64_t num_slots, int32_t B, int32_t H,
+                 uint32_t *status) {
+    constexpr int W = D / 8;
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)num_tokens * H;
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
+         r += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const int64_t i = r / H;
+        const int32_t h = (int32_t)(r - i * H);
+        const int64_t slot = slots[i];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (lane == 0 && h == 0 && status) atomicOr(status, PKV_DEV_BAD_SLOT);
+            continue;
+        }
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (lane < 2 * W) w = lane < W ? k_new[r * W + lane] : v_new[r * W + lane - W];
+        float m = q8::amax_word(w);
+#pragma unroll
+        for (int o = 1; o < W; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float scale = q8::row_scale(m);
+        if (lane < 2 * W) {
+            const int64_t blk = slot / B, off = slot - blk * B;
+            const int64_t row = (blk * H + h) * B + off;
+            reinterpret_cast<uint2 *>((lane < W ? k_layer : v_layer) + row * D)[lane % W] = q8::quantize_word(w, scale);
+            if (lane % W == 0) (lane < W ? k_scale : v_scale)[row] = scale;
+        }
+    }
+}
+
 // Block dst <- block src in every layer, K and V (hnwysp.cn/news/103996 §3.3).
 // grid.y walks (pair, layer); grid.x and the unrolled loop walk the block's words.
 __global__ void __launch_bounds__(kCopyThreads)
 copy_blocks_kernel(const int32_t *__restrict__ pairs, int32_t num_pairs, uint4 *k_pool, uint4 *v_pool,
-                   int32_t num_layers, int32_t num_blocks, int64_t block_words, uint32_t *status) {
+                   int32_t num_layers, int32_t num_blocks, int64_t block_words, uint4 *k_scale, uint4 *v_scale,
+                   int64_t scale_words, uint32_t *status) {
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
     const int64_t jobs = (int64_t)num_pairs * num_layers;
@@ -70,6 +112,14 @@ copy_blocks_kernel(const int32_t *__restrict__ pairs, int32_t num_pairs, uint4 *
         const int64_t sbase = ((int64_t)layer * num_blocks + src) * block_words;
         const int64_t dbase = ((int64_t)layer * num_blocks + dst) * block_words;
         const int64_t step = (int64_t)gridDim.x * blockDim.x;
+        if (k_scale) {  // E4M3 cache: the block's row scales, H * B floats per layer
+            const int64_t ss = ((int64_t)layer * num_blocks + src) * scale_words;
+            const int64_t sd = ((int64_t)layer * num_blocks + dst) * scale_words;
+            for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < scale_words; w += step) {
+                k_scale[sd + w] = k_scale[ss + w];
+                v_scale[sd + w] = v_scale[ss + w];
+            }
+        }
         for (int64_t w0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w0 < block_words; w0 += step * kCopyUnroll) {
             uint4 kb[kCopyUnroll], vb[kCopyUnroll];
 #pragma unroll
@@ -110,15 +160,28 @@ pkv_status pkv_append(const pkv_pool *pool, int32_t layer, const void *k_new, co
     if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
         return fail(PKV_ERR_INVALID_ARG, "k_new/v_new must be 16-byte aligned, slot_mapping 8-byte aligned");
     const int32_t wpr = d.head_dim / 8;
-    const int64_t total = (int64_t)num_tokens * d.num_heads * wpr;
-    const int64_t want = (total + kAppendThreads - 1) / kAppendThreads;
-    const int grid = (int)(want < 65535 * 16 ? want : 65535 * 16);
-    const size_t off = (size_t)layer * layer_elems(d) * 2;
-    cudaError_t e = launch_pdl(append_kernel, dim3(grid), dim3(kAppendThreads), 0, static_cast<cudaStream_t>(stream),
-                               static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
-                               num_tokens, reinterpret_cast<uint4 *>(static_cast<char *>(pool->k_pool) + off),
-                               reinterpret_cast<uint4 *>(static_cast<char *>(pool->v_pool) + off),
-                               (int64_t)d.num_blocks * d.block_size, d.block_size, d.num_heads, wpr, d.layout, status);
+    const PoolLayer pl = pool_layer(pool, layer);
+    const int64_t nslots = (int64_t)d.num_blocks * d.block_size;
+    cudaError_t e;
+    if (d.kv_dtype == PKV_KV_E4M3) {
+        if (!pl.k_scale) return fail(PKV_ERR_INVALID_ARG, "E4M3 pool without scale pools (pkv_pool_set_scales)");
+        const int64_t warps = (int64_t)num_tokens * d.num_heads;
+        const int64_t want = (warps * 32 + kAppendThreads - 1) / kAppendThreads;
+        const int grid = (int)(want < 65535 * 16 ? want : 65535 * 16);
+        auto kern = d.head_dim == 64 ? append_q8_kernel<64> : append_q8_kernel<128>;
+        e = launch_pdl(kern, dim3(grid), dim3(kAppendThreads), 0, static_cast<cudaStream_t>(stream),
+                       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
+                       reinterpret_cast<unsigned char *>(pl.k), reinterpret_cast<unsigned char *>(pl.v), pl.k_scale,
+                       pl.v_scale, nslots, d.block_size, d.num_heads, status);
+    } else {
+        const int64_t total = (int64_t)num_tokens * d.num_heads * wpr;
+        const int64_t want = (total + kAppendThreads - 1) / kAppendThreads;
+        const int grid = (int)(want < 65535 * 16 ? want : 65535 * 16);
+        e = launch_pdl(append_kernel, dim3(grid), dim3(kAppendThreads), 0, static_cast<cudaStream_t>(stream),
+                       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
+                       reinterpret_cast<uint4 *>(pl.k), reinterpret_cast<uint4 *>(pl.v), nslots, d.block_size,
+                       d.num_heads, wpr, d.layout, status);
+    }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
     return PKV_OK;
@@ -132,7 +195,10 @@ pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *pairs, int32_t n
     if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs < 0");
     if (num_pairs == 0) return PKV_OK;
     if (!pairs || (reinterpret_cast<uintptr_t>(pairs) & 3u)) return fail(PKV_ERR_INVALID_ARG, "bad pairs pointer");
-    const int64_t block_words = (int64_t)d.block_size * d.num_heads * d.head_dim / 8;
+    const bool q8 = d.kv_dtype == PKV_KV_E4M3;
+    if (q8 && !pool->k_scale) return fail(PKV_ERR_INVALID_ARG, "E4M3 pool without scale pools (pkv_pool_set_scales)");
+    const int64_t block_words = (int64_t)d.block_size * d.num_heads * d.head_dim * kv_elem_bytes(d) / 16;
+    const int64_t scale_words = q8 ? (int64_t)d.block_size * d.num_heads * 4 / 16 : 0;
     const int64_t per_row = (int64_t)kCopyThreads * kCopyUnroll;
     int gx = (int)((block_words + per_row - 1) / per_row);
     if (gx < 1) gx = 1;
@@ -141,7 +207,8 @@ pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *pairs, int32_t n
     cudaError_t e = launch_pdl(copy_blocks_kernel, dim3(gx, gy), dim3(kCopyThreads), 0,
                                static_cast<cudaStream_t>(stream), pairs, num_pairs,
                                static_cast<uint4 *>(pool->k_pool), static_cast<uint4 *>(pool->v_pool), d.num_layers,
-                               d.num_blocks, block_words, status);
+                               d.num_blocks, block_words, reinterpret_cast<uint4 *>(pool->k_scale),
+                               reinterpret_cast<uint4 *>(pool->v_scale), scale_words, status);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "copy launch: %s", cudaGetErrorString(e));
     return PKV_OK;

@@ -17,6 +17,8 @@ struct pkv_pool {
     pkv_pool_desc desc;
     void *k_pool;
     void *v_pool;
+    float *k_scale;  // E4M3 cache: per-(token, head) scales [L][N][H][B]; else null
+    float *v_scale;
     // FIFO free queue as a doubly linked list over block ids (-1 = none): O(1)
     // take from the head, return to the tail, and removal of a cached block
     // that a prefix lookup revives.
@@ -39,6 +41,28 @@ void clear_error();
 
 inline int64_t layer_elems(const pkv_pool_desc &d) {
     return (int64_t)d.num_blocks * d.block_size * d.num_heads * d.head_dim;
+}
+
+inline int kv_elem_bytes(const pkv_pool_desc &d) { return d.kv_dtype == PKV_KV_E4M3 ? 1 : 2; }
+
+// One layer's device pointers of a pool.
+struct PoolLayer {
+    char *k;
+    char *v;
+    float *k_scale;  // null for an fp16 cache
+    float *v_scale;
+};
+
+inline PoolLayer pool_layer(const pkv_pool *p, int32_t layer) {
+    const pkv_pool_desc &d = p->desc;
+    const size_t off = (size_t)layer * layer_elems(d) * kv_elem_bytes(d);
+    const size_t soff = (size_t)layer * d.num_blocks * d.num_heads * d.block_size;
+    PoolLayer pl;
+    pl.k = static_cast<char *>(p->k_pool) + off;
+    pl.v = static_cast<char *>(p->v_pool) + off;
+    pl.k_scale = p->k_scale ? p->k_scale + soff : nullptr;
+    pl.v_scale = p->v_scale ? p->v_scale + soff : nullptr;
+    return pl;
 }
 
 inline bool supported_head_dim(int32_t d) { return d == 64 || d == 128 || d == 256; }

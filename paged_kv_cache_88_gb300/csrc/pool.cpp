@@ -103,6 +103,10 @@ pkv_status check_desc(const pkv_pool_desc *d) {
         return fail(PKV_ERR_INVALID_ARG, "layout %d unknown", d->layout);
     if ((int64_t)d->num_blocks * d->block_size * d->num_heads >= (int64_t)1 << 31)
         return fail(PKV_ERR_INVALID_ARG, "num_blocks * block_size * num_heads must be < 2^31");
+    if (d->kv_dtype != PKV_KV_F16 && d->kv_dtype != PKV_KV_E4M3)
+        return fail(PKV_ERR_INVALID_ARG, "kv_dtype %d unknown", d->kv_dtype);
+    if (d->kv_dtype == PKV_KV_E4M3 && (d->layout != PKV_LAYOUT_HND || d->head_dim > 128))
+        return fail(PKV_ERR_UNSUPPORTED, "an E4M3 cache is built for the HND layout and head_dim 64 or 128");
     return PKV_OK;
 }
 
@@ -144,6 +148,8 @@ pkv_status pkv_pool_create(const pkv_pool_desc *desc, void *k_pool, void *v_pool
     p->desc = *desc;
     p->k_pool = k_pool;
     p->v_pool = v_pool;
+    p->k_scale = nullptr;
+    p->v_scale = nullptr;
     p->next.assign(N, -1);
     p->prev.assign(N, -1);
     p->head = p->tail = -1;
@@ -155,6 +161,16 @@ pkv_status pkv_pool_create(const pkv_pool_desc *desc, void *k_pool, void *v_pool
     p->has_hash.assign(N, 0);
     p->prefix_hits = p->prefix_misses = p->evictions = 0;
     *out = p;
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_set_scales(pkv_pool *pool, void *k_scale, void *v_scale) {
+    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (pool->desc.kv_dtype != PKV_KV_E4M3) return fail(PKV_ERR_INVALID_ARG, "not an E4M3 pool");
+    if (!k_scale || !v_scale || ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 15u))
+        return fail(PKV_ERR_INVALID_ARG, "scale pools must be non-NULL and 16-byte aligned");
+    pool->k_scale = static_cast<float *>(k_scale);
+    pool->v_scale = static_cast<float *>(v_scale);
     return PKV_OK;
 }
 

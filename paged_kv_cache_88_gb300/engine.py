@@ -34,7 +34,17 @@ class DecodeEngine:
         self.fused = fused      # append inside the attention launch (pkv_decode_append_attention)
         self.device = torch.device(device)
         shape = wl.pool_shape(w)
-        if fill == "numpy":
+        self.k_scale = self.v_scale = None
+        if w.kv_dtype == "e4m3":
+            if fill == "numpy":
+                self.k_pool = torch.from_numpy(wl.pool_codes_e4m3(w, 0)).to(self.device)
+                self.v_pool = torch.from_numpy(wl.pool_codes_e4m3(w, 1)).to(self.device)
+                self.k_scale = torch.from_numpy(wl.pool_scales(w, 0)).to(self.device)
+                self.v_scale = torch.from_numpy(wl.pool_scales(w, 1)).to(self.device)
+            else:
+                self.k_pool, self.k_scale = wl.torch_e4m3_pool(w, 0, self.device)
+                self.v_pool, self.v_scale = wl.torch_e4m3_pool(w, 1, self.device)
+        elif fill == "numpy":
             self.k_pool = torch.from_numpy(wl.pool_values(w, 0)).to(self.device)
             self.v_pool = torch.from_numpy(wl.pool_values(w, 1)).to(self.device)
         elif fill == "torch":
@@ -43,7 +53,8 @@ class DecodeEngine:
         else:
             raise ValueError(fill)
         self.pool = bd.Pool(w.num_layers, w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.layout,
-                            self.k_pool, self.v_pool, w.free_order)
+                            self.k_pool, self.v_pool, w.free_order, kv_dtype=w.kv_dtype, k_scale=self.k_scale,
+                            v_scale=self.v_scale)
         S, maxb = w.num_seqs, w.max_blocks
         self.tables = np.full((S, maxb), -1, dtype=np.int32)
         self.lens = np.zeros(S, dtype=np.int32)

@@ -41,15 +41,35 @@ def u16(t):
     return t.detach().cpu().numpy().view(np.uint16)
 
 
+def bits(t):
+    a = t.detach().cpu().numpy()
+    return a.view(np.uint8 if a.dtype == np.uint8 else (np.uint16 if a.itemsize == 2 else np.uint32))
+
+
+def same_pools(eng, ora, what=""):
+    """Every pool byte (and, for an E4M3 cache, every scale) equal to the oracle's."""
+    assert np.array_equal(bits(eng.k_pool), ora.k_pool.view(bits(eng.k_pool).dtype)), f"K pool differs {what}"
+    assert np.array_equal(bits(eng.v_pool), ora.v_pool.view(bits(eng.v_pool).dtype)), f"V pool differs {what}"
+    if eng.k_scale is not None:
+        assert np.array_equal(bits(eng.k_scale), ora.k_scale.view(np.uint32)), f"K scales differ {what}"
+        assert np.array_equal(bits(eng.v_scale), ora.v_scale.view(np.uint32)), f"V scales differ {what}"
+
+
+def make_oracle(w):
+    if w.kv_dtype == "e4m3":
+        return OracleEngine(w, wl.pool_codes_e4m3(w, 0), wl.pool_codes_e4m3(w, 1), wl.pool_scales(w, 0),
+                            wl.pool_scales(w, 1))
+    return OracleEngine(w, wl.pool_values(w, 0), wl.pool_values(w, 1))
+
+
 def run_parity(w, steps: int, fused: bool = True):
     eng = DecodeEngine(w, fill="numpy", fused=fused)
-    ora = OracleEngine(w, wl.pool_values(w, 0), wl.pool_values(w, 1))
+    ora = make_oracle(w)
     eng.run_script(values="numpy")
     ora.run_script()
     torch.cuda.synchronize()
     assert eng.tables.tolist() == ora.tables and eng.lens.tolist() == ora.lens
-    assert np.array_equal(u16(eng.k_pool), ora.k_pool.view(np.uint16))
-    assert np.array_equal(u16(eng.v_pool), ora.v_pool.view(np.uint16))
+    same_pools(eng, ora, "after set-up")
     for step in range(steps):
         q, k, v = ora.step_inputs(step)
         qd, kd, vd = eng.step_inputs(step, "numpy")
@@ -61,8 +81,7 @@ def run_parity(w, steps: int, fused: bool = True):
         assert eng.last_slots.tolist() == ora.last_slots
         assert [tuple(p) for p in eng.last_pairs.tolist()] == ora.last_pairs
         assert eng.tables.tolist() == ora.tables and eng.lens.tolist() == ora.lens
-        assert np.array_equal(u16(eng.k_pool), ora.k_pool.view(np.uint16)), f"K pool differs after step {step}"
-        assert np.array_equal(u16(eng.v_pool), ora.v_pool.view(np.uint16)), f"V pool differs after step {step}"
+        same_pools(eng, ora, f"after step {step}")
         assert_close(out.cpu().numpy(), ref, f"{w.name} step {step}")
         assert eng.device_status() == 0
     eng.pool.validate()
@@ -115,6 +134,56 @@ def test_13b_shape_churned_pool_reduced(layout):
 def test_long_context_block_sweep_reduced(block_size):
     w = wl.make_workload(5, num_layers=1, num_seqs=3, len_scale=0.12, decode_steps=2, block_size=block_size)
     run_parity(w, 2)
+
+
+# ----------------------------------------------------------------------------- FP8 E4M3 cache
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_e4m3_tiny(fused):
+    """head_dim 64; codes and scales written by the quantising append are bit-exact."""
+    w = wl.make_workload(1, decode_steps=3, kv_dtype="e4m3")
+    run_parity(w, 3, fused=fused)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_e4m3_7b_shape_reduced(fused):
+    w = wl.make_workload(2, num_layers=2, num_seqs=8, len_scale=0.3, decode_steps=3, kv_dtype="e4m3")
+    run_parity(w, 3, fused=fused)
+
+
+def test_e4m3_prefix_cow_reduced():
+    """COW copies the codes and the row scales of the shared block."""
+    w = wl.make_workload(3, num_layers=2, num_seqs=8, len_scale=0.25, decode_steps=2, kv_dtype="e4m3")
+    eng, _ = run_parity(w, 2)
+    assert eng.pool.stats()["cow_copies"] == w.num_seqs - 1
+
+
+def test_e4m3_13b_shape_reduced():
+    w = wl.make_workload(4, num_layers=2, num_seqs=24, len_scale=0.5, decode_steps=2, kv_dtype="e4m3")
+    run_parity(w, 2)
+
+
+@pytest.mark.parametrize("block_size", [8, 16, 256])
+def test_e4m3_long_context_reduced(block_size):
+    w = wl.make_workload(5, num_layers=1, num_seqs=3, len_scale=0.12, decode_steps=2, block_size=block_size,
+                         kv_dtype="e4m3")
+    run_parity(w, 2)
+
+
+def test_e4m3_pool_rules():
+    q = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.Pool(1, 1, 16, 1, 256, "HND", kv_dtype="e4m3")          # head_dim 256 not built for E4M3
+    assert e.value.code == "UNSUPPORTED"
+    with pytest.raises(pkv.PkvError):
+        pkv.Pool(1, 1, 16, 1, 64, "NHD", kv_dtype="e4m3")           # HND only
+    p = pkv.Pool(1, 1, 8, 1, 64, "HND", k_pool=torch.zeros(512, dtype=torch.uint8, device="cuda"),
+                 v_pool=torch.zeros(512, dtype=torch.uint8, device="cuda"), kv_dtype="e4m3")
+    kn = torch.zeros((1, 1, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:                          # no scale pools attached
+        p.append(0, kn, kn, torch.zeros(1, dtype=torch.int64, device="cuda"))
+    assert "scale" in pkv.last_error()
+    del q
 
 
 # ----------------------------------------------------------------------------- raw-call edge cases

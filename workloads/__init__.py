@@ -75,9 +75,13 @@ class Workload:
     seed: int
     layout: str = "HND"
     description: str = ""
+    kv_dtype: str = "f16"
 
     @property
     def kv_bytes_per_token_layer(self) -> int:
+        """Bytes of K and V one token holds in one layer (E4M3: codes plus the two row scales)."""
+        if self.kv_dtype == "e4m3":
+            return 2 * self.num_heads * (self.head_dim + 4)
         return 2 * self.num_heads * self.head_dim * 2
 
     def describe(self) -> dict:
@@ -86,7 +90,7 @@ class Workload:
             "layers": self.num_layers, "heads": self.num_heads, "head_dim": self.head_dim,
             "block_size": self.block_size, "batch": self.num_seqs, "pool_blocks": self.num_blocks,
             "mean_context": float(np.mean(self.context_lens)) if self.num_seqs else 0.0,
-            "layout": self.layout,
+            "layout": self.layout, "kv_dtype": self.kv_dtype,
         }
 
 
@@ -109,15 +113,23 @@ def _finish(index, name, L, H, D, B, lens, script, steps, seed, N, layout, desc,
                     seed=int(seed), layout=layout, description=desc)
 
 
-def make_workload(index: int, *, num_layers: Optional[int] = None, num_seqs: Optional[int] = None,
-                  block_size: Optional[int] = None, decode_steps: Optional[int] = None,
-                  layout: str = "HND", seed: Optional[int] = None,
-                  len_scale: float = 1.0, prefix_mode: str = "fork") -> Workload:
+def make_workload(index: int, *, kv_dtype: str = "f16", **kw) -> Workload:
     """The seeded workload ``index`` (1..5); keyword overrides shrink it for tests.
 
     ``len_scale`` multiplies sampled context lengths (tests use it to keep the
-    oracle fast while keeping the length mix).
+    oracle fast while keeping the length mix). ``kv_dtype`` "e4m3" asks for a
+    quantised cache (the pools then start with random finite E4M3 codes and
+    scales instead of fp16 draws).
     """
+    w = _make_workload(index, **kw)
+    w.kv_dtype = kv_dtype
+    return w
+
+
+def _make_workload(index: int, *, num_layers: Optional[int] = None, num_seqs: Optional[int] = None,
+                   block_size: Optional[int] = None, decode_steps: Optional[int] = None,
+                   layout: str = "HND", seed: Optional[int] = None,
+                   len_scale: float = 1.0, prefix_mode: str = "fork") -> Workload:
     seed = 1000 + index if seed is None else seed
     r = _rng(seed, 1)
     if index == 1:
@@ -249,6 +261,25 @@ def pool_shape(w: Workload) -> Tuple[int, ...]:
     return (w.num_layers, w.num_blocks, w.num_heads, w.block_size, w.head_dim)
 
 
+def pool_scale_shape(w: Workload) -> Tuple[int, ...]:
+    """Shape of a per-(token, head) scale pool (E4M3 cache): [L, N, H, B]."""
+    return (w.num_layers, w.num_blocks, w.num_heads, w.block_size)
+
+
+def pool_codes_e4m3(w: Workload, which: int) -> np.ndarray:
+    """Initial E4M3 codes of the K (0) / V (1) pool: uniform over the 254 finite codes."""
+    g = _rng(w.seed, 110 + which)
+    c = g.integers(0, 126, size=pool_shape(w), dtype=np.int64)          # 0x00..0x7D
+    c = c + (c >= 0x7F)                                                   # never 0x7F (NaN)
+    sign = g.integers(0, 2, size=pool_shape(w), dtype=np.int64) << 7
+    return (c | sign).astype(np.uint8)
+
+
+def pool_scales(w: Workload, which: int) -> np.ndarray:
+    """Initial per-(token, head) scales of the K (0) / V (1) pool: U[0.001, 0.01]."""
+    return _rng(w.seed, 120 + which).uniform(0.001, 0.01, size=pool_scale_shape(w)).astype(np.float32)
+
+
 def pool_values(w: Workload, which: int) -> np.ndarray:
     """Initial contents of the K (which=0) or V (which=1) pool: every slot is a draw."""
     return normal_fp16(w.seed, (100 + which,), pool_shape(w))
@@ -274,3 +305,15 @@ def torch_normal_fp16(seed: int, tag: Tuple[int, ...], shape: Sequence[int], dev
     g = torch.Generator(device=device)
     g.manual_seed(int(np.random.SeedSequence([int(seed)] + [int(t) for t in tag]).generate_state(1)[0]))
     return torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float16)
+
+
+def torch_e4m3_pool(w: Workload, which: int, device):
+    """E4M3 codes and scales of a pool made on ``device`` by torch (pools too big for the host)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(np.random.SeedSequence([int(w.seed), 110 + which]).generate_state(1)[0]))
+    c = torch.randint(0, 126, pool_shape(w), generator=g, device=device, dtype=torch.int16)
+    c = c + (c >= 0x7F).to(torch.int16)
+    c = c | (torch.randint(0, 2, pool_shape(w), generator=g, device=device, dtype=torch.int16) << 7)
+    s = torch.rand(pool_scale_shape(w), generator=g, device=device, dtype=torch.float32) * 0.009 + 0.001
+    return c.to(torch.uint8), s
