@@ -30,6 +30,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -50,6 +52,7 @@ def parse_args():
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling captures only)")
     ap.add_argument("--kv-dtype", default="f16", choices=["f16", "e4m3"])
+    ap.add_argument("--swap", action="store_true", help="measure swap-out / swap-in of one sequence instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -416,8 +419,49 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_swap(args):
+    """Swap-out / swap-in of the longest sequence of the workload (all layers) through pinned host memory."""
+    import torch
+    from paged_kv_cache_88_gb300.engine import DecodeEngine
+    w = make_bench_workload(args, 8)
+    eng = DecodeEngine(w, fill="torch")
+    eng.run_script(values="torch")
+    s = int(np.argmax(eng.lens))
+    n = -(-int(eng.lens[s]) // w.block_size)
+    bpb = eng.pool.swap_bytes_per_block()
+    host = torch.empty(n * bpb, dtype=torch.uint8).pin_memory()
+    staging = torch.empty(n * bpb, dtype=torch.uint8, device="cuda")
+    blocks = torch.tensor(eng.tables[s, :n], dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    times = {"gather": [], "d2h": [], "h2d": [], "scatter": []}
+    for it in range(args.warmup + args.steps):
+        ev[0].record(st)
+        eng.pool.gather_blocks(blocks, staging, stream=st)
+        ev[1].record(st)
+        host.copy_(staging, non_blocking=True)
+        ev[2].record(st)
+        staging.copy_(host, non_blocking=True)
+        ev[3].record(st)
+        eng.pool.scatter_blocks(blocks, staging, stream=st)
+        ev[4].record(st)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            for i, k in enumerate(times):
+                times[k].append(ev[i].elapsed_time(ev[i + 1]))
+    nbytes = n * bpb
+    res = {k: nbytes / (statistics.median(v) / 1e3) / 1e9 for k, v in times.items()}
+    print(json.dumps({"metric": "swap GB/s (one sequence, all layers)", "unit": "GB/s", "bytes": nbytes,
+                      "blocks": n, "config": w.describe(), **{f"{k}_gbps": v for k, v in res.items()},
+                      "swap_out_ms": statistics.median(times["gather"]) + statistics.median(times["d2h"]),
+                      "swap_in_ms": statistics.median(times["h2d"]) + statistics.median(times["scatter"])}))
+
+
 def main():
     args = parse_args()
+    if args.swap:
+        run_swap(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -238,6 +238,21 @@ pkv_status pkv_append(const pkv_pool *pool, int32_t layer, const void *k_new, co
 pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *pairs, int32_t num_pairs,
                            uint32_t *status, void *stream);
 
+/* Swap (icman.com.cn/news/78786 §4.2: a preempted request's KV goes out to host
+ * memory and comes back later). The library moves blocks between the pool and a
+ * contiguous caller-owned DEVICE buffer; the caller moves that buffer to and
+ * from (pinned) host memory with one cudaMemcpyAsync each way and frees /
+ * allocates the blocks with pkv_free / pkv_alloc, all on the same stream.
+ * Buffer layout: for i = 0..n-1 and each layer: block blocks[i]'s K bytes, V
+ * bytes, then (E4M3 pools) its K and V row scales; pkv_swap_bytes_per_block
+ * gives the bytes per block over all layers. blocks: device int32 [n]; an id
+ * outside [0, N) is skipped and flagged PKV_DEV_BAD_PAIR. Bit copies. */
+size_t pkv_swap_bytes_per_block(const pkv_pool *pool);
+pkv_status pkv_gather_blocks(const pkv_pool *pool, const int32_t *blocks, int32_t n, void *dst,
+                             uint32_t *status, void *stream);
+pkv_status pkv_scatter_blocks(const pkv_pool *pool, const int32_t *blocks, int32_t n, const void *src,
+                              uint32_t *status, void *stream);
+
 /* Paged decode attention for one layer: for every sequence s and head h,
  *   out[s][h] = softmax_t(scale * q[s][h] . K_s[t]) V_s[t],  t = 0..T_s-1,
  * where token t of sequence s is read from physical block

@@ -100,6 +100,27 @@ class OracleEngine:
             else:
                 raise ValueError(kind)
 
+    def swap_out(self, s: int):
+        """Copy sequence s's blocks (every layer) out and release them; returns the copies."""
+        B = self.w.block_size
+        n = -(-self.lens[s] // B)
+        ids = self.tables[s][:n]
+        saved = [a[:, ids].copy() for a in self._arrays()]
+        self.pool.free(ids)
+        self.tables[s] = [-1] * self.w.max_blocks
+        return saved
+
+    def swap_in(self, s: int, saved) -> None:
+        """Allocate fresh blocks for sequence s and write the copies back into them."""
+        n = saved[0].shape[1]
+        ids = self.pool.alloc(n)
+        self.tables[s] = ids + [-1] * (self.w.max_blocks - n)
+        for a, v in zip(self._arrays(), saved):
+            a[:, ids] = v
+
+    def _arrays(self):
+        return [self.k_pool, self.v_pool] + ([self.k_scale, self.v_scale] if self.q8 else [])
+
     def step(self, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, scale: Optional[float] = None,
              layers: Optional[list] = None, pairs_only: Optional[list] = None, impl: str = "numpy") -> np.ndarray:
         """One decode step: a3 (slots, COW), a4 copy, a5 append, a6/a7 attention. Returns float64 [L, S, H, D].

@@ -30,7 +30,7 @@ EXPORTED = [
     "pkv_prepare_append", "pkv_append", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_workspace_bytes",
     "pkv_pool_decode_attention", "pkv_decode_launch_info", "pkv_decode_append_attention",
     "pkv_decode_attention_static", "pkv_block_hash", "pkv_prefix_lookup", "pkv_prefix_register",
-    "pkv_pool_set_scales",
+    "pkv_pool_set_scales", "pkv_swap_bytes_per_block", "pkv_gather_blocks", "pkv_scatter_blocks",
 ]
 
 
@@ -98,6 +98,9 @@ def lib() -> ctypes.CDLL:
             "pkv_prefix_lookup": (i32, [vp, vp, i32, vp, ctypes.POINTER(i32)]),
             "pkv_prefix_register": (i32, [vp, vp, vp, i32]),
             "pkv_pool_set_scales": (i32, [vp, vp, vp]),
+            "pkv_swap_bytes_per_block": (sz, [vp]),
+            "pkv_gather_blocks": (i32, [vp, vp, i32, vp, vp, vp]),
+            "pkv_scatter_blocks": (i32, [vp, vp, i32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -303,6 +306,21 @@ class Pool:
             self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(block_tables),
             block_tables.shape[1], _ptr(context_lens), q.shape[0], float(scale), _ptr(out), _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream(stream)))
+
+    def swap_bytes_per_block(self) -> int:
+        return int(lib().pkv_swap_bytes_per_block(self._h))
+
+    def gather_blocks(self, blocks_dev, dst, status=None, stream=None) -> None:
+        """Copy the listed blocks (device int32) of every layer into ``dst`` (device bytes)."""
+        _require(blocks_dev, "int32", "blocks")
+        check(lib().pkv_gather_blocks(self._h, _ptr(blocks_dev), blocks_dev.numel(), _ptr(dst), _ptr(status),
+                                      _stream(stream)))
+
+    def scatter_blocks(self, blocks_dev, src, status=None, stream=None) -> None:
+        """Copy ``src`` (laid out as gather_blocks writes it) into the listed blocks."""
+        _require(blocks_dev, "int32", "blocks")
+        check(lib().pkv_scatter_blocks(self._h, _ptr(blocks_dev), blocks_dev.numel(), _ptr(src), _ptr(status),
+                                       _stream(stream)))
 
     def layer_view(self, which: str, layer: int):
         t = self.k_pool if which == "k" else self.v_pool

@@ -142,7 +142,71 @@ copy_blocks_kernel(const int32_t *__restrict__ pairs, int32_t num_pairs, uint4 *
     }
 }
 
+// Swap: blocks <-> a contiguous buffer, [n][L][K block, V block(, K scales, V scales)],
+// every piece a whole number of 16-byte words. gather = pool -> buffer,
+// scatter = buffer -> pool (icman.com.cn/news/78786 §4.2 swaps a preempted
+// request's KV out to host memory and back).
+__global__ void __launch_bounds__(kCopyThreads)
+swap_blocks_kernel(const int32_t *__restrict__ blocks, int32_t n, uint4 *k_pool, uint4 *v_pool, uint4 *k_scale,
+                   uint4 *v_scale, int32_t num_layers, int32_t num_blocks, int64_t block_words, int64_t scale_words,
+                   uint4 *buf, int32_t to_buffer, uint32_t *status) {
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+    const int64_t per = 2 * block_words + 2 * scale_words;      // words of one (block, layer) in the buffer
+    const int64_t jobs = (int64_t)n * num_layers;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t y = blockIdx.y; y < jobs; y += gridDim.y) {
+        const int32_t i = (int32_t)(y / num_layers);
+        const int32_t layer = (int32_t)(y - (int64_t)i * num_layers);
+        const int32_t b = blocks[i];
+        if (b < 0 || b >= num_blocks) {
+            if (status && blockIdx.x == 0 && threadIdx.x == 0 && layer == 0) atomicOr(status, PKV_DEV_BAD_PAIR);
+            continue;
+        }
+        uint4 *slot = buf + y * per;
+        const int64_t pb = ((int64_t)layer * num_blocks + b) * block_words;
+        const int64_t ps = ((int64_t)layer * num_blocks + b) * scale_words;
+        for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < per; w += step) {
+            uint4 *pool_word;
+            if (w < block_words) pool_word = k_pool + pb + w;
+            else if (w < 2 * block_words) pool_word = v_pool + pb + (w - block_words);
+            else if (w < 2 * block_words + scale_words) pool_word = k_scale + ps + (w - 2 * block_words);
+            else pool_word = v_scale + ps + (w - 2 * block_words - scale_words);
+            if (to_buffer) slot[w] = *pool_word;
+            else *pool_word = slot[w];
+        }
+    }
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status swap_blocks(const pkv_pool *pool, const int32_t *blocks, int32_t n, void *buf, bool to_buffer,
+                       uint32_t *status, void *stream) {
+    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    const pkv_pool_desc &d = pool->desc;
+    if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
+    if (n < 0) return fail(PKV_ERR_INVALID_ARG, "n < 0");
+    if (n == 0) return PKV_OK;
+    if (!blocks || !buf || (reinterpret_cast<uintptr_t>(blocks) & 3u) || !aligned16(buf))
+        return fail(PKV_ERR_INVALID_ARG, "blocks (4-byte aligned) and buffer (16-byte aligned) are required");
+    const bool q8 = d.kv_dtype == PKV_KV_E4M3;
+    if (q8 && !pool->k_scale) return fail(PKV_ERR_INVALID_ARG, "E4M3 pool without scale pools (pkv_pool_set_scales)");
+    const int64_t block_words = (int64_t)d.block_size * d.num_heads * d.head_dim * kv_elem_bytes(d) / 16;
+    const int64_t scale_words = q8 ? (int64_t)d.block_size * d.num_heads * 4 / 16 : 0;
+    const int64_t per = 2 * block_words + 2 * scale_words;
+    int gx = (int)((per + kCopyThreads - 1) / kCopyThreads);
+    gx = gx < 1 ? 1 : (gx > 64 ? 64 : gx);
+    const int64_t jobs = (int64_t)n * d.num_layers;
+    const int gy = (int)(jobs < 65535 ? jobs : 65535);
+    cudaError_t e = launch_pdl(swap_blocks_kernel, dim3(gx, gy), dim3(kCopyThreads), 0,
+                               static_cast<cudaStream_t>(stream), blocks, n, static_cast<uint4 *>(pool->k_pool),
+                               static_cast<uint4 *>(pool->v_pool), reinterpret_cast<uint4 *>(pool->k_scale),
+                               reinterpret_cast<uint4 *>(pool->v_scale), d.num_layers, d.num_blocks, block_words,
+                               scale_words, static_cast<uint4 *>(buf), to_buffer ? 1 : 0, status);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "swap launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
 
 }  // namespace
 
@@ -185,6 +249,24 @@ pkv_status pkv_append(const pkv_pool *pool, int32_t layer, const void *k_new, co
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
     return PKV_OK;
+}
+
+size_t pkv_swap_bytes_per_block(const pkv_pool *pool) {
+    if (!pool) return 0;
+    const pkv_pool_desc &d = pool->desc;
+    const size_t block = (size_t)d.block_size * d.num_heads * d.head_dim * kv_elem_bytes(d);
+    const size_t scales = d.kv_dtype == PKV_KV_E4M3 ? (size_t)d.block_size * d.num_heads * 4 : 0;
+    return (size_t)d.num_layers * 2 * (block + scales);
+}
+
+pkv_status pkv_gather_blocks(const pkv_pool *pool, const int32_t *blocks, int32_t n, void *dst, uint32_t *status,
+                             void *stream) {
+    return swap_blocks(pool, blocks, n, dst, true, status, stream);
+}
+
+pkv_status pkv_scatter_blocks(const pkv_pool *pool, const int32_t *blocks, int32_t n, const void *src,
+                              uint32_t *status, void *stream) {
+    return swap_blocks(pool, blocks, n, const_cast<void *>(src), false, status, stream);
 }
 
 pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *pairs, int32_t num_pairs, uint32_t *status,

@@ -136,6 +136,62 @@ def test_long_context_block_sweep_reduced(block_size):
     run_parity(w, 2)
 
 
+# ----------------------------------------------------------------------------- swap (preemption)
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3"])
+def test_swap_out_and_in_round_trip(kv_dtype):
+    """Two sequences are swapped to pinned host memory, their blocks reused by other requests,
+    then swapped back into new blocks; the next decode step matches the oracle exactly."""
+    w = wl.make_workload(2, num_layers=2, num_seqs=6, len_scale=0.2, decode_steps=4, kv_dtype=kv_dtype)
+    eng = DecodeEngine(w, fill="numpy")
+    ora = make_oracle(w)
+    eng.run_script()
+    ora.run_script()
+    q, k, v = ora.step_inputs(0)
+    qd, kd, vd = eng.step_inputs(0)
+    out = torch.empty_like(qd)
+    eng.step(qd, kd, vd, out)
+    ora.step(q, k, v)
+    bpb = eng.pool.swap_bytes_per_block()
+    host = torch.empty(64 * bpb, dtype=torch.uint8).pin_memory()
+    staging = torch.empty(64 * bpb, dtype=torch.uint8, device="cuda")
+    host2 = torch.empty_like(host).pin_memory()
+    n1 = eng.swap_out(1, host, staging)
+    torch.cuda.synchronize()
+    n3 = eng.swap_out(3, host2, staging)
+    s1, s3 = ora.swap_out(1), ora.swap_out(3)
+    # other requests take every free block (the freed ones included), scribble on them and finish
+    nfree = eng.pool.stats()["free_blocks"]
+    junk = eng.pool.alloc(nfree)
+    ora_junk = ora.pool.alloc(nfree)
+    assert junk == ora_junk
+    torch.cuda.synchronize()
+    jb = torch.tensor(junk, dtype=torch.int32, device="cuda")
+    scribble = torch.full((len(junk) * bpb,), 0x55, dtype=torch.uint8, device="cuda")
+    eng.pool.scatter_blocks(jb, scribble)
+    for a in ora._arrays():
+        a[:, ora_junk] = np.frombuffer(b"\x55" * a[:, ora_junk].nbytes, dtype=a.dtype).reshape(a[:, ora_junk].shape)
+    eng.pool.free(junk)
+    ora.pool.free(ora_junk)
+    eng.swap_in(1, n1, host, staging)
+    torch.cuda.synchronize()
+    eng.swap_in(3, n3, host2, staging)
+    ora.swap_in(1, s1)
+    ora.swap_in(3, s3)
+    torch.cuda.synchronize()
+    assert eng.tables.tolist() == ora.tables
+    same_pools(eng, ora, "after swap")
+    eng.upload_tables()
+    q, k, v = ora.step_inputs(1)
+    qd, kd, vd = eng.step_inputs(1)
+    eng.step(qd, kd, vd, out)
+    torch.cuda.synchronize()
+    ref = ora.step(q, k, v)
+    assert eng.device_status() == 0
+    same_pools(eng, ora, "after the step")
+    assert_close(out.cpu().numpy(), ref, "after swap")
+
+
 # ----------------------------------------------------------------------------- FP8 E4M3 cache
 
 @pytest.mark.parametrize("fused", [True, False])
