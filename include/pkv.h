@@ -324,6 +324,25 @@ pkv_status pkv_decode_attention_static(const void *q, const void *k_cache, const
                                        int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs,
                                        float scale, void *out, uint32_t *status, void *stream);
 
+/* Paged prefill (chunked, causal) attention on the tensor cores: for each
+ * sequence s, the chunk of its newest tokens -- rows q_start[s] .. q_start[s+1]-1
+ * of q, C_s of them -- has already been appended to the pool, and
+ * context_lens[s] = T_s counts it. Query i of the chunk (position
+ * p = T_s - C_s + i) attends to every cached token t <= p through the block
+ * table (m.lqnn.cn/news/240480 §3.3 remap, §4.3 causal prefill):
+ *   out[row][h] = softmax_{t <= p}(scale * q[row][h] . K_t[h]) V_t[h].
+ * q, out: device fp16 [total_q][H][D], 16-byte aligned. q_start: device int32
+ * [num_seqs + 1]. max_chunk: a host bound on every C_s (sizes the grid; larger
+ * chunks are only partly computed). status: device uint32 word (required).
+ * The pool must be fp16, HND, head_dim 128. fp16 products, fp32 accumulation;
+ * the softmax weights enter P V in fp16. T_s < C_s or T_s beyond the table is
+ * clamped and flagged PKV_DEV_BAD_LENGTH. UNSUPPORTED for other pools. */
+pkv_status pkv_prefill_attention(const pkv_pool *pool, int32_t layer, const void *q, const int32_t *q_start,
+                                 int32_t total_q, int32_t num_seqs, int32_t max_chunk,
+                                 const int32_t *block_tables, int32_t max_blocks,
+                                 const int32_t *context_lens, float scale, void *out, uint32_t *status,
+                                 void *stream);
+
 /* Bytes of workspace pkv_decode_attention needs for these sizes on the
  * current CUDA device (0 and a pkv_last_error message on bad arguments). */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim);

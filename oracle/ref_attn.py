@@ -128,3 +128,35 @@ def copy_blocks(k_pool: np.ndarray, v_pool: np.ndarray, pairs: Sequence[tuple]) 
     for src, dst in pairs:
         k_pool[:, dst] = k_pool[:, src]
         v_pool[:, dst] = v_pool[:, src]
+
+
+def prefill_attention(q: np.ndarray, k_pool_layer: np.ndarray, v_pool_layer: np.ndarray,
+                      block_tables: np.ndarray, context_lens: Sequence[int], q_start: Sequence[int],
+                      block_size: int, layout: str = "HND", scale: Optional[float] = None) -> np.ndarray:
+    """Causal (prefill) attention of each sequence's newest chunk over its paged cache, float64.
+
+    Sequence s's chunk is rows q_start[s] .. q_start[s+1]-1 of ``q`` ([rows, H, D]),
+    its C_s tokens are the last C_s of its T_s = context_lens[s] cached tokens, and
+    query i (position p = T_s - C_s + i) attends to cached tokens 0..p
+    (m.lqnn.cn/news/240480 §3.3, §4.3). Returns [rows, H, D].
+    """
+    R, H, D = q.shape
+    if scale is None:
+        scale = default_scale(D)
+    out = np.zeros((R, H, D), dtype=np.float64)
+    for s in range(len(context_lens)):
+        r0, r1 = int(q_start[s]), int(q_start[s + 1])
+        C, T = r1 - r0, int(context_lens[s])
+        if C == 0:
+            continue
+        pos = np.arange(T - C, T)
+        for h in range(H):
+            k = gather_sequence(k_pool_layer, block_tables[s], T, h, layout, H, block_size, D)
+            v = gather_sequence(v_pool_layer, block_tables[s], T, h, layout, H, block_size, D)
+            x = scale * (q[r0:r1, h].astype(np.float64) @ k.T)            # [C, T]
+            x[np.arange(T)[None, :] > pos[:, None]] = -np.inf              # causal: keys after the query
+            x = x - x.max(axis=1, keepdims=True)
+            w = np.exp(x)
+            w /= w.sum(axis=1, keepdims=True)
+            out[r0:r1, h] = w @ v
+    return out

@@ -31,6 +31,7 @@ EXPORTED = [
     "pkv_pool_decode_attention", "pkv_decode_launch_info", "pkv_decode_append_attention",
     "pkv_decode_attention_static", "pkv_block_hash", "pkv_prefix_lookup", "pkv_prefix_register",
     "pkv_pool_set_scales", "pkv_swap_bytes_per_block", "pkv_gather_blocks", "pkv_scatter_blocks",
+    "pkv_prefill_attention",
 ]
 
 
@@ -101,6 +102,7 @@ def lib() -> ctypes.CDLL:
             "pkv_swap_bytes_per_block": (sz, [vp]),
             "pkv_gather_blocks": (i32, [vp, vp, i32, vp, vp, vp]),
             "pkv_scatter_blocks": (i32, [vp, vp, i32, vp, vp, vp]),
+            "pkv_prefill_attention": (i32, [vp, i32, vp, vp, i32, i32, i32, vp, i32, vp, f32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -321,6 +323,17 @@ class Pool:
         _require(blocks_dev, "int32", "blocks")
         check(lib().pkv_scatter_blocks(self._h, _ptr(blocks_dev), blocks_dev.numel(), _ptr(src), _ptr(status),
                                        _stream(stream)))
+
+    def prefill_attention(self, layer: int, q, q_start, max_chunk: int, block_tables, context_lens, out, status,
+                          scale: float = 0.0, stream=None) -> None:
+        """Causal attention of each sequence's newest chunk over its cache (pkv_prefill_attention)."""
+        for t, dt, name in ((q, "float16", "q"), (out, "float16", "out"), (q_start, "int32", "q_start"),
+                            (block_tables, "int32", "block_tables"), (context_lens, "int32", "context_lens"),
+                            (status, "int32", "status")):
+            _require(t, dt, name)
+        check(lib().pkv_prefill_attention(self._h, layer, _ptr(q), _ptr(q_start), q.shape[0], q_start.numel() - 1,
+                                          max_chunk, _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                          float(scale), _ptr(out), _ptr(status), _stream(stream)))
 
     def layer_view(self, which: str, layer: int):
         t = self.k_pool if which == "k" else self.v_pool

@@ -1,0 +1,449 @@
+// Paged prefill attention on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// What it computes: a chunk of C_s new tokens of sequence s has been appended to
+// the paged cache (its K/V are in the pool; context_lens[s] = T_s counts them).
+// Query i of the chunk sits at position p = T_s - C_s + i and attends causally to
+// every cached token t <= p, read through the block table:
+//   out[i][h] = softmax_{t <= p}(scale * q[i][h] . K_t[h]) V_t[h].
+// This is the multi-query (prefill) counterpart of the decode kernel
+// (m.lqnn.cn/news/240480 §3.3 remaps positions through the page table inside the
+// attention kernel, §4.3 runs the causal prefill through it; icman.com.cn/news/78786
+// §2.4). Dense enough for tensor cores: a 128-query tile reuses every K/V tile
+// 128 times.
+//
+// Design (one CTA per (sequence, head, 128-query tile); 4 softmax warps + 1
+// producer/MMA warp; fp16 HND cache, head_dim 128):
+// * TMA brings the Q tile once and K/V tiles of 128 keys (one 16-row box per
+//   block of 16, two 64-element halves each) into 128-byte-swizzled shared
+//   memory, double-buffered.
+// * One elected thread issues S = Q K^T (M = N = K = 128, fp16 -> fp32) into
+//   tensor memory, then, once the softmax warps have written P (fp16, the same
+//   swizzled K-major layout), P V into a second tensor-memory tile (V read
+//   MN-major straight from its [token][dim] rows).
+// * Each softmax thread owns one query row: it reads its S row from tensor
+//   memory, applies scale and the causal mask, keeps the online softmax (m, l)
+//   and accumulates O in registers from each tile's P V (rescaled by
+//   exp2(m_old - m_new)). Rows past the sequence's tokens in the last tile are
+//   zeroed in V before P V (a zero weight times non-finite garbage would not be
+//   zero).
+// * Every wait is bounded (1 s, then PKV_DEV_TIMEOUT); tensor memory is freed on
+//   every path.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+using namespace pkv;
+
+constexpr int kQT = 128;             // queries per CTA (MMA M)
+constexpr int kKT = 128;             // keys per tile (MMA N of Q K^T, K of P V)
+constexpr int kD = 128;              // head dim (MMA K of Q K^T, N of P V)
+constexpr int kHalf = 64;            // 64 fp16 = one 128-byte swizzle row
+constexpr int kSub = kQT * 128;      // bytes of one [128 rows x 64 elements] swizzled sub-tile (16 KB)
+constexpr int kTileBytes = 2 * kSub; // a 128 x 128 fp16 tile as two sub-tiles
+constexpr int kThreads = 160;
+constexpr uint32_t kTmemCols = 256;  // S: columns [0, 128); P V: [128, 256)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// shared memory: Q | K0 | V0 | K1 | V1 | P  (each a 32 KB tile, 1024-aligned), barriers after
+constexpr int kSmemTiles = 6 * kTileBytes;
+constexpr int kSmemBytes = kSmemTiles + 1024 /* barriers + flags */ + 1024 /* alignment slack */;
+
+struct PrefillParams {
+    const int32_t *q_start;   // [S + 1] chunk rows of sequence s: q_start[s] .. q_start[s+1]-1
+    const int32_t *tables;    // [S][max_blocks]
+    const int32_t *lens;      // [S] context lengths including the chunk
+    __half *out;              // [total_q][H][D]
+    uint32_t *status;
+    int32_t S, H, max_blocks, B, N;
+    float scale_log2;
+};
+
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    // tcgen05 shared-memory matrix descriptor: start, leading and stride byte
+    // offsets (16-byte units), version 1, 128-byte swizzle
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B, M = N = 128;
+// b_mn = 1 reads B MN-major (its rows run along K).
+__device__ __forceinline__ uint32_t umma_idesc(uint32_t b_mn) {
+    return (1u << 4) | ((uint32_t)(kKT >> 3) << 17) | ((uint32_t)(kQT >> 4) << 24) | (b_mn << 16);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+struct Flags {
+    volatile int32_t timed_out;
+};
+
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int32_t *timed_out,
+                                             uint32_t *status) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*timed_out) return false;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*timed_out) return false;
+        if (ptx::global_timer_ns() - t0 > kWaitLimitNs) {
+            *timed_out = 1;
+            atomicOr(status, PKV_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                            ~uintptr_t(1023));
+    const uint32_t sQ = ptx::smem_addr(base);
+    const uint32_t sK[2] = {sQ + 1 * kTileBytes, sQ + 3 * kTileBytes};
+    const uint32_t sV[2] = {sQ + 2 * kTileBytes, sQ + 4 * kTileBytes};
+    const uint32_t sP = sQ + 5 * kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kSmemTiles);
+    // bars: 0 q_full, 1-2 kv_full[2], 3 s_full, 4 p_ready, 5 o_full
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8);
+    volatile int32_t *timed_out = reinterpret_cast<volatile int32_t *>(bars + 9);
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto BAR = [bar0](int i) { return bar0 + 8 * i; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t qt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int32_t H = p.H, B = p.B;
+
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+    const int32_t q0 = p.q_start[s];
+    const int32_t C = p.q_start[s + 1] - q0;
+    const int32_t i0 = qt * kQT;
+    if (i0 >= C) return;                               // uniform: this tile has no queries
+    int32_t T = p.lens[s];
+    const int32_t cap = p.max_blocks * B;
+    if (T < C || T > cap) {
+        if (tid == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+        T = T < C ? C : cap;
+    }
+    const int32_t rows = min(kQT, C - i0);             // valid query rows of this tile
+    const int32_t pos0 = T - C + i0;                   // position of row 0
+    const int32_t kv_end = pos0 + rows;                // keys [0, kv_end) are seen by some row
+    const int32_t nkt = (kv_end + kKT - 1) / kKT;
+
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) ptx::mbar_init(BAR(i), i == 4 ? 4 : 1);
+        *timed_out = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         ptx::smem_addr(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + kKT;
+
+    if (warp == 4) {
+        // ================= producer: TMA loads and tcgen05 MMAs (lane 0)
+        if (lane == 0) {
+            const int32_t rowsb = B < kKT ? B : kKT;   // rows per box
+            auto load_kv = [&](int32_t j, int st) {
+                const int32_t t0 = j * kKT;
+                const int32_t ntok = min(kKT, kv_end - t0);
+                const int32_t nbox = B < kKT ? (ntok + B - 1) / B : 1;
+                const uint32_t bytes = (uint32_t)nbox * rowsb * 128 * 2 /*halves*/ * 2 /*K,V*/;
+                ptx::mbar_arrive_expect_tx(BAR(1 + st), bytes);
+                for (int32_t i = 0; i < nbox; ++i) {
+                    const int32_t lb = (t0 + i * rowsb) / B;
+                    int32_t blk = lb < p.max_blocks ? p.tables[(size_t)s * p.max_blocks + lb] : -1;
+                    if (blk < 0 || blk >= p.N) {
+                        atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                        blk = 0;
+                    }
+                    const int32_t y = (blk * H + h) * B + (B < kKT ? 0 : t0 % B);
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t off = half * kSub + i * rowsb * 128;
+                        ptx::tma_load_2d(sK[st] + off, &kmap, half * kHalf, y, BAR(1 + st));
+                        ptx::tma_load_2d(sV[st] + off, &vmap, half * kHalf, y, BAR(1 + st));
+                    }
+                }
+            };
+            ptx::mbar_arrive_expect_tx(BAR(0), kTileBytes);
+            for (int half = 0; half < 2; ++half)
+                ptx::tma_load_3d(sQ + half * kSub, &qmap, half * kHalf, h, q0 + i0, BAR(0));
+            load_kv(0, 0);
+            if (nkt > 1) load_kv(1, 1);
+            bounded_wait(BAR(0), 0, timed_out, p.status);
+            const uint32_t id_qk = umma_idesc(0), id_pv = umma_idesc(1);
+            for (int32_t j = 0; j < nkt; ++j) {
+                const int st = j & 1;
+                bounded_wait(BAR(1 + st), (j >> 1) & 1, timed_out, p.status);
+                tc_fence_after();
+                // S = Q K^T over the head dim: 8 steps of 16 (4 per 64-element half)
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t koff = (ks >> 2) * kSub + (ks & 3) * 32;
+                    umma(tS, umma_desc(sQ + koff, 16, 1024), umma_desc(sK[st] + koff, 16, 1024), id_qk, ks > 0);
+                }
+                umma_commit(BAR(3));
+                bounded_wait(BAR(4), j & 1, timed_out, p.status);   // P written, S and the last P V read
+                tc_fence_after();
+                // O_j = P V over the tile's keys: A = P (K-major), B = V rows (MN-major, halves 16 KB apart)
+                for (int ks = 0; ks < kKT / 16; ++ks) {
+                    const uint32_t aoff = (ks >> 2) * kSub + (ks & 3) * 32;
+                    umma(tO, umma_desc(sP + aoff, 16, 1024), umma_desc(sV[st] + ks * 2048, kSub, 1024), id_pv,
+                         ks > 0);
+                }
+                umma_commit(BAR(5));
+                if (j + 2 < nkt) {
+                    bounded_wait(BAR(5), j & 1, timed_out, p.status);  // stage free once P V is done
+                    load_kv(j + 2, st);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax warps: thread r owns query row r
+        const int32_t r = tid;                      // 0..127 (TMEM lane r)
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const bool valid = r < rows;
+        const int32_t pr = pos0 + r;                // position of this row's query
+        float o[kD];
+#pragma unroll
+        for (int d = 0; d < kD; ++d) o[d] = 0.f;
+        float m = -INFINITY, l = 0.f;
+        unsigned char *sPp = base + 5 * kTileBytes;
+        for (int32_t j = 0; j < nkt; ++j) {
+            const int32_t t0 = j * kKT;
+            bounded_wait(BAR(3), j & 1, timed_out, p.status);
+            tc_fence_after();
+            // pass 1: masked row max
+            float mx = -INFINITY;
+            for (int c0 = 0; c0 < kKT; c0 += 32) {
+                float v[32];
+                tmem_ld32(tS + lane_base + c0, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int32_t t = t0 + c0 + i;
+                    const float x = (valid && t <= pr) ? v[i] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x);
+                }
+            }
+            const float m_new = fmaxf(m, mx);
+            const float alpha = (m_new == -INFINITY) ? 1.f : ptx::ex2(m - m_new);
+            // pass 2: P = exp2(x - m_new) in fp16 into the swizzled K-major P tile
+            float rs = 0.f;
+            for (int c0 = 0; c0 < kKT; c0 += 32) {
+                float v[32];
+                tmem_ld32(tS + lane_base + c0, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int32_t t = t0 + c0 + i;
+                    const float p0 = (valid && t <= pr && m_new != -INFINITY) ? ptx::ex2(v[i] * p.scale_log2 - m_new) : 0.f;
+                    const float p1 = (valid && t + 1 <= pr && m_new != -INFINITY)
+                                         ? ptx::ex2(v[i + 1] * p.scale_log2 - m_new)
+                                         : 0.f;
+                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    // the weights P V will use are the fp16 ones: sum those
+                    const float2 back = __half22float2(hp);
+                    rs += back.x + back.y;
+                    pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+                }
+                // 32 keys = four 16-byte chunks of the row, sub-tile (c0 / 64), chunk (c0 % 64) / 8 + k
+                const int sub = c0 >> 6;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int chunk = ((c0 & 63) >> 3) + k;
+                    const int phys = chunk ^ (r & 7);
+                    uint4 *dst = reinterpret_cast<uint4 *>(sPp + sub * kSub + r * 128 + phys * 16);
+                    *dst = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                }
+            }
+            l = l * alpha + rs;
+            m = m_new;
+            // the last tile: zero the V rows no query may see (they may hold non-finite garbage)
+            if (j == nkt - 1) {
+                const int32_t first_dead = kv_end - t0;          // rows [first_dead, 128) of the tile
+                const int st = j & 1;
+                unsigned char *sVp = base + (st == 0 ? 2 : 4) * kTileBytes;
+                const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
+                for (int32_t w = tid; w < nwords * 2; w += 128) {
+                    const int half = w / nwords, rem = w - half * nwords;
+                    const int row = first_dead + rem / 8, c = rem & 7;
+                    *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P (and zeroed V) -> MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(4));
+            // O = O * alpha + P V of this tile
+            bounded_wait(BAR(5), j & 1, timed_out, p.status);
+            tc_fence_after();
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                float v[32];
+                tmem_ld32(tO + lane_base + c0, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[c0 + i] = fmaf(o[c0 + i], alpha, v[i]);
+            }
+        }
+        if (valid) {
+            const float inv = 1.f / l;
+            __half *dst = p.out + ((size_t)(q0 + i0 + r) * H + h) * kD;
+#pragma unroll
+            for (int d = 0; d < kD; d += 8) {
+                __half2 hv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) hv[e] = __floats2half2_rn(o[d + 2 * e] * inv, o[d + 2 * e + 1] * inv);
+                *reinterpret_cast<uint4 *>(dst + d) = *reinterpret_cast<const uint4 *>(hv);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_prefill_attention(const pkv_pool *pool, int32_t layer, const void *q, const int32_t *q_start,
+                                 int32_t total_q, int32_t num_seqs, int32_t max_chunk, const int32_t *block_tables,
+                                 int32_t max_blocks, const int32_t *context_lens, float scale, void *out,
+                                 uint32_t *status, void *stream) {
+    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    const pkv_pool_desc &d = pool->desc;
+    if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
+    if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (d.head_dim != kD || d.kv_dtype != PKV_KV_F16 || d.layout != PKV_LAYOUT_HND)
+        return fail(PKV_ERR_UNSUPPORTED, "prefill attention is built for fp16 HND pools with head_dim 128");
+    if (num_seqs < 0 || total_q < 0 || max_chunk < 0 || max_blocks < 1)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes");
+    if (num_seqs == 0 || total_q == 0 || max_chunk == 0) return PKV_OK;
+    if (num_seqs > 65535) return fail(PKV_ERR_INVALID_ARG, "num_seqs > 65535");
+    if (!q || !q_start || !block_tables || !context_lens || !out || !status)
+        return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument (status is required here)");
+    if (!aligned16(q) || !aligned16(out)) return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const PoolLayer pl = pool_layer(pool, layer);
+    const int H = d.num_heads, B = d.block_size, N = d.num_blocks;
+    CUtensorMap qmap, kmap, vmap;
+    {   // q: [total_q][H][D] as a 3-D tensor (D, H, token), boxes of 64 x 1 x 128
+        const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)total_q};
+        const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+        const cuuint32_t box[3] = {kHalf, 1, kQT}, es[3] = {1, 1, 1};
+        if (fn(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(q), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(PKV_ERR_CUDA, "q tensor map");
+    }
+    for (int which = 0; which < 2; ++which) {   // pool layer: rows of D, boxes of 64 x min(B, 128)
+        const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)N * H * B};
+        const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+        const cuuint32_t box[2] = {kHalf, (cuuint32_t)(B < kKT ? B : kKT)}, es[2] = {1, 1};
+        if (fn(which ? &vmap : &kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, which ? pl.v : pl.k, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(PKV_ERR_CUDA, "pool tensor map");
+    }
+    PrefillParams prm;
+    prm.q_start = q_start;
+    prm.tables = block_tables;
+    prm.lens = context_lens;
+    prm.out = static_cast<__half *>(out);
+    prm.status = status;
+    prm.S = num_seqs;
+    prm.H = H;
+    prm.max_blocks = max_blocks;
+    prm.B = B;
+    prm.N = N;
+    const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)kD);
+    prm.scale_log2 = (float)(sc * 1.4426950408889634);
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+    const dim3 grid((max_chunk + kQT - 1) / kQT, H, num_seqs);
+    cudaError_t e = launch_pdl(prefill_attention_kernel, grid, dim3(kThreads), (size_t)kSmemBytes,
+                               static_cast<cudaStream_t>(stream), qmap, kmap, vmap, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
+}  // extern "C"
