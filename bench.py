@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling captures only)")
     ap.add_argument("--kv-dtype", default="f16", choices=["f16", "e4m3"])
     ap.add_argument("--swap", action="store_true", help="measure swap-out / swap-in of one sequence instead")
+    ap.add_argument("--prefill", type=int, default=0, metavar="CHUNK",
+                    help="measure causal prefill of CHUNK-token chunks over the workload's cache instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -457,8 +459,54 @@ def run_swap(args):
                       "swap_in_ms": statistics.median(times["h2d"]) + statistics.median(times["scatter"])}))
 
 
+def run_prefill(args):
+    """Causal prefill of the last CHUNK tokens of every sequence over its cache (tensor cores)."""
+    import torch
+    from paged_kv_cache_88_gb300.engine import DecodeEngine
+    w = make_bench_workload(args, 8)
+    eng = DecodeEngine(w, fill="torch")
+    eng.run_script(values="torch")
+    L, S, H, D = w.num_layers, w.num_seqs, w.num_heads, w.head_dim
+    chunks = np.minimum(eng.lens, args.prefill).astype(np.int64)
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    total = int(q_start[-1])
+    q = torch.randn((total, H, D), device="cuda", dtype=torch.float16)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qs = torch.from_numpy(q_start).cuda()
+    st = torch.cuda.current_stream()
+    # causal work: query i of a chunk of C over T tokens sees T - C + i + 1 keys; 4 D flops per (query, key, head)
+    keys = sum(int(np.sum(np.arange(int(T) - int(C) + 1, int(T) + 1))) for T, C in zip(eng.lens, chunks))
+    flops = 4.0 * D * H * keys
+    def one(layer):
+        eng.pool.prefill_attention(layer, q, qs, int(chunks.max()), eng.tables_d, eng.lens_d, out, status, stream=st)
+    for i in range(args.warmup):
+        one(i % L)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(args.steps):
+        one(i % L)
+    e1.record(st)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x}")
+    ms = e0.elapsed_time(e1) / args.steps
+    peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("bf16_tflops", 1957.5) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+    tf = flops / (ms / 1e3) / 1e12
+    print(json.dumps({"metric": "paged prefill attention TFLOP/s (causal, fp16, tensor cores)", "value": tf,
+                      "unit": "TFLOP/s", "ms_per_layer": ms, "flops_per_layer": flops, "chunk": args.prefill,
+                      "queries": total, "config": w.describe(),
+                      "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                                   "frac": tf / peak, "peak_source": "measured bf16 (fp16 runs at the same rate)"}}))
+
+
 def main():
     args = parse_args()
+    if args.prefill:
+        run_prefill(args)
+        return
     if args.swap:
         run_swap(args)
         return
