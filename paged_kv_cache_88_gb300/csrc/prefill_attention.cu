@@ -21,11 +21,13 @@
 //   swizzled K-major layout), P V into a second tensor-memory tile (V read
 //   MN-major straight from its [token][dim] rows).
 // * Each softmax thread owns one query row: it reads its S row from tensor
-//   memory, applies scale and the causal mask, keeps the online softmax (m, l)
-//   and accumulates O in registers from each tile's P V (rescaled by
-//   exp2(m_old - m_new)). Rows past the sequence's tokens in the last tile are
-//   zeroed in V before P V (a zero weight times non-finite garbage would not be
-//   zero).
+//   memory in one pass, applies scale and (on the diagonal tile only) the causal
+//   mask, and writes P. O accumulates in tensor memory; the softmax reference
+//   max only moves when a row's max exceeds it by more than 2^8, and only then
+//   is O rescaled in place (tcgen05.ld / st), so the previous tile's P V runs
+//   while the next S is being read. Rows past the sequence's tokens in the last
+//   tile are zeroed in V before P V (a zero weight times non-finite garbage
+//   would not be zero).
 // * Every wait is bounded (1 s, then PKV_DEV_TIMEOUT); tensor memory is freed on
 //   every path.
 #include <cuda.h>
@@ -108,6 +110,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -237,7 +254,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
                 for (int ks = 0; ks < kKT / 16; ++ks) {
                     const uint32_t aoff = (ks >> 2) * kSub + (ks & 3) * 32;
                     umma(tO, umma_desc(sP + aoff, 16, 1024), umma_desc(sV[st] + ks * 2048, kSub, 1024), id_pv,
-                         ks > 0);
+                         (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(BAR(5));
                 if (j + 2 < nkt) {
@@ -249,64 +266,74 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         __syncwarp();
     } else {
         // ================= softmax warps: thread r owns query row r
+        // O lives in tensor memory and P V accumulates onto it. The softmax runs
+        // against a reference max m_ref that only moves when a row's max exceeds
+        // it by more than 2^8 (then O and l are rescaled), so P stays <= 256 and
+        // most tiles need no O traffic at all.
         const int32_t r = tid;                      // 0..127 (TMEM lane r)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const bool valid = r < rows;
         const int32_t pr = pos0 + r;                // position of this row's query
-        float o[kD];
-#pragma unroll
-        for (int d = 0; d < kD; ++d) o[d] = 0.f;
-        float m = -INFINITY, l = 0.f;
+        constexpr float kSlack = 8.f;               // log2 of the largest P kept without rescaling
+        float m_ref = -INFINITY, l = 0.f;
         unsigned char *sPp = base + 5 * kTileBytes;
         for (int32_t j = 0; j < nkt; ++j) {
             const int32_t t0 = j * kKT;
             bounded_wait(BAR(3), j & 1, timed_out, p.status);
             tc_fence_after();
-            // pass 1: masked row max
-            float mx = -INFINITY;
+            float x[kKT];
+#pragma unroll
             for (int c0 = 0; c0 < kKT; c0 += 32) {
                 float v[32];
                 tmem_ld32(tS + lane_base + c0, v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int32_t t = t0 + c0 + i;
-                    const float x = (valid && t <= pr) ? v[i] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x);
+                for (int i = 0; i < 32; ++i) x[c0 + i] = v[i] * p.scale_log2;
+            }
+            if (!(valid && t0 + kKT - 1 <= pr)) {   // the diagonal tile (or a row past the chunk): mask
+#pragma unroll
+                for (int i = 0; i < kKT; ++i) x[i] = (valid && t0 + i <= pr) ? x[i] : -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kKT; ++i) mx = fmaxf(mx, x[i]);
+            const bool move = mx > m_ref + kSlack;  // false when mx = -inf
+            const float new_ref = move ? mx : m_ref;
+            const float alpha = move ? ptx::ex2(m_ref - new_ref) : 1.f;   // m_ref = -inf: 0
+            // P's buffer and O are free once the previous tile's P V is done
+            if (j > 0) {
+                bounded_wait(BAR(5), (j - 1) & 1, timed_out, p.status);
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, move)) {
+#pragma unroll
+                    for (int c0 = 0; c0 < kD; c0 += 32) {
+                        float v[32];
+                        tmem_ld32(tO + lane_base + c0, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                        tmem_st32(tO + lane_base + c0, v);
+                    }
                 }
             }
-            const float m_new = fmaxf(m, mx);
-            const float alpha = (m_new == -INFINITY) ? 1.f : ptx::ex2(m - m_new);
-            // pass 2: P = exp2(x - m_new) in fp16 into the swizzled K-major P tile
+            m_ref = new_ref;
+            const bool live = m_ref != -INFINITY;
             float rs = 0.f;
-            for (int c0 = 0; c0 < kKT; c0 += 32) {
-                float v[32];
-                tmem_ld32(tS + lane_base + c0, v);
-                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int32_t t = t0 + c0 + i;
-                    const float p0 = (valid && t <= pr && m_new != -INFINITY) ? ptx::ex2(v[i] * p.scale_log2 - m_new) : 0.f;
-                    const float p1 = (valid && t + 1 <= pr && m_new != -INFINITY)
-                                         ? ptx::ex2(v[i + 1] * p.scale_log2 - m_new)
-                                         : 0.f;
+            for (int c = 0; c < kKT / 8; ++c) {         // 16-byte chunks of 8 keys
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = live ? ptx::ex2(x[8 * c + 2 * e] - m_ref) : 0.f;
+                    const float p1 = live ? ptx::ex2(x[8 * c + 2 * e + 1] - m_ref) : 0.f;
                     const __half2 hp = __floats2half2_rn(p0, p1);
-                    // the weights P V will use are the fp16 ones: sum those
-                    const float2 back = __half22float2(hp);
+                    const float2 back = __half22float2(hp);   // the weights P V uses are the fp16 ones
                     rs += back.x + back.y;
-                    pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+                    pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
-                // 32 keys = four 16-byte chunks of the row, sub-tile (c0 / 64), chunk (c0 % 64) / 8 + k
-                const int sub = c0 >> 6;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int chunk = ((c0 & 63) >> 3) + k;
-                    const int phys = chunk ^ (r & 7);
-                    uint4 *dst = reinterpret_cast<uint4 *>(sPp + sub * kSub + r * 128 + phys * 16);
-                    *dst = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                }
+                const int sub = c >> 3, phys = (c & 7) ^ (r & 7);
+                *reinterpret_cast<uint4 *>(sPp + sub * kSub + r * 128 + phys * 16) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
             l = l * alpha + rs;
-            m = m_new;
             // the last tile: zero the V rows no query may see (they may hold non-finite garbage)
             if (j == nkt - 1) {
                 const int32_t first_dead = kv_end - t0;          // rows [first_dead, 128) of the tile
@@ -315,33 +342,31 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
                 const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
                 for (int32_t w = tid; w < nwords * 2; w += 128) {
                     const int half = w / nwords, rem = w - half * nwords;
-                    const int row = first_dead + rem / 8, c = rem & 7;
-                    *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                    const int row = first_dead + rem / 8, cc = rem & 7;
+                    *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P (and zeroed V) -> MMA
             tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(BAR(4));
-            // O = O * alpha + P V of this tile
-            bounded_wait(BAR(5), j & 1, timed_out, p.status);
-            tc_fence_after();
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                float v[32];
-                tmem_ld32(tO + lane_base + c0, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[c0 + i] = fmaf(o[c0 + i], alpha, v[i]);
-            }
         }
-        if (valid) {
-            const float inv = 1.f / l;
-            __half *dst = p.out + ((size_t)(q0 + i0 + r) * H + h) * kD;
+        bounded_wait(BAR(5), (nkt - 1) & 1, timed_out, p.status);
+        tc_fence_after();
+        const float inv = valid ? 1.f / l : 0.f;
+        __half *dst = p.out + ((size_t)(q0 + i0 + r) * H + h) * kD;
 #pragma unroll
-            for (int d = 0; d < kD; d += 8) {
-                __half2 hv[4];
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+            float v[32];
+            tmem_ld32(tO + lane_base + c0, v);
+            if (valid) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) hv[e] = __floats2half2_rn(o[d + 2 * e] * inv, o[d + 2 * e + 1] * inv);
-                *reinterpret_cast<uint4 *>(dst + d) = *reinterpret_cast<const uint4 *>(hv);
+                for (int d = 0; d < 32; d += 8) {
+                    __half2 hv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) hv[e] = __floats2half2_rn(v[d + 2 * e] * inv, v[d + 2 * e + 1] * inv);
+                    *reinterpret_cast<uint4 *>(dst + c0 + d) = *reinterpret_cast<const uint4 *>(hv);
+                }
             }
         }
     }
