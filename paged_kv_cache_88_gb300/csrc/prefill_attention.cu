@@ -11,24 +11,26 @@
 // §2.4). Dense enough for tensor cores: a 128-query tile reuses every K/V tile
 // 128 times.
 //
-// Design (one CTA per (sequence, head, 128-query tile); 4 softmax warps + 1
-// producer/MMA warp; fp16 HND cache, head_dim 128):
-// * TMA brings the Q tile once and K/V tiles of 128 keys (one 16-row box per
-//   block of 16, two 64-element halves each) into 128-byte-swizzled shared
-//   memory, double-buffered.
-// * One elected thread issues S = Q K^T (M = N = K = 128, fp16 -> fp32) into
-//   tensor memory, then, once the softmax warps have written P (fp16, the same
-//   swizzled K-major layout), P V into a second tensor-memory tile (V read
-//   MN-major straight from its [token][dim] rows).
+// Design (one CTA per (sequence, head, 128-query tile); 4 softmax warps, one
+// MMA-issue warp and one TMA warp; fp16 HND cache, head_dim 128):
+// * The TMA warp brings the Q tile once and K/V tiles of 128 keys (one box per
+//   block of the table, two 64-element halves each) into 128-byte-swizzled
+//   shared memory: two K slots and two V slots, each refilled as soon as the
+//   MMA that reads it has finished.
+// * One elected thread issues S = Q K^T (M = N = K = 128, fp16 -> fp32) into one
+//   of two tensor-memory S tiles, and, once the softmax warps have written P
+//   (fp16, the same swizzled K-major layout) for a tile, P V onto the O tile in
+//   tensor memory (V read MN-major straight from its [token][dim] rows). With
+//   two S tiles, the tensor cores compute the next tile's S while the softmax
+//   warps work on this one.
 // * Each softmax thread owns one query row: it reads its S row from tensor
-//   memory in one pass, applies scale and (on the diagonal tile only) the causal
-//   mask, and writes P. O accumulates in tensor memory; the softmax reference
-//   max only moves when a row's max exceeds it by more than 2^8, and only then
-//   is O rescaled in place (tcgen05.ld / st), so the previous tile's P V runs
-//   while the next S is being read. Rows past the sequence's tokens in the last
-//   tile are zeroed in V before P V (a zero weight times non-finite garbage
-//   would not be zero).
-// * Every wait is bounded (1 s, then PKV_DEV_TIMEOUT); tensor memory is freed on
+//   memory in one load, applies the causal mask on the diagonal tile only, and
+//   writes P. The softmax reference max only moves when a row's max exceeds it
+//   by more than 2^8, and only then is O rescaled in place (tcgen05.ld / st).
+//   Rows past the sequence's tokens in the last tile are zeroed in V before
+//   P V (a zero weight times non-finite garbage would not be zero).
+// * Every wait is bounded (1 s, then PKV_DEV_TIMEOUT); before exiting, the CTA
+//   waits (bounded) for its own copies and MMAs, and frees tensor memory on
 //   every path.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -51,13 +53,16 @@ constexpr int kD = 128;              // head dim (MMA K of Q K^T, N of P V)
 constexpr int kHalf = 64;            // 64 fp16 = one 128-byte swizzle row
 constexpr int kSub = kQT * 128;      // bytes of one [128 rows x 64 elements] swizzled sub-tile (16 KB)
 constexpr int kTileBytes = 2 * kSub; // a 128 x 128 fp16 tile as two sub-tiles
-constexpr int kThreads = 160;
-constexpr uint32_t kTmemCols = 256;  // S: columns [0, 128); P V: [128, 256)
+constexpr int kThreads = 192;        // warps 0-3 softmax, warp 4 MMA issue, warp 5 TMA loads
+constexpr uint32_t kTmemCols = 512;  // S0: [0, 128), S1: [128, 256), O: [256, 384)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// shared memory: Q | K0 | V0 | K1 | V1 | P  (each a 32 KB tile, 1024-aligned), barriers after
-constexpr int kSmemTiles = 6 * kTileBytes;
-constexpr int kSmemBytes = kSmemTiles + 1024 /* barriers + flags */ + 1024 /* alignment slack */;
+// shared memory: Q | K0 | K1 | V0 | V1 | P0 | P1 (each a 32 KB tile, 1024-aligned), barriers after
+constexpr int kSmemTiles = 7 * kTileBytes;
+constexpr int kSmemBytes = kSmemTiles + 256 /* barriers + flags */ + 1024 /* alignment slack */;
+
+// barrier indices (two-slot rings use index + slot)
+constexpr int kQFull = 0, kKFull = 1, kVFull = 3, kSFull = 5, kPReady = 7, kOFull = 9, kNumBars = 11;
 
 struct PrefillParams {
     const int32_t *q_start;   // [S + 1] chunk rows of sequence s: q_start[s] .. q_start[s+1]-1
@@ -97,17 +102,27 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// All 128 columns of this warp's 32 lanes in one load, completed before any
+// register is used (the wait sits in the same asm statement).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "r"(taddr) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        : "r"(taddr) : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -130,10 +145,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-struct Flags {
-    volatile int32_t timed_out;
-};
-
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int32_t *timed_out,
                                              uint32_t *status) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -151,6 +162,20 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// Before the CTA exits: wait (bounded, whatever the timeout flag says) for an
+// asynchronous operation this CTA started, so no copy or MMA outlives it.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::global_timer_ns() - t0 > kWaitLimitNs) return;
+}
+
+// Pipeline of one CTA over its key tiles j = 0 .. nkt-1 (slot b = j & 1):
+//   loader : K_j -> K[b] once S_{j-2} is done; V_j -> V[b] once P_{j-2} V is done
+//   MMA    : S_0, S_1, then per j: [P_j ready] O += P_j V_j, S_{j+2} -> S[b]
+//   softmax: per j: S[b] -> P_j (fp16) in P[b], once P_{j-2} V is done
+// so the tensor cores compute S_{j+1} (and finish P_{j-1} V) while the softmax
+// warps work on tile j. Every barrier is waited on at most one phase behind.
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -158,13 +183,12 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~uintptr_t(1023));
     const uint32_t sQ = ptx::smem_addr(base);
-    const uint32_t sK[2] = {sQ + 1 * kTileBytes, sQ + 3 * kTileBytes};
-    const uint32_t sV[2] = {sQ + 2 * kTileBytes, sQ + 4 * kTileBytes};
-    const uint32_t sP = sQ + 5 * kTileBytes;
+    auto sK = [sQ](int b) { return sQ + (uint32_t)(1 + b) * kTileBytes; };
+    auto sV = [sQ](int b) { return sQ + (uint32_t)(3 + b) * kTileBytes; };
+    auto sP = [sQ](int b) { return sQ + (uint32_t)(5 + b) * kTileBytes; };
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kSmemTiles);
-    // bars: 0 q_full, 1-2 kv_full[2], 3 s_full, 4 p_ready, 5 o_full
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 8);
-    volatile int32_t *timed_out = reinterpret_cast<volatile int32_t *>(bars + 9);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    volatile int32_t *timed_out = reinterpret_cast<volatile int32_t *>(bars + kNumBars + 1);
     const uint32_t bar0 = ptx::smem_addr(bars);
     auto BAR = [bar0](int i) { return bar0 + 8 * i; };
 
@@ -190,7 +214,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     const int32_t nkt = (kv_end + kKT - 1) / kKT;
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) ptx::mbar_init(BAR(i), i == 4 ? 4 : 1);
+        for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(BAR(i), (i == kPReady || i == kPReady + 1) ? 4 : 1);
         *timed_out = 0;
         ptx::fence_barrier_init();
     }
@@ -204,141 +228,167 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + kKT;
+    auto tS = [tmem](int b) { return tmem + (uint32_t)b * kKT; };
+    const uint32_t tO = tmem + 2 * kKT;
 
-    if (warp == 4) {
-        // ================= producer: TMA loads and tcgen05 MMAs (lane 0)
+    if (warp == 5) {
+        // ================= loader: TMA for Q, then K and V tiles (one 16-row box per block of 16)
+        const int32_t rowsb = B < kKT ? B : kKT;       // rows per box; B is a power of two, 8..256
         if (lane == 0) {
-            const int32_t rowsb = B < kKT ? B : kKT;   // rows per box
-            auto load_kv = [&](int32_t j, int st) {
-                const int32_t t0 = j * kKT;
-                const int32_t ntok = min(kKT, kv_end - t0);
-                const int32_t nbox = B < kKT ? (ntok + B - 1) / B : 1;
-                const uint32_t bytes = (uint32_t)nbox * rowsb * 128 * 2 /*halves*/ * 2 /*K,V*/;
-                ptx::mbar_arrive_expect_tx(BAR(1 + st), bytes);
-                for (int32_t i = 0; i < nbox; ++i) {
-                    const int32_t lb = (t0 + i * rowsb) / B;
-                    int32_t blk = lb < p.max_blocks ? p.tables[(size_t)s * p.max_blocks + lb] : -1;
-                    if (blk < 0 || blk >= p.N) {
-                        atomicOr(p.status, PKV_DEV_BAD_BLOCK);
-                        blk = 0;
-                    }
-                    const int32_t y = (blk * H + h) * B + (B < kKT ? 0 : t0 % B);
-                    for (int half = 0; half < 2; ++half) {
-                        const uint32_t off = half * kSub + i * rowsb * 128;
-                        ptx::tma_load_2d(sK[st] + off, &kmap, half * kHalf, y, BAR(1 + st));
-                        ptx::tma_load_2d(sV[st] + off, &vmap, half * kHalf, y, BAR(1 + st));
-                    }
-                }
-            };
-            ptx::mbar_arrive_expect_tx(BAR(0), kTileBytes);
+            ptx::mbar_arrive_expect_tx(BAR(kQFull), kTileBytes);
             for (int half = 0; half < 2; ++half)
-                ptx::tma_load_3d(sQ + half * kSub, &qmap, half * kHalf, h, q0 + i0, BAR(0));
-            load_kv(0, 0);
-            if (nkt > 1) load_kv(1, 1);
-            bounded_wait(BAR(0), 0, timed_out, p.status);
+                ptx::tma_load_3d(sQ + half * kSub, &qmap, half * kHalf, h, q0 + i0, BAR(kQFull));
+        }
+        for (int32_t j = 0; j < nkt; ++j) {
+            const int b = j & 1;
+            const int32_t t0 = j * kKT;
+            const int32_t ntok = min(kKT, kv_end - t0);
+            const int32_t nbox = B < kKT ? (ntok + B - 1) / B : 1;     // <= 16
+            const uint32_t box_bytes = (uint32_t)nbox * rowsb * 128 * 2;
+            int32_t y = 0;
+            if (lane < nbox) {                          // lane i: box i of the tile
+                const int32_t lb = (t0 + lane * rowsb) / B;
+                int32_t blk = lb < p.max_blocks ? p.tables[(size_t)s * p.max_blocks + lb] : -1;
+                if (blk < 0 || blk >= p.N) {
+                    atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                    blk = 0;
+                }
+                y = (blk * H + h) * B + (B < kKT ? 0 : t0 % B);
+            }
+            const uint32_t off = (uint32_t)lane * rowsb * 128;
+            if (j >= 2) bounded_wait(BAR(kSFull + b), ((j - 2) >> 1) & 1, timed_out, p.status);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(kKFull + b), box_bytes);
+            __syncwarp();
+            if (lane < nbox)
+                for (int half = 0; half < 2; ++half)
+                    ptx::tma_load_2d(sK(b) + half * kSub + off, &kmap, half * kHalf, y, BAR(kKFull + b));
+            if (j >= 2) bounded_wait(BAR(kOFull + b), ((j - 2) >> 1) & 1, timed_out, p.status);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(kVFull + b), box_bytes);
+            __syncwarp();
+            if (lane < nbox)
+                for (int half = 0; half < 2; ++half)
+                    ptx::tma_load_2d(sV(b) + half * kSub + off, &vmap, half * kHalf, y, BAR(kVFull + b));
+        }
+        // the last loads into each slot and Q have landed before the CTA may exit
+        drain_wait(BAR(kQFull), 0);
+        for (int32_t j = nkt - 2 < 0 ? 0 : nkt - 2; j < nkt; ++j) {
+            drain_wait(BAR(kKFull + (j & 1)), (j >> 1) & 1);
+            drain_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1);
+        }
+    } else if (warp == 4) {
+        // ================= MMA issue (one thread)
+        if (lane == 0) {
             const uint32_t id_qk = umma_idesc(0), id_pv = umma_idesc(1);
-            for (int32_t j = 0; j < nkt; ++j) {
-                const int st = j & 1;
-                bounded_wait(BAR(1 + st), (j >> 1) & 1, timed_out, p.status);
+            auto issue_s = [&](int32_t j) {
+                const int b = j & 1;
+                bounded_wait(BAR(kKFull + b), (j >> 1) & 1, timed_out, p.status);
                 tc_fence_after();
                 // S = Q K^T over the head dim: 8 steps of 16 (4 per 64-element half)
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * kSub + (ks & 3) * 32;
-                    umma(tS, umma_desc(sQ + koff, 16, 1024), umma_desc(sK[st] + koff, 16, 1024), id_qk, ks > 0);
+                    umma(tS(b), umma_desc(sQ + koff, 16, 1024), umma_desc(sK(b) + koff, 16, 1024), id_qk, ks > 0);
                 }
-                umma_commit(BAR(3));
-                bounded_wait(BAR(4), j & 1, timed_out, p.status);   // P written, S and the last P V read
+                umma_commit(BAR(kSFull + b));
+            };
+            bounded_wait(BAR(kQFull), 0, timed_out, p.status);
+            issue_s(0);
+            if (nkt > 1) issue_s(1);
+            for (int32_t j = 0; j < nkt; ++j) {
+                const int b = j & 1;
+                bounded_wait(BAR(kPReady + b), (j >> 1) & 1, timed_out, p.status);   // P_j written, S[b] read
+                bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
                 tc_fence_after();
-                // O_j = P V over the tile's keys: A = P (K-major), B = V rows (MN-major, halves 16 KB apart)
+                // O += P_j V_j over the tile's keys: A = P (K-major), B = V rows (MN-major, halves 16 KB apart)
                 for (int ks = 0; ks < kKT / 16; ++ks) {
                     const uint32_t aoff = (ks >> 2) * kSub + (ks & 3) * 32;
-                    umma(tO, umma_desc(sP + aoff, 16, 1024), umma_desc(sV[st] + ks * 2048, kSub, 1024), id_pv,
+                    umma(tO, umma_desc(sP(b) + aoff, 16, 1024), umma_desc(sV(b) + ks * 2048, kSub, 1024), id_pv,
                          (j > 0 || ks > 0) ? 1u : 0u);
                 }
-                umma_commit(BAR(5));
-                if (j + 2 < nkt) {
-                    bounded_wait(BAR(5), j & 1, timed_out, p.status);  // stage free once P V is done
-                    load_kv(j + 2, st);
-                }
+                umma_commit(BAR(kOFull + b));
+                if (j + 2 < nkt) issue_s(j + 2);
             }
+            // the last commit covers every MMA issued before it
+            drain_wait(BAR(kOFull + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1);
         }
         __syncwarp();
     } else {
-        // ================= softmax warps: thread r owns query row r
+        // ================= softmax warps: thread r owns query row r (tensor-memory lane r)
         // O lives in tensor memory and P V accumulates onto it. The softmax runs
-        // against a reference max m_ref that only moves when a row's max exceeds
-        // it by more than 2^8 (then O and l are rescaled), so P stays <= 256 and
-        // most tiles need no O traffic at all.
-        const int32_t r = tid;                      // 0..127 (TMEM lane r)
+        // against a reference max m_ref (log2 units) that only moves when a row's
+        // max exceeds it by more than 2^8 (then O and l are rescaled), so P stays
+        // <= 256 and most tiles need no O traffic at all.
+        const int32_t r = tid;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const bool valid = r < rows;
         const int32_t pr = pos0 + r;                // position of this row's query
-        constexpr float kSlack = 8.f;               // log2 of the largest P kept without rescaling
+        const float sl2 = p.scale_log2;
+        constexpr float kSlack = 8.f;
         float m_ref = -INFINITY, l = 0.f;
-        unsigned char *sPp = base + 5 * kTileBytes;
         for (int32_t j = 0; j < nkt; ++j) {
+            const int b = j & 1;
             const int32_t t0 = j * kKT;
-            bounded_wait(BAR(3), j & 1, timed_out, p.status);
+            bounded_wait(BAR(kSFull + b), (j >> 1) & 1, timed_out, p.status);
             tc_fence_after();
+            uint32_t raw[kKT];
+            tmem_ld128(tS(b) + lane_base, raw);
             float x[kKT];
 #pragma unroll
-            for (int c0 = 0; c0 < kKT; c0 += 32) {
-                float v[32];
-                tmem_ld32(tS + lane_base + c0, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[c0 + i] = v[i] * p.scale_log2;
-            }
+            for (int i = 0; i < kKT; ++i) x[i] = __uint_as_float(raw[i]);
             if (!(valid && t0 + kKT - 1 <= pr)) {   // the diagonal tile (or a row past the chunk): mask
 #pragma unroll
                 for (int i = 0; i < kKT; ++i) x[i] = (valid && t0 + i <= pr) ? x[i] : -INFINITY;
             }
-            float mx = -INFINITY;
+            float m8[8];
 #pragma unroll
-            for (int i = 0; i < kKT; ++i) mx = fmaxf(mx, x[i]);
+            for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+            for (int i = 8; i < kKT; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
             const bool move = mx > m_ref + kSlack;  // false when mx = -inf
             const float new_ref = move ? mx : m_ref;
             const float alpha = move ? ptx::ex2(m_ref - new_ref) : 1.f;   // m_ref = -inf: 0
-            // P's buffer and O are free once the previous tile's P V is done
-            if (j > 0) {
-                bounded_wait(BAR(5), (j - 1) & 1, timed_out, p.status);
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                // rescale O once P_{j-1} V is in it
+                bounded_wait(BAR(kOFull + (b ^ 1)), ((j - 1) >> 1) & 1, timed_out, p.status);
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, move)) {
 #pragma unroll
-                    for (int c0 = 0; c0 < kD; c0 += 32) {
-                        float v[32];
-                        tmem_ld32(tO + lane_base + c0, v);
+                for (int c0 = 0; c0 < kD; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tO + lane_base + c0, v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                        tmem_st32(tO + lane_base + c0, v);
-                    }
+                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                    tmem_st32(tO + lane_base + c0, v);
                 }
             }
             m_ref = new_ref;
+            if (j >= 2) bounded_wait(BAR(kOFull + b), ((j - 2) >> 1) & 1, timed_out, p.status);  // P[b] free
             const bool live = m_ref != -INFINITY;
-            float rs = 0.f;
+            const float neg = -m_ref;
+            unsigned char *sPp = base + (5 + b) * kTileBytes;
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < kKT / 8; ++c) {         // 16-byte chunks of 8 keys
                 uint32_t pk[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = live ? ptx::ex2(x[8 * c + 2 * e] - m_ref) : 0.f;
-                    const float p1 = live ? ptx::ex2(x[8 * c + 2 * e + 1] - m_ref) : 0.f;
+                    const float p0 = live ? ptx::ex2(fmaf(x[8 * c + 2 * e], sl2, neg)) : 0.f;
+                    const float p1 = live ? ptx::ex2(fmaf(x[8 * c + 2 * e + 1], sl2, neg)) : 0.f;
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     const float2 back = __half22float2(hp);   // the weights P V uses are the fp16 ones
-                    rs += back.x + back.y;
+                    rs[e] += back.x + back.y;
                     pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
                 const int sub = c >> 3, phys = (c & 7) ^ (r & 7);
                 *reinterpret_cast<uint4 *>(sPp + sub * kSub + r * 128 + phys * 16) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            l = l * alpha + rs;
+            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
             // the last tile: zero the V rows no query may see (they may hold non-finite garbage)
             if (j == nkt - 1) {
+                bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
                 const int32_t first_dead = kv_end - t0;          // rows [first_dead, 128) of the tile
-                const int st = j & 1;
-                unsigned char *sVp = base + (st == 0 ? 2 : 4) * kTileBytes;
+                unsigned char *sVp = base + (3 + b) * kTileBytes;
                 const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
                 for (int32_t w = tid; w < nwords * 2; w += 128) {
                     const int half = w / nwords, rem = w - half * nwords;
@@ -349,24 +399,23 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P (and zeroed V) -> MMA
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(BAR(4));
+            if (lane == 0) ptx::mbar_arrive(BAR(kPReady + b));
         }
-        bounded_wait(BAR(5), (nkt - 1) & 1, timed_out, p.status);
+        bounded_wait(BAR(kOFull + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1, timed_out, p.status);
         tc_fence_after();
         const float inv = valid ? 1.f / l : 0.f;
-        __half *dst = p.out + ((size_t)(q0 + i0 + r) * H + h) * kD;
+        uint32_t raw[kD];
+        tmem_ld128(tO + lane_base, raw);
+        if (valid) {
+            __half *dst = p.out + ((size_t)(q0 + i0 + r) * H + h) * kD;
 #pragma unroll
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-            float v[32];
-            tmem_ld32(tO + lane_base + c0, v);
-            if (valid) {
+            for (int d = 0; d < kD; d += 8) {
+                __half2 hv[4];
 #pragma unroll
-                for (int d = 0; d < 32; d += 8) {
-                    __half2 hv[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) hv[e] = __floats2half2_rn(v[d + 2 * e] * inv, v[d + 2 * e + 1] * inv);
-                    *reinterpret_cast<uint4 *>(dst + c0 + d) = *reinterpret_cast<const uint4 *>(hv);
-                }
+                for (int e = 0; e < 4; ++e)
+                    hv[e] = __floats2half2_rn(__uint_as_float(raw[d + 2 * e]) * inv,
+                                              __uint_as_float(raw[d + 2 * e + 1]) * inv);
+                *reinterpret_cast<uint4 *>(dst + d) = *reinterpret_cast<const uint4 *>(hv);
             }
         }
     }
