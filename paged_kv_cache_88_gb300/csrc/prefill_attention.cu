@@ -53,13 +53,16 @@ constexpr int kD = 128;              // head dim (MMA K of Q K^T, N of P V)
 constexpr int kHalf = 64;            // 64 fp16 = one 128-byte swizzle row
 constexpr int kSub = kQT * 128;      // bytes of one [128 rows x 64 elements] swizzled sub-tile (16 KB)
 constexpr int kTileBytes = 2 * kSub; // a 128 x 128 fp16 tile as two sub-tiles
-constexpr int kThreads = 192;        // warps 0-3 softmax, warp 4 MMA issue, warp 5 TMA loads
-constexpr uint32_t kTmemCols = 512;  // S0: [0, 128), S1: [128, 256), O: [256, 384)
+constexpr int kThreads = 320;        // warps 0-7 softmax, warp 8 MMA issue, warp 9 TMA loads
+constexpr int kSoftmaxThreads = 256;
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// shared memory: Q | K0 | K1 | V0 | V1 | P0 | P1 (each a 32 KB tile, 1024-aligned), barriers after
-constexpr int kSmemTiles = 7 * kTileBytes;
-constexpr int kSmemBytes = kSmemTiles + 256 /* barriers + flags */ + 1024 /* alignment slack */;
+// shared memory: Q | K0 | K1 | V0 | V1 (each a 32 KB tile, 1024-aligned), then the
+// row-max exchange [2 tiles][2 halves][128 rows] fp32, then barriers and flags
+constexpr int kSmemTiles = 5 * kTileBytes;
+constexpr int kXchgBytes = 2 * 2 * kQT * 4;
+constexpr int kSmemBytes = kSmemTiles + kXchgBytes + 256 /* barriers + flags */ + 1024 /* alignment slack */;
 
 // barrier indices (two-slot rings use index + slot)
 constexpr int kQFull = 0, kKFull = 1, kVFull = 3, kSFull = 5, kPReady = 7, kOFull = 9, kNumBars = 11;
@@ -98,39 +101,38 @@ __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, ui
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// The same MMA with A read from tensor memory (M rows on lanes, K along columns,
+// two fp16 per 32-bit column).
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// All 128 columns of this warp's 32 lanes in one load, completed before any
-// register is used (the wait sits in the same asm statement).
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+// Loads of 64 (32) consecutive columns of this warp's 32 lanes, completed
+// before any register is used (the wait sits in the same asm statement).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr) : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr) : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-    uint32_t r[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
         "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
@@ -173,7 +175,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // Pipeline of one CTA over its key tiles j = 0 .. nkt-1 (slot b = j & 1):
 //   loader : K_j -> K[b] once S_{j-2} is done; V_j -> V[b] once P_{j-2} V is done
 //   MMA    : S_0, S_1, then per j: [P_j ready] O += P_j V_j, S_{j+2} -> S[b]
-//   softmax: per j: S[b] -> P_j (fp16) in P[b], once P_{j-2} V is done
+//   softmax: per j: S[b] -> P_j (fp16, tensor memory P[b]) once P_{j-2} V is done
 // so the tensor cores compute S_{j+1} (and finish P_{j-1} V) while the softmax
 // warps work on tile j. Every barrier is waited on at most one phase behind.
 __global__ void __launch_bounds__(kThreads, 1)
@@ -185,8 +187,8 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     const uint32_t sQ = ptx::smem_addr(base);
     auto sK = [sQ](int b) { return sQ + (uint32_t)(1 + b) * kTileBytes; };
     auto sV = [sQ](int b) { return sQ + (uint32_t)(3 + b) * kTileBytes; };
-    auto sP = [sQ](int b) { return sQ + (uint32_t)(5 + b) * kTileBytes; };
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kSmemTiles);
+    float *xchg = reinterpret_cast<float *>(base + kSmemTiles);          // [2][2][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kSmemTiles + kXchgBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int32_t *timed_out = reinterpret_cast<volatile int32_t *>(bars + kNumBars + 1);
     const uint32_t bar0 = ptx::smem_addr(bars);
@@ -214,7 +216,8 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     const int32_t nkt = (kv_end + kKT - 1) / kKT;
 
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(BAR(i), (i == kPReady || i == kPReady + 1) ? 4 : 1);
+        for (int i = 0; i < kNumBars; ++i)
+            ptx::mbar_init(BAR(i), (i == kPReady || i == kPReady + 1) ? kSoftmaxThreads / 32 : 1);
         *timed_out = 0;
         ptx::fence_barrier_init();
     }
@@ -230,9 +233,10 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     const uint32_t tmem = *tmem_slot;
     auto tS = [tmem](int b) { return tmem + (uint32_t)b * kKT; };
     const uint32_t tO = tmem + 2 * kKT;
+    auto tP = [tmem](int b) { return tmem + 3 * kKT + (uint32_t)b * (kKT / 2); };
 
-    if (warp == 5) {
-        // ================= loader: TMA for Q, then K and V tiles (one 16-row box per block of 16)
+    if (warp == 9) {
+        // ================= loader: TMA for Q, then K and V tiles (one box per block of the table)
         const int32_t rowsb = B < kKT ? B : kKT;       // rows per box; B is a power of two, 8..256
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(BAR(kQFull), kTileBytes);
@@ -275,7 +279,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
             drain_wait(BAR(kKFull + (j & 1)), (j >> 1) & 1);
             drain_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1);
         }
-    } else if (warp == 4) {
+    } else if (warp == 8) {
         // ================= MMA issue (one thread)
         if (lane == 0) {
             const uint32_t id_qk = umma_idesc(0), id_pv = umma_idesc(1);
@@ -298,12 +302,11 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
                 bounded_wait(BAR(kPReady + b), (j >> 1) & 1, timed_out, p.status);   // P_j written, S[b] read
                 bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
                 tc_fence_after();
-                // O += P_j V_j over the tile's keys: A = P (K-major), B = V rows (MN-major, halves 16 KB apart)
-                for (int ks = 0; ks < kKT / 16; ++ks) {
-                    const uint32_t aoff = (ks >> 2) * kSub + (ks & 3) * 32;
-                    umma(tO, umma_desc(sP(b) + aoff, 16, 1024), umma_desc(sV(b) + ks * 2048, kSub, 1024), id_pv,
-                         (j > 0 || ks > 0) ? 1u : 0u);
-                }
+                // O += P_j V_j over the tile's keys: A = P from tensor memory (8 columns per 16 keys),
+                // B = V rows (MN-major, halves 16 KB apart)
+                for (int ks = 0; ks < kKT / 16; ++ks)
+                    umma_ts(tO, tP(b) + ks * 8, umma_desc(sV(b) + ks * 2048, kSub, 1024), id_pv,
+                            (j > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(BAR(kOFull + b));
                 if (j + 2 < nkt) issue_s(j + 2);
             }
@@ -312,104 +315,114 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         }
         __syncwarp();
     } else {
-        // ================= softmax warps: thread r owns query row r (tensor-memory lane r)
+        // ================= softmax warps: query row r (tensor-memory lane r) is shared by
+        // warps q and q + 4 (q = r / 32), each taking one 64-key half of every S tile and
+        // one 64-column half of O; the two exchange their row max once per tile.
         // O lives in tensor memory and P V accumulates onto it. The softmax runs
-        // against a reference max m_ref (log2 units) that only moves when a row's
+        // against a reference max m_ref (log2 units) that only moves when the row's
         // max exceeds it by more than 2^8 (then O and l are rescaled), so P stays
         // <= 256 and most tiles need no O traffic at all.
-        const int32_t r = tid;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int hf = warp >> 2, quad = warp & 3;
+        const int32_t r = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const bool valid = r < rows;
         const int32_t pr = pos0 + r;                // position of this row's query
         const float sl2 = p.scale_log2;
         constexpr float kSlack = 8.f;
+        constexpr int kCols = kKT / 2;              // keys of S (and columns of O) per thread
         float m_ref = -INFINITY, l = 0.f;
         for (int32_t j = 0; j < nkt; ++j) {
             const int b = j & 1;
-            const int32_t t0 = j * kKT;
+            const int32_t t0 = j * kKT + hf * kCols;   // first key of this thread's half
             bounded_wait(BAR(kSFull + b), (j >> 1) & 1, timed_out, p.status);
             tc_fence_after();
-            uint32_t raw[kKT];
-            tmem_ld128(tS(b) + lane_base, raw);
-            float x[kKT];
+            uint32_t raw[kCols];
+            tmem_ld64(tS(b) + lane_base + hf * kCols, raw);
+            float x[kCols];
 #pragma unroll
-            for (int i = 0; i < kKT; ++i) x[i] = __uint_as_float(raw[i]);
-            if (!(valid && t0 + kKT - 1 <= pr)) {   // the diagonal tile (or a row past the chunk): mask
+            for (int i = 0; i < kCols; ++i) x[i] = __uint_as_float(raw[i]);
+            if (!(valid && t0 + kCols - 1 <= pr)) {   // the diagonal tile (or a row past the chunk): mask
 #pragma unroll
-                for (int i = 0; i < kKT; ++i) x[i] = (valid && t0 + i <= pr) ? x[i] : -INFINITY;
+                for (int i = 0; i < kCols; ++i) x[i] = (valid && t0 + i <= pr) ? x[i] : -INFINITY;
             }
             float m8[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) m8[k] = x[k];
 #pragma unroll
-            for (int i = 8; i < kKT; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
-            const bool move = mx > m_ref + kSlack;  // false when mx = -inf
+            for (int i = 8; i < kCols; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            // row max across the two halves (a slot per tile parity, so a fast partner
+            // never overwrites a value not yet read)
+            float *xs = xchg + b * 2 * kQT;
+            xs[hf * kQT + r] = mx;
+            ptx::named_barrier(1 + quad, 64);
+            mx = fmaxf(mx, xs[(hf ^ 1) * kQT + r]) * sl2;
+            const bool move = mx > m_ref + kSlack;  // false when mx = -inf; the same in both halves
             const float new_ref = move ? mx : m_ref;
             const float alpha = move ? ptx::ex2(m_ref - new_ref) : 1.f;   // m_ref = -inf: 0
             if (j > 0 && __any_sync(0xffffffffu, move)) {
-                // rescale O once P_{j-1} V is in it
+                // rescale this half of O once P_{j-1} V is in it
                 bounded_wait(BAR(kOFull + (b ^ 1)), ((j - 1) >> 1) & 1, timed_out, p.status);
                 tc_fence_after();
 #pragma unroll
-                for (int c0 = 0; c0 < kD; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tO + lane_base + c0, v);
+                for (int c0 = 0; c0 < kCols; c0 += 32) {
+                    uint32_t v[32];
+                    const uint32_t ta = tO + lane_base + hf * kCols + c0;
+                    tmem_ld32(ta, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                    tmem_st32(tO + lane_base + c0, v);
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    tmem_st32(ta, v);
                 }
             }
             m_ref = new_ref;
             if (j >= 2) bounded_wait(BAR(kOFull + b), ((j - 2) >> 1) & 1, timed_out, p.status);  // P[b] free
             const bool live = m_ref != -INFINITY;
             const float neg = -m_ref;
-            unsigned char *sPp = base + (5 + b) * kTileBytes;
             float rs[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[kCols / 2];
 #pragma unroll
-            for (int c = 0; c < kKT / 8; ++c) {         // 16-byte chunks of 8 keys
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = live ? ptx::ex2(fmaf(x[8 * c + 2 * e], sl2, neg)) : 0.f;
-                    const float p1 = live ? ptx::ex2(fmaf(x[8 * c + 2 * e + 1], sl2, neg)) : 0.f;
-                    const __half2 hp = __floats2half2_rn(p0, p1);
-                    const float2 back = __half22float2(hp);   // the weights P V uses are the fp16 ones
-                    rs[e] += back.x + back.y;
-                    pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
-                }
-                const int sub = c >> 3, phys = (c & 7) ^ (r & 7);
-                *reinterpret_cast<uint4 *>(sPp + sub * kSub + r * 128 + phys * 16) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int e = 0; e < kCols / 2; ++e) {
+                const float p0 = live ? ptx::ex2(fmaf(x[2 * e], sl2, neg)) : 0.f;
+                const float p1 = live ? ptx::ex2(fmaf(x[2 * e + 1], sl2, neg)) : 0.f;
+                const __half2 hp = __floats2half2_rn(p0, p1);
+                const float2 back = __half22float2(hp);   // the weights P V uses are the fp16 ones
+                rs[e & 3] += back.x + back.y;
+                pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
             }
+            tmem_st32(tP(b) + lane_base + hf * (kCols / 2), pk);
             l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
             // the last tile: zero the V rows no query may see (they may hold non-finite garbage)
             if (j == nkt - 1) {
                 bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
-                const int32_t first_dead = kv_end - t0;          // rows [first_dead, 128) of the tile
+                const int32_t first_dead = kv_end - j * kKT;      // rows [first_dead, 128) of the tile
                 unsigned char *sVp = base + (3 + b) * kTileBytes;
                 const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
-                for (int32_t w = tid; w < nwords * 2; w += 128) {
+                for (int32_t w = tid; w < nwords * 2; w += kSoftmaxThreads) {
                     const int half = w / nwords, rem = w - half * nwords;
                     const int row = first_dead + rem / 8, cc = rem & 7;
                     *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
                 }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // zeroed V -> MMA
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P (and zeroed V) -> MMA
             tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(BAR(kPReady + b));
         }
         bounded_wait(BAR(kOFull + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1, timed_out, p.status);
         tc_fence_after();
-        const float inv = valid ? 1.f / l : 0.f;
-        uint32_t raw[kD];
-        tmem_ld128(tO + lane_base, raw);
+        // l of the whole row: both halves' sums (the slot of parity nkt & 1 is free by now)
+        float *xs = xchg + (nkt & 1) * 2 * kQT;
+        xs[hf * kQT + r] = l;
+        ptx::named_barrier(1 + quad, 64);
+        const float lt = xs[r] + xs[kQT + r];
+        const float inv = valid ? 1.f / lt : 0.f;
+        uint32_t raw[kCols];
+        tmem_ld64(tO + lane_base + hf * kCols, raw);
         if (valid) {
-            __half *dst = p.out + ((size_t)(q0 + i0 + r) * H + h) * kD;
+            __half *dst = p.out + ((size_t)(q0 + i0 + r) * H + h) * kD + hf * kCols;
 #pragma unroll
-            for (int d = 0; d < kD; d += 8) {
+            for (int d = 0; d < kCols; d += 8) {
                 __half2 hv[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
