@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--swap", action="store_true", help="measure swap-out / swap-in of one sequence instead")
     ap.add_argument("--prefill", type=int, default=0, metavar="CHUNK",
                     help="measure causal prefill of CHUNK-token chunks over the workload's cache instead")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="attend shared prefixes per sequence (no prefix pass)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -284,7 +286,7 @@ def run_ours(args):
         w = wl.make_workload(args.config, decode_steps=total_steps, layout=args.layout,
                              block_size=args.block_size, num_layers=args.layers, seed=rank_seed(args.config, rank),
                              kv_dtype=args.kv_dtype)
-    eng = DecodeEngine(w, device=str(dev), fill="torch")
+    eng = DecodeEngine(w, device=str(dev), fill="torch", cascade=not args.no_cascade)
     eng.run_script(values="torch")
     torch.cuda.synchronize()
     L, S, H, D = w.num_layers, w.num_seqs, w.num_heads, w.head_dim
@@ -311,6 +313,7 @@ def run_ours(args):
 
     # ---- timed region: K decode steps, inputs resident in HBM
     step_bytes = []
+    step_unique = []
     launches = 0
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
@@ -321,7 +324,8 @@ def run_ours(args):
         for _ in range(args.steps):
             n_slots, n_pairs = eng.step_graph(stream)
             step_bytes.append(eng.kv_bytes_per_layer())
-            launches += (L if eng.fused else 2 * L) + (1 if n_pairs else 0)
+            step_unique.append(eng.unique_kv_bytes_per_layer())
+            launches += (L if eng.fused else 2 * L) + (L if eng.plan_groups else 0) + (1 if n_pairs else 0)
         host_ms = (time.perf_counter() - h0) * 1e3 / args.steps
         t_end.record(stream)
         barrier()
@@ -340,6 +344,9 @@ def run_ours(args):
     ms = t_start.elapsed_time(t_end)
     attn_ms_total = a0.elapsed_time(a1)
     attn_launch_bytes = eng.kv_bytes_per_layer()
+    cascading = bool(eng.plan_groups)
+    if cascading:   # the layer's attention is the prefix pass + the private pass: count distinct bytes
+        attn_launch_bytes = eng.unique_kv_bytes_per_layer()
     status = eng.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status:#x} in the timed region")
@@ -354,7 +361,7 @@ def run_ours(args):
     mean_launch_ms = attn_ms_total / n_attn
     achieved = (attn_launch_bytes + extra) / (mean_launch_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = kernel_traffic(attn_launch_bytes + extra)
+    traffic = None if cascading else kernel_traffic(attn_launch_bytes + extra)
 
     # ---- end to end through the public API: inputs from pinned host memory, output read back
     e2e = None
@@ -402,12 +409,19 @@ def run_ours(args):
             "config": dict(w.describe(), l2="inputs larger than L2 (each layer's KV >> 129 MB), no flush",
                            parallelism="replicas" if world > 1 else "single",
                            mean_context_timed=float(np.mean(step_bytes)) / w.kv_bytes_per_token_layer / S,
-                           step="decode step as one CUDA graph: per layer one fused append+attention launch"),
+                           step=("decode step as one CUDA graph: per layer the shared-prefix pass, then one "
+                                 "fused append+attention launch over the private rest" if cascading else
+                                 "decode step as one CUDA graph: per layer one fused append+attention launch")),
             "seq_steps_per_s": seq_steps,
             "frac_of_hbm_peak": value / peak,
+            **({"unique_gbps": value * sum(step_unique) / sum(step_bytes),
+                "frac_unique_of_hbm_peak": value * sum(step_unique) / sum(step_bytes) / peak,
+                "cascade": {"groups": int(eng.plan_groups), "splits": int(eng.plan_splits),
+                            "prefix_tokens": int(eng.plan_prefix)}} if cascading else {}),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                         "kernel": "decode_attention_kernel<128>", "launches": n_attn,
+                         "kernel": ("prefix pass + decode_attention_kernel<128> (distinct KV bytes)"
+                                    if cascading else "decode_attention_kernel<128>"), "launches": n_attn,
                          "mean_launch_us": 1e3 * mean_launch_ms, "bytes_per_launch": attn_launch_bytes + extra,
                          "grid_ctas": info["grid_ctas"], "ctas_per_sm": info["ctas_per_sm"]},
             "clocks": clocks,

@@ -343,6 +343,90 @@ pkv_status pkv_prefill_attention(const pkv_pool *pool, int32_t layer, const void
                                  const int32_t *context_lens, float scale, void *out, uint32_t *status,
                                  void *stream);
 
+/* ------------------------------------------------ shared-prefix (cascade) decode
+ *
+ * When sequences share their leading blocks (a forked prompt, or prefix-cache
+ * hits: icman.com.cn/news/78786 §3.4, hnwysp.cn/news/103996 §3.3), the decode
+ * attention of every one of them reads the same prefix K/V. The cascade splits
+ * such a sequence's context in two: the shared prefix, attended ONCE per group
+ * of sequences by pkv_prefix_attention (all the group's queries against each
+ * prefix K/V tile, on the tensor cores), and the private rest, attended by
+ * pkv_decode_attention_ex, whose combine step merges the prefix pieces in. The
+ * result is the same attention, up to the order of rounding. */
+
+typedef struct {
+    int32_t first_seq;     /* members: sequences first_seq .. first_seq + num_seqs - 1 */
+    int32_t num_seqs;      /* 2 .. PKV_MAX_GROUP_SEQS */
+    int32_t prefix_tokens; /* shared leading tokens: whole blocks, the same ids in every member's table */
+    int32_t reserved;      /* 0 */
+} pkv_prefix_group;
+
+#define PKV_MAX_GROUP_SEQS 128
+#define PKV_MAX_PREFIX_SPLITS 8
+
+/* Host planner of the cascade for one step. block_tables: host int32
+ * [num_seqs][max_blocks]; context_lens: host int32 [num_seqs], the lengths the
+ * attention will use. A group is a run of consecutive sequences whose first
+ * blocks are the same block ids; a run grows while the common prefix keeps at
+ * least min_prefix_tokens tokens and the run holds at most PKV_MAX_GROUP_SEQS
+ * sequences; runs of fewer than min_group (>= 2) sequences are dropped. A
+ * prefix counts only blocks lying wholly inside every member's context.
+ * Writes the groups (host, at most max_groups; further runs are dropped),
+ * *num_groups, and seq_begin (host int32 [num_seqs]): the group's prefix_tokens
+ * for a member, 0 for any other sequence. Deterministic; reads no device
+ * memory. INVALID_ARG for bad sizes or NULL pointers. */
+pkv_status pkv_cascade_plan(const int32_t *block_tables, int32_t max_blocks, const int32_t *context_lens,
+                            int32_t num_seqs, int32_t block_size, int32_t min_group,
+                            int32_t min_prefix_tokens, pkv_prefix_group *groups, int32_t max_groups,
+                            int32_t *num_groups, int32_t *seq_begin);
+
+/* Bytes of the prefix-piece buffer for these sizes: num_seqs * num_heads *
+ * PKV_MAX_PREFIX_SPLITS pieces of (head_dim + 4) fp32 (0 on bad sizes). */
+size_t pkv_prefix_pieces_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim);
+
+/* Key splits per group that pkv_prefix_attention should use on the current
+ * device: enough (group, head, split) CTAs to cover the SMs once, at most one
+ * split per 128 prefix tokens, within 1 .. PKV_MAX_PREFIX_SPLITS. */
+int32_t pkv_prefix_splits(int32_t num_groups, int32_t num_heads, int32_t max_prefix_tokens);
+
+/* The prefix half of the cascade for one layer. For each group g (device array
+ * `groups` of num_groups), head h and split k < splits: the queries q[s][h] of
+ * the group's members against the keys of split k of the prefix
+ * [0, prefix_tokens) (tiles of 128 keys dealt to the splits in order), read
+ * through table row first_seq. Writes, for each member s, the piece
+ *   o[d] = sum_t 2^(x_t - m) V_t[d],  l = sum_t 2^(x_t - m),  m,
+ * with x_t = scale * log2(e) * q[s][h] . K_t and m a reference at least as
+ * large as max_t x_t - 8, as fp32 (o[0..D-1], m, l) at
+ *   pieces + ((s * H + h) * PKV_MAX_PREFIX_SPLITS + k) * (D + 4);
+ * a split with no keys writes m = -inf, l = 0, o = 0. q: device fp16
+ * [num_seqs][H][D], 16-byte aligned. pieces: device, >=
+ * pkv_prefix_pieces_bytes(num_seqs, H, D) bytes, 16-byte aligned. status:
+ * device uint32 word (required): a group outside [0, num_seqs), with more
+ * than PKV_MAX_GROUP_SEQS members or a prefix not in whole blocks inside the
+ * table is flagged PKV_DEV_BAD_LENGTH and writes no pieces. fp16 products,
+ * fp32 accumulation, weights enter P V in fp16. The pool must be fp16, HND,
+ * head_dim 128 (UNSUPPORTED otherwise). */
+pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void *q,
+                                const pkv_prefix_group *groups, int32_t num_groups, int32_t splits,
+                                const int32_t *block_tables, int32_t max_blocks, int32_t num_seqs, float scale,
+                                void *pieces, size_t pieces_bytes, uint32_t *status, void *stream);
+
+/* pkv_decode_append_attention and pkv_pool_decode_attention in one entry, with
+ * the private half of the cascade. k_new, v_new, slot_mapping: all NULL = no
+ * append (else as pkv_decode_append_attention). seq_begin, pieces: both NULL =
+ * no cascade (the plain attention). Otherwise seq_begin is device int32
+ * [num_seqs]: sequence s attends here to its tokens [seq_begin[s], T_s) and,
+ * when seq_begin[s] > 0, merges in the `splits` prefix pieces that
+ * pkv_prefix_attention wrote for it earlier on the same stream. seq_begin[s]
+ * must be a multiple of the block size in [0, T_s]; any other value is
+ * flagged PKV_DEV_BAD_LENGTH and read as 0 (no prefix). fp16 pools only when
+ * cascading (the prefix pass runs on fp16 tensor cores). */
+pkv_status pkv_decode_attention_ex(const pkv_pool *pool, int32_t layer, const void *q, const void *k_new,
+                                   const void *v_new, const int64_t *slot_mapping, const int32_t *block_tables,
+                                   int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs,
+                                   const int32_t *seq_begin, const float *pieces, int32_t splits, float scale,
+                                   void *out, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of workspace pkv_decode_attention needs for these sizes on the
  * current CUDA device (0 and a pkv_last_error message on bad arguments). */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim);

@@ -31,8 +31,12 @@ EXPORTED = [
     "pkv_pool_decode_attention", "pkv_decode_launch_info", "pkv_decode_append_attention",
     "pkv_decode_attention_static", "pkv_block_hash", "pkv_prefix_lookup", "pkv_prefix_register",
     "pkv_pool_set_scales", "pkv_swap_bytes_per_block", "pkv_gather_blocks", "pkv_scatter_blocks",
-    "pkv_prefill_attention",
+    "pkv_prefill_attention", "pkv_cascade_plan", "pkv_prefix_pieces_bytes", "pkv_prefix_splits",
+    "pkv_prefix_attention", "pkv_decode_attention_ex",
 ]
+
+MAX_GROUP_SEQS = 128
+MAX_PREFIX_SPLITS = 8
 
 
 class PkvError(RuntimeError):
@@ -46,6 +50,11 @@ class PoolDesc(ctypes.Structure):
     _fields_ = [("num_layers", ctypes.c_int32), ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("layout", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32)]
+
+
+class PrefixGroup(ctypes.Structure):
+    _fields_ = [("first_seq", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("prefix_tokens", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class Stats(ctypes.Structure):
@@ -103,6 +112,12 @@ def lib() -> ctypes.CDLL:
             "pkv_gather_blocks": (i32, [vp, vp, i32, vp, vp, vp]),
             "pkv_scatter_blocks": (i32, [vp, vp, i32, vp, vp, vp]),
             "pkv_prefill_attention": (i32, [vp, i32, vp, vp, i32, i32, i32, vp, i32, vp, f32, vp, vp, vp]),
+            "pkv_cascade_plan": (i32, [vp, i32, vp, i32, i32, i32, i32, vp, i32, ctypes.POINTER(i32), vp]),
+            "pkv_prefix_pieces_bytes": (sz, [i32, i32, i32]),
+            "pkv_prefix_splits": (i32, [i32, i32, i32]),
+            "pkv_prefix_attention": (i32, [vp, i32, vp, vp, i32, i32, vp, i32, i32, f32, vp, sz, vp, vp]),
+            "pkv_decode_attention_ex": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp,
+                                              sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -335,6 +350,29 @@ class Pool:
                                           max_chunk, _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
                                           float(scale), _ptr(out), _ptr(status), _stream(stream)))
 
+    def prefix_attention(self, layer: int, q, groups_dev, num_groups: int, splits: int, block_tables, pieces,
+                         status, scale: float = 0.0, stream=None) -> None:
+        """The cascade's prefix pass (pkv_prefix_attention); ``groups_dev``: device int32 [G, 4]."""
+        for t, dt, name in ((q, "float16", "q"), (groups_dev, "int32", "groups"),
+                            (block_tables, "int32", "block_tables"), (status, "int32", "status")):
+            _require(t, dt, name)
+        check(lib().pkv_prefix_attention(self._h, layer, _ptr(q), _ptr(groups_dev), num_groups, splits,
+                                         _ptr(block_tables), block_tables.shape[1], q.shape[0], float(scale),
+                                         _ptr(pieces), pieces.numel() * pieces.element_size(), _ptr(status),
+                                         _stream(stream)))
+
+    def decode_attention_ex(self, layer: int, q, block_tables, context_lens, out, workspace, k_new=None, v_new=None,
+                            slot_mapping=None, seq_begin=None, pieces=None, splits: int = 0, scale: float = 0.0,
+                            stream=None) -> None:
+        """pkv_decode_attention_ex: optional fused append, optional cascade (private half + merge)."""
+        for t, dt, name in ((q, "float16", "q"), (out, "float16", "out"), (block_tables, "int32", "block_tables"),
+                            (context_lens, "int32", "context_lens")):
+            _require(t, dt, name)
+        check(lib().pkv_decode_attention_ex(
+            self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(block_tables),
+            block_tables.shape[1], _ptr(context_lens), q.shape[0], _ptr(seq_begin), _ptr(pieces), int(splits),
+            float(scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
     def layer_view(self, which: str, layer: int):
         t = self.k_pool if which == "k" else self.v_pool
         d = self.desc
@@ -354,6 +392,39 @@ def prompt_block_hashes(token_ids: Sequence[int], block_size: int) -> list:
         parent = block_hash(parent, token_ids[i * block_size:(i + 1) * block_size])
         hs.append(parent)
     return hs
+
+
+def cascade_plan(block_tables: np.ndarray, context_lens: np.ndarray, block_size: int, min_group: int = 2,
+                 min_prefix_tokens: int = 0, max_groups: Optional[int] = None, groups_out: Optional[np.ndarray] = None,
+                 begin_out: Optional[np.ndarray] = None):
+    """pkv_cascade_plan on host arrays: (groups int32 [G, 4], seq_begin int32 [S]).
+
+    ``groups_out`` / ``begin_out`` (optional, e.g. pinned staging) receive the
+    plan in place; the returned arrays are views of them.
+    """
+    tab = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    S = tab.shape[0]
+    cap = S if max_groups is None else max_groups
+    groups = groups_out if groups_out is not None else np.zeros((max(cap, 1), 4), dtype=np.int32)
+    begin = begin_out if begin_out is not None else np.zeros(S, dtype=np.int32)
+    if groups.dtype != np.int32 or begin.dtype != np.int32 or groups.shape[0] < cap or begin.shape[0] < S:
+        raise ValueError("plan buffers too small or not int32")
+    n = i32()
+    check(lib().pkv_cascade_plan(_ptr(tab), tab.shape[1], _ptr(lens), S, block_size, min_group, min_prefix_tokens,
+                                 _ptr(groups), cap, ctypes.byref(n), _ptr(begin)))
+    return groups[: n.value], begin[:S]
+
+
+def prefix_pieces_bytes(num_seqs: int, num_heads: int, head_dim: int) -> int:
+    n = lib().pkv_prefix_pieces_bytes(num_seqs, num_heads, head_dim)
+    if n == 0 and num_seqs > 0:
+        raise PkvError(1, last_error())
+    return int(n)
+
+
+def prefix_splits(num_groups: int, num_heads: int, max_prefix_tokens: int) -> int:
+    return int(lib().pkv_prefix_splits(num_groups, num_heads, max_prefix_tokens))
 
 
 def decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int) -> int:

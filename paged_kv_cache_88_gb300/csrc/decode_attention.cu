@@ -66,6 +66,9 @@ using namespace pkv;
 #ifndef PKV_ATTN_MIN_CTAS
 #define PKV_ATTN_MIN_CTAS 4
 #endif
+#ifndef PKV_ATTN_ACQREL
+#define PKV_ATTN_ACQREL 1
+#endif
 
 constexpr int kTile = PKV_ATTN_TILE;              // tokens per pipeline stage
 constexpr int kConsumerWarps = PKV_ATTN_WARPS;    // warps that compute
@@ -101,6 +104,12 @@ struct Params {
     unsigned char *v_layer;
     float *k_scale;      // quantised cache: this layer's per-(token, head) scales, [N][H][B]
     float *v_scale;
+    // shared-prefix cascade (null = none): sequence s attends here to tokens
+    // [begin[s], T_s) and merges pre_splits prefix pieces (o[D], m, l) of
+    // [S][H][PKV_MAX_PREFIX_SPLITS][D + 4] when begin[s] > 0
+    const int32_t *begin;
+    const float *pre;
+    int32_t pre_splits;
     int32_t S, H, max_blocks, B, N, layout;
     float scale_log2;    // scale * log2(e)
 };
@@ -124,7 +133,7 @@ __host__ __device__ constexpr int piece_stride(int D) { return D + 4; }
 template <int D, bool Q8>
 __host__ __device__ constexpr size_t smem_bytes_t(int S) {
     return ((size_t)Stage<D, Q8>::kStages * Stage<D, Q8>::kBytes + (size_t)kConsumerWarps * (D + 2) * sizeof(float) +
-            (size_t)(2 * S + 2) * sizeof(int32_t) + 15) / 16 * 16 +
+            (size_t)(3 * S + 2) * sizeof(int32_t) + 15) / 16 * 16 +
            2 * Stage<D, Q8>::kStages * sizeof(uint64_t) + 16 + 128;  // + slack to align the base to 128 bytes
 }
 
@@ -133,7 +142,8 @@ struct Smem {
     float *red_o;          // [kConsumerWarps][D]
     float *red_m;          // [kConsumerWarps]
     float *red_l;          // [kConsumerWarps]
-    int32_t *len;          // [S]
+    int32_t *len;          // [S] tokens attended here (T_s - beg[s])
+    int32_t *beg;          // [S] first token attended here (the cascade's prefix length, else 0)
     int32_t *base;         // [S + 1] exclusive prefix of H * ntiles
     uint64_t *full;        // [kStages]
     uint64_t *empty;       // [kStages]
@@ -154,6 +164,8 @@ __device__ __forceinline__ Smem carve(unsigned char *raw, int S) {
     m.red_l = reinterpret_cast<float *>(p);
     p += kConsumerWarps * sizeof(float);
     m.len = reinterpret_cast<int32_t *>(p);
+    p += (size_t)S * sizeof(int32_t);
+    m.beg = reinterpret_cast<int32_t *>(p);
     p += (size_t)S * sizeof(int32_t);
     m.base = reinterpret_cast<int32_t *>(p);
     p += (size_t)(S + 1) * sizeof(int32_t);
@@ -234,6 +246,33 @@ __device__ __forceinline__ bool wait_phase(const Smem &sm, uint32_t bar, uint32_
     }
 }
 
+// Fold the cascade's prefix pieces of (s, h) into a combine in progress: M, L
+// and this thread's output elements O[r] (element tid + r * kConsumerThreads),
+// all relative to 2^M. The pieces were written by an earlier launch.
+template <int D, int DPT>
+__device__ __forceinline__ void merge_prefix(const Params &p, int32_t s, int32_t h, int tid, float &M, float &L,
+                                             float (&O)[DPT]) {
+    const float *base = p.pre + ((size_t)s * p.H + h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
+    float Mn = M;
+    for (int k = 0; k < p.pre_splits; ++k) Mn = fmaxf(Mn, __ldcg(base + k * (D + 4) + D));
+    if (Mn == -INFINITY) return;
+    const float a = ptx::ex2(M - Mn);          // M = -inf: 0
+    L *= a;
+#pragma unroll
+    for (int r = 0; r < DPT; ++r) O[r] *= a;
+    for (int k = 0; k < p.pre_splits; ++k) {
+        const float *pc = base + k * (D + 4);
+        const float w = ptx::ex2(__ldcg(pc + D) - Mn);   // an empty piece (m = -inf): 0
+        L = fmaf(w, __ldcg(pc + D + 1), L);
+#pragma unroll
+        for (int r = 0; r < DPT; ++r) {
+            const int d = tid + r * kConsumerThreads;
+            if (d < D) O[r] = fmaf(w, __ldcg(pc + d), O[r]);
+        }
+    }
+    M = Mn;
+}
+
 template <int D, bool Q8>
 __global__ void __launch_bounds__(kThreads, D >= 256 ? 1 : PKV_ATTN_MIN_CTAS)
 decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -273,7 +312,16 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             atomicOr(p.status, PKV_DEV_BAD_LENGTH);
             T = T < 0 ? 0 : cap;
         }
-        sm.len[s] = T;
+        int32_t b0 = 0;
+        if (p.begin != nullptr) {
+            b0 = p.begin[s];
+            if (b0 < 0 || b0 > T || b0 % p.B != 0) {   // not a prefix in whole blocks: attend all here
+                atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+                b0 = 0;
+            }
+        }
+        sm.len[s] = T - b0;
+        sm.beg[s] = b0;
     }
     __syncthreads();
     if (warp == 0) {
@@ -297,12 +345,28 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     const int32_t total = sm.base[S];
     const int32_t cta = blockIdx.x;
 
-    // Empty contexts: out = 0 (softmax over no tokens contributes nothing).
+    // Nothing to attend here: out = 0 for an empty context (softmax over no
+    // tokens contributes nothing), the merged prefix pieces for a sequence the
+    // cascade's prefix covers entirely.
     if (warp < kConsumerWarps) {
         for (int32_t i = cta; i < S * H; i += gridDim.x) {
-            if (sm.len[i / H] != 0) continue;
-            if (tid < D / 8)
+            const int32_t s = i / H;
+            if (sm.len[s] != 0) continue;
+            if (sm.beg[s] > 0) {
+                constexpr int DPT = (D + kConsumerThreads - 1) / kConsumerThreads;
+                float M = -INFINITY, L = 0.f, O[DPT];
+#pragma unroll
+                for (int r = 0; r < DPT; ++r) O[r] = 0.f;
+                merge_prefix<D, DPT>(p, s, i - s * H, tid, M, L, O);
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+                for (int r = 0; r < DPT; ++r) {
+                    const int d = tid + r * kConsumerThreads;
+                    if (d < D) p.out[(size_t)i * D + d] = __float2half_rn(O[r] * inv);
+                }
+            } else if (tid < D / 8) {
                 reinterpret_cast<uint4 *>(p.out + (size_t)i * D)[tid] = make_uint4(0, 0, 0, 0);
+            }
         }
     }
     // The tile list is split over min(CTAs, tiles) CTAs so that every working CTA
@@ -388,9 +452,9 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 new_slot = -1;
                 __syncwarp();
             }
-            const int32_t T = sm.len[c.s];
-            const int32_t t0 = c.t * kTile;
-            const int32_t ntok = min(kTile, T - t0);
+            const int32_t tt = c.t * kTile;                    // the tile's first token attended here
+            const int32_t ntok = min(kTile, sm.len[c.s] - tt);
+            const int32_t t0 = sm.beg[c.s] + tt;               // its position in the sequence
             const int32_t lb = t0 / B;                         // first logical block of the tile
             const int32_t nbox = B < kTile ? (ntok + B - 1) / B : 1;
             const int32_t r0 = B < kTile ? 0 : t0 % B;         // first row inside the block
@@ -636,6 +700,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             const int32_t cb = cta_of(total, grid, seg_hi);
             __half *dst_out = p.out + ((size_t)c.s * H + c.h) * D;
             if (ca == cb) {
+                if (sm.beg[c.s] > 0) merge_prefix<D, DPT>(p, c.s, c.h, tid, M, L, O);
                 const float inv = 1.f / L;
 #pragma unroll
                 for (int r = 0; r < DPT; ++r) {
@@ -654,13 +719,18 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                     piece[D] = M;
                     piece[D + 1] = L;
                 }
-                // piece stores -> barrier -> one fence + counter bump (release); the
-                // last arriver fences again before reading the pieces (acquire)
+                // piece stores -> barrier -> one acquire-release counter bump: it
+                // publishes this CTA's piece and, for the last arriver, makes
+                // every other piece visible (the barrier after it passes that on)
                 ptx::named_barrier(1, kConsumerThreads);
                 if (tid == 0) {
+#if PKV_ATTN_ACQREL
+                    const int32_t prev = ptx::atom_add_acq_rel_gpu(p.counters + (size_t)c.s * H + c.h, 1);
+#else
                     __threadfence();
                     const int32_t prev = atomicAdd(p.counters + (size_t)c.s * H + c.h, 1);
                     __threadfence();
+#endif
                     sm.flags[1] = (prev == cb - ca) ? 1 : 0;
                 }
                 ptx::named_barrier(1, kConsumerThreads);
@@ -687,6 +757,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                             if (d < D) Og[r] = fmaf(wc, __ldcg(pc + d), Og[r]);
                         }
                     }
+                    if (sm.beg[c.s] > 0) merge_prefix<D, DPT>(p, c.s, c.h, tid, Mg, Lg, Og);
                     const float inv = 1.f / Lg;
 #pragma unroll
                     for (int r = 0; r < DPT; ++r) {
@@ -867,8 +938,19 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
                                  int32_t num_seqs, float scale, void *out, void *workspace, size_t workspace_bytes,
                                  void *stream, const void *k_new, const void *v_new, const int64_t *slots,
                                  uint32_t *status_override = nullptr, const float *k_scale = nullptr,
-                                 const float *v_scale = nullptr) {
+                                 const float *v_scale = nullptr, const int32_t *seq_begin = nullptr,
+                                 const float *pieces = nullptr, int32_t splits = 0) {
     const bool q8 = k_scale != nullptr;
+    if ((seq_begin == nullptr) != (pieces == nullptr))
+        return fail(PKV_ERR_INVALID_ARG, "seq_begin and pieces go together (both NULL: no cascade)");
+    if (seq_begin) {
+        if (q8 || head_dim != 128)
+            return fail(PKV_ERR_UNSUPPORTED, "the cascade is built for fp16 pools with head_dim 128");
+        if (splits < 1 || splits > PKV_MAX_PREFIX_SPLITS)
+            return fail(PKV_ERR_INVALID_ARG, "splits %d outside 1..%d", splits, PKV_MAX_PREFIX_SPLITS);
+        if ((reinterpret_cast<uintptr_t>(seq_begin) & 3u) || !aligned16(pieces))
+            return fail(PKV_ERR_INVALID_ARG, "seq_begin must be 4-byte and pieces 16-byte aligned");
+    }
     if (num_seqs < 0 || num_seqs > kMaxSeqs)
         return fail(PKV_ERR_INVALID_ARG, "num_seqs %d outside [0, %d]", num_seqs, kMaxSeqs);
     if (num_seqs == 0) return PKV_OK;
@@ -929,6 +1011,9 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     prm.v_layer = static_cast<unsigned char *>(const_cast<void *>(v_cache));
     prm.k_scale = const_cast<float *>(k_scale);
     prm.v_scale = const_cast<float *>(v_scale);
+    prm.begin = seq_begin;
+    prm.pre = pieces;
+    prm.pre_splits = seq_begin ? splits : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -985,6 +1070,30 @@ pkv_status pkv_decode_append_attention(const pkv_pool *pool, int32_t layer, cons
                                  block_tables, max_blocks, context_lens, num_seqs, scale, out, workspace,
                                  workspace_bytes, stream, k_new, v_new, slot_mapping, nullptr, pl.k_scale,
                                  pl.v_scale);
+}
+
+pkv_status pkv_decode_attention_ex(const pkv_pool *pool, int32_t layer, const void *q, const void *k_new,
+                                   const void *v_new, const int64_t *slot_mapping, const int32_t *block_tables,
+                                   int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs,
+                                   const int32_t *seq_begin, const float *pieces, int32_t splits, float scale,
+                                   void *out, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    const pkv_pool_desc &d = pool->desc;
+    if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
+    if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+    const bool append = k_new || v_new || slot_mapping;
+    if (append && num_seqs > 0 && (!k_new || !v_new || !slot_mapping))
+        return fail(PKV_ERR_INVALID_ARG, "k_new, v_new and slot_mapping go together (all NULL: no append)");
+    if (append && (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)))
+        return fail(PKV_ERR_INVALID_ARG, "k_new/v_new must be 16-byte aligned, slot_mapping 8-byte aligned");
+    const PoolLayer pl = pool_layer(pool, layer);
+    if (pool->desc.kv_dtype == PKV_KV_E4M3 && !pl.k_scale)
+        return fail(PKV_ERR_INVALID_ARG, "E4M3 pool without scale pools (pkv_pool_set_scales)");
+    return decode_attention_impl(q, pl.k, pl.v, d.num_blocks, d.block_size, d.num_heads, d.head_dim, d.layout,
+                                 block_tables, max_blocks, context_lens, num_seqs, scale, out, workspace,
+                                 workspace_bytes, stream, append ? k_new : nullptr, append ? v_new : nullptr,
+                                 append ? slot_mapping : nullptr, nullptr, pl.k_scale, pl.v_scale, seq_begin, pieces,
+                                 splits);
 }
 
 pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const void *q, const int32_t *block_tables,

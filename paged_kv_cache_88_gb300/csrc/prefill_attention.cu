@@ -68,12 +68,14 @@ constexpr int kSmemBytes = kSmemTiles + kXchgBytes + 256 /* barriers + flags */ 
 constexpr int kQFull = 0, kKFull = 1, kVFull = 3, kSFull = 5, kPReady = 7, kOFull = 9, kNumBars = 11;
 
 struct PrefillParams {
-    const int32_t *q_start;   // [S + 1] chunk rows of sequence s: q_start[s] .. q_start[s+1]-1
+    const int32_t *q_start;   // prefill: [S + 1] chunk rows of sequence s: q_start[s] .. q_start[s+1]-1
     const int32_t *tables;    // [S][max_blocks]
-    const int32_t *lens;      // [S] context lengths including the chunk
-    __half *out;              // [total_q][H][D]
+    const int32_t *lens;      // prefill: [S] context lengths including the chunk
+    __half *out;              // prefill: [total_q][H][D]
+    const pkv_prefix_group *groups;  // prefix pass: [gridDim.z]
+    float *pieces;            // prefix pass: [S][H][PKV_MAX_PREFIX_SPLITS][D + 4]
     uint32_t *status;
-    int32_t S, H, max_blocks, B, N;
+    int32_t S, H, max_blocks, B, N, splits;
     float scale_log2;
 };
 
@@ -172,12 +174,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
         if (ptx::global_timer_ns() - t0 > kWaitLimitNs) return;
 }
 
+// One kernel, two uses:
+// * prefill (kPrefix = false): CTA (query tile, head, sequence) of a chunk,
+//   causal over the sequence's cache, normalised fp16 output;
+// * the cascade's prefix pass (kPrefix = true): CTA (key split, head, group),
+//   the group members' decode queries as the query tile (row r = sequence
+//   first_seq + r), every key of the split's share of the shared prefix seen by
+//   every row, unnormalised fp32 pieces (o, m, l) as output.
 // Pipeline of one CTA over its key tiles j = 0 .. nkt-1 (slot b = j & 1):
 //   loader : K_j -> K[b] once S_{j-2} is done; V_j -> V[b] once P_{j-2} V is done
 //   MMA    : S_0, S_1, then per j: [P_j ready] O += P_j V_j, S_{j+2} -> S[b]
 //   softmax: per j: S[b] -> P_j (fp16, tensor memory P[b]) once P_{j-2} V is done
 // so the tensor cores compute S_{j+1} (and finish P_{j-1} V) while the softmax
 // warps work on tile j. Every barrier is waited on at most one phase behind.
+template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -195,25 +205,61 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     auto BAR = [bar0](int i) { return bar0 + 8 * i; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int32_t qt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int32_t h = blockIdx.y;
     const int32_t H = p.H, B = p.B;
+    const int32_t cap = p.max_blocks * B;
 
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
-    const int32_t q0 = p.q_start[s];
-    const int32_t C = p.q_start[s + 1] - q0;
-    const int32_t i0 = qt * kQT;
-    if (i0 >= C) return;                               // uniform: this tile has no queries
-    int32_t T = p.lens[s];
-    const int32_t cap = p.max_blocks * B;
-    if (T < C || T > cap) {
-        if (tid == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
-        T = T < C ? C : cap;
+    // The CTA's query rows q0 .. q0 + rows - 1 (row r of the tile: query row
+    // q0 + r), the table row it reads, and its keys [kv_begin, kv_end); row r
+    // sees keys t <= lim_r (prefill: its own position; prefix: every key).
+    int32_t q0, rows, srow, kv_begin, kv_end, pos0;
+    int32_t split = 0;
+    if constexpr (kPrefix) {
+        const pkv_prefix_group g = p.groups[blockIdx.z];
+        split = blockIdx.x;
+        const int32_t P = g.prefix_tokens;
+        if (g.num_seqs < 1 || g.num_seqs > kQT || g.first_seq < 0 || g.first_seq > p.S - g.num_seqs || P < 0 ||
+            P > cap || P % B != 0) {
+            if (tid == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            return;
+        }
+        q0 = g.first_seq;
+        rows = g.num_seqs;
+        srow = g.first_seq;
+        const int32_t per = ((P + kKT - 1) / kKT + p.splits - 1) / p.splits;   // key tiles per split
+        kv_begin = min(P, split * per * kKT);
+        kv_end = min(P, kv_begin + per * kKT);
+        pos0 = kv_end - 1;
+        if (kv_begin >= kv_end) {
+            // no keys in this split: an empty piece for every member
+            for (int32_t i = tid; i < rows * (kD + 4); i += kThreads) {
+                const int32_t r = i / (kD + 4), c = i - r * (kD + 4);
+                p.pieces[(((size_t)(q0 + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4) + c] =
+                    c == kD ? -INFINITY : 0.f;
+            }
+            return;
+        }
+    } else {
+        const int32_t s = blockIdx.z;
+        const int32_t qs = p.q_start[s];
+        const int32_t C = p.q_start[s + 1] - qs;
+        const int32_t i0 = blockIdx.x * kQT;
+        if (i0 >= C) return;                           // uniform: this tile has no queries
+        int32_t T = p.lens[s];
+        if (T < C || T > cap) {
+            if (tid == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            T = T < C ? C : cap;
+        }
+        q0 = qs + i0;
+        rows = min(kQT, C - i0);                       // valid query rows of this tile
+        srow = s;
+        pos0 = T - C + i0;                             // position of row 0
+        kv_begin = 0;
+        kv_end = pos0 + rows;                          // keys [0, kv_end) are seen by some row
     }
-    const int32_t rows = min(kQT, C - i0);             // valid query rows of this tile
-    const int32_t pos0 = T - C + i0;                   // position of row 0
-    const int32_t kv_end = pos0 + rows;                // keys [0, kv_end) are seen by some row
-    const int32_t nkt = (kv_end + kKT - 1) / kKT;
+    const int32_t nkt = (kv_end - kv_begin + kKT - 1) / kKT;
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i)
@@ -241,18 +287,18 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(BAR(kQFull), kTileBytes);
             for (int half = 0; half < 2; ++half)
-                ptx::tma_load_3d(sQ + half * kSub, &qmap, half * kHalf, h, q0 + i0, BAR(kQFull));
+                ptx::tma_load_3d(sQ + half * kSub, &qmap, half * kHalf, h, q0, BAR(kQFull));
         }
         for (int32_t j = 0; j < nkt; ++j) {
             const int b = j & 1;
-            const int32_t t0 = j * kKT;
+            const int32_t t0 = kv_begin + j * kKT;
             const int32_t ntok = min(kKT, kv_end - t0);
             const int32_t nbox = B < kKT ? (ntok + B - 1) / B : 1;     // <= 16
             const uint32_t box_bytes = (uint32_t)nbox * rowsb * 128 * 2;
             int32_t y = 0;
             if (lane < nbox) {                          // lane i: box i of the tile
                 const int32_t lb = (t0 + lane * rowsb) / B;
-                int32_t blk = lb < p.max_blocks ? p.tables[(size_t)s * p.max_blocks + lb] : -1;
+                int32_t blk = lb < p.max_blocks ? p.tables[(size_t)srow * p.max_blocks + lb] : -1;
                 if (blk < 0 || blk >= p.N) {
                     atomicOr(p.status, PKV_DEV_BAD_BLOCK);
                     blk = 0;
@@ -326,14 +372,14 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         const int32_t r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const bool valid = r < rows;
-        const int32_t pr = pos0 + r;                // position of this row's query
+        const int32_t pr = kPrefix ? pos0 : pos0 + r;   // the last key this row sees
         const float sl2 = p.scale_log2;
         constexpr float kSlack = 8.f;
         constexpr int kCols = kKT / 2;              // keys of S (and columns of O) per thread
         float m_ref = -INFINITY, l = 0.f;
         for (int32_t j = 0; j < nkt; ++j) {
             const int b = j & 1;
-            const int32_t t0 = j * kKT + hf * kCols;   // first key of this thread's half
+            const int32_t t0 = kv_begin + j * kKT + hf * kCols;   // first key of this thread's half
             bounded_wait(BAR(kSFull + b), (j >> 1) & 1, timed_out, p.status);
             tc_fence_after();
             uint32_t raw[kCols];
@@ -395,7 +441,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
             // the last tile: zero the V rows no query may see (they may hold non-finite garbage)
             if (j == nkt - 1) {
                 bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
-                const int32_t first_dead = kv_end - j * kKT;      // rows [first_dead, 128) of the tile
+                const int32_t first_dead = kv_end - (kv_begin + j * kKT);   // rows [first_dead, 128) of the tile
                 unsigned char *sVp = base + (3 + b) * kTileBytes;
                 const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
                 for (int32_t w = tid; w < nwords * 2; w += kSoftmaxThreads) {
@@ -416,11 +462,21 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         xs[hf * kQT + r] = l;
         ptx::named_barrier(1 + quad, 64);
         const float lt = xs[r] + xs[kQT + r];
-        const float inv = valid ? 1.f / lt : 0.f;
         uint32_t raw[kCols];
         tmem_ld64(tO + lane_base + hf * kCols, raw);
-        if (valid) {
-            __half *dst = p.out + ((size_t)(q0 + i0 + r) * H + h) * kD + hf * kCols;
+        if constexpr (kPrefix) {
+            if (valid) {
+                float *piece = p.pieces + (((size_t)(q0 + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4);
+                float4 *o4 = reinterpret_cast<float4 *>(piece + hf * kCols);
+#pragma unroll
+                for (int d = 0; d < kCols; d += 4)
+                    o4[d / 4] = make_float4(__uint_as_float(raw[d]), __uint_as_float(raw[d + 1]),
+                                            __uint_as_float(raw[d + 2]), __uint_as_float(raw[d + 3]));
+                if (hf == 0) *reinterpret_cast<float4 *>(piece + kD) = make_float4(m_ref, lt, 0.f, 0.f);
+            }
+        } else if (valid) {
+            const float inv = 1.f / lt;
+            __half *dst = p.out + ((size_t)(q0 + r) * H + h) * kD + hf * kCols;
 #pragma unroll
             for (int d = 0; d < kCols; d += 8) {
                 __half2 hv[4];
@@ -461,6 +517,87 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// q ([rows][H][D] fp16) as a 3-D tensor (D, H, row), boxes of 64 x 1 x 128; the
+// pool layer as rows of D, boxes of 64 x min(B, 128). 128-byte swizzle.
+pkv_status encode_maps(const pkv_pool *pool, int32_t layer, const void *q, int32_t q_rows, CUtensorMap *qmap,
+                       CUtensorMap *kmap, CUtensorMap *vmap) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const pkv_pool_desc &d = pool->desc;
+    const PoolLayer pl = pool_layer(pool, layer);
+    const int H = d.num_heads, B = d.block_size, N = d.num_blocks;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)q_rows};
+        const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+        const cuuint32_t box[3] = {kHalf, 1, kQT}, es[3] = {1, 1, 1};
+        if (fn(qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(q), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(PKV_ERR_CUDA, "q tensor map");
+    }
+    for (int which = 0; which < 2; ++which) {
+        const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)N * H * B};
+        const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+        const cuuint32_t box[2] = {kHalf, (cuuint32_t)(B < kKT ? B : kKT)}, es[2] = {1, 1};
+        if (fn(which ? vmap : kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, which ? pl.v : pl.k, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(PKV_ERR_CUDA, "pool tensor map");
+    }
+    return PKV_OK;
+}
+
+pkv_status check_pool(const pkv_pool *pool, int32_t layer, const char *what) {
+    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    const pkv_pool_desc &d = pool->desc;
+    if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
+    if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (d.head_dim != kD || d.kv_dtype != PKV_KV_F16 || d.layout != PKV_LAYOUT_HND)
+        return fail(PKV_ERR_UNSUPPORTED, "%s is built for fp16 HND pools with head_dim 128", what);
+    return PKV_OK;
+}
+
+PrefillParams base_params(const pkv_pool *pool, const int32_t *block_tables, int32_t max_blocks, int32_t num_seqs,
+                          float scale, uint32_t *status) {
+    const pkv_pool_desc &d = pool->desc;
+    PrefillParams prm = {};
+    prm.tables = block_tables;
+    prm.status = status;
+    prm.S = num_seqs;
+    prm.H = d.num_heads;
+    prm.max_blocks = max_blocks;
+    prm.B = d.block_size;
+    prm.N = d.num_blocks;
+    prm.splits = 1;
+    const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)kD);
+    prm.scale_log2 = (float)(sc * 1.4426950408889634);
+    return prm;
+}
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_attr_once[kMaxDevices][2];
+cudaError_t g_attr_err[kMaxDevices][2];
+
+template <bool kPrefix>
+pkv_status launch_tc(dim3 grid, const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                     const PrefillParams &prm, void *stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(PKV_ERR_CUDA, "no usable CUDA device");
+    std::call_once(g_attr_once[dev][kPrefix], [dev] {
+        g_attr_err[dev][kPrefix] = cudaFuncSetAttribute(prefill_attention_kernel<kPrefix>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (g_attr_err[dev][kPrefix] != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(g_attr_err[dev][kPrefix]));
+    cudaError_t e = launch_pdl(prefill_attention_kernel<kPrefix>, grid, dim3(kThreads), (size_t)kSmemBytes,
+                               static_cast<cudaStream_t>(stream), qmap, kmap, vmap, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "%s launch: %s", kPrefix ? "prefix" : "prefill",
+                                      cudaGetErrorString(e));
+    return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -469,12 +606,8 @@ pkv_status pkv_prefill_attention(const pkv_pool *pool, int32_t layer, const void
                                  int32_t total_q, int32_t num_seqs, int32_t max_chunk, const int32_t *block_tables,
                                  int32_t max_blocks, const int32_t *context_lens, float scale, void *out,
                                  uint32_t *status, void *stream) {
-    if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-    const pkv_pool_desc &d = pool->desc;
-    if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
-    if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
-    if (d.head_dim != kD || d.kv_dtype != PKV_KV_F16 || d.layout != PKV_LAYOUT_HND)
-        return fail(PKV_ERR_UNSUPPORTED, "prefill attention is built for fp16 HND pools with head_dim 128");
+    pkv_status st = check_pool(pool, layer, "prefill attention");
+    if (st != PKV_OK) return st;
     if (num_seqs < 0 || total_q < 0 || max_chunk < 0 || max_blocks < 1)
         return fail(PKV_ERR_INVALID_ARG, "bad sizes");
     if (num_seqs == 0 || total_q == 0 || max_chunk == 0) return PKV_OK;
@@ -482,55 +615,43 @@ pkv_status pkv_prefill_attention(const pkv_pool *pool, int32_t layer, const void
     if (!q || !q_start || !block_tables || !context_lens || !out || !status)
         return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument (status is required here)");
     if (!aligned16(q) || !aligned16(out)) return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const PoolLayer pl = pool_layer(pool, layer);
-    const int H = d.num_heads, B = d.block_size, N = d.num_blocks;
     CUtensorMap qmap, kmap, vmap;
-    {   // q: [total_q][H][D] as a 3-D tensor (D, H, token), boxes of 64 x 1 x 128
-        const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)total_q};
-        const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-        const cuuint32_t box[3] = {kHalf, 1, kQT}, es[3] = {1, 1, 1};
-        if (fn(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(q), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return fail(PKV_ERR_CUDA, "q tensor map");
-    }
-    for (int which = 0; which < 2; ++which) {   // pool layer: rows of D, boxes of 64 x min(B, 128)
-        const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)N * H * B};
-        const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-        const cuuint32_t box[2] = {kHalf, (cuuint32_t)(B < kKT ? B : kKT)}, es[2] = {1, 1};
-        if (fn(which ? &vmap : &kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, which ? pl.v : pl.k, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return fail(PKV_ERR_CUDA, "pool tensor map");
-    }
-    PrefillParams prm;
+    st = encode_maps(pool, layer, q, total_q, &qmap, &kmap, &vmap);
+    if (st != PKV_OK) return st;
+    PrefillParams prm = base_params(pool, block_tables, max_blocks, num_seqs, scale, status);
     prm.q_start = q_start;
-    prm.tables = block_tables;
     prm.lens = context_lens;
     prm.out = static_cast<__half *>(out);
-    prm.status = status;
-    prm.S = num_seqs;
-    prm.H = H;
-    prm.max_blocks = max_blocks;
-    prm.B = B;
-    prm.N = N;
-    const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)kD);
-    prm.scale_log2 = (float)(sc * 1.4426950408889634);
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-    const dim3 grid((max_chunk + kQT - 1) / kQT, H, num_seqs);
-    cudaError_t e = launch_pdl(prefill_attention_kernel, grid, dim3(kThreads), (size_t)kSmemBytes,
-                               static_cast<cudaStream_t>(stream), qmap, kmap, vmap, prm);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
-    return PKV_OK;
+    const dim3 grid((max_chunk + kQT - 1) / kQT, pool->desc.num_heads, num_seqs);
+    return launch_tc<false>(grid, qmap, kmap, vmap, prm, stream);
+}
+
+pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void *q, const pkv_prefix_group *groups,
+                                int32_t num_groups, int32_t splits, const int32_t *block_tables, int32_t max_blocks,
+                                int32_t num_seqs, float scale, void *pieces, size_t pieces_bytes, uint32_t *status,
+                                void *stream) {
+    pkv_status st = check_pool(pool, layer, "the prefix pass");
+    if (st != PKV_OK) return st;
+    if (num_groups < 0 || num_seqs < 0 || max_blocks < 1 || splits < 1 || splits > PKV_MAX_PREFIX_SPLITS)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes (splits in 1..%d)", PKV_MAX_PREFIX_SPLITS);
+    if (num_groups == 0 || num_seqs == 0) return PKV_OK;
+    if (num_groups > 65535) return fail(PKV_ERR_INVALID_ARG, "num_groups > 65535");
+    if (!q || !groups || !block_tables || !pieces || !status)
+        return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument (status is required here)");
+    if (!aligned16(q) || !aligned16(pieces))
+        return fail(PKV_ERR_INVALID_ARG, "q and pieces must be 16-byte aligned");
+    const pkv_pool_desc &d = pool->desc;
+    const size_t need = (size_t)num_seqs * d.num_heads * PKV_MAX_PREFIX_SPLITS * (kD + 4) * sizeof(float);
+    if (pieces_bytes < need) return fail(PKV_ERR_INVALID_ARG, "pieces: %zu bytes < %zu needed", pieces_bytes, need);
+    CUtensorMap qmap, kmap, vmap;
+    st = encode_maps(pool, layer, q, num_seqs, &qmap, &kmap, &vmap);
+    if (st != PKV_OK) return st;
+    PrefillParams prm = base_params(pool, block_tables, max_blocks, num_seqs, scale, status);
+    prm.groups = groups;
+    prm.pieces = static_cast<float *>(pieces);
+    prm.splits = splits;
+    const dim3 grid(splits, d.num_heads, num_groups);
+    return launch_tc<true>(grid, qmap, kmap, vmap, prm, stream);
 }
 
 }  // extern "C"

@@ -89,6 +89,15 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Atomic add at GPU scope with acquire-release semantics: one instruction that
+// publishes the writes this thread has observed (those of its CTA after a
+// barrier) and sees the writes published by earlier adders.
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t *p, int32_t v) {
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Barrier over the first `count` threads' warps that use id `id` (not 0).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

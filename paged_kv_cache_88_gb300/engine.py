@@ -9,7 +9,11 @@ One decode step over a batch (all through the C ABI):
 3. ``pkv_copy_blocks`` once for the step, across all layers;
 4. per layer: the new token's K/V appended and attention over the cache
    including it -- one ``pkv_decode_append_attention`` launch (default), or
-   ``pkv_append`` then ``pkv_pool_decode_attention``.
+   ``pkv_append`` then ``pkv_pool_decode_attention``. With the shared-prefix
+   cascade (fp16 HND pools, head_dim 128, on by default), the host plans groups
+   of sequences that share leading blocks (``pkv_cascade_plan``) and each
+   layer first runs ``pkv_prefix_attention`` over the groups' prefixes, then
+   ``pkv_decode_attention_ex`` over the private rest (fused append included).
 
 The driver also replays a workload's set-up script (admissions, forks, dummy
 churn, multi-token writes). It holds no arithmetic of the method: slots,
@@ -29,9 +33,11 @@ from . import binding as bd
 
 class DecodeEngine:
     def __init__(self, w: wl.Workload, device: str = "cuda", fill: str = "torch", max_new_per_step: int = 1,
-                 fused: bool = True):
+                 fused: bool = True, cascade: bool = True):
         self.w = w
         self.fused = fused      # append inside the attention launch (pkv_decode_append_attention)
+        # shared-prefix cascade: only where the tensor-core prefix pass is built
+        self.cascade = bool(cascade) and w.kv_dtype == "f16" and w.layout == "HND" and w.head_dim == 128
         self.device = torch.device(device)
         shape = wl.pool_shape(w)
         self.k_scale = self.v_scale = None
@@ -63,6 +69,13 @@ class DecodeEngine:
         self.lens_d = torch.zeros(S, dtype=torch.int32, device=self.device)
         self.status = torch.zeros(4, dtype=torch.int32, device=self.device)
         self.workspace = bd.new_workspace(S, w.num_heads, w.head_dim, self.device)
+        # the cascade plan on the device (refreshed with every step's tables) and the prefix pieces
+        self.groups_d = torch.zeros((max(S, 1), 4), dtype=torch.int32, device=self.device)
+        self.begin_d = torch.zeros(max(S, 1), dtype=torch.int32, device=self.device)
+        self.pieces = (torch.empty(bd.prefix_pieces_bytes(S, w.num_heads, w.head_dim), dtype=torch.uint8,
+                                   device=self.device) if self.cascade else None)
+        self.plan_groups, self.plan_splits, self.plan_prefix = 0, 0, 0
+        self.plan = np.zeros((0, 4), dtype=np.int32)
         self._cap_slots = S * max_new_per_step
         self.slots_d = torch.zeros(max(self._cap_slots, 1), dtype=torch.int64, device=self.device)
         self.pairs_d = torch.zeros((max(self._cap_slots, 1), 2), dtype=torch.int32, device=self.device)
@@ -74,6 +87,8 @@ class DecodeEngine:
                 "lens": torch.empty(S, dtype=torch.int32).pin_memory(),
                 "slots": torch.empty(max(self._cap_slots, 1), dtype=torch.int64).pin_memory(),
                 "pairs": torch.empty((max(self._cap_slots, 1), 2), dtype=torch.int32).pin_memory(),
+                "groups": torch.zeros((max(S, 1), 4), dtype=torch.int32).pin_memory(),
+                "begin": torch.zeros(max(S, 1), dtype=torch.int32).pin_memory(),
                 "event": None,
             })
         self._buf = 0
@@ -181,6 +196,21 @@ class DecodeEngine:
     def upload_tables(self):
         self.tables_d.copy_(torch.from_numpy(self.tables))
         self.lens_d.copy_(torch.from_numpy(self.lens))
+        if self.cascade:
+            groups = np.zeros((max(self.w.num_seqs, 1), 4), dtype=np.int32)
+            begin = np.zeros(max(self.w.num_seqs, 1), dtype=np.int32)
+            self._plan(groups, begin)
+            self.groups_d.copy_(torch.from_numpy(groups))
+            self.begin_d.copy_(torch.from_numpy(begin))
+
+    def _plan(self, groups_out: np.ndarray, begin_out: np.ndarray) -> None:
+        """Cascade plan of the current host tables and lengths into the given buffers."""
+        g, _ = bd.cascade_plan(self.tables, self.lens, self.w.block_size, groups_out=groups_out,
+                               begin_out=begin_out[: self.w.num_seqs])
+        self.plan_groups = len(g)
+        self.plan = g.copy()
+        self.plan_prefix = int(g[:, 2].max()) if len(g) else 0
+        self.plan_splits = bd.prefix_splits(len(g), self.w.num_heads, self.plan_prefix) if len(g) else 0
 
     # ------------------------------------------------------------------ decode step
     def prepare_step(self, stream=None):
@@ -192,10 +222,16 @@ class DecodeEngine:
                                                 slot_out=st["slots"].numpy(), pair_out=st["pairs"].numpy())
         st["tables"].numpy()[...] = self.tables
         st["lens"].numpy()[...] = self.lens
+        if self.cascade:
+            self._plan(st["groups"].numpy(), st["begin"].numpy())
         s = stream if stream is not None else torch.cuda.current_stream()
         with torch.cuda.stream(s):
             self.tables_d.copy_(st["tables"], non_blocking=True)
             self.lens_d.copy_(st["lens"], non_blocking=True)
+            if self.cascade:
+                if self.plan_groups:
+                    self.groups_d[: self.plan_groups].copy_(st["groups"][: self.plan_groups], non_blocking=True)
+                self.begin_d.copy_(st["begin"], non_blocking=True)
             self.slots_d[: len(slots)].copy_(st["slots"][: len(slots)], non_blocking=True)
             if len(pairs):
                 self.pairs_d[: len(pairs)].copy_(st["pairs"][: len(pairs)], non_blocking=True)
@@ -233,12 +269,25 @@ class DecodeEngine:
         maxb, S = w.max_blocks, w.num_seqs
         sc = float(scale)
         fused = self.fused and n_slots == S
+        G, splits = (self.plan_groups, self.plan_splits) if self.cascade else (0, 0)
+        if G:
+            gp, bp = self.groups_d.data_ptr(), self.begin_d.data_ptr()
+            pp, pb = self.pieces.data_ptr(), self.pieces.numel()
         for layer in range(w.num_layers):
             off = layer * row
             if attn_events is not None:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(s)
-            if fused:
+            if G:
+                # the shared prefixes once per group, then each sequence's private rest (+ append)
+                bd.check(L.pkv_prefix_attention(h, layer, qp + off, gp, G, splits, tp, maxb, S, sc, pp, pb, status,
+                                                sp))
+                if not fused:
+                    bd.check(L.pkv_append(h, layer, kp + off, vp + off, slp, n_slots, status, sp))
+                bd.check(L.pkv_decode_attention_ex(h, layer, qp + off, kp + off if fused else None,
+                                                   vp + off if fused else None, slp if fused else None, tp, maxb,
+                                                   lp, S, bp, pp, splits, sc, op + off, wsp, wsb, sp))
+            elif fused:
                 bd.check(L.pkv_decode_append_attention(h, layer, qp + off, kp + off, vp + off, slp, tp, maxb, lp, S,
                                                        sc, op + off, wsp, wsb, sp))
             else:
@@ -270,13 +319,23 @@ class DecodeEngine:
         torch.cuda.synchronize()
         self._graph = g
         self._graph_tensors = (q, k_new, v_new, out)
+        self._graph_scale = scale
+        self._graph_plan = (self.plan_groups, self.plan_splits)
         return g
 
     def step_graph(self, stream=None):
-        """A decode step replaying the captured graph (COW copies, if any, run first)."""
+        """A decode step replaying the captured graph (COW copies, if any, run first).
+
+        The graph bakes in the cascade plan's shape (groups, splits); a step
+        whose plan has another shape re-captures first.
+        """
         n_slots, n_pairs = self.prepare_step(stream)
         if n_slots != self.w.num_seqs:
             raise RuntimeError("the captured step appends one token per sequence")
+        if (self.plan_groups, self.plan_splits) != self._graph_plan:
+            s = stream if stream is not None else torch.cuda.current_stream()
+            s.synchronize()
+            self.capture(*self._graph_tensors, scale=self._graph_scale)
         s = stream if stream is not None else torch.cuda.current_stream()
         if n_pairs:
             bd.check(bd.lib().pkv_copy_blocks(self.pool.handle, self.pairs_d.data_ptr(), n_pairs,
@@ -290,6 +349,18 @@ class DecodeEngine:
         w = self.w
         s = stream if stream is not None else torch.cuda.current_stream()
         off = layer * w.num_seqs * w.num_heads * w.head_dim * 2
+        if self.cascade and self.plan_groups:
+            L, S = bd.lib(), w.num_seqs
+            bd.check(L.pkv_prefix_attention(self.pool.handle, layer, q.data_ptr() + off, self.groups_d.data_ptr(),
+                                            self.plan_groups, self.plan_splits, self.tables_d.data_ptr(),
+                                            w.max_blocks, S, float(scale), self.pieces.data_ptr(),
+                                            self.pieces.numel(), self.status.data_ptr(), s.cuda_stream))
+            bd.check(L.pkv_decode_attention_ex(
+                self.pool.handle, layer, q.data_ptr() + off, None, None, None, self.tables_d.data_ptr(),
+                w.max_blocks, self.lens_d.data_ptr(), S, self.begin_d.data_ptr(), self.pieces.data_ptr(),
+                self.plan_splits, float(scale), out.data_ptr() + off, self.workspace.data_ptr(),
+                self.workspace.numel(), s.cuda_stream))
+            return
         bd.check(bd.lib().pkv_pool_decode_attention(
             self.pool.handle, layer, q.data_ptr() + off, self.tables_d.data_ptr(), w.max_blocks,
             self.lens_d.data_ptr(), w.num_seqs, float(scale), out.data_ptr() + off, self.workspace.data_ptr(),
@@ -320,3 +391,9 @@ class DecodeEngine:
     def kv_bytes_per_layer(self) -> int:
         """Algorithmic K+V bytes one attention launch reads (current lengths)."""
         return int(self.lens.astype(np.int64).sum()) * self.w.kv_bytes_per_token_layer
+
+    def unique_kv_bytes_per_layer(self) -> int:
+        """K+V bytes of the distinct tokens a layer's attention covers: every sequence's
+        context, minus all but one copy of each group's shared prefix (the cascade plan)."""
+        dup = sum((int(n) - 1) * int(P) for _, n, P, _ in self.plan.tolist()) if self.cascade else 0
+        return (int(self.lens.astype(np.int64).sum()) - dup) * self.w.kv_bytes_per_token_layer

@@ -1,0 +1,238 @@
+"""GPU parity of the shared-prefix (cascade) decode against the oracle.
+
+The prefix pass (pkv_prefix_attention) is checked piece by piece: o / l is the
+softmax-weighted mean of V over the piece's keys and m + log2(l) is
+log2 sum_t 2^(scale log2(e) q.K_t) over them, both in float64 on the host. The
+whole cascade (prefix pass, then pkv_decode_attention_ex) is checked against
+the plain float64 attention of the oracle; so is the engine's decode step with
+the cascade on, on the forked-prompt workload.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import paged_kv_cache_88_gb300 as pkv  # noqa: E402
+from paged_kv_cache_88_gb300 import binding as bd  # noqa: E402
+from oracle import ref_attn as rf  # noqa: E402
+
+ATOL, RTOL = 2e-3, 1e-2
+D = 128
+LOG2E = 1.4426950408889634
+
+
+def assert_close(got, ref, what, atol=ATOL, rtol=RTOL):
+    err = np.abs(got.astype(np.float64) - ref)
+    bad = ~(err <= atol + rtol * np.abs(ref))
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside tolerance, max err {np.nanmax(err):.3e}"
+
+
+def build_case(spec, H, B, seed):
+    """spec: list of (shared_with, shared_blocks, T): sequence s copies the first
+    shared_blocks ids of sequence shared_with (or shares none), then gets fresh
+    blocks up to T tokens. Slots past each context hold NaN."""
+    rng = np.random.default_rng(seed)
+    S = len(spec)
+    maxb = max(-(-T // B) for _, _, T in spec)
+    tables = np.full((S, maxb), -1, dtype=np.int32)
+    nxt = 0
+    for s, (src, nsh, T) in enumerate(spec):
+        nb = -(-T // B)
+        if src is not None:
+            tables[s, :nsh] = tables[src, :nsh]
+        else:
+            nsh = 0
+        tables[s, nsh:nb] = np.arange(nxt, nxt + nb - nsh)
+        nxt += nb - nsh
+    N = nxt + 2
+    perm = rng.permutation(N).astype(np.int32)     # scatter the blocks over the pool
+    tables = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+    lens = np.array([T for _, _, T in spec], dtype=np.int32)
+    kp = rng.standard_normal((N, H, B, D)).astype(np.float16)
+    vp = rng.standard_normal((N, H, B, D)).astype(np.float16)
+    for s, T in enumerate(lens):
+        nb = -(-int(T) // B)
+        off = int(T) - (nb - 1) * B
+        if off < B:
+            kp[tables[s, nb - 1], :, off:] = np.float16(np.nan)
+            vp[tables[s, nb - 1], :, off:] = np.float16(np.nan)
+    q = rng.standard_normal((S, H, D)).astype(np.float16)
+    return q, kp, vp, tables, lens, N
+
+
+class Case:
+    def __init__(self, spec, H=4, B=16, seed=0, scale=0.0):
+        self.q, self.kp, self.vp, self.tables, self.lens, self.N = build_case(spec, H, B, seed)
+        self.H, self.B, self.S = H, B, len(spec)
+        self.scale = scale if scale > 0 else 1.0 / math.sqrt(D)
+        dev = "cuda"
+        self.pool = pkv.Pool(1, self.N, B, H, D, "HND", k_pool=torch.from_numpy(self.kp).to(dev),
+                             v_pool=torch.from_numpy(self.vp).to(dev))
+        self.qd = torch.from_numpy(self.q).to(dev)
+        self.tab_d = torch.from_numpy(self.tables).to(dev)
+        self.lens_d = torch.from_numpy(self.lens).to(dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pieces = torch.full((bd.prefix_pieces_bytes(self.S, H, D) // 4,), float("nan"), device=dev)
+        self.ws = bd.new_workspace(self.S, H, D)
+
+    def plan(self, **kw):
+        g, b = bd.cascade_plan(self.tables, self.lens, self.B, **kw)
+        return g.copy(), b.copy()
+
+    def prefix(self, groups, splits, scale=0.0):
+        gd = torch.from_numpy(np.ascontiguousarray(groups, dtype=np.int32)).cuda()
+        self.pool.prefix_attention(0, self.qd, gd, len(groups), splits, self.tab_d, self.pieces, self.status,
+                                   scale=scale)
+
+    def decode(self, begin, splits, scale=0.0, **kw):
+        out = torch.full_like(self.qd, float("nan"))
+        bdv = torch.from_numpy(np.ascontiguousarray(begin, dtype=np.int32)).cuda() if begin is not None else None
+        self.pool.decode_attention_ex(0, self.qd, self.tab_d, self.lens_d, out, self.ws, seq_begin=bdv,
+                                      pieces=self.pieces if begin is not None else None, splits=splits,
+                                      scale=scale, **kw)
+        torch.cuda.synchronize()
+        return out.cpu().numpy()
+
+    def oracle(self):
+        return rf.decode_attention(self.q, self.kp, self.vp, self.tables, self.lens, self.B, layout="HND",
+                                   scale=self.scale)
+
+    def keys(self, s, h, t0, t1):
+        k = rf.gather_sequence(self.kp, self.tables[s], t1, h, "HND", self.H, self.B, D)[t0:]
+        v = rf.gather_sequence(self.vp, self.tables[s], t1, h, "HND", self.H, self.B, D)[t0:]
+        return k, v
+
+
+def forked_spec(n, shared_blocks, suffix, B, rng):
+    spec = [(None, 0, shared_blocks * B + int(rng.integers(1, suffix)))]
+    spec += [(0, shared_blocks, shared_blocks * B + int(rng.integers(1, suffix))) for _ in range(n - 1)]
+    return spec
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 8])
+def test_prefix_pieces(splits):
+    """Each piece against its keys: a ragged last key tile (P = 1040), and splits with no keys."""
+    rng = np.random.default_rng(1)
+    B = 16
+    spec = forked_spec(5, 65, 40, B, rng) + [(None, 0, 300)] + forked_spec(3, 4, 100, B, rng)
+    spec[6:] = [(6, 4, T) if src is not None else (None, 0, T) for src, _, T in spec[6:]]
+    c = Case(spec, H=3, B=B, seed=2)
+    groups, begin = c.plan()
+    assert groups[:, :3].tolist() == [[0, 5, 1040], [6, 3, 64]]
+    c.prefix(groups, splits)
+    torch.cuda.synchronize()
+    assert int(c.status.item()) == 0
+    pcs = c.pieces.cpu().numpy().reshape(c.S, c.H, bd.MAX_PREFIX_SPLITS, D + 4)
+    sl2 = c.scale * LOG2E
+    for f, n, P, _ in groups.tolist():
+        per = -(-(-(-P // 128)) // splits) * 128
+        for s in range(f, f + n):
+            for h in range(c.H):
+                for k in range(splits):
+                    t0, t1 = min(P, k * per), min(P, (k + 1) * per)
+                    o, m, l = pcs[s, h, k, :D], pcs[s, h, k, D], pcs[s, h, k, D + 1]
+                    if t0 >= t1:
+                        assert m == -np.inf and l == 0 and not o.any(), (s, h, k)
+                        continue
+                    kk, vv = c.keys(s, h, t0, t1)
+                    x = sl2 * (kk @ c.q[s, h].astype(np.float64))
+                    lse2 = x.max() + math.log2(np.exp2(x - x.max()).sum())
+                    assert abs(float(m) + math.log2(float(l)) - lse2) < 3e-3, (s, h, k)
+                    assert float(m) >= x.max() - 8.0 - 1e-3
+                    assert_close(o / l, rf.attend(c.q[s, h], kk, vv, c.scale), f"piece {(s, h, k)}")
+
+
+@pytest.mark.parametrize("B", [8, 16, 64, 256])
+def test_cascade_matches_oracle(B):
+    """Two groups, unshared sequences, and a member whose whole context is the prefix."""
+    rng = np.random.default_rng(B)
+    nsh = max(1, 600 // B)
+    spec = forked_spec(6, nsh, 3 * B, B, rng)
+    spec += [(None, 0, int(rng.integers(1, 700))), (None, 0, 5)]
+    g2 = len(spec)
+    spec += [(None, 0, 2 * B + 7), (g2, 2, 2 * B + 3), (g2, 2, 2 * B)]     # the last: no private tokens
+    c = Case(spec, H=4, B=B, seed=B + 1)
+    groups, begin = c.plan()
+    assert len(groups) == 2 and begin[-1] == c.lens[-1]
+    splits = bd.prefix_splits(len(groups), c.H, int(groups[:, 2].max()))
+    c.prefix(groups, splits)
+    got = c.decode(begin, splits)
+    assert int(c.status.item()) == 0 and bd.workspace_status(c.ws) == 0
+    assert_close(got, c.oracle(), f"cascade B={B}")
+    # the same call without the cascade
+    assert_close(c.decode(None, 0), c.oracle(), f"plain B={B}")
+
+
+def test_cascade_explicit_scale_and_forced_splits():
+    rng = np.random.default_rng(7)
+    c = Case(forked_spec(9, 40, 50, 16, rng), H=2, B=16, seed=8, scale=0.2)
+    groups, begin = c.plan()
+    for splits in (1, 5, 8):
+        c.prefix(groups, splits, scale=0.2)
+        assert_close(c.decode(begin, splits, scale=0.2), c.oracle(), f"splits {splits}")
+
+
+def test_cascade_with_fused_append():
+    """One decode step: the new token appended inside the private pass, attention over it."""
+    rng = np.random.default_rng(11)
+    B, H = 16, 4
+    spec = forked_spec(7, 20, 30, B, rng)
+    c = Case(spec, H=H, B=B, seed=12)
+    # the new token goes to the slot of position T_s - 1: the context already counts it
+    slots = np.array([int(c.tables[s, (T - 1) // B]) * B + (T - 1) % B for s, T in enumerate(c.lens)],
+                     dtype=np.int64)
+    kn = rng.standard_normal((c.S, H, D)).astype(np.float16)
+    vn = rng.standard_normal((c.S, H, D)).astype(np.float16)
+    groups, begin = c.plan()
+    assert len(groups) == 1 and (begin == 320).all()
+    c.prefix(groups, 2)
+    got = c.decode(begin, 2, k_new=torch.from_numpy(kn).cuda(), v_new=torch.from_numpy(vn).cuda(),
+                   slot_mapping=torch.from_numpy(slots).cuda())
+    rf.append_kv(c.kp, c.vp, kn, vn, slots, B, "HND")
+    assert_close(got, c.oracle(), "cascade + append")
+    assert np.array_equal(c.pool.k_pool.cpu().numpy().reshape(-1).view(np.uint16), c.kp.reshape(-1).view(np.uint16))
+
+
+def test_bad_begin_is_flagged_and_attends_everything():
+    rng = np.random.default_rng(5)
+    c = Case(forked_spec(4, 10, 40, 16, rng), H=2, B=16, seed=6)
+    groups, begin = c.plan()
+    c.prefix(groups, 1)
+    begin = begin.copy()
+    begin[1] = 17                       # not whole blocks: read as 0, the whole context attended here
+    got = c.decode(begin, 1)
+    assert bd.workspace_status(c.ws) & 0x2
+    assert_close(got, c.oracle(), "bad begin")
+
+
+def test_cascade_argument_errors():
+    rng = np.random.default_rng(9)
+    c = Case(forked_spec(3, 10, 20, 16, rng), H=2, B=16, seed=10)
+    groups, begin = c.plan()
+    gd = torch.from_numpy(groups).cuda()
+    for splits in (0, bd.MAX_PREFIX_SPLITS + 1):
+        with pytest.raises(bd.PkvError) as e:
+            c.pool.prefix_attention(0, c.qd, gd, len(groups), splits, c.tab_d, c.pieces, c.status)
+        assert e.value.code == "INVALID_ARG"
+    with pytest.raises(bd.PkvError) as e:    # pieces too small
+        c.pool.prefix_attention(0, c.qd, gd, len(groups), 1, c.tab_d, c.pieces[:16], c.status)
+    assert e.value.code == "INVALID_ARG"
+    with pytest.raises(bd.PkvError) as e:    # seq_begin without pieces
+        c.pool.decode_attention_ex(0, c.qd, c.tab_d, c.lens_d, torch.empty_like(c.qd), c.ws,
+                                   seq_begin=torch.from_numpy(begin).cuda(), splits=1)
+    assert e.value.code == "INVALID_ARG"
+    # an fp16 pool with head_dim 64 has no prefix pass
+    small = pkv.Pool(1, 8, 16, 2, 64, "HND", k_pool=torch.zeros((8, 2, 16, 64), dtype=torch.float16, device="cuda"),
+                     v_pool=torch.zeros((8, 2, 16, 64), dtype=torch.float16, device="cuda"))
+    with pytest.raises(bd.PkvError) as e:
+        small.prefix_attention(0, torch.zeros((3, 2, 64), dtype=torch.float16, device="cuda"), gd, 1, 1, c.tab_d,
+                               c.pieces, c.status)
+    assert e.value.code == "UNSUPPORTED"
+    torch.cuda.synchronize()

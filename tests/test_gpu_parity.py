@@ -62,8 +62,8 @@ def make_oracle(w):
     return OracleEngine(w, wl.pool_values(w, 0), wl.pool_values(w, 1))
 
 
-def run_parity(w, steps: int, fused: bool = True):
-    eng = DecodeEngine(w, fill="numpy", fused=fused)
+def run_parity(w, steps: int, fused: bool = True, cascade: bool = True):
+    eng = DecodeEngine(w, fill="numpy", fused=fused, cascade=cascade)
     ora = make_oracle(w)
     eng.run_script(values="numpy")
     ora.run_script()
@@ -104,9 +104,13 @@ def test_7b_shape_reduced(layout, fused):
     run_parity(w, 3, fused=fused)
 
 
-def test_prefix_sharing_cow_reduced():
+@pytest.mark.parametrize("cascade", [True, False])
+@pytest.mark.parametrize("fused", [True, False])
+def test_prefix_sharing_cow_reduced(cascade, fused):
+    """The forked prompt: with the cascade (prefix pass + private pass) and without."""
     w = wl.make_workload(3, num_layers=2, num_seqs=8, len_scale=0.25, decode_steps=3)
-    eng, ora = run_parity(w, 3)
+    eng, ora = run_parity(w, 3, fused=fused, cascade=cascade)
+    assert (eng.plan_groups == 1) == cascade
     st = eng.pool.stats()
     assert st["cow_copies"] == w.num_seqs - 1
 
