@@ -387,7 +387,6 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         const int32_t B = p.B;
         const int32_t rows = B < kTile ? B : kTile;           // rows per TMA box
         const uint32_t box_bytes = (uint32_t)rows * St::kRow;
-        const uint32_t scale_bytes = (uint32_t)rows * 4;
         constexpr int W = D / 8;                              // 16-byte fp16 words per new row
         constexpr int NW = (2 * W + 31) / 32;                 // words of the new K+V rows per lane
         Cursor c = locate(sm, S, H, g0);
@@ -465,10 +464,26 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 win_val = e < p.max_blocks ? __ldg(p.tables + (size_t)c.s * p.max_blocks + e) : 0;
             }
             const bool first = (k == 0) || (c.t == 0);
-            const uint32_t bytes =
-                (uint32_t)nbox * (box_bytes * 2 + (Q8 ? scale_bytes * 2 : 0)) + (first ? D * 2 : 0);
+            const uint32_t bytes = (uint32_t)nbox * box_bytes * 2 + (first ? D * 2 : 0);
             const uint32_t dst = stage0 + stage * SB;
             const uint32_t bar = full0 + 8 * stage;
+            if constexpr (Q8) {
+                // the tile's scales ([N][H][B]: token i of the tile is row y_i): lane i
+                // copies token i's K and V scale with 4-byte asynchronous copies (one
+                // coalesced request each, not two small bulk copies per block), and the
+                // stage's phase waits for them; issued before lane 0's arrival so the
+                // phase cannot complete without them
+                const int32_t t = t0 + min(lane, ntok - 1);
+                int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
+                if (blk < 0 || blk >= p.N) blk = 0;          // flagged with the boxes below
+                const size_t y = ((size_t)blk * H + c.h) * B + t % B;
+                if (lane < ntok) {
+                    ptx::cp_async_4(dst + St::kScales + lane * 4, p.k_scale + y);
+                    ptx::cp_async_4(dst + St::kScales + kTile * 4 + lane * 4, p.v_scale + y);
+                }
+                ptx::cp_async_mbar_arrive(bar);
+                __syncwarp();
+            }
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar, bytes);
             for (int32_t i = 0; i < nbox; ++i) {
                 int32_t blk = __shfl_sync(0xffffffffu, win_val, lb + i - win_lb0);
@@ -487,11 +502,6 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                     }
                     ptx::tma_load_2d(dst + i * box_bytes, &kmap, x, y, bar);
                     ptx::tma_load_2d(dst + St::kTileBytes + i * box_bytes, &vmap, x, y, bar);
-                    if constexpr (Q8) {   // the rows' scales ([N][H][B] layout: rows contiguous)
-                        ptx::bulk_load(dst + St::kScales + i * scale_bytes, p.k_scale + y, scale_bytes, bar);
-                        ptx::bulk_load(dst + St::kScales + kTile * 4 + i * scale_bytes, p.v_scale + y, scale_bytes,
-                                       bar);
-                    }
                 }
             }
             if (lane == 0 && first)

@@ -89,6 +89,18 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (the non-bulk async copy; cached in L1).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Keep the current phase of mbarrier `bar` open until every cp.async this thread
+// issued so far has landed (the arrival it adds is taken back when they land, so
+// the barrier's expected count is unchanged).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Atomic add at GPU scope with acquire-release semantics: one instruction that
 // publishes the writes this thread has observed (those of its CTA after a
 // barrier) and sees the writes published by earlier adders.
