@@ -80,11 +80,13 @@ def measured_peak():
 
 
 def device_code_hash() -> str:
-    """Hash of the attention kernel's device code: its .cu up to the host-side section, plus ptx.cuh."""
+    """Hash of the attention kernel's device code: its .cu up to the host-side section, plus the
+    device headers it includes (ptx.cuh, quant.cuh)."""
     text = open(KERNEL_SRC).read()
     cut = text.find("// ------------------------------------------------------------------ host side")
     h = hashlib.sha256(text[:cut].encode())
-    h.update(open(os.path.join(os.path.dirname(KERNEL_SRC), "ptx.cuh")).read().encode())
+    for hdr in ("ptx.cuh", "quant.cuh"):
+        h.update(open(os.path.join(os.path.dirname(KERNEL_SRC), hdr)).read().encode())
     return h.hexdigest()[:16]
 
 
