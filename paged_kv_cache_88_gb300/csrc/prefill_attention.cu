@@ -146,6 +146,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two fp32 values rounded to fp16 (nearest even), packed low = lo, high = hi.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -391,13 +404,16 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) x[i] = (valid && t0 + i <= pr) ? x[i] : -INFINITY;
             }
+            // row max of this half: a tree of three-input maxima (64 -> 22 -> 8 -> 3 -> 1)
+            float m22[22];
+#pragma unroll
+            for (int k = 0; k < 21; ++k) m22[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+            m22[21] = x[63];
             float m8[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = x[k];
-#pragma unroll
-            for (int i = 8; i < kCols; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int k = 0; k < 7; ++k) m8[k] = fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
+            m8[7] = m22[21];
+            float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             // row max across the two halves (a slot per tile parity, so a fast partner
             // never overwrites a value not yet read)
             float *xs = xchg + b * 2 * kQT;
@@ -423,21 +439,21 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
             }
             m_ref = new_ref;
             if (j >= 2) bounded_wait(BAR(kOFull + b), ((j - 2) >> 1) & 1, timed_out, p.status);  // P[b] free
-            const bool live = m_ref != -INFINITY;
-            const float neg = -m_ref;
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
+            // P = 2^(x * scale log2(e) - m_ref), pairs at a time; a row with no live key
+            // yet (m_ref = -inf: every x is -inf) gets 2^-inf = 0
+            const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
+            float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[kCols / 2];
 #pragma unroll
             for (int e = 0; e < kCols / 2; ++e) {
-                const float p0 = live ? ptx::ex2(fmaf(x[2 * e], sl2, neg)) : 0.f;
-                const float p1 = live ? ptx::ex2(fmaf(x[2 * e + 1], sl2, neg)) : 0.f;
-                const __half2 hp = __floats2half2_rn(p0, p1);
-                const float2 back = __half22float2(hp);   // the weights P V uses are the fp16 ones
-                rs[e & 3] += back.x + back.y;
-                pk[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                const float2 a = ptx::ffma2(make_float2(x[2 * e], x[2 * e + 1]), make_float2(sl2, sl2),
+                                            make_float2(neg, neg));
+                const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+                pk[e] = pack_half2(pp.x, pp.y);
+                rs2[e & 1] = ptx::fadd2(rs2[e & 1], pp);
             }
             tmem_st32(tP(b) + lane_base + hf * (kCols / 2), pk);
-            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+            l = l * alpha + ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y));
             // the last tile: zero the V rows no query may see (they may hold non-finite garbage)
             if (j == nkt - 1) {
                 bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
