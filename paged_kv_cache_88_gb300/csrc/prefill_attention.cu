@@ -53,7 +53,7 @@ constexpr int kD = 128;              // head dim (MMA K of Q K^T, N of P V)
 constexpr int kHalf = 64;            // 64 fp16 = one 128-byte swizzle row
 constexpr int kSub = kQT * 128;      // bytes of one [128 rows x 64 elements] swizzled sub-tile (16 KB)
 constexpr int kTileBytes = 2 * kSub; // a 128 x 128 fp16 tile as two sub-tiles
-constexpr int kThreads = 320;        // warps 0-7 softmax, warp 8 MMA issue, warp 9 TMA loads
+constexpr int kThreads = 352;        // warps 0-7 softmax, warp 8 MMA issue, warps 9-10 TMA loads (K, V)
 constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -294,14 +294,20 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     const uint32_t tO = tmem + 2 * kKT;
     auto tP = [tmem](int b) { return tmem + 3 * kKT + (uint32_t)b * (kKT / 2); };
 
-    if (warp == 9) {
-        // ================= loader: TMA for Q, then K and V tiles (one box per block of the table)
+    if (warp == 9 || warp == 10) {
+        // ================= loaders: warp 9 brings Q and the K tiles, warp 10 the V tiles
+        // (one box per block of the table, lane i box i). Separate warps, so a K tile
+        // is refilled as soon as its S MMA is done, whatever the V side waits for.
+        const bool is_k = warp == 9;
         const int32_t rowsb = B < kKT ? B : kKT;       // rows per box; B is a power of two, 8..256
-        if (lane == 0) {
+        if (is_k && lane == 0) {
             ptx::mbar_arrive_expect_tx(BAR(kQFull), kTileBytes);
             for (int half = 0; half < 2; ++half)
                 ptx::tma_load_3d(sQ + half * kSub, &qmap, half * kHalf, h, q0, BAR(kQFull));
         }
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        const int full0 = is_k ? kKFull : kVFull;
+        const int free0 = is_k ? kSFull : kOFull;     // slot b is free once S_{j-2} (K) / P_{j-2} V (V) is done
         for (int32_t j = 0; j < nkt; ++j) {
             const int b = j & 1;
             const int32_t t0 = kv_begin + j * kKT;
@@ -313,31 +319,23 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
                 const int32_t lb = (t0 + lane * rowsb) / B;
                 int32_t blk = lb < p.max_blocks ? p.tables[(size_t)srow * p.max_blocks + lb] : -1;
                 if (blk < 0 || blk >= p.N) {
-                    atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                    if (is_k) atomicOr(p.status, PKV_DEV_BAD_BLOCK);
                     blk = 0;
                 }
                 y = (blk * H + h) * B + (B < kKT ? 0 : t0 % B);
             }
             const uint32_t off = (uint32_t)lane * rowsb * 128;
-            if (j >= 2) bounded_wait(BAR(kSFull + b), ((j - 2) >> 1) & 1, timed_out, p.status);
-            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(kKFull + b), box_bytes);
+            const uint32_t dst = (is_k ? sK(b) : sV(b)) + off;
+            if (j >= 2) bounded_wait(BAR(free0 + b), ((j - 2) >> 1) & 1, timed_out, p.status);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(full0 + b), box_bytes);
             __syncwarp();
             if (lane < nbox)
                 for (int half = 0; half < 2; ++half)
-                    ptx::tma_load_2d(sK(b) + half * kSub + off, &kmap, half * kHalf, y, BAR(kKFull + b));
-            if (j >= 2) bounded_wait(BAR(kOFull + b), ((j - 2) >> 1) & 1, timed_out, p.status);
-            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(kVFull + b), box_bytes);
-            __syncwarp();
-            if (lane < nbox)
-                for (int half = 0; half < 2; ++half)
-                    ptx::tma_load_2d(sV(b) + half * kSub + off, &vmap, half * kHalf, y, BAR(kVFull + b));
+                    ptx::tma_load_2d(dst + half * kSub, map, half * kHalf, y, BAR(full0 + b));
         }
-        // the last loads into each slot and Q have landed before the CTA may exit
-        drain_wait(BAR(kQFull), 0);
-        for (int32_t j = nkt - 2 < 0 ? 0 : nkt - 2; j < nkt; ++j) {
-            drain_wait(BAR(kKFull + (j & 1)), (j >> 1) & 1);
-            drain_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1);
-        }
+        // the last loads into each slot (and Q) have landed before the CTA may exit
+        if (is_k) drain_wait(BAR(kQFull), 0);
+        for (int32_t j = nkt - 2 < 0 ? 0 : nkt - 2; j < nkt; ++j) drain_wait(BAR(full0 + (j & 1)), (j >> 1) & 1);
     } else if (warp == 8) {
         // ================= MMA issue (one thread)
         if (lane == 0) {
@@ -359,6 +357,14 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
             for (int32_t j = 0; j < nkt; ++j) {
                 const int b = j & 1;
                 bounded_wait(BAR(kPReady + b), (j >> 1) & 1, timed_out, p.status);   // P_j written, S[b] read
+                tc_fence_after();
+                // S_{j+2} first when its K tile is already in: the softmax needs it one tile
+                // from now, while P_j V is only needed before P_{j+2} is written
+                bool s_next = j + 2 < nkt;
+                if (s_next && ptx::mbar_test_wait(BAR(kKFull + b), ((j + 2) >> 1) & 1)) {
+                    issue_s(j + 2);
+                    s_next = false;
+                }
                 bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
                 tc_fence_after();
                 // O += P_j V_j over the tile's keys: A = P from tensor memory (8 columns per 16 keys),
@@ -367,7 +373,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
                     umma_ts(tO, tP(b) + ks * 8, umma_desc(sV(b) + ks * 2048, kSub, 1024), id_pv,
                             (j > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(BAR(kOFull + b));
-                if (j + 2 < nkt) issue_s(j + 2);
+                if (s_next) issue_s(j + 2);
             }
             // the last commit covers every MMA issued before it
             drain_wait(BAR(kOFull + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1);
