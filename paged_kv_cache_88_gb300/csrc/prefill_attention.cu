@@ -11,24 +11,26 @@
 // §2.4). Dense enough for tensor cores: a 128-query tile reuses every K/V tile
 // 128 times.
 //
-// Design (one CTA per (sequence, head, 128-query tile); 4 softmax warps, one
-// MMA-issue warp and one TMA warp; fp16 HND cache, head_dim 128):
-// * The TMA warp brings the Q tile once and K/V tiles of 128 keys (one box per
-//   block of the table, two 64-element halves each) into 128-byte-swizzled
-//   shared memory: two K slots and two V slots, each refilled as soon as the
-//   MMA that reads it has finished.
+// Design (one CTA per (sequence, head, 128-query tile); 8 softmax warps, one
+// MMA-issue warp and two TMA warps; fp16 HND cache, head_dim 128):
+// * One TMA warp brings the Q tile and the K tiles, the other the V tiles, 128 keys
+//   at a time (one box per block of the table, two 64-element halves each) into
+//   128-byte-swizzled shared memory: two K slots and two V slots, each refilled as
+//   soon as the MMA that reads it has finished. Separate warps, so a K slot does
+//   not wait behind a V slot.
 // * One elected thread issues S = Q K^T (M = N = K = 128, fp16 -> fp32) into one
-//   of two tensor-memory S tiles, and, once the softmax warps have written P
-//   (fp16, the same swizzled K-major layout) for a tile, P V onto the O tile in
-//   tensor memory (V read MN-major straight from its [token][dim] rows). With
-//   two S tiles, the tensor cores compute the next tile's S while the softmax
-//   warps work on this one.
-// * Each softmax thread owns one query row: it reads its S row from tensor
-//   memory in one load, applies the causal mask on the diagonal tile only, and
-//   writes P. The softmax reference max only moves when a row's max exceeds it
-//   by more than 2^8, and only then is O rescaled in place (tcgen05.ld / st).
-//   Rows past the sequence's tokens in the last tile are zeroed in V before
-//   P V (a zero weight times non-finite garbage would not be zero).
+//   of two tensor-memory S tiles, and, once the softmax warps have written P_j,
+//   O += P_j V_j onto the O tile in tensor memory (P read from tensor memory as the
+//   A operand; V read MN-major straight from its [token][dim] rows). With two S
+//   tiles, the tensor cores compute the next tile's S while the softmax warps work
+//   on this one; S_{j+2} goes before P_j V when its K tile is already in.
+// * Query row r is tensor-memory lane r, shared by two softmax warps (one 64-key
+//   half of each S row each; they exchange the row max once per tile). The causal
+//   mask is applied on the diagonal tile only. The softmax reference max only
+//   moves when a row's max exceeds it by more than 2^8, and only then is O
+//   rescaled in place (tcgen05.ld / st). Rows past the sequence's tokens in the
+//   last tile are zeroed in V before P V (a zero weight times non-finite garbage
+//   would not be zero).
 // * Every wait is bounded (1 s, then PKV_DEV_TIMEOUT); before exiting, the CTA
 //   waits (bounded) for its own copies and MMAs, and frees tensor memory on
 //   every path.
@@ -55,20 +57,19 @@ constexpr int kSub = kQT * 128;      // bytes of one [128 rows x 64 elements] sw
 constexpr int kTileBytes = 2 * kSub; // a 128 x 128 fp16 tile as two sub-tiles
 constexpr int kThreads = 352;        // warps 0-7 softmax, warp 8 MMA issue, warps 9-10 TMA loads (K, V)
 constexpr int kSoftmaxThreads = 256;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,384) Q [384,448) P [448,512)
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// shared memory: K0 | K1 | V0 | V1 (each a 32 KB tile, 1024-aligned), then the
+// shared memory: Q | K0 | K1 | V0 | V1 (each a 32 KB tile, 1024-aligned), then the
 // row-max exchange [2 tiles][2 halves][128 rows] fp32, then barriers and flags
-constexpr int kSmemTiles = 4 * kTileBytes;
+constexpr int kSmemTiles = 5 * kTileBytes;
 constexpr int kXchgBytes = 2 * 2 * kQT * 4;
 constexpr int kSmemBytes = kSmemTiles + kXchgBytes + 256 /* barriers + flags */ + 1024 /* alignment slack */;
 
 // barrier indices (two-slot rings use index + slot)
-constexpr int kQReady = 0, kKFull = 1, kVFull = 3, kSFull = 5, kPReady = 7, kOFull = 9, kNumBars = 11;
+constexpr int kQFull = 0, kKFull = 1, kVFull = 3, kSFull = 5, kPReady = 7, kOFull = 9, kNumBars = 11;
 
 struct PrefillParams {
-    const __half *q;          // prefill: [total_q][H][D]; prefix pass: [S][H][D]
     const int32_t *q_start;   // prefill: [S + 1] chunk rows of sequence s: q_start[s] .. q_start[s+1]-1
     const int32_t *tables;    // [S][max_blocks]
     const int32_t *lens;      // prefill: [S] context lengths including the chunk
@@ -97,9 +98,15 @@ __device__ __forceinline__ uint32_t umma_idesc(uint32_t b_mn) {
     return (1u << 4) | ((uint32_t)(kKT >> 3) << 17) | ((uint32_t)(kQT >> 4) << 24) | (b_mn << 16);
 }
 
-// tcgen05 MMA, D (tensor memory) [+]= A B: A read from tensor memory (M rows on
-// lanes, K along columns, two fp16 per 32-bit column), B from shared memory by
-// descriptor.
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// The same MMA with A read from tensor memory (M rows on lanes, K along columns,
+// two fp16 per 32-bit column).
 __device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
                                         uint32_t accumulate) {
     asm volatile(
@@ -197,14 +204,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // warps work on tile j. Every barrier is waited on at most one phase behind.
 template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                         const PrefillParams p) {
+prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~uintptr_t(1023));
-    const uint32_t s0 = ptx::smem_addr(base);
-    auto sK = [s0](int b) { return s0 + (uint32_t)b * kTileBytes; };
-    auto sV = [s0](int b) { return s0 + (uint32_t)(2 + b) * kTileBytes; };
+    const uint32_t sQ = ptx::smem_addr(base);
+    auto sK = [sQ](int b) { return sQ + (uint32_t)(1 + b) * kTileBytes; };
+    auto sV = [sQ](int b) { return sQ + (uint32_t)(3 + b) * kTileBytes; };
     float *xchg = reinterpret_cast<float *>(base + kSmemTiles);          // [2][2][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kSmemTiles + kXchgBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
@@ -271,7 +278,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i)
-            ptx::mbar_init(BAR(i), (i == kPReady || i == kPReady + 1 || i == kQReady) ? kSoftmaxThreads / 32 : 1);
+            ptx::mbar_init(BAR(i), (i == kPReady || i == kPReady + 1) ? kSoftmaxThreads / 32 : 1);
         *timed_out = 0;
         ptx::fence_barrier_init();
     }
@@ -287,15 +294,19 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_
     const uint32_t tmem = *tmem_slot;
     auto tS = [tmem](int b) { return tmem + (uint32_t)b * kKT; };
     const uint32_t tO = tmem + 2 * kKT;
-    const uint32_t tQ = tmem + 3 * kKT;            // Q as the A operand of S (fp16 pairs, 64 columns)
-    const uint32_t tP = tQ + kD / 2;               // P_j (fp16 pairs, 64 columns)
+    auto tP = [tmem](int b) { return tmem + 3 * kKT + (uint32_t)b * (kKT / 2); };
 
     if (warp == 9 || warp == 10) {
-        // ================= loaders: warp 9 brings the K tiles, warp 10 the V tiles
+        // ================= loaders: warp 9 brings Q and the K tiles, warp 10 the V tiles
         // (one box per block of the table, lane i box i). Separate warps, so a K tile
         // is refilled as soon as its S MMA is done, whatever the V side waits for.
         const bool is_k = warp == 9;
         const int32_t rowsb = B < kKT ? B : kKT;       // rows per box; B is a power of two, 8..256
+        if (is_k && lane == 0) {
+            ptx::mbar_arrive_expect_tx(BAR(kQFull), kTileBytes);
+            for (int half = 0; half < 2; ++half)
+                ptx::tma_load_3d(sQ + half * kSub, &qmap, half * kHalf, h, q0, BAR(kQFull));
+        }
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         const int full0 = is_k ? kKFull : kVFull;
         const int free0 = is_k ? kSFull : kOFull;     // slot b is free once S_{j-2} (K) / P_{j-2} V (V) is done
@@ -324,7 +335,8 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_
                 for (int half = 0; half < 2; ++half)
                     ptx::tma_load_2d(dst + half * kSub, map, half * kHalf, y, BAR(full0 + b));
         }
-        // the last loads into each slot have landed before the CTA may exit
+        // the last loads into each slot (and Q) have landed before the CTA may exit
+        if (is_k) drain_wait(BAR(kQFull), 0);
         for (int32_t j = nkt - 2 < 0 ? 0 : nkt - 2; j < nkt; ++j) drain_wait(BAR(full0 + (j & 1)), (j >> 1) & 1);
     } else if (warp == 8) {
         // ================= MMA issue (one thread)
@@ -334,16 +346,14 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_
                 const int b = j & 1;
                 bounded_wait(BAR(kKFull + b), (j >> 1) & 1, timed_out, p.status);
                 tc_fence_after();
-                // S = Q K^T over the head dim: 8 steps of 16 (4 per 64-element half of K); A = Q
-                // from tensor memory (8 columns per step), B = K rows (K-major, 128-byte swizzle)
+                // S = Q K^T over the head dim: 8 steps of 16 (4 per 64-element half)
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * kSub + (ks & 3) * 32;
-                    umma_ts(tS(b), tQ + ks * 8, umma_desc(sK(b) + koff, 16, 1024), id_qk, ks > 0);
+                    umma(tS(b), umma_desc(sQ + koff, 16, 1024), umma_desc(sK(b) + koff, 16, 1024), id_qk, ks > 0);
                 }
                 umma_commit(BAR(kSFull + b));
             };
-            bounded_wait(BAR(kQReady), 0, timed_out, p.status);   // Q in tensor memory
-            tc_fence_after();
+            bounded_wait(BAR(kQFull), 0, timed_out, p.status);
             issue_s(0);
             if (nkt > 1) issue_s(1);
             for (int32_t j = 0; j < nkt; ++j) {
@@ -362,7 +372,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_
                 // O += P_j V_j over the tile's keys: A = P from tensor memory (8 columns per 16 keys),
                 // B = V rows (MN-major, halves 16 KB apart)
                 for (int ks = 0; ks < kKT / 16; ++ks)
-                    umma_ts(tO, tP + ks * 8, umma_desc(sV(b) + ks * 2048, kSub, 1024), id_pv,
+                    umma_ts(tO, tP(b) + ks * 8, umma_desc(sV(b) + ks * 2048, kSub, 1024), id_pv,
                             (j > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(BAR(kOFull + b));
                 if (s_next) issue_s(j + 2);
@@ -388,28 +398,6 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_
         constexpr float kSlack = 8.f;
         constexpr int kCols = kKT / 2;              // keys of S (and columns of O) per thread
         float m_ref = -INFINITY, l = 0.f;
-        {   // this thread's half of its query row into tensor memory (fp16 pairs), the A
-            // operand of every S MMA; rows past the tile's queries are zero
-            uint32_t qw[32];
-            if (valid) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)(q0 + r) * H + h) * kD + hf * kCols);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 v = __ldg(src + i);
-                    qw[4 * i] = v.x;
-                    qw[4 * i + 1] = v.y;
-                    qw[4 * i + 2] = v.z;
-                    qw[4 * i + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) qw[i] = 0u;
-            }
-            tmem_st32(tQ + lane_base + hf * (kCols / 2), qw);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(BAR(kQReady));
-        }
         for (int32_t j = 0; j < nkt; ++j) {
             const int b = j & 1;
             const int32_t t0 = kv_begin + j * kKT + hf * kCols;   // first key of this thread's half
@@ -472,15 +460,13 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_
                 pk[e] = pack_half2(pp.x, pp.y);
                 rs2[e & 1] = ptx::fadd2(rs2[e & 1], pp);
             }
-            // one P buffer: P_{j-1} V must be done reading it
-            if (j > 0) bounded_wait(BAR(kOFull + (b ^ 1)), ((j - 1) >> 1) & 1, timed_out, p.status);
-            tmem_st32(tP + lane_base + hf * (kCols / 2), pk);
+            tmem_st32(tP(b) + lane_base + hf * (kCols / 2), pk);
             l = l * alpha + ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y));
             // the last tile: zero the V rows no query may see (they may hold non-finite garbage)
             if (j == nkt - 1) {
                 bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
                 const int32_t first_dead = kv_end - (kv_begin + j * kKT);   // rows [first_dead, 128) of the tile
-                unsigned char *sVp = base + (2 + b) * kTileBytes;
+                unsigned char *sVp = base + (3 + b) * kTileBytes;
                 const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
                 for (int32_t w = tid; w < nwords * 2; w += kSoftmaxThreads) {
                     const int half = w / nwords, rem = w - half * nwords;
@@ -555,13 +541,24 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The pool layer as rows of D, boxes of 64 x min(B, 128), 128-byte swizzle.
-pkv_status encode_maps(const pkv_pool *pool, int32_t layer, CUtensorMap *kmap, CUtensorMap *vmap) {
+// q ([rows][H][D] fp16) as a 3-D tensor (D, H, row), boxes of 64 x 1 x 128; the
+// pool layer as rows of D, boxes of 64 x min(B, 128). 128-byte swizzle.
+pkv_status encode_maps(const pkv_pool *pool, int32_t layer, const void *q, int32_t q_rows, CUtensorMap *qmap,
+                       CUtensorMap *kmap, CUtensorMap *vmap) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const pkv_pool_desc &d = pool->desc;
     const PoolLayer pl = pool_layer(pool, layer);
     const int H = d.num_heads, B = d.block_size, N = d.num_blocks;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)q_rows};
+        const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+        const cuuint32_t box[3] = {kHalf, 1, kQT}, es[3] = {1, 1, 1};
+        if (fn(qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(q), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(PKV_ERR_CUDA, "q tensor map");
+    }
     for (int which = 0; which < 2; ++which) {
         const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)N * H * B};
         const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
@@ -606,7 +603,7 @@ std::once_flag g_attr_once[kMaxDevices][2];
 cudaError_t g_attr_err[kMaxDevices][2];
 
 template <bool kPrefix>
-pkv_status launch_tc(dim3 grid, const CUtensorMap &kmap, const CUtensorMap &vmap,
+pkv_status launch_tc(dim3 grid, const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                      const PrefillParams &prm, void *stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -618,7 +615,7 @@ pkv_status launch_tc(dim3 grid, const CUtensorMap &kmap, const CUtensorMap &vmap
     if (g_attr_err[dev][kPrefix] != cudaSuccess)
         return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(g_attr_err[dev][kPrefix]));
     cudaError_t e = launch_pdl(prefill_attention_kernel<kPrefix>, grid, dim3(kThreads), (size_t)kSmemBytes,
-                               static_cast<cudaStream_t>(stream), kmap, vmap, prm);
+                               static_cast<cudaStream_t>(stream), qmap, kmap, vmap, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "%s launch: %s", kPrefix ? "prefix" : "prefill",
                                       cudaGetErrorString(e));
@@ -642,16 +639,15 @@ pkv_status pkv_prefill_attention(const pkv_pool *pool, int32_t layer, const void
     if (!q || !q_start || !block_tables || !context_lens || !out || !status)
         return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument (status is required here)");
     if (!aligned16(q) || !aligned16(out)) return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
-    CUtensorMap kmap, vmap;
-    st = encode_maps(pool, layer, &kmap, &vmap);
+    CUtensorMap qmap, kmap, vmap;
+    st = encode_maps(pool, layer, q, total_q, &qmap, &kmap, &vmap);
     if (st != PKV_OK) return st;
     PrefillParams prm = base_params(pool, block_tables, max_blocks, num_seqs, scale, status);
-    prm.q = static_cast<const __half *>(q);
     prm.q_start = q_start;
     prm.lens = context_lens;
     prm.out = static_cast<__half *>(out);
     const dim3 grid((max_chunk + kQT - 1) / kQT, pool->desc.num_heads, num_seqs);
-    return launch_tc<false>(grid, kmap, vmap, prm, stream);
+    return launch_tc<false>(grid, qmap, kmap, vmap, prm, stream);
 }
 
 pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void *q, const pkv_prefix_group *groups,
@@ -671,16 +667,15 @@ pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void 
     const pkv_pool_desc &d = pool->desc;
     const size_t need = (size_t)num_seqs * d.num_heads * PKV_MAX_PREFIX_SPLITS * (kD + 4) * sizeof(float);
     if (pieces_bytes < need) return fail(PKV_ERR_INVALID_ARG, "pieces: %zu bytes < %zu needed", pieces_bytes, need);
-    CUtensorMap kmap, vmap;
-    st = encode_maps(pool, layer, &kmap, &vmap);
+    CUtensorMap qmap, kmap, vmap;
+    st = encode_maps(pool, layer, q, num_seqs, &qmap, &kmap, &vmap);
     if (st != PKV_OK) return st;
     PrefillParams prm = base_params(pool, block_tables, max_blocks, num_seqs, scale, status);
-    prm.q = static_cast<const __half *>(q);
     prm.groups = groups;
     prm.pieces = static_cast<float *>(pieces);
     prm.splits = splits;
     const dim3 grid(splits, d.num_heads, num_groups);
-    return launch_tc<true>(grid, kmap, vmap, prm, stream);
+    return launch_tc<true>(grid, qmap, kmap, vmap, prm, stream);
 }
 
 }  // extern "C"
