@@ -362,6 +362,7 @@ typedef struct {
 } pkv_prefix_group;
 
 #define PKV_MAX_GROUP_SEQS 128
+#define PKV_ATTN_INPUTS_EARLY 0x1u /* pkv_decode_attention_ex flag, see there */
 #define PKV_MAX_PREFIX_SPLITS 8
 
 /* Host planner of the cascade for one step. block_tables: host int32
@@ -420,12 +421,23 @@ pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void 
  * pkv_prefix_attention wrote for it earlier on the same stream. seq_begin[s]
  * must be a multiple of the block size in [0, T_s]; any other value is
  * flagged PKV_DEV_BAD_LENGTH and read as 0 (no prefix). fp16 pools only when
- * cascading (the prefix pass runs on fp16 tensor cores). */
+ * cascading (the prefix pass runs on fp16 tensor cores).
+ * flags: 0, or PKV_ATTN_INPUTS_EARLY. With it, the kernel reads the block
+ * tables, the lengths, seq_begin and the cached K/V rows -- and issues its first
+ * tiles' loads -- before the kernel that precedes it on the stream has finished;
+ * it touches q, k_new, v_new, the workspace, the pieces and out only after. The
+ * caller promises that the preceding kernel writes none of the former (e.g. it is
+ * the previous layer's attention, or the prefix pass): then the load latency at
+ * the start of the launch overlaps the end of the previous one. Every libpkv
+ * kernel lets its successor start only after its own inputs are final, so
+ * anything launched before that preceding kernel is complete. Other flag bits:
+ * INVALID_ARG. */
 pkv_status pkv_decode_attention_ex(const pkv_pool *pool, int32_t layer, const void *q, const void *k_new,
                                    const void *v_new, const int64_t *slot_mapping, const int32_t *block_tables,
                                    int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs,
                                    const int32_t *seq_begin, const float *pieces, int32_t splits, float scale,
-                                   void *out, void *workspace, size_t workspace_bytes, void *stream);
+                                   void *out, void *workspace, size_t workspace_bytes, uint32_t flags,
+                                   void *stream);
 
 /* Bytes of workspace pkv_decode_attention needs for these sizes on the
  * current CUDA device (0 and a pkv_last_error message on bad arguments). */

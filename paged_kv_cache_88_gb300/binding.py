@@ -36,6 +36,7 @@ EXPORTED = [
 ]
 
 MAX_GROUP_SEQS = 128
+ATTN_INPUTS_EARLY = 0x1
 MAX_PREFIX_SPLITS = 8
 
 
@@ -117,7 +118,7 @@ def lib() -> ctypes.CDLL:
             "pkv_prefix_splits": (i32, [i32, i32, i32]),
             "pkv_prefix_attention": (i32, [vp, i32, vp, vp, i32, i32, vp, i32, i32, f32, vp, sz, vp, vp]),
             "pkv_decode_attention_ex": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp,
-                                              sz, vp]),
+                                              sz, ctypes.c_uint32, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -363,15 +364,17 @@ class Pool:
 
     def decode_attention_ex(self, layer: int, q, block_tables, context_lens, out, workspace, k_new=None, v_new=None,
                             slot_mapping=None, seq_begin=None, pieces=None, splits: int = 0, scale: float = 0.0,
-                            stream=None) -> None:
-        """pkv_decode_attention_ex: optional fused append, optional cascade (private half + merge)."""
+                            flags: int = 0, stream=None) -> None:
+        """pkv_decode_attention_ex: optional fused append, optional cascade (private half + merge);
+        ``flags`` = ATTN_INPUTS_EARLY lets the launch start reading before its predecessor ends."""
         for t, dt, name in ((q, "float16", "q"), (out, "float16", "out"), (block_tables, "int32", "block_tables"),
                             (context_lens, "int32", "context_lens")):
             _require(t, dt, name)
         check(lib().pkv_decode_attention_ex(
             self._h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(block_tables),
             block_tables.shape[1], _ptr(context_lens), q.shape[0], _ptr(seq_begin), _ptr(pieces), int(splits),
-            float(scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+            float(scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), int(flags),
+            _stream(stream)))
 
     def layer_view(self, which: str, layer: int):
         t = self.k_pool if which == "k" else self.v_pool

@@ -110,6 +110,11 @@ struct Params {
     const int32_t *begin;
     const float *pre;
     int32_t pre_splits;
+    // 1: the tables, lengths, seq_begin and cached K/V rows were final before the
+    // preceding kernel on the stream started, so they are read (and the first tiles'
+    // K/V loads issued) before the grid dependency resolves; q, k_new, v_new, the
+    // workspace and out are touched only after it
+    int32_t early;
     int32_t S, H, max_blocks, B, N, layout;
     float scale_log2;    // scale * log2(e)
 };
@@ -290,8 +295,10 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     const int32_t cap = p.max_blocks * p.B;
 
     // ---- set-up: barriers (before the grid dependency resolves), then lengths
-    // and the tile prefix over sequences
-    ptx::launch_dependents();
+    // and the tile prefix over sequences. Dependents are let launch only once this
+    // grid's own dependency has resolved, so a kernel that starts early finds every
+    // kernel before its predecessor complete.
+    const bool early = p.early != 0;
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sm.full[i]), 1);
@@ -305,7 +312,10 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         ptx::prefetch_tensormap(&kmap);
         ptx::prefetch_tensormap(&vmap);
     }
-    ptx::grid_dependency_wait();
+    if (!early) {
+        ptx::grid_dependency_wait();
+        ptx::launch_dependents();
+    }
     for (int32_t s = tid; s < S; s += kThreads) {
         int32_t T = p.lens[s];
         if (T < 0 || T > cap) {
@@ -345,6 +355,8 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     const int32_t total = sm.base[S];
     const int32_t cta = blockIdx.x;
 
+    // The consumers touch out and the workspace: after the grid dependency.
+    if (early && warp < kConsumerWarps) ptx::grid_dependency_wait();
     // Nothing to attend here: out = 0 for an empty context (softmax over no
     // tokens contributes nothing), the merged prefix pieces for a sequence the
     // cascade's prefix covers entirely.
@@ -393,9 +405,90 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         int32_t win_s = -1, win_lb0 = 0, win_val = 0;
         uint4 nw[NW];                                         // the new token's K/V row words
         int64_t new_slot = -1;                                // pending append of the current (s, h)
-        for (int32_t k = 0; k < n; ++k) {
+        // K/V boxes (and, for E4M3, the scales) of the tile at cursor cc into `stage`,
+        // with the stage's expected bytes including the q row when `first`
+        auto issue_kv = [&](const Cursor &cc, int32_t stage, bool first) {
+            const int32_t tt = cc.t * kTile;                   // the tile's first token attended here
+            const int32_t ntok = min(kTile, sm.len[cc.s] - tt);
+            const int32_t t0 = sm.beg[cc.s] + tt;              // its position in the sequence
+            const int32_t lb = t0 / B;                         // first logical block of the tile
+            const int32_t nbox = B < kTile ? (ntok + B - 1) / B : 1;
+            const int32_t r0 = B < kTile ? 0 : t0 % B;         // first row inside the block
+            if (cc.s != win_s || lb < win_lb0 || lb + nbox > win_lb0 + 32) {
+                win_s = cc.s;
+                win_lb0 = lb;
+                const int32_t e = lb + lane;
+                win_val = e < p.max_blocks ? __ldg(p.tables + (size_t)cc.s * p.max_blocks + e) : 0;
+            }
+            const uint32_t bytes = (uint32_t)nbox * box_bytes * 2 + (first ? D * 2 : 0);
+            const uint32_t dst = stage0 + stage * SB;
+            const uint32_t bar = full0 + 8 * stage;
+            if constexpr (Q8) {
+                // the tile's scales ([N][H][B]: token i of the tile is row y_i): lane i
+                // copies token i's K and V scale with 4-byte asynchronous copies (one
+                // coalesced request each, not two small bulk copies per block), and the
+                // stage's phase waits for them; issued before lane 0's arrival so the
+                // phase cannot complete without them
+                const int32_t t = t0 + min(lane, ntok - 1);
+                int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
+                if (blk < 0 || blk >= p.N) blk = 0;          // flagged with the boxes below
+                const size_t y = ((size_t)blk * H + cc.h) * B + t % B;
+                if (lane < ntok) {
+                    ptx::cp_async_4(dst + St::kScales + lane * 4, p.k_scale + y);
+                    ptx::cp_async_4(dst + St::kScales + kTile * 4 + lane * 4, p.v_scale + y);
+                }
+                ptx::cp_async_mbar_arrive(bar);
+                __syncwarp();
+            }
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar, bytes);
+            for (int32_t i = 0; i < nbox; ++i) {
+                int32_t blk = __shfl_sync(0xffffffffu, win_val, lb + i - win_lb0);
+                if (lane == 0) {
+                    if (blk < 0 || blk >= p.N) {
+                        atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                        blk = 0;
+                    }
+                    int32_t x, y;
+                    if (p.layout == PKV_LAYOUT_NHD) {
+                        x = cc.h * D;
+                        y = blk * B + r0;
+                    } else {
+                        x = 0;
+                        y = (blk * H + cc.h) * B + r0;
+                    }
+                    ptx::tma_load_2d(dst + i * box_bytes, &kmap, x, y, bar);
+                    ptx::tma_load_2d(dst + St::kTileBytes + i * box_bytes, &vmap, x, y, bar);
+                }
+            }
+        };
+        auto issue_q = [&](const Cursor &cc, int32_t stage) {
+            if (lane == 0)
+                ptx::bulk_load(stage0 + stage * SB + St::kQ, p.q + ((size_t)cc.s * H + cc.h) * D, D * 2,
+                               full0 + 8 * stage);
+        };
+        int32_t k0 = 0;   // the first tile of the main loop
+        if (early) {
+            // the first stages' K/V before the grid dependency resolves (not the tile the
+            // appended token goes to: it is stored first); their q rows after it
+            Cursor pend[NS];
+            bool pend_q[NS];
+            for (; k0 < n && k0 < NS; ++k0) {
+                if (p.k_new != nullptr && c.t == c.nt - 1 && sm.base[c.s] + c.h * c.nt + c.nt - 1 < g1) break;
+                const bool first = (k0 == 0) || (c.t == 0);
+                issue_kv(c, k0, first);
+                pend[k0] = c;
+                pend_q[k0] = first;
+                advance(c, sm, S, H);
+            }
+            ptx::grid_dependency_wait();
+            ptx::launch_dependents();
+            for (int32_t k = 0; k < k0; ++k)
+                if (pend_q[k]) issue_q(pend[k], k);
+            __syncwarp();
+        }
+        for (int32_t k = k0; k < n; ++k) {
             const int32_t stage = k % NS;
-            if (p.k_new != nullptr && ((k == 0) || (c.t == 0))) {
+            if (p.k_new != nullptr && ((k == k0) || (c.t == 0))) {
                 // a new (s, h): if its last tile is ours, fetch the appended token's rows now
                 const int32_t seg_last = sm.base[c.s] + c.h * c.nt + c.nt - 1;
                 new_slot = -1;
@@ -451,61 +544,9 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 new_slot = -1;
                 __syncwarp();
             }
-            const int32_t tt = c.t * kTile;                    // the tile's first token attended here
-            const int32_t ntok = min(kTile, sm.len[c.s] - tt);
-            const int32_t t0 = sm.beg[c.s] + tt;               // its position in the sequence
-            const int32_t lb = t0 / B;                         // first logical block of the tile
-            const int32_t nbox = B < kTile ? (ntok + B - 1) / B : 1;
-            const int32_t r0 = B < kTile ? 0 : t0 % B;         // first row inside the block
-            if (c.s != win_s || lb < win_lb0 || lb + nbox > win_lb0 + 32) {
-                win_s = c.s;
-                win_lb0 = lb;
-                const int32_t e = lb + lane;
-                win_val = e < p.max_blocks ? __ldg(p.tables + (size_t)c.s * p.max_blocks + e) : 0;
-            }
             const bool first = (k == 0) || (c.t == 0);
-            const uint32_t bytes = (uint32_t)nbox * box_bytes * 2 + (first ? D * 2 : 0);
-            const uint32_t dst = stage0 + stage * SB;
-            const uint32_t bar = full0 + 8 * stage;
-            if constexpr (Q8) {
-                // the tile's scales ([N][H][B]: token i of the tile is row y_i): lane i
-                // copies token i's K and V scale with 4-byte asynchronous copies (one
-                // coalesced request each, not two small bulk copies per block), and the
-                // stage's phase waits for them; issued before lane 0's arrival so the
-                // phase cannot complete without them
-                const int32_t t = t0 + min(lane, ntok - 1);
-                int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
-                if (blk < 0 || blk >= p.N) blk = 0;          // flagged with the boxes below
-                const size_t y = ((size_t)blk * H + c.h) * B + t % B;
-                if (lane < ntok) {
-                    ptx::cp_async_4(dst + St::kScales + lane * 4, p.k_scale + y);
-                    ptx::cp_async_4(dst + St::kScales + kTile * 4 + lane * 4, p.v_scale + y);
-                }
-                ptx::cp_async_mbar_arrive(bar);
-                __syncwarp();
-            }
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar, bytes);
-            for (int32_t i = 0; i < nbox; ++i) {
-                int32_t blk = __shfl_sync(0xffffffffu, win_val, lb + i - win_lb0);
-                if (lane == 0) {
-                    if (blk < 0 || blk >= p.N) {
-                        atomicOr(p.status, PKV_DEV_BAD_BLOCK);
-                        blk = 0;
-                    }
-                    int32_t x, y;
-                    if (p.layout == PKV_LAYOUT_NHD) {
-                        x = c.h * D;
-                        y = blk * B + r0;
-                    } else {
-                        x = 0;
-                        y = (blk * H + c.h) * B + r0;
-                    }
-                    ptx::tma_load_2d(dst + i * box_bytes, &kmap, x, y, bar);
-                    ptx::tma_load_2d(dst + St::kTileBytes + i * box_bytes, &vmap, x, y, bar);
-                }
-            }
-            if (lane == 0 && first)
-                ptx::bulk_load(dst + St::kQ, p.q + ((size_t)c.s * H + c.h) * D, D * 2, bar);
+            issue_kv(c, stage, first);
+            if (first) issue_q(c, stage);
             __syncwarp();
             advance(c, sm, S, H);
         }
@@ -949,7 +990,7 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
                                  void *stream, const void *k_new, const void *v_new, const int64_t *slots,
                                  uint32_t *status_override = nullptr, const float *k_scale = nullptr,
                                  const float *v_scale = nullptr, const int32_t *seq_begin = nullptr,
-                                 const float *pieces = nullptr, int32_t splits = 0) {
+                                 const float *pieces = nullptr, int32_t splits = 0, uint32_t flags = 0) {
     const bool q8 = k_scale != nullptr;
     if ((seq_begin == nullptr) != (pieces == nullptr))
         return fail(PKV_ERR_INVALID_ARG, "seq_begin and pieces go together (both NULL: no cascade)");
@@ -1024,6 +1065,7 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     prm.begin = seq_begin;
     prm.pre = pieces;
     prm.pre_splits = seq_begin ? splits : 0;
+    prm.early = (flags & PKV_ATTN_INPUTS_EARLY) ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -1086,8 +1128,10 @@ pkv_status pkv_decode_attention_ex(const pkv_pool *pool, int32_t layer, const vo
                                    const void *v_new, const int64_t *slot_mapping, const int32_t *block_tables,
                                    int32_t max_blocks, const int32_t *context_lens, int32_t num_seqs,
                                    const int32_t *seq_begin, const float *pieces, int32_t splits, float scale,
-                                   void *out, void *workspace, size_t workspace_bytes, void *stream) {
+                                   void *out, void *workspace, size_t workspace_bytes, uint32_t flags,
+                                   void *stream) {
     if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+    if (flags & ~(uint32_t)PKV_ATTN_INPUTS_EARLY) return fail(PKV_ERR_INVALID_ARG, "unknown flags %#x", flags);
     const pkv_pool_desc &d = pool->desc;
     if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
     if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
@@ -1103,7 +1147,7 @@ pkv_status pkv_decode_attention_ex(const pkv_pool *pool, int32_t layer, const vo
                                  block_tables, max_blocks, context_lens, num_seqs, scale, out, workspace,
                                  workspace_bytes, stream, append ? k_new : nullptr, append ? v_new : nullptr,
                                  append ? slot_mapping : nullptr, nullptr, pl.k_scale, pl.v_scale, seq_begin, pieces,
-                                 splits);
+                                 splits, flags);
 }
 
 pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const void *q, const int32_t *block_tables,

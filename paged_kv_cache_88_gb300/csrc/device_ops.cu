@@ -27,8 +27,8 @@ __global__ void __launch_bounds__(kAppendThreads)
 append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, const int64_t *__restrict__ slots,
               int32_t num_tokens, uint4 *__restrict__ k_layer, uint4 *__restrict__ v_layer, int64_t num_slots,
               int32_t B, int32_t H, int32_t words_per_row, int32_t layout, uint32_t *status) {
-    ptx::launch_dependents();
     ptx::grid_dependency_wait();
+    ptx::launch_dependents();   // successors start once this grid's inputs are final
     const int64_t words_per_token = (int64_t)H * words_per_row;
     const int64_t total = (int64_t)num_tokens * words_per_token;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -62,8 +62,8 @@ append_q8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_ne
                  float *__restrict__ k_scale, float *__restrict__ v_scale, int64_t num_slots, int32_t B, int32_t H,
                  uint32_t *status) {
     constexpr int W = D / 8;
-    ptx::launch_dependents();
     ptx::grid_dependency_wait();
+    ptx::launch_dependents();   // successors start once this grid's inputs are final
     const int lane = threadIdx.x & 31;
     const int64_t rows = (int64_t)num_tokens * H;
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
@@ -97,8 +97,8 @@ __global__ void __launch_bounds__(kCopyThreads)
 copy_blocks_kernel(const int32_t *__restrict__ pairs, int32_t num_pairs, uint4 *k_pool, uint4 *v_pool,
                    int32_t num_layers, int32_t num_blocks, int64_t block_words, uint4 *k_scale, uint4 *v_scale,
                    int64_t scale_words, uint32_t *status) {
-    ptx::launch_dependents();
     ptx::grid_dependency_wait();
+    ptx::launch_dependents();   // successors start once this grid's inputs are final
     const int64_t jobs = (int64_t)num_pairs * num_layers;
     for (int64_t y = blockIdx.y; y < jobs; y += gridDim.y) {
         const int32_t pr = (int32_t)(y / num_layers);
@@ -150,8 +150,8 @@ __global__ void __launch_bounds__(kCopyThreads)
 swap_blocks_kernel(const int32_t *__restrict__ blocks, int32_t n, uint4 *k_pool, uint4 *v_pool, uint4 *k_scale,
                    uint4 *v_scale, int32_t num_layers, int32_t num_blocks, int64_t block_words, int64_t scale_words,
                    uint4 *buf, int32_t to_buffer, uint32_t *status) {
-    ptx::launch_dependents();
     ptx::grid_dependency_wait();
+    ptx::launch_dependents();   // successors start once this grid's inputs are final
     const int64_t per = 2 * block_words + 2 * scale_words;      // words of one (block, layer) in the buffer
     const int64_t jobs = (int64_t)n * num_layers;
     const int64_t step = (int64_t)gridDim.x * blockDim.x;

@@ -224,8 +224,8 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     const int32_t H = p.H, B = p.B;
     const int32_t cap = p.max_blocks * B;
 
-    ptx::launch_dependents();
     ptx::grid_dependency_wait();
+    ptx::launch_dependents();   // successors start once this grid's inputs are final
     // The CTA's query rows q0 .. q0 + rows - 1 (row r of the tile: query row
     // q0 + r), the table row it reads, and its keys [kv_begin, kv_end); row r
     // sees keys t <= lim_r (prefill: its own position; prefix: every key).

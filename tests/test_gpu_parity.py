@@ -536,3 +536,35 @@ def test_long_context_full_size_sampled(free_gpu_memory):
     """16 sequences of 4k-16k tokens in 4 MiB pages, full size (32 layers)."""
     w = wl.make_workload(5, decode_steps=4)
     _full_size(w, [0, w.num_layers - 1], steps=2)
+
+
+def test_early_start_back_to_back_layers():
+    """Attention launches flagged to start before their predecessor ends (each follows the previous
+    layer's launch, which writes none of its inputs) give the oracle's result on every layer."""
+    w = wl.make_workload(2, num_layers=4, num_seqs=8, len_scale=0.3, decode_steps=1)
+    eng = DecodeEngine(w, fill="numpy", cascade=False)
+    eng.run_script(values="numpy")
+    torch.cuda.synchronize()
+    q, _, _ = eng.step_inputs(0, "numpy")
+    out = torch.full_like(q, float("nan"))
+    for rep in range(3):
+        for layer in range(w.num_layers):
+            eng.attention(layer, q, out, early=rep > 0 or layer > 0)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+    kp, vp = wl.pool_values(w, 0), wl.pool_values(w, 1)
+    for layer in range(w.num_layers):
+        ref = rf.decode_attention(q[layer].cpu().numpy(), kp[layer], vp[layer], eng.tables, eng.lens,
+                                  w.block_size, w.layout)
+        assert_close(out[layer].cpu().numpy(), ref, f"early layer {layer}")
+
+
+def test_attention_ex_rejects_unknown_flags():
+    w = wl.make_workload(1, decode_steps=1)
+    eng = DecodeEngine(w, fill="numpy", cascade=False)
+    eng.run_script(values="numpy")
+    q, _, _ = eng.step_inputs(0, "numpy")
+    with pytest.raises(pkv.binding.PkvError) as e:
+        eng.pool.decode_attention_ex(0, q[0], eng.tables_d, eng.lens_d, torch.empty_like(q[0]), eng.workspace,
+                                     flags=0x2)
+    assert e.value.code == "INVALID_ARG"
