@@ -11,26 +11,26 @@
 // §2.4). Dense enough for tensor cores: a 128-query tile reuses every K/V tile
 // 128 times.
 //
-// Design (one CTA per (sequence, head, 128-query tile); 8 softmax warps, one
-// MMA-issue warp and two TMA warps; fp16 HND cache, head_dim 128):
-// * One TMA warp brings the Q tile and the K tiles, the other the V tiles, 128 keys
-//   at a time (one box per block of the table, two 64-element halves each) into
-//   128-byte-swizzled shared memory: two K slots and two V slots, each refilled as
-//   soon as the MMA that reads it has finished. Separate warps, so a K slot does
-//   not wait behind a V slot.
-// * One elected thread issues S = Q K^T (M = N = K = 128, fp16 -> fp32) into one
-//   of two tensor-memory S tiles, and, once the softmax warps have written P_j,
-//   O += P_j V_j onto the O tile in tensor memory (P read from tensor memory as the
-//   A operand; V read MN-major straight from its [token][dim] rows). With two S
-//   tiles, the tensor cores compute the next tile's S while the softmax warps work
-//   on this one; S_{j+2} goes before P_j V when its K tile is already in.
+// Design (one CTA per (sequence, head, two 128-query tiles A and B); 8 softmax
+// warps, one MMA-issue warp and two TMA warps; fp16 HND cache, head_dim 128):
+// * One TMA warp brings the two Q tiles and the K tiles, the other the V tiles, 128
+//   keys at a time (one box per block of the table, two 64-element halves each)
+//   into 128-byte-swizzled shared memory: two K slots and two V slots, each
+//   refilled as soon as the MMAs that read it have finished. Both query tiles use
+//   every K/V tile the CTA loads, halving the K/V traffic per FLOP.
+// * One elected thread issues S_x = Q_x K^T (M = N = K = 128, fp16 -> fp32) into
+//   tile x's tensor-memory S, and, once the softmax warps have written P_x (fp16,
+//   over S_x), O_x += P_x V onto tile x's O in tensor memory (P read from tensor
+//   memory as the A operand; V read MN-major straight from its [token][dim] rows).
+//   The softmax warps take tile A's key tile j, then B's: while they work on one
+//   tile, the tensor cores run the other's P V and next S.
 // * Query row r is tensor-memory lane r, shared by two softmax warps (one 64-key
 //   half of each S row each; they exchange the row max once per tile). The causal
 //   mask is applied on the diagonal tile only. The softmax reference max only
 //   moves when a row's max exceeds it by more than 2^8, and only then is O
 //   rescaled in place (tcgen05.ld / st). Rows past the sequence's tokens in the
-//   last tile are zeroed in V before P V (a zero weight times non-finite garbage
-//   would not be zero).
+//   last key tile are zeroed in V before P V (a zero weight times non-finite
+//   garbage would not be zero).
 // * Every wait is bounded (1 s, then PKV_DEV_TIMEOUT); before exiting, the CTA
 //   waits (bounded) for its own copies and MMAs, and frees tensor memory on
 //   every path.
@@ -57,17 +57,19 @@ constexpr int kSub = kQT * 128;      // bytes of one [128 rows x 64 elements] sw
 constexpr int kTileBytes = 2 * kSub; // a 128 x 128 fp16 tile as two sub-tiles
 constexpr int kThreads = 352;        // warps 0-7 softmax, warp 8 MMA issue, warps 9-10 TMA loads (K, V)
 constexpr int kSoftmaxThreads = 256;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512)
+constexpr int kTiles = 2;            // query tiles per CTA (A, B: 128 positions apart)
+constexpr uint32_t kTmemCols = 512;  // S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512); P_X over S_X
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // shared memory: Q | K0 | K1 | V0 | V1 (each a 32 KB tile, 1024-aligned), then the
 // row-max exchange [2 tiles][2 halves][128 rows] fp32, then barriers and flags
-constexpr int kSmemTiles = 5 * kTileBytes;
-constexpr int kXchgBytes = 2 * 2 * kQT * 4;
+constexpr int kSmemTiles = 6 * kTileBytes;                 // Q_A | Q_B | K0 | K1 | V0 | V1
+constexpr int kXchgBytes = kTiles * 2 * 2 * kQT * 4;     // row-max exchange [tile][slot][half][row]
 constexpr int kSmemBytes = kSmemTiles + kXchgBytes + 256 /* barriers + flags */ + 1024 /* alignment slack */;
 
 // barrier indices (two-slot rings use index + slot)
-constexpr int kQFull = 0, kKFull = 1, kVFull = 3, kSFull = 5, kPReady = 7, kOFull = 9, kNumBars = 11;
+constexpr int kQFull = 0, kKFull = 1, kVFull = 3, kKFree = 5, kVFree = 7, kSFull = 9, kPReady = 11, kOFull = 13,
+              kNumBars = 15;
 
 struct PrefillParams {
     const int32_t *q_start;   // prefill: [S + 1] chunk rows of sequence s: q_start[s] .. q_start[s+1]-1
@@ -190,18 +192,21 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // One kernel, two uses:
-// * prefill (kPrefix = false): CTA (query tile, head, sequence) of a chunk,
-//   causal over the sequence's cache, normalised fp16 output;
-// * the cascade's prefix pass (kPrefix = true): CTA (key split, head, group),
-//   the group members' decode queries as the query tile (row r = sequence
-//   first_seq + r), every key of the split's share of the shared prefix seen by
-//   every row, unnormalised fp32 pieces (o, m, l) as output.
-// Pipeline of one CTA over its key tiles j = 0 .. nkt-1 (slot b = j & 1):
-//   loader : K_j -> K[b] once S_{j-2} is done; V_j -> V[b] once P_{j-2} V is done
-//   MMA    : S_0, S_1, then per j: [P_j ready] O += P_j V_j, S_{j+2} -> S[b]
-//   softmax: per j: S[b] -> P_j (fp16, tensor memory P[b]) once P_{j-2} V is done
-// so the tensor cores compute S_{j+1} (and finish P_{j-1} V) while the softmax
-// warps work on tile j. Every barrier is waited on at most one phase behind.
+// * prefill (kPrefix = false): CTA (pair of 128-query tiles A and B, head,
+//   sequence) of a chunk, causal over the sequence's cache, normalised fp16 output;
+// * the cascade's prefix pass (kPrefix = true): CTA (key split, head, group), the
+//   group members' decode queries as query tile A (row r = sequence first_seq + r;
+//   no tile B), every key of the split's share of the shared prefix seen by every
+//   row, unnormalised fp32 pieces (o, m, l) as output.
+// Tiles A and B share every K/V tile the CTA loads (B, 128 positions later, sees at
+// most one key tile more), which halves the K/V traffic per FLOP. Each has its own S
+// and O in tensor memory; the softmax warps take A's tile j, then B's, and while they
+// work on one, the tensor cores run the other's P V and next S. Pipeline over key
+// tiles j (slot b = j & 1):
+//   loaders: K_j -> K[b] once both S_{j-2} are done; V_j -> V[b] once both P_{j-2} V are
+//   MMA    : S_A,0, S_B,0; per j: [P_A,j] O_A += P_A,j V_j, S_A,j+1; [P_B,j] likewise for B
+//   softmax: per j: S_A -> P_A,j, then S_B -> P_B,j (fp16, over S in tensor memory)
+// Every barrier is waited on at most one phase behind.
 template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -209,10 +214,11 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~uintptr_t(1023));
-    const uint32_t sQ = ptx::smem_addr(base);
-    auto sK = [sQ](int b) { return sQ + (uint32_t)(1 + b) * kTileBytes; };
-    auto sV = [sQ](int b) { return sQ + (uint32_t)(3 + b) * kTileBytes; };
-    float *xchg = reinterpret_cast<float *>(base + kSmemTiles);          // [2][2][128]
+    const uint32_t s0 = ptx::smem_addr(base);
+    auto sQ = [s0](int x) { return s0 + (uint32_t)x * kTileBytes; };
+    auto sK = [s0](int b) { return s0 + (uint32_t)(2 + b) * kTileBytes; };
+    auto sV = [s0](int b) { return s0 + (uint32_t)(4 + b) * kTileBytes; };
+    float *xchg = reinterpret_cast<float *>(base + kSmemTiles);          // [2][2][2][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kSmemTiles + kXchgBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int32_t *timed_out = reinterpret_cast<volatile int32_t *>(bars + kNumBars + 1);
@@ -226,10 +232,12 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
 
     ptx::grid_dependency_wait();
     ptx::launch_dependents();   // successors start once this grid's inputs are final
-    // The CTA's query rows q0 .. q0 + rows - 1 (row r of the tile: query row
-    // q0 + r), the table row it reads, and its keys [kv_begin, kv_end); row r
-    // sees keys t <= lim_r (prefill: its own position; prefix: every key).
-    int32_t q0, rows, srow, kv_begin, kv_end, pos0;
+    // Query tile x covers query rows q0[x] .. q0[x] + rows[x] - 1 (row r: query row
+    // q0[x] + r); row r of tile x sees keys t <= its limit: its own position pos0[x] + r
+    // (prefill) or every key of the split (prefix). The CTA reads keys [kv_begin,
+    // kv_end) through table row srow; tile x needs the first nkt_x of its key tiles.
+    int32_t q0[kTiles], rows[kTiles] = {0, 0}, pos0[kTiles] = {0, 0}, kv_end_x[kTiles] = {0, 0};
+    int32_t srow, kv_begin, kv_end;
     int32_t split = 0;
     if constexpr (kPrefix) {
         const pkv_prefix_group g = p.groups[blockIdx.z];
@@ -240,18 +248,19 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
             if (tid == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
             return;
         }
-        q0 = g.first_seq;
-        rows = g.num_seqs;
         srow = g.first_seq;
         const int32_t per = ((P + kKT - 1) / kKT + p.splits - 1) / p.splits;   // key tiles per split
         kv_begin = min(P, split * per * kKT);
         kv_end = min(P, kv_begin + per * kKT);
-        pos0 = kv_end - 1;
+        q0[0] = q0[1] = g.first_seq;
+        rows[0] = g.num_seqs;
+        pos0[0] = kv_end - 1;
+        kv_end_x[0] = kv_end;
         if (kv_begin >= kv_end) {
             // no keys in this split: an empty piece for every member
-            for (int32_t i = tid; i < rows * (kD + 4); i += kThreads) {
+            for (int32_t i = tid; i < rows[0] * (kD + 4); i += kThreads) {
                 const int32_t r = i / (kD + 4), c = i - r * (kD + 4);
-                p.pieces[(((size_t)(q0 + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4) + c] =
+                p.pieces[(((size_t)(q0[0] + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4) + c] =
                     c == kD ? -INFINITY : 0.f;
             }
             return;
@@ -260,21 +269,29 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         const int32_t s = blockIdx.z;
         const int32_t qs = p.q_start[s];
         const int32_t C = p.q_start[s + 1] - qs;
-        const int32_t i0 = blockIdx.x * kQT;
-        if (i0 >= C) return;                           // uniform: this tile has no queries
+        const int32_t i0 = blockIdx.x * (kTiles * kQT);
+        if (i0 >= C) return;                           // uniform: this pair of tiles has no queries
         int32_t T = p.lens[s];
         if (T < C || T > cap) {
             if (tid == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
             T = T < C ? C : cap;
         }
-        q0 = qs + i0;
-        rows = min(kQT, C - i0);                       // valid query rows of this tile
         srow = s;
-        pos0 = T - C + i0;                             // position of row 0
         kv_begin = 0;
-        kv_end = pos0 + rows;                          // keys [0, kv_end) are seen by some row
+        for (int x = 0; x < kTiles; ++x) {
+            q0[x] = qs + i0 + x * kQT;
+            rows[x] = max(0, min(kQT, C - i0 - x * kQT));
+            pos0[x] = T - C + i0 + x * kQT;            // position of row 0
+            kv_end_x[x] = rows[x] ? pos0[x] + rows[x] : 0;
+        }
+        kv_end = max(kv_end_x[0], kv_end_x[1]);
     }
-    const int32_t nkt = (kv_end - kv_begin + kKT - 1) / kKT;
+    int32_t nkt_x[kTiles];
+    for (int x = 0; x < kTiles; ++x) nkt_x[x] = rows[x] ? (kv_end_x[x] - kv_begin + kKT - 1) / kKT : 0;
+    const int32_t nkt = max(nkt_x[0], nkt_x[1]);
+    const bool has_b = nkt_x[1] > 0;
+    // the tile whose P V reads the CTA's last key tile first zeroes its dead V rows
+    const int zero_tile = nkt_x[0] == nkt ? 0 : 1;
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i)
@@ -292,24 +309,25 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    auto tS = [tmem](int b) { return tmem + (uint32_t)b * kKT; };
-    const uint32_t tO = tmem + 2 * kKT;
-    auto tP = [tmem](int b) { return tmem + 3 * kKT + (uint32_t)b * (kKT / 2); };
+    auto tS = [tmem](int x) { return tmem + (uint32_t)x * kKT; };            // P_x is written over it
+    auto tO = [tmem](int x) { return tmem + (uint32_t)(2 + x) * kKT; };
 
     if (warp == 9 || warp == 10) {
         // ================= loaders: warp 9 brings Q and the K tiles, warp 10 the V tiles
         // (one box per block of the table, lane i box i). Separate warps, so a K tile
-        // is refilled as soon as its S MMA is done, whatever the V side waits for.
+        // is refilled as soon as its S MMAs are done, whatever the V side waits for.
         const bool is_k = warp == 9;
         const int32_t rowsb = B < kKT ? B : kKT;       // rows per box; B is a power of two, 8..256
         if (is_k && lane == 0) {
-            ptx::mbar_arrive_expect_tx(BAR(kQFull), kTileBytes);
-            for (int half = 0; half < 2; ++half)
-                ptx::tma_load_3d(sQ + half * kSub, &qmap, half * kHalf, h, q0, BAR(kQFull));
+            ptx::mbar_arrive_expect_tx(BAR(kQFull), (has_b ? 2 : 1) * kTileBytes);
+            for (int x = 0; x < kTiles; ++x)
+                if (nkt_x[x] > 0)
+                    for (int half = 0; half < 2; ++half)
+                        ptx::tma_load_3d(sQ(x) + half * kSub, &qmap, half * kHalf, h, q0[x], BAR(kQFull));
         }
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         const int full0 = is_k ? kKFull : kVFull;
-        const int free0 = is_k ? kSFull : kOFull;     // slot b is free once S_{j-2} (K) / P_{j-2} V (V) is done
+        const int free0 = is_k ? kKFree : kVFree;     // slot b is free once the MMAs of tile j-2 reading it are done
         for (int32_t j = 0; j < nkt; ++j) {
             const int b = j & 1;
             const int32_t t0 = kv_begin + j * kKT;
@@ -342,173 +360,204 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         // ================= MMA issue (one thread)
         if (lane == 0) {
             const uint32_t id_qk = umma_idesc(0), id_pv = umma_idesc(1);
-            auto issue_s = [&](int32_t j) {
+            auto issue_s = [&](int x, int32_t j) {   // S_x = Q_x K_j^T over the head dim, 8 steps of 16
                 const int b = j & 1;
-                bounded_wait(BAR(kKFull + b), (j >> 1) & 1, timed_out, p.status);
-                tc_fence_after();
-                // S = Q K^T over the head dim: 8 steps of 16 (4 per 64-element half)
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * kSub + (ks & 3) * 32;
-                    umma(tS(b), umma_desc(sQ + koff, 16, 1024), umma_desc(sK(b) + koff, 16, 1024), id_qk, ks > 0);
+                    umma(tS(x), umma_desc(sQ(x) + koff, 16, 1024), umma_desc(sK(b) + koff, 16, 1024), id_qk,
+                         ks > 0);
                 }
-                umma_commit(BAR(kSFull + b));
+                umma_commit(BAR(kSFull + x));
+            };
+            auto issue_pv = [&](int x, int32_t j) {  // O_x += P_x V_j: A = P (tensor memory), B = V (MN-major)
+                const int b = j & 1;
+                for (int ks = 0; ks < kKT / 16; ++ks)
+                    umma_ts(tO(x), tS(x) + ks * 8, umma_desc(sV(b) + ks * 2048, kSub, 1024), id_pv,
+                            (j > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(BAR(kOFull + x));
             };
             bounded_wait(BAR(kQFull), 0, timed_out, p.status);
-            issue_s(0);
-            if (nkt > 1) issue_s(1);
+            bounded_wait(BAR(kKFull), 0, timed_out, p.status);
+            tc_fence_after();
+            for (int x = 0; x < kTiles; ++x)
+                if (nkt_x[x] > 0) issue_s(x, 0);
+            umma_commit(BAR(kKFree));                    // both S of tile 0 issued
             for (int32_t j = 0; j < nkt; ++j) {
                 const int b = j & 1;
-                bounded_wait(BAR(kPReady + b), (j >> 1) & 1, timed_out, p.status);   // P_j written, S[b] read
-                tc_fence_after();
-                // S_{j+2} first when its K tile is already in: the softmax needs it one tile
-                // from now, while P_j V is only needed before P_{j+2} is written
-                bool s_next = j + 2 < nkt;
-                if (s_next && ptx::mbar_test_wait(BAR(kKFull + b), ((j + 2) >> 1) & 1)) {
-                    issue_s(j + 2);
-                    s_next = false;
-                }
+                const int32_t jn = j + 1;
+                bool k_next_in = false;
                 bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
-                tc_fence_after();
-                // O += P_j V_j over the tile's keys: A = P from tensor memory (8 columns per 16 keys),
-                // B = V rows (MN-major, halves 16 KB apart)
-                for (int ks = 0; ks < kKT / 16; ++ks)
-                    umma_ts(tO, tP(b) + ks * 8, umma_desc(sV(b) + ks * 2048, kSub, 1024), id_pv,
-                            (j > 0 || ks > 0) ? 1u : 0u);
-                umma_commit(BAR(kOFull + b));
-                if (s_next) issue_s(j + 2);
+                for (int x = 0; x < kTiles; ++x) {
+                    if (j >= nkt_x[x]) continue;
+                    bounded_wait(BAR(kPReady + x), j & 1, timed_out, p.status);   // P_x,j written, S_x read
+                    tc_fence_after();
+                    issue_pv(x, j);
+                    if (jn < nkt_x[x]) {   // S_x,j+1 overwrites P_x,j: issued after the P V that reads it
+                        if (!k_next_in) {
+                            bounded_wait(BAR(kKFull + (jn & 1)), (jn >> 1) & 1, timed_out, p.status);
+                            tc_fence_after();
+                            k_next_in = true;
+                        }
+                        issue_s(x, jn);
+                    }
+                }
+                umma_commit(BAR(kVFree + b));            // both P V of tile j issued
+                if (jn < nkt) umma_commit(BAR(kKFree + (jn & 1)));   // both S of tile j+1 issued
             }
             // the last commit covers every MMA issued before it
-            drain_wait(BAR(kOFull + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1);
+            drain_wait(BAR(kVFree + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1);
         }
         __syncwarp();
     } else {
-        // ================= softmax warps: query row r (tensor-memory lane r) is shared by
-        // warps q and q + 4 (q = r / 32), each taking one 64-key half of every S tile and
-        // one 64-column half of O; the two exchange their row max once per tile.
-        // O lives in tensor memory and P V accumulates onto it. The softmax runs
-        // against a reference max m_ref (log2 units) that only moves when the row's
-        // max exceeds it by more than 2^8 (then O and l are rescaled), so P stays
-        // <= 256 and most tiles need no O traffic at all.
+        // ================= softmax warps: query row r of each tile (tensor-memory lane r) is
+        // shared by warps q and q + 4 (q = r / 32), each taking one 64-key half of every S
+        // tile and one 64-column half of O; the two exchange their row max once per tile.
+        // O lives in tensor memory and P V accumulates onto it. The softmax runs against a
+        // reference max m_ref (log2 units) that only moves when the row's max exceeds it
+        // by more than 2^8 (then O and l are rescaled), so P stays <= 256 and most tiles
+        // need no O traffic at all.
         const int hf = warp >> 2, quad = warp & 3;
         const int32_t r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const bool valid = r < rows;
-        const int32_t pr = kPrefix ? pos0 : pos0 + r;   // the last key this row sees
         const float sl2 = p.scale_log2;
         constexpr float kSlack = 8.f;
         constexpr int kCols = kKT / 2;              // keys of S (and columns of O) per thread
-        float m_ref = -INFINITY, l = 0.f;
+        // per-tile state in scalars (selected by x, not indexed: nothing goes to local memory)
+        float m_ref0 = -INFINITY, m_ref1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        const int32_t nk0 = nkt_x[0], nk1 = nkt_x[1];
+        const int32_t rows0 = rows[0], rows1 = rows[1], p00 = pos0[0], p01 = pos0[1];
         for (int32_t j = 0; j < nkt; ++j) {
             const int b = j & 1;
-            const int32_t t0 = kv_begin + j * kKT + hf * kCols;   // first key of this thread's half
-            bounded_wait(BAR(kSFull + b), (j >> 1) & 1, timed_out, p.status);
-            tc_fence_after();
-            uint32_t raw[kCols];
-            tmem_ld64(tS(b) + lane_base + hf * kCols, raw);
-            float x[kCols];
-#pragma unroll
-            for (int i = 0; i < kCols; ++i) x[i] = __uint_as_float(raw[i]);
-            if (!(valid && t0 + kCols - 1 <= pr)) {   // the diagonal tile (or a row past the chunk): mask
-#pragma unroll
-                for (int i = 0; i < kCols; ++i) x[i] = (valid && t0 + i <= pr) ? x[i] : -INFINITY;
-            }
-            // row max of this half: a tree of three-input maxima (64 -> 22 -> 8 -> 3 -> 1)
-            float m22[22];
-#pragma unroll
-            for (int k = 0; k < 21; ++k) m22[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
-            m22[21] = x[63];
-            float m8[8];
-#pragma unroll
-            for (int k = 0; k < 7; ++k) m8[k] = fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
-            m8[7] = m22[21];
-            float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            // row max across the two halves (a slot per tile parity, so a fast partner
-            // never overwrites a value not yet read)
-            float *xs = xchg + b * 2 * kQT;
-            xs[hf * kQT + r] = mx;
-            ptx::named_barrier(1 + quad, 64);
-            mx = fmaxf(mx, xs[(hf ^ 1) * kQT + r]) * sl2;
-            const bool move = mx > m_ref + kSlack;  // false when mx = -inf; the same in both halves
-            const float new_ref = move ? mx : m_ref;
-            const float alpha = move ? ptx::ex2(m_ref - new_ref) : 1.f;   // m_ref = -inf: 0
-            if (j > 0 && __any_sync(0xffffffffu, move)) {
-                // rescale this half of O once P_{j-1} V is in it
-                bounded_wait(BAR(kOFull + (b ^ 1)), ((j - 1) >> 1) & 1, timed_out, p.status);
+#pragma unroll 1
+            for (int x = 0; x < kTiles; ++x) {
+                if (j >= (x ? nk1 : nk0)) continue;
+                const bool valid = r < (x ? rows1 : rows0);
+                const int32_t pr = kPrefix ? p00 : (x ? p01 : p00) + r;   // the last key this row sees
+                const int32_t t0 = kv_begin + j * kKT + hf * kCols;   // first key of this thread's half
+                bounded_wait(BAR(kSFull + x), j & 1, timed_out, p.status);
                 tc_fence_after();
+                uint32_t raw[kCols];
+                tmem_ld64(tS(x) + lane_base + hf * kCols, raw);
+                float xv[kCols];
 #pragma unroll
-                for (int c0 = 0; c0 < kCols; c0 += 32) {
-                    uint32_t v[32];
-                    const uint32_t ta = tO + lane_base + hf * kCols + c0;
-                    tmem_ld32(ta, v);
+                for (int i = 0; i < kCols; ++i) xv[i] = __uint_as_float(raw[i]);
+                if (!(valid && t0 + kCols - 1 <= pr)) {   // the diagonal tile (or a row past the chunk): mask
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st32(ta, v);
+                    for (int i = 0; i < kCols; ++i) xv[i] = (valid && t0 + i <= pr) ? xv[i] : -INFINITY;
                 }
-            }
-            m_ref = new_ref;
-            if (j >= 2) bounded_wait(BAR(kOFull + b), ((j - 2) >> 1) & 1, timed_out, p.status);  // P[b] free
-            // P = 2^(x * scale log2(e) - m_ref), pairs at a time; a row with no live key
-            // yet (m_ref = -inf: every x is -inf) gets 2^-inf = 0
-            const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
-            float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            uint32_t pk[kCols / 2];
+                // row max of this half: a tree of three-input maxima (64 -> 22 -> 8 -> 3 -> 1)
+                float m22[22];
 #pragma unroll
-            for (int e = 0; e < kCols / 2; ++e) {
-                const float2 a = ptx::ffma2(make_float2(x[2 * e], x[2 * e + 1]), make_float2(sl2, sl2),
-                                            make_float2(neg, neg));
-                const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
-                pk[e] = pack_half2(pp.x, pp.y);
-                rs2[e & 1] = ptx::fadd2(rs2[e & 1], pp);
-            }
-            tmem_st32(tP(b) + lane_base + hf * (kCols / 2), pk);
-            l = l * alpha + ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y));
-            // the last tile: zero the V rows no query may see (they may hold non-finite garbage)
-            if (j == nkt - 1) {
-                bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
-                const int32_t first_dead = kv_end - (kv_begin + j * kKT);   // rows [first_dead, 128) of the tile
-                unsigned char *sVp = base + (3 + b) * kTileBytes;
-                const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
-                for (int32_t w = tid; w < nwords * 2; w += kSoftmaxThreads) {
-                    const int half = w / nwords, rem = w - half * nwords;
-                    const int row = first_dead + rem / 8, cc = rem & 7;
-                    *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < 21; ++k) m22[k] = fmax3(xv[3 * k], xv[3 * k + 1], xv[3 * k + 2]);
+                m22[21] = xv[63];
+                float m8[8];
+#pragma unroll
+                for (int k = 0; k < 7; ++k) m8[k] = fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
+                m8[7] = m22[21];
+                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                // row max across the two halves (a slot per tile and parity, so a fast
+                // partner never overwrites a value not yet read)
+                float *xs = xchg + (x * 2 + b) * 2 * kQT;
+                xs[hf * kQT + r] = mx;
+                ptx::named_barrier(1 + quad, 64);
+                mx = fmaxf(mx, xs[(hf ^ 1) * kQT + r]) * sl2;
+                const float mr = x ? m_ref1 : m_ref0;
+                const bool move = mx > mr + kSlack;  // false when mx = -inf; the same in both halves
+                const float new_ref = move ? mx : mr;
+                const float alpha = move ? ptx::ex2(mr - new_ref) : 1.f;   // m_ref = -inf: 0
+                if (j > 0 && __any_sync(0xffffffffu, move)) {
+                    // rescale this half of O_x once P_x,j-1 V is in it
+                    bounded_wait(BAR(kOFull + x), (j - 1) & 1, timed_out, p.status);
+                    tc_fence_after();
+#pragma unroll
+                    for (int c0 = 0; c0 < kCols; c0 += 32) {
+                        uint32_t v[32];
+                        const uint32_t ta = tO(x) + lane_base + hf * kCols + c0;
+                        tmem_ld32(ta, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tmem_st32(ta, v);
+                    }
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // zeroed V -> MMA
+                if (x) m_ref1 = new_ref;
+                else m_ref0 = new_ref;
+                // P = 2^(x * scale log2(e) - m_ref), pairs at a time, written over S_x (the
+                // partner half has read its S columns before the exchange above; S_x,j has
+                // landed, so P_x,j-1 V is done reading them). A row with no live key yet
+                // (m_ref = -inf: every x is -inf) gets 2^-inf = 0.
+                const float neg = new_ref == -INFINITY ? 0.f : -new_ref;
+                float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                uint32_t pk[kCols / 2];
+#pragma unroll
+                for (int e = 0; e < kCols / 2; ++e) {
+                    const float2 a = ptx::ffma2(make_float2(xv[2 * e], xv[2 * e + 1]), make_float2(sl2, sl2),
+                                                make_float2(neg, neg));
+                    const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+                    pk[e] = pack_half2(pp.x, pp.y);
+                    rs2[e & 1] = ptx::fadd2(rs2[e & 1], pp);
+                }
+                tmem_st32(tS(x) + lane_base + hf * (kCols / 2), pk);
+                const float rsum = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+                if (x) l1 = l1 * alpha + rsum;
+                else l0 = l0 * alpha + rsum;
+                // the CTA's last key tile: zero the V rows no query of the CTA may see (they
+                // may hold non-finite garbage), before the first P V that reads the tile
+                if (j == nkt - 1 && x == zero_tile) {
+                    bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
+                    const int32_t first_dead = kv_end - (kv_begin + j * kKT);   // rows [first_dead, 128)
+                    unsigned char *sVp = base + (4 + b) * kTileBytes;
+                    const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
+                    for (int32_t w = tid; w < nwords * 2; w += kSoftmaxThreads) {
+                        const int half = w / nwords, rem = w - half * nwords;
+                        const int row = first_dead + rem / 8, cc = rem & 7;
+                        *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + cc * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // zeroed V -> MMA
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(BAR(kPReady + x));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(BAR(kPReady + b));
         }
-        bounded_wait(BAR(kOFull + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1, timed_out, p.status);
-        tc_fence_after();
-        // l of the whole row: both halves' sums (the slot of parity nkt & 1 is free by now)
-        float *xs = xchg + (nkt & 1) * 2 * kQT;
-        xs[hf * kQT + r] = l;
-        ptx::named_barrier(1 + quad, 64);
-        const float lt = xs[r] + xs[kQT + r];
-        uint32_t raw[kCols];
-        tmem_ld64(tO + lane_base + hf * kCols, raw);
-        if constexpr (kPrefix) {
-            if (valid) {
-                float *piece = p.pieces + (((size_t)(q0 + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4);
-                float4 *o4 = reinterpret_cast<float4 *>(piece + hf * kCols);
+#pragma unroll 1
+        for (int x = 0; x < kTiles; ++x) {
+            const int32_t nk = x ? nk1 : nk0;
+            if (nk == 0) continue;
+            const bool valid = r < (x ? rows1 : rows0);
+            const int32_t q0x = x ? q0[1] : q0[0];
+            bounded_wait(BAR(kOFull + x), (nk - 1) & 1, timed_out, p.status);
+            tc_fence_after();
+            // l of the whole row: both halves' sums (the slot of parity nk & 1 is free by now)
+            float *xs = xchg + (x * 2 + (nk & 1)) * 2 * kQT;
+            xs[hf * kQT + r] = x ? l1 : l0;
+            ptx::named_barrier(1 + quad, 64);
+            const float lt = xs[r] + xs[kQT + r];
+            uint32_t raw[kCols];
+            tmem_ld64(tO(x) + lane_base + hf * kCols, raw);
+            if constexpr (kPrefix) {
+                if (valid) {
+                    float *piece =
+                        p.pieces + (((size_t)(q0x + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4);
+                    float4 *o4 = reinterpret_cast<float4 *>(piece + hf * kCols);
 #pragma unroll
-                for (int d = 0; d < kCols; d += 4)
-                    o4[d / 4] = make_float4(__uint_as_float(raw[d]), __uint_as_float(raw[d + 1]),
-                                            __uint_as_float(raw[d + 2]), __uint_as_float(raw[d + 3]));
-                if (hf == 0) *reinterpret_cast<float4 *>(piece + kD) = make_float4(m_ref, lt, 0.f, 0.f);
-            }
-        } else if (valid) {
-            const float inv = 1.f / lt;
-            __half *dst = p.out + ((size_t)(q0 + r) * H + h) * kD + hf * kCols;
+                    for (int d = 0; d < kCols; d += 4)
+                        o4[d / 4] = make_float4(__uint_as_float(raw[d]), __uint_as_float(raw[d + 1]),
+                                                __uint_as_float(raw[d + 2]), __uint_as_float(raw[d + 3]));
+                    if (hf == 0) *reinterpret_cast<float4 *>(piece + kD) = make_float4(x ? m_ref1 : m_ref0, lt, 0.f, 0.f);
+                }
+            } else if (valid) {
+                const float inv = 1.f / lt;
+                __half *dst = p.out + ((size_t)(q0x + r) * H + h) * kD + hf * kCols;
 #pragma unroll
-            for (int d = 0; d < kCols; d += 8) {
-                __half2 hv[4];
+                for (int d = 0; d < kCols; d += 8) {
+                    __half2 hv[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    hv[e] = __floats2half2_rn(__uint_as_float(raw[d + 2 * e]) * inv,
-                                              __uint_as_float(raw[d + 2 * e + 1]) * inv);
-                *reinterpret_cast<uint4 *>(dst + d) = *reinterpret_cast<const uint4 *>(hv);
+                    for (int e = 0; e < 4; ++e)
+                        hv[e] = __floats2half2_rn(__uint_as_float(raw[d + 2 * e]) * inv,
+                                                  __uint_as_float(raw[d + 2 * e + 1]) * inv);
+                    *reinterpret_cast<uint4 *>(dst + d) = *reinterpret_cast<const uint4 *>(hv);
+                }
             }
         }
     }
@@ -646,7 +695,7 @@ pkv_status pkv_prefill_attention(const pkv_pool *pool, int32_t layer, const void
     prm.q_start = q_start;
     prm.lens = context_lens;
     prm.out = static_cast<__half *>(out);
-    const dim3 grid((max_chunk + kQT - 1) / kQT, pool->desc.num_heads, num_seqs);
+    const dim3 grid((max_chunk + kTiles * kQT - 1) / (kTiles * kQT), pool->desc.num_heads, num_seqs);
     return launch_tc<false>(grid, qmap, kmap, vmap, prm, stream);
 }
 
