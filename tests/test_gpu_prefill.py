@@ -68,6 +68,20 @@ def test_prefill_mixed_chunks(B):
     _check(got, ref, f"B={B}")
 
 
+@pytest.mark.parametrize("B", [16, 128])
+def test_prefill_tile_pairs(B):
+    """Each CTA takes two query tiles: the second may be absent or ragged, and may need the
+    same number of key tiles as the first (then the first zeroes the last tile's dead V rows)
+    or one more (then the second does); NaN canaries sit past every context."""
+    H = 2
+    lens, chunks = [190, 140, 400, 256, 257], [180, 140, 390, 256, 129]
+    q, qs, kp, vp, tab, ln, N = _case(lens, chunks, H, B, seed=11 + B)
+    got, st = _run(q, qs, kp, vp, tab, ln, N, H, B, max(chunks))
+    assert st == 0
+    ref = rf.prefill_attention(q, kp, vp, tab, ln, qs, B, layout="HND")
+    _check(got, ref, f"tile pairs B={B}")
+
+
 def test_prefill_long_context_several_tiles():
     H, B = 4, 16
     lens, chunks = [2048, 1500, 700], [512, 300, 700]
