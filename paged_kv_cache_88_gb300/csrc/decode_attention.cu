@@ -55,7 +55,7 @@ namespace {
 using namespace pkv;
 
 #ifndef PKV_ATTN_TILE
-#define PKV_ATTN_TILE 32
+#define PKV_ATTN_TILE 64
 #endif
 #ifndef PKV_ATTN_WARPS
 #define PKV_ATTN_WARPS 4
@@ -64,7 +64,7 @@ using namespace pkv;
 #define PKV_ATTN_STAGES 2
 #endif
 #ifndef PKV_ATTN_MIN_CTAS
-#define PKV_ATTN_MIN_CTAS 4
+#define PKV_ATTN_MIN_CTAS 3
 #endif
 #ifndef PKV_ATTN_ACQREL
 #define PKV_ATTN_ACQREL 1
@@ -424,18 +424,23 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             const uint32_t dst = stage0 + stage * SB;
             const uint32_t bar = full0 + 8 * stage;
             if constexpr (Q8) {
-                // the tile's scales ([N][H][B]: token i of the tile is row y_i): lane i
-                // copies token i's K and V scale with 4-byte asynchronous copies (one
-                // coalesced request each, not two small bulk copies per block), and the
+                // the tile's scales ([N][H][B]: token i of the tile is row y_i): lane l
+                // copies the K and V scales of tokens l, l + 32, ... with 4-byte
+                // asynchronous copies (coalesced requests, not two small bulk copies per
+                // block), and the
                 // stage's phase waits for them; issued before lane 0's arrival so the
                 // phase cannot complete without them
-                const int32_t t = t0 + min(lane, ntok - 1);
-                int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
-                if (blk < 0 || blk >= p.N) blk = 0;          // flagged with the boxes below
-                const size_t y = ((size_t)blk * H + cc.h) * B + t % B;
-                if (lane < ntok) {
-                    ptx::cp_async_4(dst + St::kScales + lane * 4, p.k_scale + y);
-                    ptx::cp_async_4(dst + St::kScales + kTile * 4 + lane * 4, p.v_scale + y);
+#pragma unroll
+                for (int i0 = 0; i0 < kTile; i0 += 32) {
+                    const int32_t i = i0 + lane;
+                    const int32_t t = t0 + min(i, ntok - 1);
+                    int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
+                    if (blk < 0 || blk >= p.N) blk = 0;      // flagged with the boxes below
+                    const size_t y = ((size_t)blk * H + cc.h) * B + t % B;
+                    if (i < ntok) {
+                        ptx::cp_async_4(dst + St::kScales + i * 4, p.k_scale + y);
+                        ptx::cp_async_4(dst + St::kScales + kTile * 4 + i * 4, p.v_scale + y);
+                    }
                 }
                 ptx::cp_async_mbar_arrive(bar);
                 __syncwarp();
