@@ -1,0 +1,131 @@
+"""Full-size GPU parity of the E4M3 decode step and of the tensor-core prefill, each in the
+launch configuration bench.py times, checked against the oracle on sampled outputs.
+
+* E4M3: the engine's default step (separate quantising append, then attention) on the
+  full 7B and long-context workloads; the appended codes and scales of the checked
+  layers are compared bit for bit with the oracle quantiser, and the attention of the
+  sampled sequences (every head) with the float64 definition on code x scale.
+* Prefill: the benchmark's causal prefill (whole prompts of the 7B workload; chunks of
+  4096 over the long contexts), every row of the sampled (sequence, head) pairs against
+  the float64 causal definition, computed on just that sequence's blocks.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from paged_kv_cache_88_gb300.engine import DecodeEngine  # noqa: E402
+from oracle import fp8  # noqa: E402
+from oracle import ref_attn as rf  # noqa: E402
+import workloads as wl  # noqa: E402
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def assert_close(gpu: np.ndarray, ref: np.ndarray, what: str):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    err = np.abs(gpu - ref)
+    bad = ~(err <= ATOL + RTOL * np.abs(ref))
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside tolerance, max err {np.nanmax(err):.3e}"
+
+
+@pytest.fixture
+def free_gpu_memory():
+    yield
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _sample(lens: np.ndarray, n: int) -> list:
+    """The longest, the shortest and evenly spread others (sequence indices)."""
+    order = np.argsort(lens, kind="stable")
+    pick = {int(order[-1]), int(order[0])}
+    for i in np.linspace(0, len(lens) - 1, num=max(n - 2, 0) + 2)[1:-1]:
+        pick.add(int(order[int(round(i))]))
+    return sorted(pick)
+
+
+def _e4m3_full(cfg: int, check_layers, n_seqs=None, **kw):
+    w = wl.make_workload(cfg, kv_dtype="e4m3", **kw)
+    eng = DecodeEngine(w, fill="torch")
+    assert not eng.fused, "the benchmark's E4M3 step appends with the separate launch"
+    eng.run_script(values="torch")
+    qd, kd, vd = eng.step_inputs(0, "torch")
+    before = {l: [t[l].cpu().numpy() for t in (eng.k_pool, eng.v_pool, eng.k_scale, eng.v_scale)]
+              for l in check_layers}
+    out = torch.empty_like(qd)
+    eng.step(qd, kd, vd, out)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+    assert len(eng.last_pairs) == 0
+    tab, lens = eng.tables.copy(), eng.lens.copy()
+    seqs = list(range(w.num_seqs)) if n_seqs is None else _sample(lens, n_seqs)
+    for l in check_layers:
+        kc, vc, ks, vs = before[l]
+        fp8.append_kv(kc, vc, ks, vs, kd[l].cpu().numpy(), vd[l].cpu().numpy(), eng.last_slots, w.block_size)
+        assert np.array_equal(kc, eng.k_pool[l].cpu().numpy()), f"K codes layer {l}"
+        assert np.array_equal(vc, eng.v_pool[l].cpu().numpy()), f"V codes layer {l}"
+        assert np.array_equal(ks.view(np.uint32), eng.k_scale[l].cpu().numpy().view(np.uint32)), f"K scales {l}"
+        assert np.array_equal(vs.view(np.uint32), eng.v_scale[l].cpu().numpy().view(np.uint32)), f"V scales {l}"
+        q = qd[l].cpu().numpy()[seqs]
+        ref = fp8.decode_attention(q, kc, vc, ks, vs, tab[seqs], lens[seqs], w.block_size)
+        assert_close(out[l].cpu().numpy()[seqs], ref, f"E4M3 cfg {cfg} layer {l}")
+
+
+def test_e4m3_7b_full_size_sampled(free_gpu_memory):
+    """7B shape, batch 32, 32 layers: layers 0 and 31, every sequence and head."""
+    _e4m3_full(2, [0, 31])
+
+
+def test_e4m3_long_context_full_size_sampled(free_gpu_memory):
+    """16 sequences of 4k-16k tokens, block 256: layer 0, four sequences, every head."""
+    _e4m3_full(5, [0], n_seqs=4)
+
+
+def _prefill_full(cfg: int, chunk: int, n_seqs: int, heads, block_size=None):
+    w = wl.make_workload(cfg, decode_steps=8, block_size=block_size)
+    eng = DecodeEngine(w, fill="torch")
+    eng.run_script(values="torch")
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    lens = eng.lens.copy()
+    chunks = np.minimum(lens, chunk).astype(np.int64)
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234 + cfg)
+    q = torch.randn((int(q_start[-1]), H, D), generator=g, device="cuda").to(torch.float16)
+    out = torch.full_like(q, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    eng.pool.prefill_attention(0, q, torch.from_numpy(q_start).cuda(), int(chunks.max()), eng.tables_d, eng.lens_d,
+                               out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for s in _sample(lens, n_seqs):
+        T, C = int(lens[s]), int(chunks[s])
+        nb = -(-T // B)
+        blocks = torch.from_numpy(eng.tables[s, :nb].astype(np.int64)).cuda()
+        tab = np.arange(nb, dtype=np.int32)[None]
+        r0, r1 = int(q_start[s]), int(q_start[s + 1])
+        for h in heads:
+            kp = eng.k_pool[0][blocks][:, h:h + 1].cpu().numpy()        # [nb, 1, B, D]: this head's blocks
+            vp = eng.v_pool[0][blocks][:, h:h + 1].cpu().numpy()
+            qs = q[r0:r1, h:h + 1].cpu().numpy()
+            ref = rf.prefill_attention(qs, kp, vp, tab, [T], [0, C], B, layout="HND")
+            assert_close(out[r0:r1, h:h + 1].cpu().numpy(), ref, f"prefill cfg {cfg} seq {s} head {h}")
+
+
+def test_prefill_whole_prompts_7b_full_size_sampled(free_gpu_memory):
+    """The benchmark's whole-prompt prefill (chunks of up to 2048) on the 7B workload:
+    four sequences, heads 0 and 31, every row."""
+    _prefill_full(2, 2048, 4, [0, 31])
+
+
+def test_prefill_long_chunks_full_size_sampled(free_gpu_memory):
+    """The benchmark's 4096-token chunks over the long contexts (block 256): the longest and
+    the shortest sequence, heads 0 and 17, every row."""
+    _prefill_full(5, 4096, 2, [0, 17])
