@@ -22,15 +22,15 @@
 //   tile x's tensor-memory S, and, once the softmax warps have written P_x (fp16,
 //   over S_x), O_x += P_x V onto tile x's O in tensor memory (P read from tensor
 //   memory as the A operand; V read MN-major straight from its [token][dim] rows).
-//   The softmax warps take tile A's key tile j, then B's: while they work on one
-//   tile, the tensor cores run the other's P V and next S.
-// * Query row r is tensor-memory lane r, shared by two softmax warps (one 64-key
-//   half of each S row each; they exchange the row max once per tile). The causal
-//   mask is applied on the diagonal tile only. The softmax reference max only
-//   moves when a row's max exceeds it by more than 2^8, and only then is O
-//   rescaled in place (tcgen05.ld / st). Rows past the sequence's tokens in the
-//   last key tile are zeroed in V before P V (a zero weight times non-finite
-//   garbage would not be zero).
+//   Each tile has its own four softmax warps, so the two tiles' softmax run side by
+//   side while the tensor cores alternate between the tiles' P V and next S.
+// * Query row r of a tile is tensor-memory lane r and one softmax thread: both
+//   64-column halves of its S row come in with one wait, and its max and sum never
+//   leave the thread. The causal mask is applied on the diagonal tile only. The
+//   softmax reference max only moves when a row's max exceeds it by more than 2^8,
+//   and only then is O rescaled in place (tcgen05.ld / st). Rows past the
+//   sequence's tokens in the last key tile are zeroed in V before P V (a zero
+//   weight times non-finite garbage would not be zero).
 // * Every wait is bounded (1 s, then PKV_DEV_TIMEOUT); before exiting, the CTA
 //   waits (bounded) for its own copies and MMAs, and frees tensor memory on
 //   every path.
@@ -56,15 +56,15 @@ constexpr int kHalf = 64;            // 64 fp16 = one 128-byte swizzle row
 constexpr int kSub = kQT * 128;      // bytes of one [128 rows x 64 elements] swizzled sub-tile (16 KB)
 constexpr int kTileBytes = 2 * kSub; // a 128 x 128 fp16 tile as two sub-tiles
 constexpr int kThreads = 352;        // warps 0-7 softmax, warp 8 MMA issue, warps 9-10 TMA loads (K, V)
-constexpr int kSoftmaxThreads = 256;
+constexpr int kGroupThreads = 128;   // softmax threads of one query tile (one per row)
 constexpr int kTiles = 2;            // query tiles per CTA (A, B: 128 positions apart)
 constexpr uint32_t kTmemCols = 512;  // S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512); P_X over S_X
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// shared memory: Q | K0 | K1 | V0 | V1 (each a 32 KB tile, 1024-aligned), then the
-// row-max exchange [2 tiles][2 halves][128 rows] fp32, then barriers and flags
+// shared memory: Q_A | Q_B | K0 | K1 | V0 | V1 (each a 32 KB tile, 1024-aligned), the
+// prefix pass's row-max exchange, then barriers and flags
 constexpr int kSmemTiles = 6 * kTileBytes;                 // Q_A | Q_B | K0 | K1 | V0 | V1
-constexpr int kXchgBytes = kTiles * 2 * 2 * kQT * 4;     // row-max exchange [tile][slot][half][row]
+constexpr int kXchgBytes = 2 * 2 * kQT * 4;    // prefix pass: row-max exchange [slot][half][row]
 constexpr int kSmemBytes = kSmemTiles + kXchgBytes + 256 /* barriers + flags */ + 1024 /* alignment slack */;
 
 // barrier indices (two-slot rings use index + slot)
@@ -129,6 +129,16 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
         : "r"(taddr) : "memory");
+}
+// Two 64-column loads in flight together, then one wait (both completed before any
+// register is used).
+__device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t tb, uint32_t (&a)[64], uint32_t (&b)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%129];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(a[32]), "=r"(a[33]), "=r"(a[34]), "=r"(a[35]), "=r"(a[36]), "=r"(a[37]), "=r"(a[38]), "=r"(a[39]), "=r"(a[40]), "=r"(a[41]), "=r"(a[42]), "=r"(a[43]), "=r"(a[44]), "=r"(a[45]), "=r"(a[46]), "=r"(a[47]), "=r"(a[48]), "=r"(a[49]), "=r"(a[50]), "=r"(a[51]), "=r"(a[52]), "=r"(a[53]), "=r"(a[54]), "=r"(a[55]), "=r"(a[56]), "=r"(a[57]), "=r"(a[58]), "=r"(a[59]), "=r"(a[60]), "=r"(a[61]), "=r"(a[62]), "=r"(a[63]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31]), "=r"(b[32]), "=r"(b[33]), "=r"(b[34]), "=r"(b[35]), "=r"(b[36]), "=r"(b[37]), "=r"(b[38]), "=r"(b[39]), "=r"(b[40]), "=r"(b[41]), "=r"(b[42]), "=r"(b[43]), "=r"(b[44]), "=r"(b[45]), "=r"(b[46]), "=r"(b[47]), "=r"(b[48]), "=r"(b[49]), "=r"(b[50]), "=r"(b[51]), "=r"(b[52]), "=r"(b[53]), "=r"(b[54]), "=r"(b[55]), "=r"(b[56]), "=r"(b[57]), "=r"(b[58]), "=r"(b[59]), "=r"(b[60]), "=r"(b[61]), "=r"(b[62]), "=r"(b[63])
+        : "r"(ta), "r"(tb) : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -218,7 +228,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     auto sQ = [s0](int x) { return s0 + (uint32_t)x * kTileBytes; };
     auto sK = [s0](int b) { return s0 + (uint32_t)(2 + b) * kTileBytes; };
     auto sV = [s0](int b) { return s0 + (uint32_t)(4 + b) * kTileBytes; };
-    float *xchg = reinterpret_cast<float *>(base + kSmemTiles);          // [2][2][2][128]
+    float *xchg = reinterpret_cast<float *>(base + kSmemTiles);          // prefix pass: [2][2][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kSmemTiles + kXchgBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile int32_t *timed_out = reinterpret_cast<volatile int32_t *>(bars + kNumBars + 1);
@@ -295,7 +305,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i)
-            ptx::mbar_init(BAR(i), (i == kPReady || i == kPReady + 1) ? kSoftmaxThreads / 32 : 1);
+            ptx::mbar_init(BAR(i), (i == kPReady || i == kPReady + 1) ? (kPrefix ? 8 : kGroupThreads / 32) : 1);
         *timed_out = 0;
         ptx::fence_barrier_init();
     }
@@ -408,155 +418,252 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
             drain_wait(BAR(kVFree + ((nkt - 1) & 1)), ((nkt - 1) >> 1) & 1);
         }
         __syncwarp();
-    } else {
-        // ================= softmax warps: query row r of each tile (tensor-memory lane r) is
-        // shared by warps q and q + 4 (q = r / 32), each taking one 64-key half of every S
-        // tile and one 64-column half of O; the two exchange their row max once per tile.
-        // O lives in tensor memory and P V accumulates onto it. The softmax runs against a
-        // reference max m_ref (log2 units) that only moves when the row's max exceeds it
-        // by more than 2^8 (then O and l are rescaled), so P stays <= 256 and most tiles
-        // need no O traffic at all.
+    } else if constexpr (kPrefix) {
+        // ================= prefix pass softmax: one query tile, so all eight warps work on it:
+        // row r (tensor-memory lane r) is shared by warps q and q + 4 (q = r / 32), each
+        // taking one 64-key half of every S tile and one 64-column half of O; the two
+        // exchange their row max (and, at the end, their sums) through shared memory.
         const int hf = warp >> 2, quad = warp & 3;
         const int32_t r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const float sl2 = p.scale_log2;
         constexpr float kSlack = 8.f;
-        constexpr int kCols = kKT / 2;              // keys of S (and columns of O) per thread
-        // per-tile state in scalars (selected by x, not indexed: nothing goes to local memory)
-        float m_ref0 = -INFINITY, m_ref1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        const int32_t nk0 = nkt_x[0], nk1 = nkt_x[1];
-        const int32_t rows0 = rows[0], rows1 = rows[1], p00 = pos0[0], p01 = pos0[1];
-        for (int32_t j = 0; j < nkt; ++j) {
+        constexpr int kCols = kKT / 2;
+        const int32_t nk = nkt_x[0];
+        const bool valid = r < rows[0];
+        float m_ref = -INFINITY, l = 0.f;
+        for (int32_t j = 0; j < nk; ++j) {
             const int b = j & 1;
-#pragma unroll 1
-            for (int x = 0; x < kTiles; ++x) {
-                if (j >= (x ? nk1 : nk0)) continue;
-                const bool valid = r < (x ? rows1 : rows0);
-                const int32_t pr = kPrefix ? p00 : (x ? p01 : p00) + r;   // the last key this row sees
-                const int32_t t0 = kv_begin + j * kKT + hf * kCols;   // first key of this thread's half
-                bounded_wait(BAR(kSFull + x), j & 1, timed_out, p.status);
-                tc_fence_after();
-                uint32_t raw[kCols];
-                tmem_ld64(tS(x) + lane_base + hf * kCols, raw);
-                float xv[kCols];
-#pragma unroll
-                for (int i = 0; i < kCols; ++i) xv[i] = __uint_as_float(raw[i]);
-                if (!(valid && t0 + kCols - 1 <= pr)) {   // the diagonal tile (or a row past the chunk): mask
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) xv[i] = (valid && t0 + i <= pr) ? xv[i] : -INFINITY;
-                }
-                // row max of this half: a tree of three-input maxima (64 -> 22 -> 8 -> 3 -> 1)
-                float m22[22];
-#pragma unroll
-                for (int k = 0; k < 21; ++k) m22[k] = fmax3(xv[3 * k], xv[3 * k + 1], xv[3 * k + 2]);
-                m22[21] = xv[63];
-                float m8[8];
-#pragma unroll
-                for (int k = 0; k < 7; ++k) m8[k] = fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
-                m8[7] = m22[21];
-                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-                // row max across the two halves (a slot per tile and parity, so a fast
-                // partner never overwrites a value not yet read)
-                float *xs = xchg + (x * 2 + b) * 2 * kQT;
-                xs[hf * kQT + r] = mx;
-                ptx::named_barrier(1 + quad, 64);
-                mx = fmaxf(mx, xs[(hf ^ 1) * kQT + r]) * sl2;
-                const float mr = x ? m_ref1 : m_ref0;
-                const bool move = mx > mr + kSlack;  // false when mx = -inf; the same in both halves
-                const float new_ref = move ? mx : mr;
-                const float alpha = move ? ptx::ex2(mr - new_ref) : 1.f;   // m_ref = -inf: 0
-                if (j > 0 && __any_sync(0xffffffffu, move)) {
-                    // rescale this half of O_x once P_x,j-1 V is in it
-                    bounded_wait(BAR(kOFull + x), (j - 1) & 1, timed_out, p.status);
-                    tc_fence_after();
-#pragma unroll
-                    for (int c0 = 0; c0 < kCols; c0 += 32) {
-                        uint32_t v[32];
-                        const uint32_t ta = tO(x) + lane_base + hf * kCols + c0;
-                        tmem_ld32(ta, v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                        tmem_st32(ta, v);
-                    }
-                }
-                if (x) m_ref1 = new_ref;
-                else m_ref0 = new_ref;
-                // P = 2^(x * scale log2(e) - m_ref), pairs at a time, written over S_x (the
-                // partner half has read its S columns before the exchange above; S_x,j has
-                // landed, so P_x,j-1 V is done reading them). A row with no live key yet
-                // (m_ref = -inf: every x is -inf) gets 2^-inf = 0.
-                const float neg = new_ref == -INFINITY ? 0.f : -new_ref;
-                float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                uint32_t pk[kCols / 2];
-#pragma unroll
-                for (int e = 0; e < kCols / 2; ++e) {
-                    const float2 a = ptx::ffma2(make_float2(xv[2 * e], xv[2 * e + 1]), make_float2(sl2, sl2),
-                                                make_float2(neg, neg));
-                    const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
-                    pk[e] = pack_half2(pp.x, pp.y);
-                    rs2[e & 1] = ptx::fadd2(rs2[e & 1], pp);
-                }
-                tmem_st32(tS(x) + lane_base + hf * (kCols / 2), pk);
-                const float rsum = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
-                if (x) l1 = l1 * alpha + rsum;
-                else l0 = l0 * alpha + rsum;
-                // the CTA's last key tile: zero the V rows no query of the CTA may see (they
-                // may hold non-finite garbage), before the first P V that reads the tile
-                if (j == nkt - 1 && x == zero_tile) {
-                    bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
-                    const int32_t first_dead = kv_end - (kv_begin + j * kKT);   // rows [first_dead, 128)
-                    unsigned char *sVp = base + (4 + b) * kTileBytes;
-                    const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
-                    for (int32_t w = tid; w < nwords * 2; w += kSoftmaxThreads) {
-                        const int half = w / nwords, rem = w - half * nwords;
-                        const int row = first_dead + rem / 8, cc = rem & 7;
-                        *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + cc * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // zeroed V -> MMA
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(BAR(kPReady + x));
-            }
-        }
-#pragma unroll 1
-        for (int x = 0; x < kTiles; ++x) {
-            const int32_t nk = x ? nk1 : nk0;
-            if (nk == 0) continue;
-            const bool valid = r < (x ? rows1 : rows0);
-            const int32_t q0x = x ? q0[1] : q0[0];
-            bounded_wait(BAR(kOFull + x), (nk - 1) & 1, timed_out, p.status);
+            bounded_wait(BAR(kSFull), j & 1, timed_out, p.status);
             tc_fence_after();
-            // l of the whole row: both halves' sums (the slot of parity nk & 1 is free by now)
-            float *xs = xchg + (x * 2 + (nk & 1)) * 2 * kQT;
-            xs[hf * kQT + r] = x ? l1 : l0;
+            uint32_t raw[kCols];
+            tmem_ld64(tS(0) + lane_base + hf * kCols, raw);
+            float xv[kCols];
+#pragma unroll
+            for (int i = 0; i < kCols; ++i) xv[i] = __uint_as_float(raw[i]);
+            const int32_t t0 = kv_begin + j * kKT + hf * kCols;   // first key of this half
+            if (!(valid && t0 + kCols - 1 < kv_end)) {   // a ragged last tile (or a row past the group)
+#pragma unroll
+                for (int i = 0; i < kCols; ++i) xv[i] = (valid && t0 + i < kv_end) ? xv[i] : -INFINITY;
+            }
+            float m22[22];
+#pragma unroll
+            for (int k = 0; k < 21; ++k) m22[k] = fmax3(xv[3 * k], xv[3 * k + 1], xv[3 * k + 2]);
+            m22[21] = xv[63];
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 7; ++k) m8[k] = fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
+            m8[7] = m22[21];
+            float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+            // a slot per parity, so a fast partner never overwrites a value not yet read
+            float *xs = xchg + b * 2 * kQT;
+            xs[hf * kQT + r] = mx;
+            ptx::named_barrier(1 + quad, 64);
+            mx = fmaxf(mx, xs[(hf ^ 1) * kQT + r]) * sl2;
+            const bool move = mx > m_ref + kSlack;      // the same in both halves
+            const float new_ref = move ? mx : m_ref;
+            const float alpha = move ? ptx::ex2(m_ref - new_ref) : 1.f;
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                bounded_wait(BAR(kOFull), (j - 1) & 1, timed_out, p.status);
+                tc_fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < kCols; c0 += 32) {
+                    uint32_t w[32];
+                    const uint32_t ta = tO(0) + lane_base + hf * kCols + c0;
+                    tmem_ld32(ta, w);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+                    tmem_st32(ta, w);
+                }
+            }
+            m_ref = new_ref;
+            // P over S: the partner half has read its S columns before the exchange above
+            const float neg = new_ref == -INFINITY ? 0.f : -new_ref;
+            float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            uint32_t pk[kCols / 2];
+#pragma unroll
+            for (int e = 0; e < kCols / 2; ++e) {
+                const float2 a = ptx::ffma2(make_float2(xv[2 * e], xv[2 * e + 1]), make_float2(sl2, sl2),
+                                            make_float2(neg, neg));
+                const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+                pk[e] = pack_half2(pp.x, pp.y);
+                rs2[e & 1] = ptx::fadd2(rs2[e & 1], pp);
+            }
+            tmem_st32(tS(0) + lane_base + hf * (kCols / 2), pk);
+            l = l * alpha + ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y));
+            if (j == nk - 1) {
+                // the split's last key tile: zero the V rows past the split (a prefix is
+                // whole blocks, so only a ragged final tile has them)
+                bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
+                const int32_t first_dead = kv_end - (kv_begin + j * kKT);
+                unsigned char *sVp = base + (4 + b) * kTileBytes;
+                const int32_t nwords = (kKT - first_dead) * 8;
+                for (int32_t w = tid; w < nwords * 2; w += 2 * kGroupThreads) {
+                    const int half = w / nwords, rem = w - half * nwords;
+                    const int row = first_dead + rem / 8, cc = rem & 7;
+                    *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(kPReady));
+        }
+        if (nk > 0) {
+            bounded_wait(BAR(kOFull), (nk - 1) & 1, timed_out, p.status);
+            tc_fence_after();
+            float *xs = xchg + (nk & 1) * 2 * kQT;   // the slot of parity nk & 1 is free by now
+            xs[hf * kQT + r] = l;
             ptx::named_barrier(1 + quad, 64);
             const float lt = xs[r] + xs[kQT + r];
             uint32_t raw[kCols];
-            tmem_ld64(tO(x) + lane_base + hf * kCols, raw);
-            if constexpr (kPrefix) {
-                if (valid) {
-                    float *piece =
-                        p.pieces + (((size_t)(q0x + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4);
-                    float4 *o4 = reinterpret_cast<float4 *>(piece + hf * kCols);
+            tmem_ld64(tO(0) + lane_base + hf * kCols, raw);
+            if (valid) {
+                float *piece = p.pieces + (((size_t)(q0[0] + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4);
+                float4 *o4 = reinterpret_cast<float4 *>(piece + hf * kCols);
 #pragma unroll
-                    for (int d = 0; d < kCols; d += 4)
-                        o4[d / 4] = make_float4(__uint_as_float(raw[d]), __uint_as_float(raw[d + 1]),
-                                                __uint_as_float(raw[d + 2]), __uint_as_float(raw[d + 3]));
-                    if (hf == 0) *reinterpret_cast<float4 *>(piece + kD) = make_float4(x ? m_ref1 : m_ref0, lt, 0.f, 0.f);
+                for (int d = 0; d < kCols; d += 4)
+                    o4[d / 4] = make_float4(__uint_as_float(raw[d]), __uint_as_float(raw[d + 1]),
+                                            __uint_as_float(raw[d + 2]), __uint_as_float(raw[d + 3]));
+                if (hf == 0) *reinterpret_cast<float4 *>(piece + kD) = make_float4(m_ref, lt, 0.f, 0.f);
+            }
+        }
+    } else {
+        // ================= softmax warps: warps 0-3 own query tile A, warps 4-7 tile B, one
+        // thread per query row (row r = tensor-memory lane r, warp 4x + r / 32), so the two
+        // tiles' softmax run side by side and a row's max and sum never leave its thread.
+        // O lives in tensor memory and P V accumulates onto it. The softmax runs against a
+        // reference max m_ref (log2 units) that only moves when the row's max exceeds it
+        // by more than 2^8 (then O and l are rescaled), so P stays <= 256 and most tiles
+        // need no O traffic at all.
+        const int x = warp >> 2, quad = warp & 3;
+        const int32_t r = quad * 32 + lane;
+        const int gtid = tid - x * kGroupThreads;       // thread index inside the tile's group
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const float sl2 = p.scale_log2;
+        constexpr float kSlack = 8.f;
+        constexpr int kHalfKeys = kKT / 2;              // keys of one tensor-memory load
+        const int32_t nk = nkt_x[x];
+        const bool valid = r < rows[x];
+        const int32_t pr = pos0[x] + r;                 // the last key this row sees
+        float m_ref = -INFINITY, l = 0.f;
+        // row max of 64 scores: a tree of three-input maxima (64 -> 22 -> 8 -> 3 -> 1)
+        auto max64 = [](const float (&v)[kHalfKeys]) {
+            float m22[22];
+#pragma unroll
+            for (int k = 0; k < 21; ++k) m22[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+            m22[21] = v[63];
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 7; ++k) m8[k] = fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
+            m8[7] = m22[21];
+            return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        };
+        // mask one half (64 keys from t0) of this row's scores past the row's last key
+        auto mask_half = [&](int half, int32_t t0, float (&v)[kHalfKeys]) {
+            const int32_t k0 = t0 + half * kHalfKeys;
+            if (!(valid && k0 + kHalfKeys - 1 <= pr)) {   // the diagonal tile (or a row past the chunk)
+#pragma unroll
+                for (int i = 0; i < kHalfKeys; ++i) v[i] = (valid && k0 + i <= pr) ? v[i] : -INFINITY;
+            }
+        };
+        // P = 2^(x * scale log2(e) - m_ref) of one half, pairs at a time, packed fp16 into
+        // tensor-memory columns [32 half, 32 half + 32) of S; returns the half's sum
+        auto store_p = [&](int half, const float (&v)[kHalfKeys], float neg) {
+            float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            uint32_t pk[kHalfKeys / 2];
+#pragma unroll
+            for (int e = 0; e < kHalfKeys / 2; ++e) {
+                const float2 a = ptx::ffma2(make_float2(v[2 * e], v[2 * e + 1]), make_float2(sl2, sl2),
+                                            make_float2(neg, neg));
+                const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+                pk[e] = pack_half2(pp.x, pp.y);
+                rs2[e & 1] = ptx::fadd2(rs2[e & 1], pp);
+            }
+            tmem_st32(tS(x) + lane_base + half * (kHalfKeys / 2), pk);
+            return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+        };
+        for (int32_t j = 0; j < nk; ++j) {
+            const int b = j & 1;
+            const int32_t t0 = kv_begin + j * kKT;      // first key of the tile
+            bounded_wait(BAR(kSFull + x), j & 1, timed_out, p.status);
+            tc_fence_after();
+            // both halves of this row's scores at once
+            float v0[kHalfKeys], v1[kHalfKeys];
+            {
+                uint32_t r0[kHalfKeys], r1[kHalfKeys];
+                tmem_ld64x2(tS(x) + lane_base, tS(x) + lane_base + kHalfKeys, r0, r1);
+#pragma unroll
+                for (int i = 0; i < kHalfKeys; ++i) {
+                    v0[i] = __uint_as_float(r0[i]);
+                    v1[i] = __uint_as_float(r1[i]);
                 }
-            } else if (valid) {
-                const float inv = 1.f / lt;
-                __half *dst = p.out + ((size_t)(q0x + r) * H + h) * kD + hf * kCols;
+            }
+            mask_half(0, t0, v0);
+            mask_half(1, t0, v1);
+            const float mx = fmaxf(max64(v0), max64(v1)) * sl2;
+            const bool move = mx > m_ref + kSlack;      // false when mx = -inf
+            const float new_ref = move ? mx : m_ref;
+            const float alpha = move ? ptx::ex2(m_ref - new_ref) : 1.f;   // m_ref = -inf: 0
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                // rescale this row of O once P V of the previous key tile is in it
+                bounded_wait(BAR(kOFull + x), (j - 1) & 1, timed_out, p.status);
+                tc_fence_after();
 #pragma unroll
-                for (int d = 0; d < kCols; d += 8) {
-                    __half2 hv[4];
+                for (int c0 = 0; c0 < kD; c0 += 32) {
+                    uint32_t w[32];
+                    const uint32_t ta = tO(x) + lane_base + c0;
+                    tmem_ld32(ta, w);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        hv[e] = __floats2half2_rn(__uint_as_float(raw[d + 2 * e]) * inv,
-                                                  __uint_as_float(raw[d + 2 * e + 1]) * inv);
-                    *reinterpret_cast<uint4 *>(dst + d) = *reinterpret_cast<const uint4 *>(hv);
+                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+                    tmem_st32(ta, w);
+                }
+            }
+            m_ref = new_ref;
+            // P over S: both halves are in registers, so the columns may be overwritten. A
+            // row with no live key yet (m_ref = -inf: every score is -inf) gets 0.
+            const float neg = new_ref == -INFINITY ? 0.f : -new_ref;
+            float rsum = store_p(0, v0, neg);            // columns [0, 32)
+            rsum += store_p(1, v1, neg);                 // columns [32, 64)
+            l = l * alpha + rsum;
+            // the CTA's last key tile: zero the V rows no query of the CTA may see (they
+            // may hold non-finite garbage), before the first P V that reads the tile
+            if (j == nkt - 1 && x == zero_tile) {
+                bounded_wait(BAR(kVFull + b), (j >> 1) & 1, timed_out, p.status);
+                const int32_t first_dead = kv_end - t0;  // rows [first_dead, 128)
+                unsigned char *sVp = base + (4 + b) * kTileBytes;
+                const int32_t nwords = (kKT - first_dead) * 8;    // 16-byte words per half
+                for (int32_t w = gtid; w < nwords * 2; w += kGroupThreads) {
+                    const int half = w / nwords, rem = w - half * nwords;
+                    const int row = first_dead + rem / 8, cc = rem & 7;
+                    *reinterpret_cast<uint4 *>(sVp + half * kSub + row * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // zeroed V -> MMA
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(kPReady + x));
+        }
+        if (nk > 0) {
+            bounded_wait(BAR(kOFull + x), (nk - 1) & 1, timed_out, p.status);
+            tc_fence_after();
+            const int32_t qrow = q0[x] + r;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t raw[kHalfKeys];
+                tmem_ld64(tO(x) + lane_base + half * kHalfKeys, raw);
+                if (valid) {
+                    const float inv = 1.f / l;
+                    __half *dst = p.out + ((size_t)qrow * H + h) * kD + half * kHalfKeys;
+#pragma unroll
+                    for (int d = 0; d < kHalfKeys; d += 8) {
+                        __half2 hv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            hv[e] = __floats2half2_rn(__uint_as_float(raw[d + 2 * e]) * inv,
+                                                      __uint_as_float(raw[d + 2 * e + 1]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + d) = *reinterpret_cast<const uint4 *>(hv);
+                    }
                 }
             }
         }
