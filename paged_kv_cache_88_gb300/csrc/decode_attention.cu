@@ -12,19 +12,19 @@
 // Design (GB300-first; the pages' A100 kernel advice -- table in shared memory,
 // vectorised loads, many heads per launch -- is prior art, not the blueprint):
 //
-// * Work unit = one tile of 32 tokens of one (sequence, head). All tiles of the
+// * Work unit = one tile of 64 tokens of one (sequence, head). All tiles of the
 //   batch are numbered (s, h, t) and the launch's CTAs take equal contiguous
 //   ranges of that list (a persistent grid of SMs x resident CTAs). Mixed
 //   context lengths therefore cost no tail imbalance: every CTA streams the same
 //   number of tiles (+-1).
 // * A producer warp walks the CTA's range and issues TMA tensor loads of each
-//   tile's K and V rows (one box per block, or a 32-row box inside a large
+//   tile's K and V rows (one box per block, or a 64-row box inside a large
 //   block) into a multi-stage shared-memory ring guarded by mbarriers; it keeps a
 //   window of 32 block-table entries of the current sequence in registers (one
 //   coalesced load serves every head of the sequence). The query row of a new
 //   (s, h) rides along in the same stage as a 1-D bulk copy.
 // * Four consumer warps split each tile into 16 groups of 8 lanes; a group owns
-//   two rows (tokens) of the tile, a lane 8 x (D / 64) elements of the head dim.
+//   four rows (tokens) of the tile, a lane 8 x (D / 64) elements of the head dim.
 //   Rows are read from shared memory as 16-byte words, a group covering 128
 //   contiguous bytes per load (no bank conflicts). q.K accumulates fp16 x fp16
 //   products in fp32 (mixed-precision FMA; the products are exact) and finishes
