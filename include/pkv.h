@@ -332,8 +332,9 @@ pkv_status pkv_decode_attention_static(const void *q, const void *k_cache, const
  * table (m.lqnn.cn/news/240480 §3.3 remap, §4.3 causal prefill):
  *   out[row][h] = softmax_{t <= p}(scale * q[row][h] . K_t[h]) V_t[h].
  * q, out: device fp16 [total_q][H][D], 16-byte aligned. q_start: device int32
- * [num_seqs + 1]. max_chunk: a host bound on every C_s (sizes the grid; larger
- * chunks are only partly computed). status: device uint32 word (required).
+ * [num_seqs + 1]. max_chunk: a host bound on every C_s (sizes the grid; rows of a
+ * chunk past the grid's ceil(max_chunk / 256) * 256 are not computed, and the call
+ * is flagged PKV_DEV_BAD_LENGTH). status: device uint32 word (required).
  * The pool must be fp16, HND, head_dim 128. fp16 products, fp32 accumulation;
  * the softmax weights enter P V in fp16. T_s < C_s or T_s beyond the table is
  * clamped and flagged PKV_DEV_BAD_LENGTH. UNSUPPORTED for other pools. */

@@ -280,6 +280,10 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         const int32_t qs = p.q_start[s];
         const int32_t C = p.q_start[s + 1] - qs;
         const int32_t i0 = blockIdx.x * (kTiles * kQT);
+        // a chunk longer than the grid covers (max_chunk too small): its last rows are
+        // not computed, and the call is flagged
+        if (blockIdx.x == gridDim.x - 1 && C > (int32_t)gridDim.x * (kTiles * kQT) && tid == 0)
+            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
         if (i0 >= C) return;                           // uniform: this pair of tiles has no queries
         int32_t T = p.lens[s];
         if (T < C || T > cap) {

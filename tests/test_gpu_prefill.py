@@ -113,3 +113,19 @@ def test_prefill_rejects_other_pools():
                                torch.ones(1, dtype=torch.int32, device="cuda"), z, torch.zeros(1, dtype=torch.int32,
                                                                                               device="cuda"))
     assert e.value.code == "UNSUPPORTED"
+
+
+def test_prefill_flags_chunk_beyond_max_chunk():
+    """max_chunk sizes the grid: a chunk longer than the grid covers is flagged, and the
+    rows the grid does cover are still right."""
+    H, B = 2, 16
+    lens, chunks = [300, 100], [300, 100]
+    q, qs, kp, vp, tab, ln, N = _case(lens, chunks, H, B, seed=5)
+    got, st = _run(q, qs, kp, vp, tab, ln, N, H, B, max_chunk=200)     # grid covers 256 rows a chunk
+    assert st & pkv.DEV_BAD_LENGTH
+    ref = rf.prefill_attention(q, kp, vp, tab, ln, qs, B, layout="HND")
+    covered = np.r_[0:256, 300:400]
+    _check(got[covered], ref[covered], "covered rows")
+    got, st = _run(q, qs, kp, vp, tab, ln, N, H, B, max_chunk=300)     # the true bound: no flag
+    assert st == 0
+    _check(got, ref, "all rows")
