@@ -258,22 +258,36 @@ template <int D, int DPT>
 __device__ __forceinline__ void merge_prefix(const Params &p, int32_t s, int32_t h, int tid, float &M, float &L,
                                              float (&O)[DPT]) {
     const float *base = p.pre + ((size_t)s * p.H + h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
+    // every piece's m, l and this thread's o elements in one round of loads (unrolled to
+    // the largest split count, predicated on the actual one), then the arithmetic
+    float pm[PKV_MAX_PREFIX_SPLITS], pl[PKV_MAX_PREFIX_SPLITS], po[PKV_MAX_PREFIX_SPLITS][DPT];
+#pragma unroll
+    for (int k = 0; k < PKV_MAX_PREFIX_SPLITS; ++k) {
+        const bool in = k < p.pre_splits;
+        const float *pc = base + k * (D + 4);
+        pm[k] = in ? __ldcg(pc + D) : -INFINITY;
+        pl[k] = in ? __ldcg(pc + D + 1) : 0.f;
+#pragma unroll
+        for (int r = 0; r < DPT; ++r) {
+            const int d = tid + r * kConsumerThreads;
+            po[k][r] = (in && d < D) ? __ldcg(pc + d) : 0.f;
+        }
+    }
     float Mn = M;
-    for (int k = 0; k < p.pre_splits; ++k) Mn = fmaxf(Mn, __ldcg(base + k * (D + 4) + D));
+#pragma unroll
+    for (int k = 0; k < PKV_MAX_PREFIX_SPLITS; ++k) Mn = fmaxf(Mn, pm[k]);
     if (Mn == -INFINITY) return;
     const float a = ptx::ex2(M - Mn);          // M = -inf: 0
     L *= a;
 #pragma unroll
     for (int r = 0; r < DPT; ++r) O[r] *= a;
-    for (int k = 0; k < p.pre_splits; ++k) {
-        const float *pc = base + k * (D + 4);
-        const float w = ptx::ex2(__ldcg(pc + D) - Mn);   // an empty piece (m = -inf): 0
-        L = fmaf(w, __ldcg(pc + D + 1), L);
 #pragma unroll
-        for (int r = 0; r < DPT; ++r) {
-            const int d = tid + r * kConsumerThreads;
-            if (d < D) O[r] = fmaf(w, __ldcg(pc + d), O[r]);
-        }
+    for (int k = 0; k < PKV_MAX_PREFIX_SPLITS; ++k) {
+        if (k >= p.pre_splits) break;
+        const float w = ptx::ex2(pm[k] - Mn);  // an empty piece (m = -inf): 0
+        L = fmaf(w, pl[k], L);
+#pragma unroll
+        for (int r = 0; r < DPT; ++r) O[r] = fmaf(w, po[k][r], O[r]);
     }
     M = Mn;
 }
