@@ -134,16 +134,22 @@ struct Stage {
 
 __host__ __device__ constexpr int piece_stride(int D) { return D + 4; }
 
-// Shared memory: [stages][reduction][seq arrays][barriers + flags]
+// The cascade's prefix pieces of the current (s, h), staged in shared memory while its
+// tiles stream (fp16 caches only: the cascade is built for them).
+template <int D, bool Q8>
+__host__ __device__ constexpr int pre_buf_floats() { return Q8 ? 0 : PKV_MAX_PREFIX_SPLITS * (D + 4); }
+
+// Shared memory: [stages][prefix pieces][reduction][seq arrays][barriers + flags]
 template <int D, bool Q8>
 __host__ __device__ constexpr size_t smem_bytes_t(int S) {
-    return ((size_t)Stage<D, Q8>::kStages * Stage<D, Q8>::kBytes + (size_t)kConsumerWarps * (D + 2) * sizeof(float) +
-            (size_t)(3 * S + 2) * sizeof(int32_t) + 15) / 16 * 16 +
+    return ((size_t)Stage<D, Q8>::kStages * Stage<D, Q8>::kBytes + (size_t)pre_buf_floats<D, Q8>() * sizeof(float) +
+            (size_t)kConsumerWarps * (D + 2) * sizeof(float) + (size_t)(3 * S + 2) * sizeof(int32_t) + 15) / 16 * 16 +
            2 * Stage<D, Q8>::kStages * sizeof(uint64_t) + 16 + 128;  // + slack to align the base to 128 bytes
 }
 
 struct Smem {
     unsigned char *stage;  // kStages * stage bytes
+    float *pre;            // [PKV_MAX_PREFIX_SPLITS][D + 4] (fp16 caches)
     float *red_o;          // [kConsumerWarps][D]
     float *red_m;          // [kConsumerWarps]
     float *red_l;          // [kConsumerWarps]
@@ -162,6 +168,8 @@ __device__ __forceinline__ Smem carve(unsigned char *raw, int S) {
     uintptr_t p = (reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127);
     m.stage = reinterpret_cast<unsigned char *>(p);
     p += (size_t)NS * Stage<D, Q8>::kBytes;
+    m.pre = reinterpret_cast<float *>(p);
+    p += (size_t)pre_buf_floats<D, Q8>() * sizeof(float);
     m.red_o = reinterpret_cast<float *>(p);
     p += (size_t)kConsumerWarps * D * sizeof(float);
     m.red_m = reinterpret_cast<float *>(p);
@@ -254,10 +262,11 @@ __device__ __forceinline__ bool wait_phase(const Smem &sm, uint32_t bar, uint32_
 // Fold the cascade's prefix pieces of (s, h) into a combine in progress: M, L
 // and this thread's output elements O[r] (element tid + r * kConsumerThreads),
 // all relative to 2^M. The pieces were written by an earlier launch.
-template <int D, int DPT>
-__device__ __forceinline__ void merge_prefix(const Params &p, int32_t s, int32_t h, int tid, float &M, float &L,
-                                             float (&O)[DPT]) {
-    const float *base = p.pre + ((size_t)s * p.H + h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
+template <int D, int DPT, bool kStaged>
+__device__ __forceinline__ void merge_prefix(const Params &p, const float *staged, int32_t s, int32_t h, int tid,
+                                             float &M, float &L, float (&O)[DPT]) {
+    const float *base = kStaged ? staged : p.pre + ((size_t)s * p.H + h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
+    auto ld = [](const float *a) { return kStaged ? *a : __ldcg(a); };
     // every piece's m, l and this thread's o elements in one round of loads (unrolled to
     // the largest split count, predicated on the actual one), then the arithmetic
     float pm[PKV_MAX_PREFIX_SPLITS], pl[PKV_MAX_PREFIX_SPLITS], po[PKV_MAX_PREFIX_SPLITS][DPT];
@@ -265,12 +274,12 @@ __device__ __forceinline__ void merge_prefix(const Params &p, int32_t s, int32_t
     for (int k = 0; k < PKV_MAX_PREFIX_SPLITS; ++k) {
         const bool in = k < p.pre_splits;
         const float *pc = base + k * (D + 4);
-        pm[k] = in ? __ldcg(pc + D) : -INFINITY;
-        pl[k] = in ? __ldcg(pc + D + 1) : 0.f;
+        pm[k] = in ? ld(pc + D) : -INFINITY;
+        pl[k] = in ? ld(pc + D + 1) : 0.f;
 #pragma unroll
         for (int r = 0; r < DPT; ++r) {
             const int d = tid + r * kConsumerThreads;
-            po[k][r] = (in && d < D) ? __ldcg(pc + d) : 0.f;
+            po[k][r] = (in && d < D) ? ld(pc + d) : 0.f;
         }
     }
     float Mn = M;
@@ -383,7 +392,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 float M = -INFINITY, L = 0.f, O[DPT];
 #pragma unroll
                 for (int r = 0; r < DPT; ++r) O[r] = 0.f;
-                merge_prefix<D, DPT>(p, s, i - s * H, tid, M, L, O);
+                merge_prefix<D, DPT, false>(p, nullptr, s, i - s * H, tid, M, L, O);
                 const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
                 for (int r = 0; r < DPT; ++r) {
@@ -602,6 +611,18 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             m = -INFINITY;
             l = 0.f;
             seg_g0 = g0 + k;
+            if constexpr (!Q8) {
+                // a cascade member: stage its prefix pieces now, so the combine at the end
+                // of the (s, h) reads them from shared memory (the previous combine's last
+                // barrier has released the buffer)
+                if (sm.beg[c.s] > 0) {
+                    const float *src = p.pre + ((size_t)c.s * H + c.h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
+                    const int n16 = p.pre_splits * (D + 4) / 4;
+                    for (int i = tid; i < n16; i += kConsumerThreads)
+                        ptx::cp_async_16_cg(ptx::smem_addr(sm.pre) + i * 16, src + i * 4);
+                    ptx::cp_async_commit();
+                }
+            }
         }
         // this group's rows of the tile: grp, grp + kGroups, ...; kr/vr hold each
         // chunk's 8 elements as four fp16 pairs
@@ -741,6 +762,9 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                     sm.red_l[warp] = lw;
                 }
             }
+            if constexpr (!Q8) {
+                if (sm.beg[c.s] > 0) ptx::cp_async_wait_all();   // this thread's staged pieces (the barrier shares them)
+            }
             ptx::named_barrier(1, kConsumerThreads);
             float M = -INFINITY;
 #pragma unroll
@@ -770,7 +794,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             const int32_t cb = cta_of(total, grid, seg_hi);
             __half *dst_out = p.out + ((size_t)c.s * H + c.h) * D;
             if (ca == cb) {
-                if (sm.beg[c.s] > 0) merge_prefix<D, DPT>(p, c.s, c.h, tid, M, L, O);
+                if (sm.beg[c.s] > 0) merge_prefix<D, DPT, !Q8>(p, sm.pre, c.s, c.h, tid, M, L, O);
                 const float inv = 1.f / L;
 #pragma unroll
                 for (int r = 0; r < DPT; ++r) {
@@ -827,7 +851,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                             if (d < D) Og[r] = fmaf(wc, __ldcg(pc + d), Og[r]);
                         }
                     }
-                    if (sm.beg[c.s] > 0) merge_prefix<D, DPT>(p, c.s, c.h, tid, Mg, Lg, Og);
+                    if (sm.beg[c.s] > 0) merge_prefix<D, DPT, !Q8>(p, sm.pre, c.s, c.h, tid, Mg, Lg, Og);
                     const float inv = 1.f / Lg;
 #pragma unroll
                     for (int r = 0; r < DPT; ++r) {

@@ -107,6 +107,15 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 only (no L1 allocation).
+__device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Close this thread's group of cp.async copies / wait until all of its copies landed.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Keep the current phase of mbarrier `bar` open until every cp.async this thread
 // issued so far has landed (the arrival it adds is taken back when they land, so
 // the barrier's expected count is unchanged).
