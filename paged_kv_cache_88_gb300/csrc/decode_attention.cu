@@ -830,25 +830,52 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 ptx::named_barrier(1, kConsumerThreads);
                 if (sm.flags[1]) {
                     const int32_t start_a = range_start(total, grid, ca);
-                    float Mg = -INFINITY;
-                    for (int32_t cc = ca; cc <= cb; ++cc) {
+                    auto piece_of = [&](int32_t cc) {
                         const int sl = (cc > ca || start_a == seg_lo) ? 0 : 1;
-                        const float *pc = p.pieces + ((size_t)cc * 2 + sl) * piece_stride(D);
-                        Mg = fmaxf(Mg, __ldcg(pc + D));
-                    }
+                        return p.pieces + ((size_t)cc * 2 + sl) * piece_stride(D);
+                    };
+                    float Mg = -INFINITY;
                     float Lg = 0.f;
                     float Og[DPT];
 #pragma unroll
                     for (int r = 0; r < DPT; ++r) Og[r] = 0.f;
-                    for (int32_t cc = ca; cc <= cb; ++cc) {
-                        const int sl = (cc > ca || start_a == seg_lo) ? 0 : 1;
-                        const float *pc = p.pieces + ((size_t)cc * 2 + sl) * piece_stride(D);
-                        const float wc = ptx::ex2(__ldcg(pc + D) - Mg);
-                        Lg = fmaf(wc, __ldcg(pc + D + 1), Lg);
+                    constexpr int kFew = 4;                  // pieces merged with one round of loads
+                    // (fp16 caches: on an E4M3 cache the unrolled merge measured 2 % slower)
+                    if (!Q8 && cb - ca < kFew) {
+                        float cm[kFew], cl[kFew], co[kFew][DPT];
 #pragma unroll
-                        for (int r = 0; r < DPT; ++r) {
-                            const int d = tid + r * kConsumerThreads;
-                            if (d < D) Og[r] = fmaf(wc, __ldcg(pc + d), Og[r]);
+                        for (int u = 0; u < kFew; ++u) {
+                            const bool in = u <= cb - ca;
+                            const float *pc = piece_of(ca + (in ? u : 0));
+                            cm[u] = in ? __ldcg(pc + D) : -INFINITY;
+                            cl[u] = in ? __ldcg(pc + D + 1) : 0.f;
+#pragma unroll
+                            for (int r = 0; r < DPT; ++r) {
+                                const int d = tid + r * kConsumerThreads;
+                                co[u][r] = (in && d < D) ? __ldcg(pc + d) : 0.f;
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < kFew; ++u) Mg = fmaxf(Mg, cm[u]);
+#pragma unroll
+                        for (int u = 0; u < kFew; ++u) {
+                            if (u > cb - ca) break;
+                            const float wc = ptx::ex2(cm[u] - Mg);
+                            Lg = fmaf(wc, cl[u], Lg);
+#pragma unroll
+                            for (int r = 0; r < DPT; ++r) Og[r] = fmaf(wc, co[u][r], Og[r]);
+                        }
+                    } else {
+                        for (int32_t cc = ca; cc <= cb; ++cc) Mg = fmaxf(Mg, __ldcg(piece_of(cc) + D));
+                        for (int32_t cc = ca; cc <= cb; ++cc) {
+                            const float *pc = piece_of(cc);
+                            const float wc = ptx::ex2(__ldcg(pc + D) - Mg);
+                            Lg = fmaf(wc, __ldcg(pc + D + 1), Lg);
+#pragma unroll
+                            for (int r = 0; r < DPT; ++r) {
+                                const int d = tid + r * kConsumerThreads;
+                                if (d < D) Og[r] = fmaf(wc, __ldcg(pc + d), Og[r]);
+                            }
                         }
                     }
                     if (sm.beg[c.s] > 0) merge_prefix<D, DPT, !Q8>(p, sm.pre, c.s, c.h, tid, Mg, Lg, Og);
