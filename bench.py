@@ -446,7 +446,10 @@ def run_ours(args):
                            mean_context_timed=float(np.mean(step_bytes)) / w.kv_bytes_per_token_layer / S,
                            step=("decode step as one CUDA graph: per layer the shared-prefix pass, then one "
                                  "fused append+attention launch over the private rest" if cascading else
-                                 "decode step as one CUDA graph: per layer one fused append+attention launch")),
+                                 "decode step as one CUDA graph: per layer one fused append+attention launch"
+                                 if eng.fused else
+                                 "decode step as one CUDA graph: per layer one append launch (quantising for "
+                                 "an E4M3 cache), then one attention launch")),
             "seq_steps_per_s": seq_steps,
             "frac_of_hbm_peak": value / peak,
             **({"unique_gbps": value * sum(step_unique) / sum(step_bytes),

@@ -8,8 +8,9 @@ One decode step over a batch (all through the C ABI):
    double-buffered staging (the host can prepare step k+1 while step k runs);
 3. ``pkv_copy_blocks`` once for the step, across all layers;
 4. per layer: the new token's K/V appended and attention over the cache
-   including it -- one ``pkv_decode_append_attention`` launch (default), or
-   ``pkv_append`` then ``pkv_pool_decode_attention``. With the shared-prefix
+   including it -- one ``pkv_decode_append_attention`` launch (the default for an
+   fp16 cache), or ``pkv_append`` then ``pkv_pool_decode_attention`` (the default
+   for an E4M3 cache). With the shared-prefix
    cascade (fp16 HND pools, head_dim 128, on by default), the host plans groups
    of sequences that share leading blocks (``pkv_cascade_plan``) and each
    layer first runs ``pkv_prefix_attention`` over the groups' prefixes, then
