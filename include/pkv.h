@@ -440,6 +440,13 @@ pkv_status pkv_decode_attention_ex(const pkv_pool *pool, int32_t layer, const vo
                                    void *out, void *workspace, size_t workspace_bytes, uint32_t flags,
                                    void *stream);
 
+/* Self-test of the device wait limit (failure detection without a fault): one CTA
+ * waits, with the bounded wait every pipeline stage of the attention kernels uses, on
+ * an mbarrier that nothing ever completes. After the limit (1 s) it ORs
+ * PKV_DEV_TIMEOUT into *status (device uint32) and exits; the context stays usable.
+ * Errors: INVALID_ARG (status NULL), CUDA (launch failure). */
+pkv_status pkv_check_wait_limit(uint32_t *status, void *stream);
+
 /* Bytes of workspace pkv_decode_attention needs for these sizes on the
  * current CUDA device (0 and a pkv_last_error message on bad arguments). */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim);

@@ -32,7 +32,7 @@ EXPORTED = [
     "pkv_decode_attention_static", "pkv_block_hash", "pkv_prefix_lookup", "pkv_prefix_register",
     "pkv_pool_set_scales", "pkv_swap_bytes_per_block", "pkv_gather_blocks", "pkv_scatter_blocks",
     "pkv_prefill_attention", "pkv_cascade_plan", "pkv_prefix_pieces_bytes", "pkv_prefix_splits",
-    "pkv_prefix_attention", "pkv_decode_attention_ex",
+    "pkv_prefix_attention", "pkv_decode_attention_ex", "pkv_check_wait_limit",
 ]
 
 MAX_GROUP_SEQS = 128
@@ -99,6 +99,7 @@ def lib() -> ctypes.CDLL:
             "pkv_decode_attention": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
                                            vp]),
             "pkv_decode_workspace_bytes": (sz, [i32, i32, i32]),
+            "pkv_check_wait_limit": (i32, [vp, vp]),
             "pkv_pool_decode_attention": (i32, [vp, i32, vp, vp, i32, vp, i32, f32, vp, vp, sz, vp]),
             "pkv_decode_launch_info": (i32, [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                              ctypes.POINTER(i32)]),
@@ -417,6 +418,12 @@ def cascade_plan(block_tables: np.ndarray, context_lens: np.ndarray, block_size:
     check(lib().pkv_cascade_plan(_ptr(tab), tab.shape[1], _ptr(lens), S, block_size, min_group, min_prefix_tokens,
                                  _ptr(groups), cap, ctypes.byref(n), _ptr(begin)))
     return groups[: n.value], begin[:S]
+
+
+def check_wait_limit(status, stream=None) -> None:
+    """pkv_check_wait_limit: a probe whose wait runs out; ``status``: device int32 [>= 1]."""
+    _require(status, "int32", "status")
+    check(lib().pkv_check_wait_limit(_ptr(status), _stream(stream)))
 
 
 def prefix_pieces_bytes(num_seqs: int, num_heads: int, head_dim: int) -> int:

@@ -259,6 +259,24 @@ __device__ __forceinline__ bool wait_phase(const Smem &sm, uint32_t bar, uint32_
     }
 }
 
+// Self-test of the wait limit: one thread waits, with the attention kernels' bounded
+// wait, on an mbarrier that nothing ever completes. It gives up after the limit,
+// flags PKV_DEV_TIMEOUT and the CTA exits (the context stays usable).
+__global__ void wait_limit_probe_kernel(uint32_t *status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int32_t flags[2];
+    const uint32_t b = ptx::smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(b, 1);
+        flags[0] = flags[1] = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    Smem sm = {};
+    sm.flags = flags;
+    if (threadIdx.x == 0) wait_phase(sm, b, 0, status);
+}
+
 // Fold the cascade's prefix pieces of (s, h) into a combine in progress: M, L
 // and this thread's output elements O[r] (element tid + r * kConsumerThreads),
 // all relative to 2^M. The pieces were written by an earlier launch.
@@ -1016,6 +1034,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 
 extern "C" {
+
+pkv_status pkv_check_wait_limit(uint32_t *status, void *stream) {
+    if (!status) return fail(PKV_ERR_INVALID_ARG, "status is NULL");
+    wait_limit_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "wait-limit probe launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
 
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim) {
     if (num_seqs < 0 || num_seqs > kMaxSeqs || num_heads < 1 || !supported_head_dim(head_dim)) {

@@ -568,3 +568,16 @@ def test_attention_ex_rejects_unknown_flags():
         eng.pool.decode_attention_ex(0, q[0], eng.tables_d, eng.lens_d, torch.empty_like(q[0]), eng.workspace,
                                      flags=0x2)
     assert e.value.code == "INVALID_ARG"
+
+
+def test_wait_limit_flags_timeout_and_context_survives():
+    """Failure detection without a fault: a wait that nothing satisfies gives up after its
+    limit, flags PKV_DEV_TIMEOUT, and the context keeps working (an attention step after
+    it is still right)."""
+    from paged_kv_cache_88_gb300 import binding as bd
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.check_wait_limit(st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & pkv.DEV_TIMEOUT
+    w = wl.make_workload(1, decode_steps=1)
+    run_parity(w, 1)
