@@ -236,3 +236,91 @@ def test_cascade_argument_errors():
                                c.pieces, c.status)
     assert e.value.code == "UNSUPPORTED"
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("splits", [1, 3, 8])
+def test_merge_of_given_pieces(splits):
+    """pkv_decode_attention_ex merges whatever prefix pieces it is given: pieces written
+    here (random m, l and o, one of them empty), private contexts of every kind (several
+    tiles, one token, none at all, no cascade for the sequence). Expected: the float64
+    merge of the pieces with the softmax sums of the private keys."""
+    hd = 128
+    rng = np.random.default_rng(hd * 10 + splits)
+    H, B = 3, 16
+    lens = np.array([300, 41, 16, 128, 70, 200, 1], dtype=np.int32)
+    begin = np.array([96, 32, 16, 0, 64, 0, 0], dtype=np.int32)     # whole blocks; 16 of 16: no private part
+    S = len(lens)
+    nb = [-(-int(T) // B) for T in lens]
+    N = sum(nb) + 2
+    perm = rng.permutation(N).astype(np.int32)
+    tables = np.full((S, max(nb)), -1, dtype=np.int32)
+    i = 0
+    for s, n in enumerate(nb):
+        tables[s, :n] = perm[i:i + n]
+        i += n
+    kp = rng.standard_normal((N, H, B, hd)).astype(np.float16)
+    vp = rng.standard_normal((N, H, B, hd)).astype(np.float16)
+    q = rng.standard_normal((S, H, hd)).astype(np.float16)
+    scale = 1.0 / math.sqrt(hd)
+    sl2 = scale * LOG2E
+    pcs = np.zeros((S, H, bd.MAX_PREFIX_SPLITS, hd + 4), dtype=np.float32)
+    pcs[..., hd] = -np.inf
+    for s in range(S):
+        for h in range(H):
+            for k in range(splits):
+                if k == splits // 2 and splits > 1:
+                    continue                               # an empty piece: m = -inf, l = 0, o = 0
+                l = rng.uniform(0.5, 50.0)
+                pcs[s, h, k, hd] = rng.uniform(-4.0, 4.0)
+                pcs[s, h, k, hd + 1] = l
+                pcs[s, h, k, :hd] = rng.standard_normal(hd) * l
+    dev = "cuda"
+    pool = pkv.Pool(1, N, B, H, hd, "HND", k_pool=torch.from_numpy(kp).to(dev), v_pool=torch.from_numpy(vp).to(dev))
+    out = torch.full((S, H, hd), float("nan"), dtype=torch.float16, device=dev)
+    ws = bd.new_workspace(S, H, hd)
+    pool.decode_attention_ex(0, torch.from_numpy(q).to(dev), torch.from_numpy(tables).to(dev),
+                             torch.from_numpy(lens).to(dev), out, ws, seq_begin=torch.from_numpy(begin).to(dev),
+                             pieces=torch.from_numpy(pcs.reshape(-1)).to(dev), splits=splits)
+    torch.cuda.synchronize()
+    assert bd.workspace_status(ws) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    ref = np.zeros((S, H, hd))
+    for s in range(S):
+        T, b0 = int(lens[s]), int(begin[s])
+        for h in range(H):
+            k = rf.gather_sequence(kp, tables[s], T, h, "HND", H, B, hd)[b0:]
+            v = rf.gather_sequence(vp, tables[s], T, h, "HND", H, B, hd)[b0:]
+            x = sl2 * (k @ q[s, h].astype(np.float64))
+            ms, ls, os_ = [], [], []
+            if b0 > 0:
+                for kk in range(splits):
+                    m = float(pcs[s, h, kk, hd])
+                    if m == -np.inf:
+                        continue
+                    ms.append(m)
+                    ls.append(float(pcs[s, h, kk, hd + 1]))
+                    os_.append(pcs[s, h, kk, :hd].astype(np.float64))
+            M = max(ms + ([x.max()] if len(x) else []))
+            num = sum(2.0 ** (m - M) * o for m, o in zip(ms, os_)) + (2.0 ** (x - M)) @ v if len(x) else \
+                sum(2.0 ** (m - M) * o for m, o in zip(ms, os_))
+            den = sum(2.0 ** (m - M) * l for m, l in zip(ms, ls)) + (np.exp2(x - M).sum() if len(x) else 0.0)
+            ref[s, h] = num / den
+    assert_close(got, ref, f"merge splits={splits}")
+
+
+@pytest.mark.parametrize("hd", [64, 256])
+def test_pieces_refused_for_other_head_dims(hd):
+    """The cascade is built for head_dim 128: other pools refuse pieces before any launch."""
+    H, B, S = 2, 16, 2
+    kv = torch.zeros((8, H, B, hd), dtype=torch.float16, device="cuda")
+    pool = pkv.Pool(1, 8, B, H, hd, "HND", k_pool=kv, v_pool=kv.clone())
+    q = torch.zeros((S, H, hd), dtype=torch.float16, device="cuda")
+    out = torch.empty_like(q)
+    tab = torch.zeros((S, 2), dtype=torch.int32, device="cuda")
+    lens = torch.full((S,), 20, dtype=torch.int32, device="cuda")
+    begin = torch.full((S,), 16, dtype=torch.int32, device="cuda")
+    pcs = torch.zeros((S * H * bd.MAX_PREFIX_SPLITS * (hd + 4),), device="cuda")
+    with pytest.raises(bd.PkvError) as e:
+        pool.decode_attention_ex(0, q, tab, lens, out, bd.new_workspace(S, H, hd), seq_begin=begin, pieces=pcs,
+                                 splits=1)
+    assert e.value.code == "UNSUPPORTED", str(e.value)
