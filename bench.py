@@ -37,7 +37,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak); seq·steps/s at 7B shape"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.txt")
+TRAFFIC_FILES = {"f16": os.path.join(ROOT, "profiles", "decode_attention_traffic.txt"),
+                 "e4m3": os.path.join(ROOT, "profiles", "decode_attention_e4m3_traffic.txt")}
 KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_88_gb300", "csrc", "decode_attention.cu")
 
 
@@ -90,8 +91,9 @@ def device_code_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_traffic(bytes_per_launch: float):
-    """DRAM bytes per launch from the committed ncu summary, scaled to this launch's KV bytes.
+def kernel_traffic(bytes_per_launch: float, kv_dtype: str = "f16"):
+    """DRAM bytes per launch from the committed ncu summary of the kernel variant for
+    kv_dtype, scaled to this launch's KV bytes.
 
     The summary holds dram__bytes_read.sum + dram__bytes_write.sum of one captured
     launch and that launch's algorithmic KV bytes; traffic grows in proportion to
@@ -99,7 +101,7 @@ def kernel_traffic(bytes_per_launch: float):
     changed since the capture (the hash of its device code is recorded in the summary).
     """
     try:
-        text = open(TRAFFIC_FILE).read()
+        text = open(TRAFFIC_FILES[kv_dtype]).read()
         vals = {}
         for line in text.splitlines():
             if ":" in line and not line.lstrip().startswith("#"):
@@ -363,7 +365,7 @@ def run_ours(args):
     mean_launch_ms = attn_ms_total / n_attn
     achieved = (attn_launch_bytes + extra) / (mean_launch_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = None if cascading else kernel_traffic(attn_launch_bytes + extra)
+    traffic = None if cascading else kernel_traffic(attn_launch_bytes + extra, w.kv_dtype)
 
     # ---- end to end through the public API: inputs from pinned host memory, output read back.
     # A serving loop overlaps the transfers with the steps: a copy stream brings step n+1's
@@ -433,7 +435,8 @@ def run_ours(args):
         vs = eng.v_scale[0].cpu().numpy() if eng.v_scale is not None else None
         cpu = cpu_baseline_oracle(w, kl, vl, eng.tables.copy(), eng.lens.copy(), args.cpu_seconds, ks, vs)
 
-    info = pkv.decode_launch_info(S, D)
+    info = pkv.decode_launch_info(S, D, w.kv_dtype)
+    kname = f"decode_attention_kernel<{D}{', E4M3' if w.kv_dtype == 'e4m3' else ''}>"
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -458,8 +461,8 @@ def run_ours(args):
                             "prefix_tokens": int(eng.plan_prefix)}} if cascading else {}),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                         "kernel": ("prefix pass + decode_attention_kernel<128> (distinct KV bytes)"
-                                    if cascading else "decode_attention_kernel<128>"), "launches": n_attn,
+                         "kernel": (f"prefix pass + {kname} (distinct KV bytes)" if cascading else kname),
+                         "launches": n_attn,
                          "mean_launch_us": 1e3 * mean_launch_ms, "bytes_per_launch": attn_launch_bytes + extra,
                          "grid_ctas": info["grid_ctas"], "ctas_per_sm": info["ctas_per_sm"]},
             "clocks": clocks,

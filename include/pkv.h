@@ -459,9 +459,13 @@ pkv_status pkv_pool_decode_attention(const pkv_pool *pool, int32_t layer, const 
                                      void *out, void *workspace, size_t workspace_bytes,
                                      void *stream);
 
-/* Launch geometry of pkv_decode_attention on the current device, for
- * reporting: CTAs per launch, CTAs per SM, and the SM count. */
-pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t *grid_ctas,
+/* Launch geometry of the decode attention kernel on the current device, for
+ * reporting: CTAs per launch, CTAs per SM, and the SM count, for a cache of
+ * kv_dtype (PKV_KV_F16 or PKV_KV_E4M3: the two variants differ in registers,
+ * pipeline depth and so in CTAs per SM). Any output pointer may be NULL.
+ * PKV_ERR_INVALID_ARG for an unsupported head_dim, a num_seqs outside
+ * [0, 4096] or an unknown kv_dtype (checked before any CUDA call). */
+pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t kv_dtype, int32_t *grid_ctas,
                                   int32_t *ctas_per_sm, int32_t *num_sms);
 
 #ifdef __cplusplus

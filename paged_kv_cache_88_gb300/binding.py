@@ -101,7 +101,7 @@ def lib() -> ctypes.CDLL:
             "pkv_decode_workspace_bytes": (sz, [i32, i32, i32]),
             "pkv_check_wait_limit": (i32, [vp, vp]),
             "pkv_pool_decode_attention": (i32, [vp, i32, vp, vp, i32, vp, i32, f32, vp, vp, sz, vp]),
-            "pkv_decode_launch_info": (i32, [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+            "pkv_decode_launch_info": (i32, [i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                              ctypes.POINTER(i32)]),
             "pkv_decode_append_attention": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, f32, vp, vp, sz, vp]),
             "pkv_decode_attention_static": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32, vp,
@@ -476,7 +476,9 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, num_blo
     return out
 
 
-def decode_launch_info(num_seqs: int, head_dim: int) -> dict:
+def decode_launch_info(num_seqs: int, head_dim: int, kv_dtype: str = "f16") -> dict:
+    """Grid of the decode attention kernel for a cache of kv_dtype ("f16" or "e4m3")."""
     g, per, sms = i32(), i32(), i32()
-    check(lib().pkv_decode_launch_info(num_seqs, head_dim, ctypes.byref(g), ctypes.byref(per), ctypes.byref(sms)))
+    check(lib().pkv_decode_launch_info(num_seqs, head_dim, KV_DTYPES[kv_dtype] if kv_dtype in KV_DTYPES else -1,
+                                       ctypes.byref(g), ctypes.byref(per), ctypes.byref(sms)))
     return {"grid_ctas": g.value, "ctas_per_sm": per.value, "num_sms": sms.value}

@@ -66,6 +66,11 @@ using namespace pkv;
 #ifndef PKV_ATTN_MIN_CTAS
 #define PKV_ATTN_MIN_CTAS 3
 #endif
+// The E4M3 tile is half the bytes of the fp16 one and its consumers are issue-bound, so
+// that variant runs 4 CTAs per SM (96 registers a thread) with one more stage each.
+#ifndef PKV_ATTN_MIN_CTAS_Q8
+#define PKV_ATTN_MIN_CTAS_Q8 4
+#endif
 #ifndef PKV_ATTN_ACQREL
 #define PKV_ATTN_ACQREL 1
 #endif
@@ -78,7 +83,7 @@ constexpr int kGroups = kConsumerWarps * 4;       // 8-lane groups
 constexpr int kTokPerGroup = kTile / kGroups;     // rows of a tile one group owns
 constexpr int kStagesF16 = PKV_ATTN_STAGES;
 #ifndef PKV_ATTN_STAGES_Q8
-#define PKV_ATTN_STAGES_Q8 4
+#define PKV_ATTN_STAGES_Q8 3
 #endif
 constexpr int kStagesQ8 = PKV_ATTN_STAGES_Q8;
 static_assert(kTile % kGroups == 0 && kTokPerGroup >= 1 && kTokPerGroup <= 4, "tile / group split");
@@ -320,7 +325,7 @@ __device__ __forceinline__ void merge_prefix(const Params &p, const float *stage
 }
 
 template <int D, bool Q8>
-__global__ void __launch_bounds__(kThreads, D >= 256 ? 1 : PKV_ATTN_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, D >= 256 ? 1 : (Q8 ? PKV_ATTN_MIN_CTAS_Q8 : PKV_ATTN_MIN_CTAS))
 decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const Params p) {
     using St = Stage<D, Q8>;
@@ -643,36 +648,38 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             }
         }
         // this group's rows of the tile: grp, grp + kGroups, ...; kr/vr hold each
-        // chunk's 8 elements as four fp16 pairs
+        // chunk's 8 elements as four fp16 pairs (fp16 cache), kcw/vcw the row's E4M3
+        // codes, four to a word, converted where they are used (fewer live registers)
         const bool full = ntok == kTile;
         bool vld[kTokPerGroup];
         uint32_t kr[kTokPerGroup][NCH][4], vr[kTokPerGroup][NCH][4];
+        uint32_t kcw[kTokPerGroup][NCH * 2], vcw[kTokPerGroup][NCH * 2];
         float ksc[kTokPerGroup], vsc[kTokPerGroup];
+        // element pair e of chunk ch of row u as fp16x2
+        auto kpair = [&](int u, int ch, int e) {
+            if constexpr (Q8) return q8::e4m3x2_to_half2(kcw[u][ch * 2 + (e >> 1)] >> (16 * (e & 1)));
+            else return kr[u][ch][e];
+        };
+        auto vpair = [&](int u, int ch, int e) {
+            if constexpr (Q8) return q8::e4m3x2_to_half2(vcw[u][ch * 2 + (e >> 1)] >> (16 * (e & 1)));
+            else return vr[u][ch][e];
+        };
 #pragma unroll
         for (int u = 0; u < kTokPerGroup; ++u) {
             const int row = grp + kGroups * u;
             vld[u] = full || row < ntok;
             if constexpr (Q8) {
-                uint32_t kc[NCH * 2], vc[NCH * 2];   // 4 codes per word
                 if constexpr (NCH == 2) {
                     const uint4 a = ptx::lds128(kb + row * St::kRow + j * 16);
                     const uint4 b = ptx::lds128(vb + row * St::kRow + j * 16);
-                    kc[0] = a.x; kc[1] = a.y; kc[2] = a.z; kc[3] = a.w;
-                    vc[0] = b.x; vc[1] = b.y; vc[2] = b.z; vc[3] = b.w;
+                    kcw[u][0] = a.x; kcw[u][1] = a.y; kcw[u][2] = a.z; kcw[u][3] = a.w;
+                    vcw[u][0] = b.x; vcw[u][1] = b.y; vcw[u][2] = b.z; vcw[u][3] = b.w;
                 } else {
                     const uint2 a = ptx::lds64(kb + row * St::kRow + j * 8);
                     const uint2 b = ptx::lds64(vb + row * St::kRow + j * 8);
-                    kc[0] = a.x; kc[1] = a.y;
-                    vc[0] = b.x; vc[1] = b.y;
+                    kcw[u][0] = a.x; kcw[u][1] = a.y;
+                    vcw[u][0] = b.x; vcw[u][1] = b.y;
                 }
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int w = ch * 2 + (e >> 1), sh = 16 * (e & 1);
-                        kr[u][ch][e] = q8::e4m3x2_to_half2(kc[w] >> sh);
-                        vr[u][ch][e] = q8::e4m3x2_to_half2(vc[w] >> sh);
-                    }
                 ksc[u] = ptx::ldsf(kb + St::kScales + row * 4);
                 vsc[u] = ptx::ldsf(kb + St::kScales + kTile * 4 + row * 4);
             } else {
@@ -697,7 +704,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     uint16_t klo, khi;
-                    ptx::split_half2(kr[u][ch][e], klo, khi);
+                    ptx::split_half2(kpair(u, ch, e), klo, khi);
                     a0 = ptx::fma_f16_f32(qlo[ch * 4 + e], klo, a0);
                     a1 = ptx::fma_f16_f32(qhi[ch * 4 + e], khi, a1);
                 }
@@ -732,7 +739,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(vr[u][ch][e]),
+                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(vpair(u, ch, e)),
                                                    o[ch * 4 + e]);
         } else {
 #pragma unroll
@@ -742,7 +749,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(vr[u][ch][e]),
+                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(vpair(u, ch, e)),
                                                    o[ch * 4 + e]);
             }
         }
@@ -1057,15 +1064,16 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t h
     return workspace_bytes_for(num_seqs, num_heads, head_dim, sms);
 }
 
-pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t *grid_ctas, int32_t *ctas_per_sm,
-                                  int32_t *num_sms) {
+pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t kv_dtype, int32_t *grid_ctas,
+                                  int32_t *ctas_per_sm, int32_t *num_sms) {
     if (!supported_head_dim(head_dim) || num_seqs < 0 || num_seqs > kMaxSeqs)
         return fail(PKV_ERR_INVALID_ARG, "bad sizes");
+    if (kv_dtype != PKV_KV_F16 && kv_dtype != PKV_KV_E4M3) return fail(PKV_ERR_INVALID_ARG, "bad kv_dtype");
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(PKV_ERR_CUDA, "no CUDA device");
     int g = 0, per = 0, sms = 0;
     size_t smem = 0;
-    pkv_status st = launch_shape(dev, head_dim, false, num_seqs, &g, &per, &sms, &smem);
+    pkv_status st = launch_shape(dev, head_dim, kv_dtype == PKV_KV_E4M3, num_seqs, &g, &per, &sms, &smem);
     if (st != PKV_OK) return st;
     if (grid_ctas) *grid_ctas = g;
     if (ctas_per_sm) *ctas_per_sm = per;

@@ -243,6 +243,15 @@ def test_device_ops_refuse_host_only_pool():
     assert rc == 1
 
 
+def test_launch_info_checks_arguments_before_any_cuda_call():
+    for args in ((32, 96, 0), (-1, 128, 0), (5000, 128, 0), (32, 128, 2), (32, 128, -1)):
+        rc = pkv.lib().pkv_decode_launch_info(*args, None, None, None)
+        assert rc == 1, args
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.decode_launch_info(32, 128, "bf16")
+    assert e.value.code == "INVALID_ARG"
+
+
 # ------------------------------------------------------------------ prefix cache: library vs oracle
 
 def test_block_hash_matches_oracle():

@@ -570,6 +570,17 @@ def test_attention_ex_rejects_unknown_flags():
     assert e.value.code == "INVALID_ARG"
 
 
+def test_launch_info_per_cache_dtype():
+    """Persistent grid = CTAs per SM x SMs; the E4M3 variant (96 registers, 3 stages of half
+    the bytes) fits more CTAs per SM than the fp16 one."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    f = pkv.decode_launch_info(32, 128, "f16")
+    e = pkv.decode_launch_info(32, 128, "e4m3")
+    for i in (f, e):
+        assert i["num_sms"] == sms and i["grid_ctas"] == i["ctas_per_sm"] * sms and i["ctas_per_sm"] >= 1
+    assert e["ctas_per_sm"] > f["ctas_per_sm"]
+
+
 def test_wait_limit_flags_timeout_and_context_survives():
     """Failure detection without a fault: a wait that nothing satisfies gives up after its
     limit, flags PKV_DEV_TIMEOUT, and the context keeps working (an attention step after
