@@ -139,6 +139,15 @@ struct Stage {
 
 __host__ __device__ constexpr int piece_stride(int D) { return D + 4; }
 
+// Element pair e (0..3) of chunk ch of one K or V row as fp16x2: from the fp16 words
+// (fp16 cache), or converted from the row's E4M3 codes, four to a word, where it is used.
+template <bool Q8, int NCH>
+__device__ __forceinline__ uint32_t pair_of(const uint32_t (&codes)[NCH * 2], const uint32_t (&halves)[NCH][4],
+                                            int ch, int e) {
+    if constexpr (Q8) return q8::e4m3x2_to_half2(codes[ch * 2 + (e >> 1)] >> (16 * (e & 1)));
+    else return halves[ch][e];
+}
+
 // The cascade's prefix pieces of the current (s, h), staged in shared memory while its
 // tiles stream (fp16 caches only: the cascade is built for them).
 template <int D, bool Q8>
@@ -655,15 +664,6 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         uint32_t kr[kTokPerGroup][NCH][4], vr[kTokPerGroup][NCH][4];
         uint32_t kcw[kTokPerGroup][NCH * 2], vcw[kTokPerGroup][NCH * 2];
         float ksc[kTokPerGroup], vsc[kTokPerGroup];
-        // element pair e of chunk ch of row u as fp16x2
-        auto kpair = [&](int u, int ch, int e) {
-            if constexpr (Q8) return q8::e4m3x2_to_half2(kcw[u][ch * 2 + (e >> 1)] >> (16 * (e & 1)));
-            else return kr[u][ch][e];
-        };
-        auto vpair = [&](int u, int ch, int e) {
-            if constexpr (Q8) return q8::e4m3x2_to_half2(vcw[u][ch * 2 + (e >> 1)] >> (16 * (e & 1)));
-            else return vr[u][ch][e];
-        };
 #pragma unroll
         for (int u = 0; u < kTokPerGroup; ++u) {
             const int row = grp + kGroups * u;
@@ -704,7 +704,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     uint16_t klo, khi;
-                    ptx::split_half2(kpair(u, ch, e), klo, khi);
+                    ptx::split_half2(pair_of<Q8, NCH>(kcw[u], kr[u], ch, e), klo, khi);
                     a0 = ptx::fma_f16_f32(qlo[ch * 4 + e], klo, a0);
                     a1 = ptx::fma_f16_f32(qhi[ch * 4 + e], khi, a1);
                 }
@@ -739,7 +739,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(vpair(u, ch, e)),
+                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e)),
                                                    o[ch * 4 + e]);
         } else {
 #pragma unroll
@@ -749,7 +749,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(vpair(u, ch, e)),
+                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e)),
                                                    o[ch * 4 + e]);
             }
         }
