@@ -715,7 +715,11 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             dot += __shfl_xor_sync(0xffffffffu, dot, 1);
             if constexpr (Q8) dot *= ksc[u];
             x[u] = vld[u] ? dot * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, x[u]);
+            // E4M3: the reference max covers x + log2(V row scale), so that every weight
+            // 2^(x - m) * scale is at most 1 and fits fp16 for the p.V products
+            // (a scale of 0, which the quantiser never writes, counts as 2^-100)
+            if constexpr (Q8) mx = fmaxf(mx, vld[u] ? x[u] + ptx::lg2(fmaxf(vsc[u], 0x1p-100f)) : -INFINITY);
+            else mx = fmaxf(mx, x[u]);
         }
         if (mx > m) {                          // new running max: rescale (group-uniform branch)
             const float alpha = ptx::ex2(m - mx);
@@ -730,9 +734,27 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         for (int u = 0; u < kTokPerGroup; ++u) {
             pw[u] = vld[u] ? ptx::ex2(x[u] - m) : 0.f;
             l += pw[u];
-            if constexpr (Q8) pw[u] *= vsc[u];   // the V row's scale folds into its weight
         }
-        if (full) {
+        if constexpr (Q8) {
+            // o += (weight x V row scale) in fp16 x the row's codes as fp16 (exact), one
+            // mixed-precision FMA per element with fp32 accumulation
+            uint16_t wh[kTokPerGroup];
+#pragma unroll
+            for (int u = 0; u < kTokPerGroup; ++u) wh[u] = __half_as_ushort(__float2half_rn(pw[u] * vsc[u]));
+#pragma unroll
+            for (int u = 0; u < kTokPerGroup; ++u) {
+                if (!full && !vld[u]) continue;
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint16_t vlo, vhi;
+                        ptx::split_half2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e), vlo, vhi);
+                        o[ch * 4 + e].x = ptx::fma_f16_f32(wh[u], vlo, o[ch * 4 + e].x);
+                        o[ch * 4 + e].y = ptx::fma_f16_f32(wh[u], vhi, o[ch * 4 + e].y);
+                    }
+            }
+        } else if (full) {
 #pragma unroll
             for (int u = 0; u < kTokPerGroup; ++u)
 #pragma unroll

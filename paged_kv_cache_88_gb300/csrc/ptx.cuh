@@ -209,6 +209,14 @@ __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontr
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// log2(x) (lg2.approx); used only to place a softmax reference, where a small error
+// moves the reference, not the result
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // 2^x with the SFU (max relative error about 2^-22); 2^-inf = +0.
 __device__ __forceinline__ float ex2(float x) {
     float y;

@@ -246,6 +246,71 @@ def test_e4m3_pool_rules():
     del q
 
 
+def test_e4m3_row_scales_over_many_octaves():
+    """V row scales from 2^-40 to 2^6 within one sequence, a sequence whose V scales are
+    all tiny, a zero row (codes 0, scale 1), a row whose V scale is 0, one-token and empty
+    contexts, and NaN codes and scales past every context (never read): the attention of
+    code x scale, each (sequence, head) within the usual 2e-3 abs + 1e-2 rel taken
+    relative to its largest output (plus the fp16 subnormal step)."""
+    from oracle import fp8
+    rng = np.random.default_rng(41)
+    H, D, B = 2, 128, 16
+    lens = [37, 200, 513, 1, 0]
+    nb = [-(-t // B) for t in lens]
+    N = sum(nb) + 3
+    perm = rng.permutation(N)
+    tab = np.zeros((len(lens), max(nb)), dtype=np.int32)
+    i = 0
+    for s_, n_ in enumerate(nb):
+        tab[s_, :n_] = perm[i:i + n_]
+        i += n_
+    kc = rng.integers(0, 256, size=(N, H, B, D), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(N, H, B, D), dtype=np.uint8)
+    for c_ in (kc, vc):
+        c_[(c_ & 0x7F) == 0x7F] ^= 1                       # no NaN codes inside the contexts
+    ks = np.exp2(rng.uniform(-7, -5, size=(N, H, B))).astype(np.float32)
+    vs = np.exp2(rng.uniform(-40, 6, size=(N, H, B))).astype(np.float32)
+    lo = {1: (-22, -20), 2: (-2, 6), 3: (-30, -30)}
+    for s_, T in enumerate(lens):
+        for t in range(T):
+            b_, o_ = tab[s_, t // B], t % B
+            if s_ in lo:
+                vs[b_, :, o_] = np.exp2(rng.uniform(*lo[s_], size=H))
+        if T % B:                                          # past the context: NaN codes and scales
+            b_ = tab[s_, T // B]
+            kc[b_, :, T % B:] = 0x7F
+            vc[b_, :, T % B:] = 0xFF
+            ks[b_, :, T % B:] = np.nan
+            vs[b_, :, T % B:] = np.nan
+    b_, o_ = tab[2, 100 // B], 100 % B                     # a zero row
+    kc[b_, :, o_] = 0
+    vc[b_, :, o_] = 0
+    ks[b_, :, o_] = 1.0
+    vs[b_, :, o_] = 1.0
+    b_, o_ = tab[2, 300 // B], 300 % B                     # a V scale of 0
+    vs[b_, :, o_] = 0.0
+    q = rng.standard_normal((len(lens), H, D)).astype(np.float16)
+    dev = "cuda"
+    pool = pkv.Pool(1, N, B, H, D, "HND", k_pool=torch.from_numpy(kc).to(dev), v_pool=torch.from_numpy(vc).to(dev),
+                    kv_dtype="e4m3", k_scale=torch.from_numpy(ks).to(dev), v_scale=torch.from_numpy(vs).to(dev))
+    qd = torch.from_numpy(q).to(dev)
+    out = torch.full_like(qd, float("nan"))
+    ws = pkv.new_workspace(len(lens), H, D, dev)
+    pool.decode_attention(0, qd, torch.from_numpy(tab).to(dev), torch.from_numpy(np.array(lens, dtype=np.int32)).to(dev),
+                          out, ws)
+    torch.cuda.synchronize()
+    assert pkv.workspace_status(ws) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    ref = fp8.decode_attention(q, kc, vc, ks, vs, tab, np.array(lens), B)
+    assert np.all(got[4] == 0)
+    for s_ in range(len(lens) - 1):
+        for h in range(H):
+            big = np.abs(ref[s_, h]).max()
+            err = np.abs(got[s_, h] - ref[s_, h])
+            assert (err <= 2e-3 * big + 1e-2 * np.abs(ref[s_, h]) + 6e-8).all(), \
+                (s_, h, float(err.max()), float(big))
+
+
 # ----------------------------------------------------------------------------- raw-call edge cases
 
 def _raw_case(lens, H=3, D=128, B=16, N=None, seed=0, layout="NHD", canary_nan=True):
@@ -341,6 +406,25 @@ def test_many_short_sequences():
     out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N)
     assert st == 0
     assert_close(out, rc.decode_attention(q, kp, vp, tab, ln, B), "many short")
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_maximum_batch(layout):
+    """The largest batch one launch takes (4096 sequences: the per-sequence lengths, starts
+    and tile offsets fill the most shared memory), lengths 0..48 with empty contexts among
+    them; one more sequence is refused."""
+    rng = np.random.default_rng(31)
+    lens = rng.integers(0, 49, size=4096).tolist()
+    q, kp, vp, tab, ln, B, N = _raw_case(lens, H=2, D=128, B=16, canary_nan=False, seed=32, layout=layout)
+    out, st, ws = _gpu_attn(q, kp, vp, tab, ln, B, N, layout)
+    assert st == 0
+    assert np.all(out[ln == 0] == 0)
+    assert_close(out, rc.decode_attention(q, kp, vp, tab, ln, B, layout), f"4096 sequences {layout}")
+    q1 = np.zeros((4097, 2, 128), dtype=np.float16)
+    t1 = np.zeros((4097, tab.shape[1]), dtype=np.int32)
+    with pytest.raises(pkv.binding.PkvError) as e:
+        _gpu_attn(q1, kp, vp, t1, np.zeros(4097, dtype=np.int32), B, N, layout, ws=ws)
+    assert e.value.code == "INVALID_ARG"
 
 
 def test_bad_block_id_is_flagged_not_faulted():
