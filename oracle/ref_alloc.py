@@ -28,7 +28,7 @@ What it follows:
   blocks with no reference stay evictable in LRU order and a later hit revives
   them (icman.com.cn/news/78786 §3.1-§3.4; hnwysp.cn/news/103996 §4.3).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * Allocation is all-or-nothing and a failed call changes nothing.
 * COW fires iff the refcount of the block being written is > 1 at the moment of
