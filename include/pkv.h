@@ -407,11 +407,18 @@ int32_t pkv_prefix_splits(int32_t num_groups, int32_t num_heads, int32_t max_pre
  * than PKV_MAX_GROUP_SEQS members or a prefix not in whole blocks inside the
  * table is flagged PKV_DEV_BAD_LENGTH and writes no pieces. fp16 products,
  * fp32 accumulation, weights enter P V in fp16. The pool must be fp16, HND,
- * head_dim 128 (UNSUPPORTED otherwise). */
+ * head_dim 128 (UNSUPPORTED otherwise). flags: 0, or PKV_ATTN_INPUTS_EARLY:
+ * the groups, the block tables and the prefix's cached K/V are read -- and the
+ * K/V tiles' loads issued -- before the kernel that precedes it on the stream
+ * has finished; q is read and the pieces written only after. The caller
+ * promises that the preceding kernel writes none of the former (e.g. it is the
+ * previous layer's private pass, which writes that layer's cache, out and the
+ * workspace). Other flag bits: INVALID_ARG. */
 pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void *q,
                                 const pkv_prefix_group *groups, int32_t num_groups, int32_t splits,
                                 const int32_t *block_tables, int32_t max_blocks, int32_t num_seqs, float scale,
-                                void *pieces, size_t pieces_bytes, uint32_t *status, void *stream);
+                                void *pieces, size_t pieces_bytes, uint32_t *status, uint32_t flags,
+                                void *stream);
 
 /* pkv_decode_append_attention and pkv_pool_decode_attention in one entry, with
  * the private half of the cascade. k_new, v_new, slot_mapping: all NULL = no

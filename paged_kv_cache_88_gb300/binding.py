@@ -117,7 +117,8 @@ def lib() -> ctypes.CDLL:
             "pkv_cascade_plan": (i32, [vp, i32, vp, i32, i32, i32, i32, vp, i32, ctypes.POINTER(i32), vp]),
             "pkv_prefix_pieces_bytes": (sz, [i32, i32, i32]),
             "pkv_prefix_splits": (i32, [i32, i32, i32]),
-            "pkv_prefix_attention": (i32, [vp, i32, vp, vp, i32, i32, vp, i32, i32, f32, vp, sz, vp, vp]),
+            "pkv_prefix_attention": (i32, [vp, i32, vp, vp, i32, i32, vp, i32, i32, f32, vp, sz, vp,
+                                           ctypes.c_uint32, vp]),
             "pkv_decode_attention_ex": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32, f32, vp, vp,
                                               sz, ctypes.c_uint32, vp]),
         }
@@ -353,15 +354,16 @@ class Pool:
                                           float(scale), _ptr(out), _ptr(status), _stream(stream)))
 
     def prefix_attention(self, layer: int, q, groups_dev, num_groups: int, splits: int, block_tables, pieces,
-                         status, scale: float = 0.0, stream=None) -> None:
-        """The cascade's prefix pass (pkv_prefix_attention); ``groups_dev``: device int32 [G, 4]."""
+                         status, scale: float = 0.0, flags: int = 0, stream=None) -> None:
+        """The cascade's prefix pass (pkv_prefix_attention); ``groups_dev``: device int32 [G, 4];
+        ``flags`` = ATTN_INPUTS_EARLY lets the launch start reading before its predecessor ends."""
         for t, dt, name in ((q, "float16", "q"), (groups_dev, "int32", "groups"),
                             (block_tables, "int32", "block_tables"), (status, "int32", "status")):
             _require(t, dt, name)
         check(lib().pkv_prefix_attention(self._h, layer, _ptr(q), _ptr(groups_dev), num_groups, splits,
                                          _ptr(block_tables), block_tables.shape[1], q.shape[0], float(scale),
                                          _ptr(pieces), pieces.numel() * pieces.element_size(), _ptr(status),
-                                         _stream(stream)))
+                                         flags, _stream(stream)))
 
     def decode_attention_ex(self, layer: int, q, block_tables, context_lens, out, workspace, k_new=None, v_new=None,
                             slot_mapping=None, seq_begin=None, pieces=None, splits: int = 0, scale: float = 0.0,

@@ -81,6 +81,7 @@ struct PrefillParams {
     uint32_t *status;
     int32_t S, H, max_blocks, B, N, splits;
     float scale_log2;
+    int32_t early;            // prefix pass: tables, groups and K/V read before the grid dependency
 };
 
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -240,8 +241,15 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
     const int32_t H = p.H, B = p.B;
     const int32_t cap = p.max_blocks * B;
 
-    ptx::grid_dependency_wait();
-    ptx::launch_dependents();   // successors start once this grid's inputs are final
+    // The prefix pass may start early (p.early): groups, tables and the prefix's K/V --
+    // which the preceding kernel does not write -- are read, and the K/V tiles' loads
+    // issued, before the grid dependency resolves; q is loaded and the pieces written
+    // only after it. Dependents are let launch only once it has resolved.
+    const bool early = kPrefix && p.early != 0;
+    if (!early) {
+        ptx::grid_dependency_wait();
+        ptx::launch_dependents();   // successors start once this grid's inputs are final
+    }
     // Query tile x covers query rows q0[x] .. q0[x] + rows[x] - 1 (row r: query row
     // q0[x] + r); row r of tile x sees keys t <= its limit: its own position pos0[x] + r
     // (prefill) or every key of the split (prefix). The CTA reads keys [kv_begin,
@@ -256,6 +264,10 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         if (g.num_seqs < 1 || g.num_seqs > kQT || g.first_seq < 0 || g.first_seq > p.S - g.num_seqs || P < 0 ||
             P > cap || P % B != 0) {
             if (tid == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            if (early) {
+                ptx::grid_dependency_wait();
+                ptx::launch_dependents();
+            }
             return;
         }
         srow = g.first_seq;
@@ -268,6 +280,10 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         kv_end_x[0] = kv_end;
         if (kv_begin >= kv_end) {
             // no keys in this split: an empty piece for every member
+            if (early) {
+                ptx::grid_dependency_wait();
+                ptx::launch_dependents();
+            }
             for (int32_t i = tid; i < rows[0] * (kD + 4); i += kThreads) {
                 const int32_t r = i / (kD + 4), c = i - r * (kD + 4);
                 p.pieces[(((size_t)(q0[0] + r) * H + h) * PKV_MAX_PREFIX_SPLITS + split) * (kD + 4) + c] =
@@ -332,17 +348,29 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         // is refilled as soon as its S MMAs are done, whatever the V side waits for.
         const bool is_k = warp == 9;
         const int32_t rowsb = B < kKT ? B : kKT;       // rows per box; B is a power of two, 8..256
-        if (is_k && lane == 0) {
-            ptx::mbar_arrive_expect_tx(BAR(kQFull), (has_b ? 2 : 1) * kTileBytes);
-            for (int x = 0; x < kTiles; ++x)
-                if (nkt_x[x] > 0)
-                    for (int half = 0; half < 2; ++half)
-                        ptx::tma_load_3d(sQ(x) + half * kSub, &qmap, half * kHalf, h, q0[x], BAR(kQFull));
-        }
+        auto issue_q = [&] {
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(BAR(kQFull), (has_b ? 2 : 1) * kTileBytes);
+                for (int x = 0; x < kTiles; ++x)
+                    if (nkt_x[x] > 0)
+                        for (int half = 0; half < 2; ++half)
+                            ptx::tma_load_3d(sQ(x) + half * kSub, &qmap, half * kHalf, h, q0[x], BAR(kQFull));
+            }
+        };
+        // early: Q once the K tiles that fit the two slots are issued (before any wait
+        // for a free slot, which needs Q's first S done)
+        const int32_t jq = early ? min(nkt, 2) : 0;
+        auto q_after_wait = [&] {
+            ptx::grid_dependency_wait();
+            ptx::launch_dependents();
+            issue_q();
+        };
+        if (is_k && !early) issue_q();
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         const int full0 = is_k ? kKFull : kVFull;
         const int free0 = is_k ? kKFree : kVFree;     // slot b is free once the MMAs of tile j-2 reading it are done
         for (int32_t j = 0; j < nkt; ++j) {
+            if (is_k && early && j == jq) q_after_wait();
             const int b = j & 1;
             const int32_t t0 = kv_begin + j * kKT;
             const int32_t ntok = min(kKT, kv_end - t0);
@@ -367,6 +395,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
                 for (int half = 0; half < 2; ++half)
                     ptx::tma_load_2d(dst + half * kSub, map, half * kHalf, y, BAR(full0 + b));
         }
+        if (is_k && early && jq == nkt) q_after_wait();
         // the last loads into each slot (and Q) have landed before the CTA may exit
         if (is_k) drain_wait(BAR(kQFull), 0);
         for (int32_t j = nkt - 2 < 0 ? 0 : nkt - 2; j < nkt; ++j) drain_wait(BAR(full0 + (j & 1)), (j >> 1) & 1);
@@ -427,6 +456,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         // row r (tensor-memory lane r) is shared by warps q and q + 4 (q = r / 32), each
         // taking one 64-key half of every S tile and one 64-column half of O; the two
         // exchange their row max (and, at the end, their sums) through shared memory.
+        if (early) ptx::grid_dependency_wait();    // the pieces are written only after it
         const int hf = warp >> 2, quad = warp & 3;
         const int32_t r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -813,9 +843,10 @@ pkv_status pkv_prefill_attention(const pkv_pool *pool, int32_t layer, const void
 pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void *q, const pkv_prefix_group *groups,
                                 int32_t num_groups, int32_t splits, const int32_t *block_tables, int32_t max_blocks,
                                 int32_t num_seqs, float scale, void *pieces, size_t pieces_bytes, uint32_t *status,
-                                void *stream) {
+                                uint32_t flags, void *stream) {
     pkv_status st = check_pool(pool, layer, "the prefix pass");
     if (st != PKV_OK) return st;
+    if (flags & ~(uint32_t)PKV_ATTN_INPUTS_EARLY) return fail(PKV_ERR_INVALID_ARG, "unknown flags %#x", flags);
     if (num_groups < 0 || num_seqs < 0 || max_blocks < 1 || splits < 1 || splits > PKV_MAX_PREFIX_SPLITS)
         return fail(PKV_ERR_INVALID_ARG, "bad sizes (splits in 1..%d)", PKV_MAX_PREFIX_SPLITS);
     if (num_groups == 0 || num_seqs == 0) return PKV_OK;
@@ -834,6 +865,7 @@ pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void 
     prm.groups = groups;
     prm.pieces = static_cast<float *>(pieces);
     prm.splits = splits;
+    prm.early = (flags & PKV_ATTN_INPUTS_EARLY) ? 1 : 0;
     const dim3 grid(splits, d.num_heads, num_groups);
     return launch_tc<true>(grid, qmap, kmap, vmap, prm, stream);
 }

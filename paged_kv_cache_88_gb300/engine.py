@@ -285,9 +285,11 @@ class DecodeEngine:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(s)
             if G:
-                # the shared prefixes once per group, then each sequence's private rest (+ append)
+                # the shared prefixes once per group, then each sequence's private rest (+ append);
+                # layers after the first follow the previous layer's private pass, which writes
+                # none of the groups, tables or this layer's cache: the prefix pass starts early
                 bd.check(L.pkv_prefix_attention(h, layer, qp + off, gp, G, splits, tp, maxb, S, sc, pp, pb, status,
-                                                sp))
+                                                bd.ATTN_INPUTS_EARLY if layer > 0 else 0, sp))
                 if not fused:
                     bd.check(L.pkv_append(h, layer, kp + off, vp + off, slp, n_slots, status, sp))
                 # after the prefix pass (which writes only pieces) the private pass may start early
@@ -371,7 +373,8 @@ class DecodeEngine:
             bd.check(L.pkv_prefix_attention(self.pool.handle, layer, q.data_ptr() + off, self.groups_d.data_ptr(),
                                             self.plan_groups, self.plan_splits, self.tables_d.data_ptr(),
                                             w.max_blocks, S, float(scale), self.pieces.data_ptr(),
-                                            self.pieces.numel(), self.status.data_ptr(), s.cuda_stream))
+                                            self.pieces.numel(), self.status.data_ptr(),
+                                            bd.ATTN_INPUTS_EARLY if early else 0, s.cuda_stream))
             bd.check(L.pkv_decode_attention_ex(
                 self.pool.handle, layer, q.data_ptr() + off, None, None, None, self.tables_d.data_ptr(),
                 w.max_blocks, self.lens_d.data_ptr(), S, self.begin_d.data_ptr(), self.pieces.data_ptr(),

@@ -149,6 +149,35 @@ def test_prefix_pieces(splits):
                     assert_close(o / l, rf.attend(c.q[s, h], kk, vv, c.scale), f"piece {(s, h, k)}")
 
 
+@pytest.mark.parametrize("splits", [1, 3])
+def test_prefix_pieces_early_start_identical(splits):
+    """Started early behind a preceding attention launch, the prefix pass writes the same
+    pieces, bit for bit, as started after it (and over pieces that launch left as NaN)."""
+    rng = np.random.default_rng(3)
+    B = 16
+    spec = forked_spec(6, 40, 60, B, rng) + forked_spec(4, 9, 30, B, rng)
+    spec[6:] = [(6, 9, T) if src is not None else (None, 0, T) for src, _, T in spec[6:]]
+    c = Case(spec, H=4, B=B, seed=4)
+    groups, begin = c.plan()
+    assert groups[:, :3].tolist() == [[0, 6, 640], [6, 4, 144]]
+    c.prefix(groups, splits)
+    torch.cuda.synchronize()
+    ref = c.pieces.clone()
+    gd = torch.from_numpy(np.ascontiguousarray(groups, dtype=np.int32)).cuda()
+    for _ in range(2):
+        c.pieces.fill_(float("nan"))
+        # a preceding kernel on the stream, then the prefix pass that may start before it ends
+        c.pool.decode_attention_ex(0, c.qd, c.tab_d, c.lens_d, torch.empty_like(c.qd), c.ws)
+        c.pool.prefix_attention(0, c.qd, gd, len(groups), splits, c.tab_d, c.pieces, c.status,
+                                flags=bd.ATTN_INPUTS_EARLY)
+        torch.cuda.synchronize()
+        assert int(c.status.item()) == 0
+        for f, n, _, _ in groups.tolist():
+            got = c.pieces.view(c.S, c.H, bd.MAX_PREFIX_SPLITS, D + 4)[f:f + n, :, :splits]
+            want = ref.view(c.S, c.H, bd.MAX_PREFIX_SPLITS, D + 4)[f:f + n, :, :splits]
+            assert torch.equal(got, want)
+
+
 @pytest.mark.parametrize("B", [8, 16, 64, 256])
 def test_cascade_matches_oracle(B):
     """Two groups, unshared sequences, and a member whose whole context is the prefix."""
@@ -223,6 +252,9 @@ def test_cascade_argument_errors():
         assert e.value.code == "INVALID_ARG"
     with pytest.raises(bd.PkvError) as e:    # pieces too small
         c.pool.prefix_attention(0, c.qd, gd, len(groups), 1, c.tab_d, c.pieces[:16], c.status)
+    assert e.value.code == "INVALID_ARG"
+    with pytest.raises(bd.PkvError) as e:    # an unknown flag bit
+        c.pool.prefix_attention(0, c.qd, gd, len(groups), 1, c.tab_d, c.pieces, c.status, flags=0x2)
     assert e.value.code == "INVALID_ARG"
     with pytest.raises(bd.PkvError) as e:    # seq_begin without pieces
         c.pool.decode_attention_ex(0, c.qd, c.tab_d, c.lens_d, torch.empty_like(c.qd), c.ws,
