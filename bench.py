@@ -490,8 +490,10 @@ def run_swap(args):
     staging = torch.empty(n * bpb, dtype=torch.uint8, device="cuda")
     blocks = torch.tensor(eng.tables[s, :n], dtype=torch.int32, device="cuda")
     st = torch.cuda.current_stream()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-    times = {"gather": [], "d2h": [], "h2d": [], "scatter": []}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    # staged: gather into device memory, one copy to pinned host (and back, then scatter);
+    # direct: the kernels write / read the pinned host buffer themselves
+    times = {"gather": [], "d2h": [], "h2d": [], "scatter": [], "gather_direct": [], "scatter_direct": []}
     for it in range(args.warmup + args.steps):
         ev[0].record(st)
         eng.pool.gather_blocks(blocks, staging, stream=st)
@@ -502,16 +504,21 @@ def run_swap(args):
         ev[3].record(st)
         eng.pool.scatter_blocks(blocks, staging, stream=st)
         ev[4].record(st)
+        eng.pool.gather_blocks(blocks, host, stream=st)
+        ev[5].record(st)
+        eng.pool.scatter_blocks(blocks, host, stream=st)
+        ev[6].record(st)
         torch.cuda.synchronize()
         if it >= args.warmup:
             for i, k in enumerate(times):
                 times[k].append(ev[i].elapsed_time(ev[i + 1]))
     nbytes = n * bpb
-    res = {k: nbytes / (statistics.median(v) / 1e3) / 1e9 for k, v in times.items()}
+    med = {k: statistics.median(v) for k, v in times.items()}
+    res = {k: nbytes / (v / 1e3) / 1e9 for k, v in med.items()}
     print(json.dumps({"metric": "swap GB/s (one sequence, all layers)", "unit": "GB/s", "bytes": nbytes,
                       "blocks": n, "config": w.describe(), **{f"{k}_gbps": v for k, v in res.items()},
-                      "swap_out_ms": statistics.median(times["gather"]) + statistics.median(times["d2h"]),
-                      "swap_in_ms": statistics.median(times["h2d"]) + statistics.median(times["scatter"])}))
+                      "swap_out_ms": med["gather"] + med["d2h"], "swap_in_ms": med["h2d"] + med["scatter"],
+                      "swap_out_direct_ms": med["gather_direct"], "swap_in_direct_ms": med["scatter_direct"]}))
 
 
 def run_prefill(args):

@@ -240,9 +240,15 @@ pkv_status pkv_copy_blocks(const pkv_pool *pool, const int32_t *pairs, int32_t n
 
 /* Swap (icman.com.cn/news/78786 §4.2: a preempted request's KV goes out to host
  * memory and comes back later). The library moves blocks between the pool and a
- * contiguous caller-owned DEVICE buffer; the caller moves that buffer to and
- * from (pinned) host memory with one cudaMemcpyAsync each way and frees /
- * allocates the blocks with pkv_free / pkv_alloc, all on the same stream.
+ * contiguous caller-owned buffer, and the caller frees / allocates the blocks
+ * with pkv_free / pkv_alloc, all on the same stream. The buffer is either
+ * device memory (the caller then moves it to and from pinned host memory with
+ * one cudaMemcpyAsync each way) or pinned host memory that is mapped into the
+ * device's address space (cudaHostAlloc / cudaHostRegister on a system with
+ * unified addressing): the kernel then reads or writes host memory directly
+ * over the host link, one pass, no staging copy. The buffer must be 16-byte
+ * aligned; any other pointer (pageable host memory, an unmapped host
+ * allocation) is refused with INVALID_ARG before anything is launched.
  * Buffer layout: for i = 0..n-1 and each layer: block blocks[i]'s K bytes, V
  * bytes, then (E4M3 pools) its K and V row scales; pkv_swap_bytes_per_block
  * gives the bytes per block over all layers. blocks: device int32 [n]; an id

@@ -331,7 +331,8 @@ class Pool:
         return int(lib().pkv_swap_bytes_per_block(self._h))
 
     def gather_blocks(self, blocks_dev, dst, status=None, stream=None) -> None:
-        """Copy the listed blocks (device int32) of every layer into ``dst`` (device bytes)."""
+        """Copy the listed blocks (device int32) of every layer into ``dst`` (device bytes, or
+        pinned host bytes mapped into the device's address space)."""
         _require(blocks_dev, "int32", "blocks")
         check(lib().pkv_gather_blocks(self._h, _ptr(blocks_dev), blocks_dev.numel(), _ptr(dst), _ptr(status),
                                       _stream(stream)))

@@ -18,6 +18,8 @@ using namespace pkv;
 constexpr int kAppendThreads = 256;
 constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
+constexpr int kSwapUnroll = 8;
+constexpr int64_t kSwapChunk = (int64_t)kCopyThreads * kSwapUnroll;   // words per CTA pass
 
 // Token i of the batch goes to slot slot_mapping[i]: physical block slot / B,
 // offset slot % B (m.lqnn.cn/news/240480 §3.2 step 3). One thread per 16-byte
@@ -154,7 +156,6 @@ swap_blocks_kernel(const int32_t *__restrict__ blocks, int32_t n, uint4 *k_pool,
     ptx::launch_dependents();   // successors start once this grid's inputs are final
     const int64_t per = 2 * block_words + 2 * scale_words;      // words of one (block, layer) in the buffer
     const int64_t jobs = (int64_t)n * num_layers;
-    const int64_t step = (int64_t)gridDim.x * blockDim.x;
     for (int64_t y = blockIdx.y; y < jobs; y += gridDim.y) {
         const int32_t i = (int32_t)(y / num_layers);
         const int32_t layer = (int32_t)(y - (int64_t)i * num_layers);
@@ -166,14 +167,30 @@ swap_blocks_kernel(const int32_t *__restrict__ blocks, int32_t n, uint4 *k_pool,
         uint4 *slot = buf + y * per;
         const int64_t pb = ((int64_t)layer * num_blocks + b) * block_words;
         const int64_t ps = ((int64_t)layer * num_blocks + b) * scale_words;
-        for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < per; w += step) {
-            uint4 *pool_word;
-            if (w < block_words) pool_word = k_pool + pb + w;
-            else if (w < 2 * block_words) pool_word = v_pool + pb + (w - block_words);
-            else if (w < 2 * block_words + scale_words) pool_word = k_scale + ps + (w - 2 * block_words);
-            else pool_word = v_scale + ps + (w - 2 * block_words - scale_words);
-            if (to_buffer) slot[w] = *pool_word;
-            else *pool_word = slot[w];
+        // kSwapUnroll independent 16-byte loads in flight per thread, then their stores
+        // (one word per thread per CTA left too few bytes in flight to cover the latency)
+        for (int64_t w0 = (int64_t)blockIdx.x * kSwapChunk + threadIdx.x; w0 < per; w0 += (int64_t)gridDim.x * kSwapChunk) {
+            uint4 *pool_word[kSwapUnroll];
+            uint4 val[kSwapUnroll];
+#pragma unroll
+            for (int u = 0; u < kSwapUnroll; ++u) {
+                const int64_t w = w0 + u * kCopyThreads;
+                pool_word[u] = nullptr;
+                if (w >= per) continue;
+                if (w < block_words) pool_word[u] = k_pool + pb + w;
+                else if (w < 2 * block_words) pool_word[u] = v_pool + pb + (w - block_words);
+                else if (w < 2 * block_words + scale_words) pool_word[u] = k_scale + ps + (w - 2 * block_words);
+                else pool_word[u] = v_scale + ps + (w - 2 * block_words - scale_words);
+                val[u] = to_buffer ? __ldcs(pool_word[u]) : __ldcs(slot + w);
+            }
+#pragma unroll
+            for (int u = 0; u < kSwapUnroll; ++u) {
+                const int64_t w = w0 + u * kCopyThreads;
+                if (w < per) {
+                    if (to_buffer) __stcs(slot + w, val[u]);
+                    else *pool_word[u] = val[u];
+                }
+            }
         }
     }
 }
@@ -191,10 +208,24 @@ pkv_status swap_blocks(const pkv_pool *pool, const int32_t *blocks, int32_t n, v
         return fail(PKV_ERR_INVALID_ARG, "blocks (4-byte aligned) and buffer (16-byte aligned) are required");
     const bool q8 = d.kv_dtype == PKV_KV_E4M3;
     if (q8 && !pool->k_scale) return fail(PKV_ERR_INVALID_ARG, "E4M3 pool without scale pools (pkv_pool_set_scales)");
+    // The buffer may be device memory or pinned host memory mapped into the device's
+    // address space (the kernel then moves the blocks over the host link itself, with
+    // no staging copy). Anything else would fault in the kernel, so it is refused here.
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, buf) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PKV_ERR_INVALID_ARG, "swap buffer: not a CUDA-visible pointer");
+    }
+    if (attr.type == cudaMemoryTypeHost) {
+        if (!attr.devicePointer) return fail(PKV_ERR_INVALID_ARG, "swap buffer: pinned host memory not mapped to the device");
+        buf = attr.devicePointer;
+    } else if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) {
+        return fail(PKV_ERR_INVALID_ARG, "swap buffer: must be device memory or pinned (mapped) host memory");
+    }
     const int64_t block_words = (int64_t)d.block_size * d.num_heads * d.head_dim * kv_elem_bytes(d) / 16;
     const int64_t scale_words = q8 ? (int64_t)d.block_size * d.num_heads * 4 / 16 : 0;
     const int64_t per = 2 * block_words + 2 * scale_words;
-    int gx = (int)((per + kCopyThreads - 1) / kCopyThreads);
+    int gx = (int)((per + kSwapChunk - 1) / kSwapChunk);
     gx = gx < 1 ? 1 : (gx > 64 ? 64 : gx);
     const int64_t jobs = (int64_t)n * d.num_layers;
     const int gy = (int)(jobs < 65535 ? jobs : 65535);

@@ -171,9 +171,11 @@ class DecodeEngine:
             self.pool.prefix_register(hashes[len(hit):], self.tables[s, len(hit):full])
 
     # ------------------------------------------------------------------ swap (preemption)
-    def swap_out(self, s: int, host_buf, staging, stream=None) -> int:
-        """Move sequence s's blocks (all layers) to ``host_buf`` (pinned uint8) through the device
-        ``staging`` buffer, then release them; its length is kept. Returns the number of blocks."""
+    def swap_out(self, s: int, host_buf, staging=None, stream=None) -> int:
+        """Move sequence s's blocks (all layers) to ``host_buf`` (pinned uint8), then release
+        them; its length is kept. With a device ``staging`` buffer the blocks are gathered there
+        and copied to the host; without one the gather kernel writes ``host_buf`` directly over
+        the host link. Returns the number of blocks."""
         w, B = self.w, self.w.block_size
         n = -(-int(self.lens[s]) // B)
         ids = self.tables[s, :n].copy()
@@ -181,22 +183,29 @@ class DecodeEngine:
         st = stream if stream is not None else torch.cuda.current_stream()
         with torch.cuda.stream(st):
             blocks = torch.from_numpy(ids).to(self.device, non_blocking=False)
-            self.pool.gather_blocks(blocks, staging, status=self.status, stream=st)
-            host_buf[:nbytes].copy_(staging[:nbytes], non_blocking=True)
+            if staging is None:
+                self.pool.gather_blocks(blocks, host_buf, status=self.status, stream=st)
+            else:
+                self.pool.gather_blocks(blocks, staging, status=self.status, stream=st)
+                host_buf[:nbytes].copy_(staging[:nbytes], non_blocking=True)
         self.pool.free(ids)
         self.tables[s, :] = -1
         return n
 
-    def swap_in(self, s: int, n: int, host_buf, staging, stream=None) -> None:
-        """Bring sequence s's n swapped blocks back into freshly allocated blocks."""
+    def swap_in(self, s: int, n: int, host_buf, staging=None, stream=None) -> None:
+        """Bring sequence s's n swapped blocks back into freshly allocated blocks (through the
+        device ``staging`` buffer if one is given, else read from ``host_buf`` by the kernel)."""
         ids = self.pool.alloc(n)
         self.tables[s, :n] = ids
         nbytes = n * self.pool.swap_bytes_per_block()
         st = stream if stream is not None else torch.cuda.current_stream()
         with torch.cuda.stream(st):
             blocks = torch.tensor(ids, dtype=torch.int32, device=self.device)
-            staging[:nbytes].copy_(host_buf[:nbytes], non_blocking=True)
-            self.pool.scatter_blocks(blocks, staging, status=self.status, stream=st)
+            if staging is None:
+                self.pool.scatter_blocks(blocks, host_buf, status=self.status, stream=st)
+            else:
+                staging[:nbytes].copy_(host_buf[:nbytes], non_blocking=True)
+                self.pool.scatter_blocks(blocks, staging, status=self.status, stream=st)
 
     def upload_tables(self):
         self.tables_d.copy_(torch.from_numpy(self.tables))

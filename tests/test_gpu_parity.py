@@ -142,10 +142,11 @@ def test_long_context_block_sweep_reduced(block_size):
 
 # ----------------------------------------------------------------------------- swap (preemption)
 
-@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3"])
-def test_swap_out_and_in_round_trip(kv_dtype):
+@pytest.mark.parametrize("kv_dtype,direct", [("f16", False), ("e4m3", False), ("f16", True), ("e4m3", True)])
+def test_swap_out_and_in_round_trip(kv_dtype, direct):
     """Two sequences are swapped to pinned host memory, their blocks reused by other requests,
-    then swapped back into new blocks; the next decode step matches the oracle exactly."""
+    then swapped back into new blocks; the next decode step matches the oracle exactly.
+    direct: the kernels read and write the pinned host buffers themselves (no device staging)."""
     w = wl.make_workload(2, num_layers=2, num_seqs=6, len_scale=0.2, decode_steps=4, kv_dtype=kv_dtype)
     eng = DecodeEngine(w, fill="numpy")
     ora = make_oracle(w)
@@ -158,7 +159,7 @@ def test_swap_out_and_in_round_trip(kv_dtype):
     ora.step(q, k, v)
     bpb = eng.pool.swap_bytes_per_block()
     host = torch.empty(64 * bpb, dtype=torch.uint8).pin_memory()
-    staging = torch.empty(64 * bpb, dtype=torch.uint8, device="cuda")
+    staging = None if direct else torch.empty(64 * bpb, dtype=torch.uint8, device="cuda")
     host2 = torch.empty_like(host).pin_memory()
     n1 = eng.swap_out(1, host, staging)
     torch.cuda.synchronize()
@@ -194,6 +195,23 @@ def test_swap_out_and_in_round_trip(kv_dtype):
     assert eng.device_status() == 0
     same_pools(eng, ora, "after the step")
     assert_close(out.cpu().numpy(), ref, "after swap")
+
+
+def test_swap_refuses_pageable_host_buffer():
+    """A buffer the device cannot address (pageable host memory) is refused before any launch."""
+    w = wl.make_workload(2, num_layers=2, num_seqs=2, len_scale=0.1, decode_steps=1)
+    eng = DecodeEngine(w, fill="numpy")
+    eng.run_script()
+    bpb = eng.pool.swap_bytes_per_block()
+    blocks = torch.tensor(eng.tables[0, :1], dtype=torch.int32, device="cuda")
+    pageable = torch.empty(bpb, dtype=torch.uint8)
+    with pytest.raises(pkv.PkvError) as ei:
+        eng.pool.gather_blocks(blocks, pageable)
+    assert ei.value.code == "INVALID_ARG"
+    with pytest.raises(pkv.PkvError):
+        eng.pool.scatter_blocks(blocks, pageable)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
 
 
 # ----------------------------------------------------------------------------- FP8 E4M3 cache
