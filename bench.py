@@ -268,6 +268,46 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def measure_cow(eng, w, dev, peak):
+    """The copy-on-write the workload's first write after the fork needed (pkv_copy_blocks over
+    all layers), re-timed after the decode steps: the same source blocks copied into freshly
+    allocated ones, so the cache the steps read is untouched. Also the blocks the pool holds
+    against the blocks an unshared layout of the same sequences would need."""
+    import numpy as np
+    import torch
+    pairs = np.concatenate(eng.cow_log)
+    st = eng.pool.stats()
+    unshared = int(sum(-(-int(t) // w.block_size) for t in eng.lens[:w.num_seqs]))
+    n = min(len(pairs), int(st["free_blocks"]))
+    res = {"pairs": int(len(pairs)), "layers": w.num_layers, "blocks_used": int(st["used_blocks"]),
+           "blocks_unshared": unshared}
+    if n == 0:
+        return res
+    fresh = eng.pool.alloc(n)
+    pd = torch.tensor(np.stack([pairs[:n, 0], np.asarray(fresh, dtype=np.int32)], 1), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    times = []
+    for it in range(13):
+        ev[0].record(stream)
+        eng.pool.copy_blocks(pd, status=eng.status, stream=stream)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        if it >= 3:
+            times.append(ev[0].elapsed_time(ev[1]))
+    eng.pool.free(fresh)
+    ms = float(np.median(times))
+    per_block = w.num_layers * w.block_size * w.kv_bytes_per_token_layer   # K and V of a block, all layers
+    copied = n * per_block
+    # distinct bytes: each source block read once (forked sequences share one source), every copy written
+    distinct = (len(np.unique(pairs[:n, 0])) + n) * per_block
+    res.update({"timed_pairs": n, "distinct_src_blocks": int(len(np.unique(pairs[:n, 0]))),
+                "bytes_copied": int(copied), "ms": ms,
+                "gbps_distinct": distinct / (ms / 1e3) / 1e9,
+                "frac_distinct_of_hbm_peak": distinct / (ms / 1e3) / 1e9 / peak})
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -437,6 +477,7 @@ def run_ours(args):
 
     info = pkv.decode_launch_info(S, D, w.kv_dtype)
     kname = f"decode_attention_kernel<{D}{', E4M3' if w.kv_dtype == 'e4m3' else ''}>"
+    cow = measure_cow(eng, w, dev, peak) if eng.cow_log else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -459,6 +500,7 @@ def run_ours(args):
                 "frac_unique_of_hbm_peak": value * sum(step_unique) / sum(step_bytes) / peak,
                 "cascade": {"groups": int(eng.plan_groups), "splits": int(eng.plan_splits),
                             "prefix_tokens": int(eng.plan_prefix)}} if cascading else {}),
+            **({"cow": cow} if cow else {}),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
                          "kernel": (f"prefix pass + {kname} (distinct KV bytes)" if cascading else kname),

@@ -98,6 +98,7 @@ class DecodeEngine:
             })
         self._buf = 0
         self.last_pairs = np.zeros((0, 2), dtype=np.int32)
+        self.cow_log = []             # every copy-on-write pair array the script's writes produced
         self.last_slots = np.zeros(0, dtype=np.int64)
 
     # ------------------------------------------------------------------ set-up script
@@ -142,6 +143,7 @@ class DecodeEngine:
         slots_d = torch.from_numpy(slots.copy()).to(self.device)
         if len(pairs):
             self.pool.copy_blocks(torch.from_numpy(pairs.copy()).to(self.device), status=self.status, stream=stream)
+            self.cow_log.append(pairs.copy())
         for layer in range(w.num_layers):
             if values == "numpy":
                 kn = torch.from_numpy(wl.write_values(w, op_index, layer, 0, total)).to(self.device)
