@@ -216,18 +216,56 @@ def cpu_baseline_oracle(w, k_layer, v_layer, tables, lens, seconds: float, k_sca
                 "sample": f"{passes} sequence(s) of one layer, NumPy E4M3 oracle (dequantise, float64), {el:.1f} s"}
     rng = np.random.default_rng(0)
     q = rng.standard_normal((w.num_seqs, w.num_heads, w.head_dim)).astype(np.float16)
-    bytes_per = int(np.asarray(lens, dtype=np.int64).sum()) * w.kv_bytes_per_token_layer
+    lens64 = np.asarray(lens, dtype=np.int64)
+    bytes_per = int(lens64.sum()) * w.kv_bytes_per_token_layer
+    cores = rc.max_threads()
+    # one core first (the thread count a call sets stays for the next call), on the
+    # batch's first eighth of sequences
+    sub = max(1, w.num_seqs // 8)
+    t0 = time.perf_counter()
+    p1 = 0
+    while True:
+        rc.decode_attention(q[:sub], k_layer, v_layer, tables[:sub], lens[:sub], w.block_size, w.layout,
+                            num_threads=1)
+        p1 += 1
+        el1 = time.perf_counter() - t0
+        if el1 >= seconds / 4 or p1 >= 64:
+            break
+    one_core = int(lens64[:sub].sum()) * w.kv_bytes_per_token_layer * p1 / el1 / 1e9
     t0 = time.perf_counter()
     passes = 0
     while True:
-        rc.decode_attention(q, k_layer, v_layer, tables, lens, w.block_size, w.layout)
+        rc.decode_attention(q, k_layer, v_layer, tables, lens, w.block_size, w.layout, num_threads=cores)
         passes += 1
         el = time.perf_counter() - t0
         if el >= seconds or passes >= 64:
             break
-    return {"value": bytes_per * passes / el / 1e9, "unit": "GB/s", "cores": rc.max_threads(), "kind": "oracle",
+    return {"value": bytes_per * passes / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "one_core_value": one_core, "cpu_model": cpu_model(),
             "sample": f"{passes} pass(es) of one layer ({w.num_seqs} seqs x {w.num_heads} heads, "
-                      f"{int(np.sum(lens))} tokens) of the same workload, fp64 C oracle, {el:.1f} s"}
+                      f"{int(np.sum(lens))} tokens) of the same workload, fp64 C oracle, {el:.1f} s; one core: "
+                      f"{p1} pass(es) of its first {sub} seqs, {el1:.1f} s"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    import platform
+    import subprocess
+    try:
+        outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in outp.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def run_reference(args):
