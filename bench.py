@@ -187,6 +187,12 @@ def rank_seed(config: int, rank: int) -> int:
     return 1000 + config + 7919 * rank
 
 
+def bench_total_steps(args) -> int:
+    """Decode steps the pool is sized for: warm-up (eager and graph), timed, end-to-end, spare."""
+    e2e_steps = 0 if args.no_e2e else args.steps
+    return 3 * args.warmup + args.steps + e2e_steps + 4
+
+
 def make_bench_workload(args, extra_steps: int):
     import workloads as wl
     w = wl.make_workload(args.config, decode_steps=extra_steps, layout=args.layout, block_size=args.block_size,
@@ -277,7 +283,7 @@ def run_reference(args):
     import workloads as wl
     from oracle import ref_alloc as ra
     from oracle import ref_attn_c as rc
-    w = make_bench_workload(args, 8)
+    w = make_bench_workload(args, bench_total_steps(args))   # the GPU arm's workload, pool size included
     op = ra.RefPool(w.num_blocks, [int(x) for x in w.free_order])
     tables = np.asarray([ra.admit(op, int(t), w.block_size, w.max_blocks) for t in w.context_lens], dtype=np.int32)
     lens = np.asarray(w.context_lens, dtype=np.int32)
@@ -361,7 +367,7 @@ def run_ours(args):
     import paged_kv_cache_88_gb300 as pkv
 
     e2e_steps = 0 if args.no_e2e else args.steps
-    total_steps = 3 * args.warmup + args.steps + e2e_steps + 4
+    total_steps = bench_total_steps(args)
     w = make_bench_workload(args, total_steps)
     if world > 1:                         # weak scaling: each rank serves its own batch
         import workloads as wl
@@ -422,6 +428,18 @@ def run_ours(args):
             eng.attention(i % L, q, out, stream, early=i > 0)
         a1.record(stream)
         barrier()
+        # serialised pass: each launch alone, as when the kernel before it on the stream is not
+        # one of ours (no early start, no programmatic overlap): a small torch kernel runs
+        # between launches, outside each launch's pair of CUDA events
+        n_ser = max(2, args.steps // 8) * L
+        gap = torch.zeros(1024, dtype=torch.float32, device=dev)
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ser)]
+        for i in range(n_ser):
+            gap.add_(1.0)
+            sev[i][0].record(stream)
+            eng.attention(i % L, q, out, stream, early=False)
+            sev[i][1].record(stream)
+        barrier()
     clocks = clk.summary()
     ms = t_start.elapsed_time(t_end)
     attn_ms_total = a0.elapsed_time(a1)
@@ -442,6 +460,8 @@ def run_ours(args):
     extra = 2 * S * H * D * 2 + S * 4 + int(np.sum(-(-eng.lens // w.block_size))) * 4
     mean_launch_ms = attn_ms_total / n_attn
     achieved = (attn_launch_bytes + extra) / (mean_launch_ms / 1e3) / 1e9
+    serial_ms = float(np.mean([a.elapsed_time(b) for a, b in sev]))
+    serial_achieved = (attn_launch_bytes + extra) / (serial_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
     traffic = None if cascading else kernel_traffic(attn_launch_bytes + extra, w.kv_dtype)
 
@@ -544,7 +564,13 @@ def run_ours(args):
                          "kernel": (f"prefix pass + {kname} (distinct KV bytes)" if cascading else kname),
                          "launches": n_attn,
                          "mean_launch_us": 1e3 * mean_launch_ms, "bytes_per_launch": attn_launch_bytes + extra,
-                         "grid_ctas": info["grid_ctas"], "ctas_per_sm": info["ctas_per_sm"]},
+                         "grid_ctas": info["grid_ctas"], "ctas_per_sm": info["ctas_per_sm"],
+                         "timing": "back to back over the step's layers, each launch flagged to start early "
+                                   "behind the previous one (CUDA events around the whole pass)",
+                         "serial": {"achieved": serial_achieved, "frac": serial_achieved / peak,
+                                    "mean_launch_us": 1e3 * serial_ms, "launches": n_ser,
+                                    "timing": "each launch alone: no early start, a torch kernel between "
+                                              "launches, CUDA events around each launch"}},
             "clocks": clocks,
             "gpu_launches": launches,
             "e2e": e2e,

@@ -177,6 +177,16 @@ pkv_status pkv_validate(const pkv_pool *pool);
  * bytes little-endian each). */
 uint64_t pkv_block_hash(uint64_t parent, const int32_t *token_ids, int32_t n);
 
+/* The chained hashes of every FULL block of a prompt (icman.com.cn/news/78786 §3.2:
+ * a block's key covers its tokens and, through the parent hash, every token
+ * before it): out[i] = pkv_block_hash(out[i-1], tokens of block i, block_size),
+ * with parent 0 for block 0. token_ids: host int32 [num_tokens]; out: host
+ * uint64 [capacity]; *num_hashes = num_tokens / block_size (a partial last block
+ * is not hashed). INVALID_ARG for a negative count, block_size < 1, NULL arrays
+ * or capacity < num_tokens / block_size (nothing written then). */
+pkv_status pkv_prompt_block_hashes(const int32_t *token_ids, int32_t num_tokens, int32_t block_size,
+                                   uint64_t *out, int32_t capacity, int32_t *num_hashes);
+
 /* For i = 0, 1, ... look hashes[i] up; stop at the first miss. Each hit gets
  * one more reference (a cached block in the free queue is taken out of it and
  * gets refcount 1) and its id goes to out_ids[i]. *num_hits = the hits.
@@ -321,9 +331,12 @@ pkv_status pkv_decode_append_attention(const pkv_pool *pool, int32_t layer, cons
  * Every GPU that loads the library holds the 4 MiB until the process exits.
  * The first call on a device, made with that device current, looks the
  * array's device address up once (cudaGetSymbolAddress); make that first call
- * before any stream capture. All calls share the one array and each clears its
- * counters on `stream` first, so calls that overlap on the GPU (other streams,
- * other threads) race: serialise them. */
+ * before any stream capture. The address is kept for the life of the process:
+ * tearing the device's primary context down (cudaDeviceReset) invalidates it,
+ * so do not call this entry point again on that device after such a reset.
+ * All calls share the one array and each clears its counters on `stream`
+ * first, so calls that overlap on the GPU (other streams, other threads) race:
+ * serialise them. */
 pkv_status pkv_decode_attention_static(const void *q, const void *k_cache, const void *v_cache,
                                        int32_t num_blocks, int32_t block_size, int32_t num_heads,
                                        int32_t head_dim, int32_t layout, const int32_t *block_tables,

@@ -29,7 +29,7 @@ EXPORTED = [
     "pkv_incref", "pkv_free", "pkv_refcount", "pkv_get_stats", "pkv_free_queue", "pkv_validate",
     "pkv_prepare_append", "pkv_append", "pkv_copy_blocks", "pkv_decode_attention", "pkv_decode_workspace_bytes",
     "pkv_pool_decode_attention", "pkv_decode_launch_info", "pkv_decode_append_attention",
-    "pkv_decode_attention_static", "pkv_block_hash", "pkv_prefix_lookup", "pkv_prefix_register",
+    "pkv_decode_attention_static", "pkv_block_hash", "pkv_prompt_block_hashes", "pkv_prefix_lookup", "pkv_prefix_register",
     "pkv_pool_set_scales", "pkv_swap_bytes_per_block", "pkv_gather_blocks", "pkv_scatter_blocks",
     "pkv_prefill_attention", "pkv_cascade_plan", "pkv_prefix_pieces_bytes", "pkv_prefix_splits",
     "pkv_prefix_attention", "pkv_decode_attention_ex", "pkv_check_wait_limit",
@@ -107,6 +107,7 @@ def lib() -> ctypes.CDLL:
             "pkv_decode_attention_static": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, i32, f32, vp,
                                                   vp, vp]),
             "pkv_block_hash": (u64, [u64, vp, i32]),
+            "pkv_prompt_block_hashes": (i32, [vp, i32, i32, vp, i32, ctypes.POINTER(i32)]),
             "pkv_prefix_lookup": (i32, [vp, vp, i32, vp, ctypes.POINTER(i32)]),
             "pkv_prefix_register": (i32, [vp, vp, vp, i32]),
             "pkv_pool_set_scales": (i32, [vp, vp, vp]),
@@ -393,12 +394,13 @@ def block_hash(parent: int, token_ids: Sequence[int]) -> int:
 
 
 def prompt_block_hashes(token_ids: Sequence[int], block_size: int) -> list:
-    """Chained hashes of the full blocks of a prompt (pkv_block_hash per block)."""
-    hs, parent = [], 0
-    for i in range(len(token_ids) // block_size):
-        parent = block_hash(parent, token_ids[i * block_size:(i + 1) * block_size])
-        hs.append(parent)
-    return hs
+    """pkv_prompt_block_hashes: chained hashes of the full blocks of a prompt."""
+    t = np.ascontiguousarray(token_ids, dtype=np.int32)
+    cap = t.size // block_size if block_size > 0 else 0
+    out = np.zeros(max(cap, 1), dtype=np.uint64)
+    n = ctypes.c_int32(0)
+    check(lib().pkv_prompt_block_hashes(_ptr(t), t.size, block_size, _ptr(out), cap, ctypes.byref(n)))
+    return [int(x) for x in out[:n.value]]
 
 
 def cascade_plan(block_tables: np.ndarray, context_lens: np.ndarray, block_size: int, min_group: int = 2,

@@ -476,41 +476,22 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             const uint32_t dst = stage0 + stage * SB;
             const uint32_t bar = full0 + 8 * stage;
             if constexpr (Q8) {
-                // the tile's scales ([N][H][B]: token i of the tile is row y_i): lane l
-                // copies the K and V scales of tokens l, l + 32, ... with 4-byte
-                // asynchronous copies (coalesced requests, not two small bulk copies per
-                // block), and the
-                // stage's phase waits for them; issued before lane 0's arrival so the
-                // phase cannot complete without them
+                // the tile's scales ([N][H][B]: token i of the tile is row y_i) as 16-byte
+                // asynchronous copies of four tokens each: lanes 0-15 the K scales of tokens
+                // 4l..4l+3, lanes 16-31 the V scales. A run of four never leaves its block and
+                // every copy is 16-byte aligned, because the block size (8..256) and the tile
+                // start (a multiple of 64: an E4M3 cache takes no cascade, so beg = 0) are
+                // multiples of 4 and the host refuses scale pools that are not 16-byte aligned.
+                // Issued before lane 0's arrival, so the stage's phase cannot complete without them.
                 static_assert(kTile == 64, "16-byte scale copies: 16 lanes x 4 tokens per pool");
-                const bool vec = ((t0 | B) & 3) == 0 &&
-                                 ((reinterpret_cast<uintptr_t>(p.k_scale) | reinterpret_cast<uintptr_t>(p.v_scale)) & 15) == 0;
-                if (vec) {
-                    // four scales per 16-byte copy (a run of four tokens never leaves its
-                    // block when B and the tile start are multiples of 4): lanes 0-15 the K
-                    // scales of tokens 4l..4l+3, lanes 16-31 the V scales
-                    const int32_t i = (lane & 15) * 4;
-                    const int32_t t = t0 + min(i, ntok - 1);
-                    int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
-                    if (blk < 0 || blk >= p.N) blk = 0;      // flagged with the boxes below
-                    const size_t y = ((size_t)blk * H + cc.h) * B + t % B;
-                    if (i < ntok) {
-                        if (lane < 16) ptx::cp_async_16_cg(dst + St::kScales + i * 4, p.k_scale + y);
-                        else ptx::cp_async_16_cg(dst + St::kScales + kTile * 4 + i * 4, p.v_scale + y);
-                    }
-                } else {
-#pragma unroll
-                    for (int i0 = 0; i0 < kTile; i0 += 32) {
-                        const int32_t i = i0 + lane;
-                        const int32_t t = t0 + min(i, ntok - 1);
-                        int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
-                        if (blk < 0 || blk >= p.N) blk = 0;  // flagged with the boxes below
-                        const size_t y = ((size_t)blk * H + cc.h) * B + t % B;
-                        if (i < ntok) {
-                            ptx::cp_async_4(dst + St::kScales + i * 4, p.k_scale + y);
-                            ptx::cp_async_4(dst + St::kScales + kTile * 4 + i * 4, p.v_scale + y);
-                        }
-                    }
+                const int32_t i = (lane & 15) * 4;
+                const int32_t t = t0 + min(i, ntok - 1);
+                int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
+                if (blk < 0 || blk >= p.N) blk = 0;      // flagged with the boxes below
+                const size_t y = ((size_t)blk * H + cc.h) * B + t % B;
+                if (i < ntok) {
+                    if (lane < 16) ptx::cp_async_16_cg(dst + St::kScales + i * 4, p.k_scale + y);
+                    else ptx::cp_async_16_cg(dst + St::kScales + kTile * 4 + i * 4, p.v_scale + y);
                 }
                 ptx::cp_async_mbar_arrive(bar);
                 __syncwarp();

@@ -286,6 +286,22 @@ uint64_t pkv_block_hash(uint64_t parent, const int32_t *token_ids, int32_t n) {
     return h;
 }
 
+pkv_status pkv_prompt_block_hashes(const int32_t *token_ids, int32_t num_tokens, int32_t block_size,
+                                   uint64_t *out, int32_t capacity, int32_t *num_hashes) {
+    if (!num_hashes) return fail(PKV_ERR_INVALID_ARG, "num_hashes is NULL");
+    if (num_tokens < 0 || block_size < 1) return fail(PKV_ERR_INVALID_ARG, "bad token count or block size");
+    const int32_t full = num_tokens / block_size;  // a partial last block has no hash
+    if (full > 0 && (!token_ids || !out)) return fail(PKV_ERR_INVALID_ARG, "NULL token_ids or out");
+    if (capacity < full) return fail(PKV_ERR_INVALID_ARG, "capacity %d < %d full blocks", capacity, full);
+    uint64_t parent = 0;  // the first block chains on 0
+    for (int32_t i = 0; i < full; ++i) {
+        parent = pkv_block_hash(parent, token_ids + (size_t)i * block_size, block_size);
+        out[i] = parent;
+    }
+    *num_hashes = full;
+    return PKV_OK;
+}
+
 pkv_status pkv_prefix_lookup(pkv_pool *pool, const uint64_t *hashes, int32_t n, int32_t *out_ids,
                              int32_t *num_hits) {
     if (!pool || !num_hits) return fail(PKV_ERR_INVALID_ARG, "NULL argument");

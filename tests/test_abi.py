@@ -1,5 +1,6 @@
 """CPU tests of the C ABI: the library loads, exports every declared symbol, and its
 host allocator reproduces the allocator oracle bit for bit (no GPU needed)."""
+import ctypes
 import os
 import random
 import re
@@ -262,6 +263,31 @@ def test_block_hash_matches_oracle():
         assert bd.block_hash(parent, toks) == ra.block_hash(parent, toks)
     toks = [rng.randrange(32000) for _ in range(100)]
     assert bd.prompt_block_hashes(toks, 16) == ra.prompt_block_hashes(toks, 16)
+
+
+def test_prompt_block_hashes_matches_oracle():
+    """pkv_prompt_block_hashes chains the per-block hashes in the library: equal to the oracle's
+    chain for every block size, prompt lengths with and without a partial last block, and empty."""
+    rng = random.Random(11)
+    for B in (1, 8, 16, 32, 256):
+        for n in (0, B - 1, B, 3 * B + 5, 40 * B):
+            toks = [rng.randrange(-2**31, 2**31) for _ in range(n)]
+            assert bd.prompt_block_hashes(toks, B) == ra.prompt_block_hashes(toks, B), (B, n)
+
+
+def test_prompt_block_hashes_argument_errors():
+    L = bd.lib()
+    toks = np.arange(64, dtype=np.int32)
+    out = np.zeros(4, dtype=np.uint64)
+    n = ctypes.c_int32(-7)
+    # capacity below the number of full blocks: refused, nothing written
+    assert L.pkv_prompt_block_hashes(toks.ctypes.data, 64, 16, out.ctypes.data, 3, ctypes.byref(n)) == 1
+    assert n.value == -7 and not out.any()
+    assert L.pkv_prompt_block_hashes(toks.ctypes.data, 64, 0, out.ctypes.data, 4, ctypes.byref(n)) == 1
+    assert L.pkv_prompt_block_hashes(toks.ctypes.data, -1, 16, out.ctypes.data, 4, ctypes.byref(n)) == 1
+    assert L.pkv_prompt_block_hashes(toks.ctypes.data, 64, 16, out.ctypes.data, 4, None) == 1
+    assert L.pkv_prompt_block_hashes(toks.ctypes.data, 64, 16, out.ctypes.data, 4, ctypes.byref(n)) == 0
+    assert n.value == 4 and [int(x) for x in out] == ra.prompt_block_hashes(toks.tolist(), 16)
 
 
 def _same_prefix_state(c, o):

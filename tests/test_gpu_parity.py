@@ -634,9 +634,13 @@ def test_13b_full_size_sampled(free_gpu_memory):
     _full_size(w, [0, w.num_layers - 1], steps=2)
 
 
-def test_long_context_full_size_sampled(free_gpu_memory):
-    """16 sequences of 4k-16k tokens in 4 MiB pages, full size (32 layers)."""
-    w = wl.make_workload(5, decode_steps=4)
+@pytest.mark.parametrize("block_size", [256, 8, 64])
+def test_long_context_full_size_sampled(block_size, free_gpu_memory):
+    """16 sequences of 4k-16k tokens, full size (32 layers): in 4 MiB pages (block 256), and the
+    block-size sweep's ends with the same token data -- block 8 gives tables of up to 2049 entries
+    (the producer's 32-entry table window is refilled 64 times per (sequence, head)), block 64
+    one TMA box per 64-token tile."""
+    w = wl.make_workload(5, decode_steps=4, block_size=block_size)
     _full_size(w, [0, w.num_layers - 1], steps=2)
 
 
