@@ -288,6 +288,11 @@ pkv_status pkv_scatter_blocks(const pkv_pool *pool, const int32_t *blocks, int32
  *   same stream (calls that overlap on the GPU must use distinct workspaces).
  *   Its first 4 bytes are the device status word of the call (PKV_DEV_* bits,
  *   sticky: clear it to reset).
+ * Limits (every decode-attention entry point): num_seqs <= 4096 per launch (the
+ *   kernel keeps three int32 per sequence in shared memory, and every CTA scans
+ *   the lengths in its prologue); head_dim 64, 128 or 256 for an fp16 cache, 64
+ *   or 128 for an E4M3 cache, which also needs the HND layout; block_size 8, 16,
+ *   32, 64, 128 or 256; num_blocks * block_size * num_heads < 2^31.
  * Errors: INVALID_ARG (sizes, alignment, workspace too small), UNSUPPORTED
  *   (head_dim or block_size not built), CUDA (launch failure). */
 pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *v_cache,
@@ -442,7 +447,8 @@ pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void 
 /* pkv_decode_append_attention and pkv_pool_decode_attention in one entry, with
  * the private half of the cascade. k_new, v_new, slot_mapping: all NULL = no
  * append (else as pkv_decode_append_attention). seq_begin, pieces: both NULL =
- * no cascade (the plain attention). Otherwise seq_begin is device int32
+ * no cascade (the plain attention); the cascade needs an fp16 pool with head_dim
+ * 128 (UNSUPPORTED otherwise), and its prefix pass the HND layout. Otherwise seq_begin is device int32
  * [num_seqs]: sequence s attends here to its tokens [seq_begin[s], T_s) and,
  * when seq_begin[s] > 0, merges in the `splits` prefix pieces that
  * pkv_prefix_attention wrote for it earlier on the same stream. seq_begin[s]

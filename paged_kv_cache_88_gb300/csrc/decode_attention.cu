@@ -71,6 +71,11 @@ using namespace pkv;
 #ifndef PKV_ATTN_MIN_CTAS_Q8
 #define PKV_ATTN_MIN_CTAS_Q8 4
 #endif
+// The E4M3 head_dim-128 variant (tensor-core consumers) holds q and the output as MMA
+// fragments.
+#ifndef PKV_ATTN_MIN_CTAS_MMA
+#define PKV_ATTN_MIN_CTAS_MMA 4
+#endif
 #ifndef PKV_ATTN_ACQREL
 #define PKV_ATTN_ACQREL 1
 #endif
@@ -121,20 +126,27 @@ struct Params {
     // workspace and out are touched only after it
     int32_t early;
     int32_t S, H, max_blocks, B, N, layout;
+    int32_t lgB;         // log2(B): B is a power of two
     float scale_log2;    // scale * log2(e)
 };
 
 // Shape of one pipeline stage: [K tile][V tile][q row][K scales][V scales].
-// Q8 = the cache holds E4M3 codes with a scale per (token, head) row.
+// Q8 = the cache holds E4M3 codes with a scale per (token, head) row. kMma = the E4M3
+// head_dim-128 variant, whose consumers run q.K and p.V on the warp-level tensor cores:
+// its K and V tiles arrive 128-byte swizzled (16-byte chunk k of token row r at chunk
+// k ^ (r & 7)), which needs every tile to start on a 1024-byte boundary.
 template <int D, bool Q8>
 struct Stage {
+    static constexpr bool kMma = Q8 && D == 128;
+    static constexpr int kAlign = kMma ? 1024 : 128;
     static constexpr int kElem = Q8 ? 1 : 2;          // bytes per K/V element
     static constexpr int kRow = D * kElem;            // bytes per token row
     static constexpr int kTileBytes = kTile * kRow;   // one K (or V) tile
     static constexpr int kQ = 2 * kTileBytes;         // offset of the query row (fp16)
     static constexpr int kScales = kQ + D * 2;        // offset of the K scales, then the V scales
-    static constexpr int kBytes = ((kScales + (Q8 ? 2 * kTile * 4 : 0)) + 127) / 128 * 128;
+    static constexpr int kBytes = ((kScales + (Q8 ? 2 * kTile * 4 : 0)) + kAlign - 1) / kAlign * kAlign;
     static constexpr int kStages = Q8 ? kStagesQ8 : kStagesF16;
+    static_assert(kTileBytes % kAlign == 0, "tiles start on the stage alignment");
 };
 
 __host__ __device__ constexpr int piece_stride(int D) { return D + 4; }
@@ -158,7 +170,7 @@ template <int D, bool Q8>
 __host__ __device__ constexpr size_t smem_bytes_t(int S) {
     return ((size_t)Stage<D, Q8>::kStages * Stage<D, Q8>::kBytes + (size_t)pre_buf_floats<D, Q8>() * sizeof(float) +
             (size_t)kConsumerWarps * (D + 2) * sizeof(float) + (size_t)(3 * S + 2) * sizeof(int32_t) + 15) / 16 * 16 +
-           2 * Stage<D, Q8>::kStages * sizeof(uint64_t) + 16 + 128;  // + slack to align the base to 128 bytes
+           2 * Stage<D, Q8>::kStages * sizeof(uint64_t) + 16 + Stage<D, Q8>::kAlign;  // + slack to align the base
 }
 
 struct Smem {
@@ -178,8 +190,9 @@ struct Smem {
 template <int D, bool Q8>
 __device__ __forceinline__ Smem carve(unsigned char *raw, int S) {
     constexpr int NS = Stage<D, Q8>::kStages;
+    constexpr uintptr_t A = Stage<D, Q8>::kAlign;
     Smem m;
-    uintptr_t p = (reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127);
+    uintptr_t p = (reinterpret_cast<uintptr_t>(raw) + A - 1) & ~(A - 1);
     m.stage = reinterpret_cast<unsigned char *>(p);
     p += (size_t)NS * Stage<D, Q8>::kBytes;
     m.pre = reinterpret_cast<float *>(p);
@@ -333,11 +346,19 @@ __device__ __forceinline__ void merge_prefix(const Params &p, const float *stage
     M = Mn;
 }
 
+// Resident CTAs per SM the register budget is set for.
 template <int D, bool Q8>
-__global__ void __launch_bounds__(kThreads, D >= 256 ? 1 : (Q8 ? PKV_ATTN_MIN_CTAS_Q8 : PKV_ATTN_MIN_CTAS))
+constexpr int min_ctas() {
+    return D >= 256 ? 1 : (Stage<D, Q8>::kMma ? PKV_ATTN_MIN_CTAS_MMA : (Q8 ? PKV_ATTN_MIN_CTAS_Q8 : PKV_ATTN_MIN_CTAS));
+}
+
+template <int D, bool Q8>
+__global__ void __launch_bounds__(kThreads, min_ctas<D, Q8>())
 decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const Params p) {
     using St = Stage<D, Q8>;
+    constexpr bool kMma = St::kMma;
+    static_assert(!kMma || kTile == 16 * kConsumerWarps, "kMma: 16 tokens of the tile per consumer warp");
     constexpr int NCH = D / 64;      // chunks of 8 elements per lane per row
     constexpr int SB = St::kBytes;
     constexpr int NS = St::kStages;
@@ -448,29 +469,47 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
 
     if (warp == kConsumerWarps) {
         // ================= producer warp
-        const int32_t B = p.B;
+        const int32_t B = p.B, lgB = p.lgB;
         const int32_t rows = B < kTile ? B : kTile;           // rows per TMA box
         const uint32_t box_bytes = (uint32_t)rows * St::kRow;
         constexpr int W = D / 8;                              // 16-byte fp16 words per new row
         constexpr int NW = (2 * W + 31) / 32;                 // words of the new K+V rows per lane
         Cursor c = locate(sm, S, H, g0);
-        int32_t win_s = -1, win_lb0 = 0, win_val = 0;
+        // a window of 32 KW block-table entries of the current sequence in registers: lane l
+        // holds entry win_lb0 + 32 j + l in win[j] (one load round serves every head of the
+        // sequence while the window covers the tiles)
+        constexpr int KW = 4;
+        int32_t win_s = -1, win_lb0 = 0, win[KW];
         uint4 nw[NW];                                         // the new token's K/V row words
         int64_t new_slot = -1;                                // pending append of the current (s, h)
+        // table entry win_lb0 + e (e per lane, 0 <= e < 32 KW)
+        auto entry = [&](int32_t e) {
+            int32_t v = 0;
+#pragma unroll
+            for (int jj = 0; jj < KW; ++jj) {
+                const int32_t x = __shfl_sync(0xffffffffu, win[jj], e & 31);
+                if ((e >> 5) == jj) v = x;
+            }
+            return v;
+        };
         // K/V boxes (and, for E4M3, the scales) of the tile at cursor cc into `stage`,
         // with the stage's expected bytes including the q row when `first`
         auto issue_kv = [&](const Cursor &cc, int32_t stage, bool first) {
             const int32_t tt = cc.t * kTile;                   // the tile's first token attended here
             const int32_t ntok = min(kTile, sm.len[cc.s] - tt);
             const int32_t t0 = sm.beg[cc.s] + tt;              // its position in the sequence
-            const int32_t lb = t0 / B;                         // first logical block of the tile
-            const int32_t nbox = B < kTile ? (ntok + B - 1) / B : 1;
-            const int32_t r0 = B < kTile ? 0 : t0 % B;         // first row inside the block
-            if (cc.s != win_s || lb < win_lb0 || lb + nbox > win_lb0 + 32) {
+            const int32_t lb = t0 >> lgB;                      // first logical block of the tile
+            const int32_t nbox = B < kTile ? (ntok + B - 1) >> lgB : 1;
+            const int32_t r0 = B < kTile ? 0 : t0 & (B - 1);   // first row inside the block
+            if (cc.s != win_s || lb < win_lb0 || lb + nbox > win_lb0 + 32 * KW) {
                 win_s = cc.s;
                 win_lb0 = lb;
-                const int32_t e = lb + lane;
-                win_val = e < p.max_blocks ? __ldg(p.tables + (size_t)cc.s * p.max_blocks + e) : 0;
+                const int32_t *row = p.tables + (size_t)cc.s * p.max_blocks;
+#pragma unroll
+                for (int jj = 0; jj < KW; ++jj) {
+                    const int32_t e = lb + 32 * jj + lane;
+                    win[jj] = e < p.max_blocks ? __ldg(row + e) : 0;
+                }
             }
             const uint32_t bytes = (uint32_t)nbox * box_bytes * 2 + (first ? D * 2 : 0);
             const uint32_t dst = stage0 + stage * SB;
@@ -486,9 +525,9 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 static_assert(kTile == 64, "16-byte scale copies: 16 lanes x 4 tokens per pool");
                 const int32_t i = (lane & 15) * 4;
                 const int32_t t = t0 + min(i, ntok - 1);
-                int32_t blk = __shfl_sync(0xffffffffu, win_val, t / B - win_lb0);
+                int32_t blk = entry((t >> lgB) - win_lb0);
                 if (blk < 0 || blk >= p.N) blk = 0;      // flagged with the boxes below
-                const size_t y = ((size_t)blk * H + cc.h) * B + t % B;
+                const size_t y = ((size_t)blk * H + cc.h) * B + (t & (B - 1));
                 if (i < ntok) {
                     if (lane < 16) ptx::cp_async_16_cg(dst + St::kScales + i * 4, p.k_scale + y);
                     else ptx::cp_async_16_cg(dst + St::kScales + kTile * 4 + i * 4, p.v_scale + y);
@@ -497,24 +536,23 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 __syncwarp();
             }
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar, bytes);
-            for (int32_t i = 0; i < nbox; ++i) {
-                int32_t blk = __shfl_sync(0xffffffffu, win_val, lb + i - win_lb0);
-                if (lane == 0) {
-                    if (blk < 0 || blk >= p.N) {
-                        atomicOr(p.status, PKV_DEV_BAD_BLOCK);
-                        blk = 0;
-                    }
-                    int32_t x, y;
-                    if (p.layout == PKV_LAYOUT_NHD) {
-                        x = cc.h * D;
-                        y = blk * B + r0;
-                    } else {
-                        x = 0;
-                        y = (blk * H + cc.h) * B + r0;
-                    }
-                    ptx::tma_load_2d(dst + i * box_bytes, &kmap, x, y, bar);
-                    ptx::tma_load_2d(dst + St::kTileBytes + i * box_bytes, &vmap, x, y, bar);
+            // lane i < nbox loads box i (block lb + i) of K and of V
+            int32_t blk = entry(lb + lane - win_lb0);
+            if (lane < nbox) {
+                if (blk < 0 || blk >= p.N) {
+                    atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                    blk = 0;
                 }
+                int32_t x, y;
+                if (p.layout == PKV_LAYOUT_NHD) {
+                    x = cc.h * D;
+                    y = (blk << lgB) + r0;
+                } else {
+                    x = 0;
+                    y = ((blk * H + cc.h) << lgB) + r0;
+                }
+                ptx::tma_load_2d(dst + lane * box_bytes, &kmap, x, y, bar);
+                ptx::tma_load_2d(dst + St::kTileBytes + lane * box_bytes, &vmap, x, y, bar);
             }
         };
         auto issue_q = [&](const Cursor &cc, int32_t stage) {
@@ -567,7 +605,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 // E4M3 cache), then order the generic-proxy stores before the
                 // tile's TMA (async-proxy) read
                 if (new_slot < (int64_t)p.N * p.B) {
-                    const int64_t blk = new_slot / p.B, off = new_slot - blk * p.B;
+                    const int64_t blk = new_slot >> lgB, off = new_slot & (p.B - 1);
                     const int64_t row = p.layout == PKV_LAYOUT_NHD ? (blk * p.B + off) * H + c.h
                                                                    : (blk * H + c.h) * p.B + off;
                     if constexpr (Q8) {
@@ -621,9 +659,12 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
     // q of the current (s, h): this lane's 8 x NCH elements as fp16 halves
     uint16_t qlo[NCH * 4], qhi[NCH * 4];
     float2 o[NCH * 4];                        // unnormalised output, this lane's elements
+    // kMma: q as the B operand (lanes 0-3: 16 fp16 pairs each, zero elsewhere) and the
+    // unnormalised output, dims 16 u + 2 (lane / 4) + {0, 1} in lanes 4 (lane / 4)
+    uint32_t qa[16];
+    float oacc[16];
     float m = -INFINITY, l = 0.f;             // running max (log2 units) and sum
     Cursor c = locate(sm, S, H, g0);
-    int32_t seg_g0 = g0;                      // first tile of the current (s, h) inside this CTA
 
     for (int32_t k = 0; k < n; ++k) {
         const int32_t stage = k % NS;
@@ -632,149 +673,266 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         wait_phase(sm, full0 + 8 * stage, (k / NS) & 1, p.status);
         const bool first = (k == 0) || (c.t == 0);
         const int32_t ntok = min(kTile, sm.len[c.s] - c.t * kTile);
-        if (first) {
+        if constexpr (kMma) {
+            // ---- E4M3, head_dim 128: q.K and p.V on the warp-level tensor cores (m16n8k16,
+            // fp16 operands, fp32 sums). Warp w takes tokens [16 w, 16 w + 16) of the tile;
+            // the query is column 0 of the products' 8 columns, the others are zero padding.
+            const int g = lane >> 2, c4 = lane & 3;
+            const int tok0 = warp * 16;
+            const bool full = ntok == kTile;
+            if (first) {
+                // q dims [32 c4, 32 c4 + 32) as the B column of lanes 0-3 (zero elsewhere);
+                // lanes with c4 >= 2 read the 16-byte groups of each pair in swapped order, so
+                // that the four lanes' loads fall in distinct banks
+                const int sw = c4 >> 1;
+                uint4 v[4];
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-                const uint4 raw = ptx::lds128(kb + St::kQ + chunk_elem<D, Q8>(j, ch) * 2);
-                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+                for (int i = 0; i < 4; ++i) v[i] = ptx::lds128(kb + St::kQ + c4 * 64 + (i ^ sw) * 16);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ptx::split_half2(wv[e], qlo[ch * 4 + e], qhi[ch * 4 + e]);
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 w = sw ? v[i ^ 1] : v[i];
+                    qa[4 * i + 0] = g == 0 ? w.x : 0u;
+                    qa[4 * i + 1] = g == 0 ? w.y : 0u;
+                    qa[4 * i + 2] = g == 0 ? w.z : 0u;
+                    qa[4 * i + 3] = g == 0 ? w.w : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) oacc[i] = 0.f;
+                m = -INFINITY;
+                l = 0.f;
+            }
+            // S^T = K q^T: A rows g, g + 8 = tokens tok0 + g, tok0 + g + 8 (bytes [32 c4, 32 c4 + 32)
+            // of each, 128-byte swizzled: (token & 7) == g); k step st pairs their word st (dims
+            // 32 c4 + 4 st .. + 3) with q's words 2 st, 2 st + 1 (the same dims), a consistent
+            // order of the dot product's terms
+            uint32_t kw[16];
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+                const uint32_t row = kb + (tok0 + 8 * r2 + g) * 128;
+                const uint4 w0 = ptx::lds128(row + (((2 * c4) ^ g) << 4));
+                const uint4 w1 = ptx::lds128(row + (((2 * c4 + 1) ^ g) << 4));
+                kw[8 * r2 + 0] = w0.x; kw[8 * r2 + 1] = w0.y; kw[8 * r2 + 2] = w0.z; kw[8 * r2 + 3] = w0.w;
+                kw[8 * r2 + 4] = w1.x; kw[8 * r2 + 5] = w1.y; kw[8 * r2 + 6] = w1.z; kw[8 * r2 + 7] = w1.w;
+            }
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+#pragma unroll
+            for (int st = 0; st < 8; st += 2) {       // two accumulation chains
+                uint32_t a0, a1, a2, a3, e0, e1, e2, e3;
+                q8::e4m3x4_to_half2x2(kw[st], a0, a2);
+                q8::e4m3x4_to_half2x2(kw[8 + st], a1, a3);
+                q8::e4m3x4_to_half2x2(kw[st + 1], e0, e2);
+                q8::e4m3x4_to_half2x2(kw[9 + st], e1, e3);
+                ptx::mma_16816(s0, s1, s2, s3, a0, a1, a2, a3, qa[2 * st], qa[2 * st + 1], s0, s1, s2, s3);
+                ptx::mma_16816(t0, t1, t2, t3, e0, e1, e2, e3, qa[2 * st + 2], qa[2 * st + 3], t0, t1, t2, t3);
+            }
+            // lanes 4 g hold the scores of tokens tok0 + g (s0 + t0) and tok0 + g + 8 (s2 + t2)
+            const int ta = tok0 + g, tb = ta + 8;
+            const bool oka = full || ta < ntok, okb = full || tb < ntok;
+            const float ksa = ptx::ldsf(kb + St::kScales + ta * 4), ksb = ptx::ldsf(kb + St::kScales + tb * 4);
+            const float vsa = ptx::ldsf(kb + St::kScales + (kTile + ta) * 4);
+            const float vsb = ptx::ldsf(kb + St::kScales + (kTile + tb) * 4);
+            const float xa = oka ? (s0 + t0) * ksa * p.scale_log2 : -INFINITY;
+            const float xb = okb ? (s2 + t2) * ksb * p.scale_log2 : -INFINITY;
+            // the reference covers x + log2(V row scale): weight x scale <= 1 fits fp16
+            float mx = fmaxf(oka ? xa + ptx::lg2(fmaxf(vsa, 0x1p-100f)) : -INFINITY,
+                             okb ? xb + ptx::lg2(fmaxf(vsb, 0x1p-100f)) : -INFINITY);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            mx = __shfl_sync(0xffffffffu, mx, 0);    // lane 0's (= every 4 g lane's): warp-uniform
+            if (mx > m) {
+                const float alpha = ptx::ex2(m - mx);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) oacc[i] *= alpha;
+                l *= alpha;
+                m = mx;
+            }
+            // weights; a token past the context weighs 0 whatever its stale scale holds
+            const float pa = oka ? ptx::ex2(xa - m) : 0.f, pb = okb ? ptx::ex2(xb - m) : 0.f;
+            l += pa + pb;
+            const uint32_t pk = ptx::pack_half2(oka ? pa * vsa : 0.f, okb ? pb * vsb : 0.f);
+            // B = (weight x V scale)^T, column 0 = lanes 0-3: tokens 2 c4, 2 c4 + 1 (b0) and
+            // 2 c4 + 8, 2 c4 + 9 (b1), gathered from lanes 8 c4 and 8 c4 + 4
+            const uint32_t xw = __shfl_sync(0xffffffffu, pk, 8 * c4);
+            const uint32_t yw = __shfl_sync(0xffffffffu, pk, 8 * c4 + 4);
+            const uint32_t pb0 = g == 0 ? ptx::prmt(xw, yw, 0x5410u) : 0u;
+            const uint32_t pb1 = g == 0 ? ptx::prmt(xw, yw, 0x7632u) : 0u;
+            // O^T += V^T P^T over 8 chunks of 16 dims. ldmatrix (transposed) gives lane (g, c4)
+            // the codes of tokens 2 c4, 2 c4 + 1 at dims 2 g, 2 g + 1 of a chunk; the chunk's
+            // A rows are g <-> dim 16 u + 2 g and g + 8 <-> dim 16 u + 2 g + 1
+            const int mi = lane >> 3;                  // the matrix whose row this lane addresses
+            const uint32_t vrow = vb + (tok0 + (mi & 1) * 8 + (lane & 7)) * 128;
+            if (!full && tok0 + 16 > ntok) {
+                // rows past the context may hold any codes (NaN ones included) and a zero
+                // weight does not cancel a NaN in the product: zero this warp's such V rows
+                const int r0 = max(ntok, tok0);
+                for (int i = lane; i < (tok0 + 16 - r0) * 8; i += 32)
+                    ptx::sts128(vb + (r0 + (i >> 3)) * 128 + (i & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
+                ptx::fence_proxy_async_shared();       // before the stage's next TMA fill
+                __syncwarp();
             }
 #pragma unroll
-            for (int e = 0; e < NCH * 4; ++e) o[e] = make_float2(0.f, 0.f);
-            m = -INFINITY;
-            l = 0.f;
-            seg_g0 = g0 + k;
-            if constexpr (!Q8) {
-                // a cascade member: stage its prefix pieces now, so the combine at the end
-                // of the (s, h) reads them from shared memory (the previous combine's last
-                // barrier has released the buffer)
-                if (sm.beg[c.s] > 0) {
-                    const float *src = p.pre + ((size_t)c.s * H + c.h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
-                    const int n16 = p.pre_splits * (D + 4) / 4;
-                    for (int i = tid; i < n16; i += kConsumerThreads)
-                        ptx::cp_async_16_cg(ptx::smem_addr(sm.pre) + i * 16, src + i * 4);
-                    ptx::cp_async_commit();
+            for (int hh = 0; hh < 4; ++hh) {
+                uint32_t r[4];
+                ptx::ldmatrix_x4_trans(vrow + (((2 * hh + (mi >> 1)) ^ (lane & 7)) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int uu = 0; uu < 2; ++uu) {
+                    const int u = 2 * hh + uu;
+                    // bytes [t dim, t+1 dim, t dim+1, t+1 dim+1] of tokens 0-7 and 8-15 ->
+                    // [t dim, t+1 dim] (A rows g) and [t dim+1, t+1 dim+1] (A rows g + 8)
+                    uint32_t a0, a1, a2, a3;
+                    q8::e4m3x4_to_half2x2(ptx::prmt(r[2 * uu], 0u, 0x3120u), a0, a1);
+                    q8::e4m3x4_to_half2x2(ptx::prmt(r[2 * uu + 1], 0u, 0x3120u), a2, a3);
+                    float d0, d1, d2, d3;
+                    ptx::mma_16816(d0, d1, d2, d3, a0, a1, a2, a3, pb0, pb1, 0.f, 0.f, 0.f, 0.f);
+                    oacc[2 * u] += d0;
+                    oacc[2 * u + 1] += d2;
                 }
             }
-        }
-        // this group's rows of the tile: grp, grp + kGroups, ...; kr/vr hold each
-        // chunk's 8 elements as four fp16 pairs (fp16 cache), kcw/vcw the row's E4M3
-        // codes, four to a word, converted where they are used (fewer live registers)
-        const bool full = ntok == kTile;
-        bool vld[kTokPerGroup];
-        uint32_t kr[kTokPerGroup][NCH][4], vr[kTokPerGroup][NCH][4];
-        uint32_t kcw[kTokPerGroup][NCH * 2], vcw[kTokPerGroup][NCH * 2];
-        float ksc[kTokPerGroup], vsc[kTokPerGroup];
-#pragma unroll
-        for (int u = 0; u < kTokPerGroup; ++u) {
-            const int row = grp + kGroups * u;
-            vld[u] = full || row < ntok;
-            if constexpr (Q8) {
-                if constexpr (NCH == 2) {
-                    const uint4 a = ptx::lds128(kb + row * St::kRow + j * 16);
-                    const uint4 b = ptx::lds128(vb + row * St::kRow + j * 16);
-                    kcw[u][0] = a.x; kcw[u][1] = a.y; kcw[u][2] = a.z; kcw[u][3] = a.w;
-                    vcw[u][0] = b.x; vcw[u][1] = b.y; vcw[u][2] = b.z; vcw[u][3] = b.w;
-                } else {
-                    const uint2 a = ptx::lds64(kb + row * St::kRow + j * 8);
-                    const uint2 b = ptx::lds64(vb + row * St::kRow + j * 8);
-                    kcw[u][0] = a.x; kcw[u][1] = a.y;
-                    vcw[u][0] = b.x; vcw[u][1] = b.y;
-                }
-                ksc[u] = ptx::ldsf(kb + St::kScales + row * 4);
-                vsc[u] = ptx::ldsf(kb + St::kScales + kTile * 4 + row * 4);
-            } else {
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    const uint4 a = ptx::lds128(kb + row * St::kRow + chunk_elem<D, Q8>(j, ch) * 2);
-                    const uint4 b = ptx::lds128(vb + row * St::kRow + chunk_elem<D, Q8>(j, ch) * 2);
-                    kr[u][ch][0] = a.x; kr[u][ch][1] = a.y; kr[u][ch][2] = a.z; kr[u][ch][3] = a.w;
-                    vr[u][ch][0] = b.x; vr[u][ch][1] = b.y; vr[u][ch][2] = b.z; vr[u][ch][3] = b.w;
-                }
-                ksc[u] = 1.f;
-                vsc[u] = 1.f;
-            }
-        }
-        float x[kTokPerGroup];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < kTokPerGroup; ++u) {
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    uint16_t klo, khi;
-                    ptx::split_half2(pair_of<Q8, NCH>(kcw[u], kr[u], ch, e), klo, khi);
-                    a0 = ptx::fma_f16_f32(qlo[ch * 4 + e], klo, a0);
-                    a1 = ptx::fma_f16_f32(qhi[ch * 4 + e], khi, a1);
-                }
-            }
-            float dot = a0 + a1;
-            dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-            if constexpr (Q8) dot *= ksc[u];
-            x[u] = vld[u] ? dot * p.scale_log2 : -INFINITY;
-            // E4M3: the reference max covers x + log2(V row scale), so that every weight
-            // 2^(x - m) * scale is at most 1 and fits fp16 for the p.V products
-            // (a scale of 0, which the quantiser never writes, counts as 2^-100)
-            if constexpr (Q8) mx = fmaxf(mx, vld[u] ? x[u] + ptx::lg2(fmaxf(vsc[u], 0x1p-100f)) : -INFINITY);
-            else mx = fmaxf(mx, x[u]);
-        }
-        if (mx > m) {                          // new running max: rescale (group-uniform branch)
-            const float alpha = ptx::ex2(m - mx);
-#pragma unroll
-            for (int e = 0; e < NCH * 4; ++e) o[e] = make_float2(o[e].x * alpha, o[e].y * alpha);
-            l *= alpha;
-            m = mx;
-        }
-        // rows past the context may hold any bits (NaN included): weight 0 and V skipped
-        float pw[kTokPerGroup];
-#pragma unroll
-        for (int u = 0; u < kTokPerGroup; ++u) {
-            pw[u] = vld[u] ? ptx::ex2(x[u] - m) : 0.f;
-            l += pw[u];
-        }
-        if constexpr (Q8) {
-            // o += (weight x V row scale) in fp16 x the row's codes as fp16 (exact), one
-            // mixed-precision FMA per element with fp32 accumulation
-            uint16_t wh[kTokPerGroup];
-#pragma unroll
-            for (int u = 0; u < kTokPerGroup; ++u) wh[u] = __half_as_ushort(__float2half_rn(pw[u] * vsc[u]));
-#pragma unroll
-            for (int u = 0; u < kTokPerGroup; ++u) {
-                if (!full && !vld[u]) continue;
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint16_t vlo, vhi;
-                        ptx::split_half2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e), vlo, vhi);
-                        o[ch * 4 + e].x = ptx::fma_f16_f32(wh[u], vlo, o[ch * 4 + e].x);
-                        o[ch * 4 + e].y = ptx::fma_f16_f32(wh[u], vhi, o[ch * 4 + e].y);
-                    }
-            }
-        } else if (full) {
-#pragma unroll
-            for (int u = 0; u < kTokPerGroup; ++u)
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e)),
-                                                   o[ch * 4 + e]);
         } else {
-#pragma unroll
+            if (first) {
+    #pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const uint4 raw = ptx::lds128(kb + St::kQ + chunk_elem<D, Q8>(j, ch) * 2);
+                    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) ptx::split_half2(wv[e], qlo[ch * 4 + e], qhi[ch * 4 + e]);
+                }
+    #pragma unroll
+                for (int e = 0; e < NCH * 4; ++e) o[e] = make_float2(0.f, 0.f);
+                m = -INFINITY;
+                l = 0.f;
+                if constexpr (!Q8) {
+                    // a cascade member: stage its prefix pieces now, so the combine at the end
+                    // of the (s, h) reads them from shared memory (the previous combine's last
+                    // barrier has released the buffer)
+                    if (sm.beg[c.s] > 0) {
+                        const float *src = p.pre + ((size_t)c.s * H + c.h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
+                        const int n16 = p.pre_splits * (D + 4) / 4;
+                        for (int i = tid; i < n16; i += kConsumerThreads)
+                            ptx::cp_async_16_cg(ptx::smem_addr(sm.pre) + i * 16, src + i * 4);
+                        ptx::cp_async_commit();
+                    }
+                }
+            }
+            // this group's rows of the tile: grp, grp + kGroups, ...; kr/vr hold each
+            // chunk's 8 elements as four fp16 pairs (fp16 cache), kcw/vcw the row's E4M3
+            // codes, four to a word, converted where they are used (fewer live registers)
+            const bool full = ntok == kTile;
+            bool vld[kTokPerGroup];
+            uint32_t kr[kTokPerGroup][NCH][4], vr[kTokPerGroup][NCH][4];
+            uint32_t kcw[kTokPerGroup][NCH * 2], vcw[kTokPerGroup][NCH * 2];
+            float ksc[kTokPerGroup], vsc[kTokPerGroup];
+    #pragma unroll
             for (int u = 0; u < kTokPerGroup; ++u) {
-                if (!vld[u]) continue;
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e)),
-                                                   o[ch * 4 + e]);
+                const int row = grp + kGroups * u;
+                vld[u] = full || row < ntok;
+                if constexpr (Q8) {
+                    if constexpr (NCH == 2) {
+                        const uint4 a = ptx::lds128(kb + row * St::kRow + j * 16);
+                        const uint4 b = ptx::lds128(vb + row * St::kRow + j * 16);
+                        kcw[u][0] = a.x; kcw[u][1] = a.y; kcw[u][2] = a.z; kcw[u][3] = a.w;
+                        vcw[u][0] = b.x; vcw[u][1] = b.y; vcw[u][2] = b.z; vcw[u][3] = b.w;
+                    } else {
+                        const uint2 a = ptx::lds64(kb + row * St::kRow + j * 8);
+                        const uint2 b = ptx::lds64(vb + row * St::kRow + j * 8);
+                        kcw[u][0] = a.x; kcw[u][1] = a.y;
+                        vcw[u][0] = b.x; vcw[u][1] = b.y;
+                    }
+                    ksc[u] = ptx::ldsf(kb + St::kScales + row * 4);
+                    vsc[u] = ptx::ldsf(kb + St::kScales + kTile * 4 + row * 4);
+                } else {
+    #pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        const uint4 a = ptx::lds128(kb + row * St::kRow + chunk_elem<D, Q8>(j, ch) * 2);
+                        const uint4 b = ptx::lds128(vb + row * St::kRow + chunk_elem<D, Q8>(j, ch) * 2);
+                        kr[u][ch][0] = a.x; kr[u][ch][1] = a.y; kr[u][ch][2] = a.z; kr[u][ch][3] = a.w;
+                        vr[u][ch][0] = b.x; vr[u][ch][1] = b.y; vr[u][ch][2] = b.z; vr[u][ch][3] = b.w;
+                    }
+                    ksc[u] = 1.f;
+                    vsc[u] = 1.f;
+                }
+            }
+            float x[kTokPerGroup];
+            float mx = -INFINITY;
+    #pragma unroll
+            for (int u = 0; u < kTokPerGroup; ++u) {
+                float a0 = 0.f, a1 = 0.f;
+    #pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint16_t klo, khi;
+                        ptx::split_half2(pair_of<Q8, NCH>(kcw[u], kr[u], ch, e), klo, khi);
+                        a0 = ptx::fma_f16_f32(qlo[ch * 4 + e], klo, a0);
+                        a1 = ptx::fma_f16_f32(qhi[ch * 4 + e], khi, a1);
+                    }
+                }
+                float dot = a0 + a1;
+                dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                if constexpr (Q8) dot *= ksc[u];
+                x[u] = vld[u] ? dot * p.scale_log2 : -INFINITY;
+                // E4M3: the reference max covers x + log2(V row scale), so that every weight
+                // 2^(x - m) * scale is at most 1 and fits fp16 for the p.V products
+                // (a scale of 0, which the quantiser never writes, counts as 2^-100)
+                if constexpr (Q8) mx = fmaxf(mx, vld[u] ? x[u] + ptx::lg2(fmaxf(vsc[u], 0x1p-100f)) : -INFINITY);
+                else mx = fmaxf(mx, x[u]);
+            }
+            if (mx > m) {                          // new running max: rescale (group-uniform branch)
+                const float alpha = ptx::ex2(m - mx);
+    #pragma unroll
+                for (int e = 0; e < NCH * 4; ++e) o[e] = make_float2(o[e].x * alpha, o[e].y * alpha);
+                l *= alpha;
+                m = mx;
+            }
+            // rows past the context may hold any bits (NaN included): weight 0 and V skipped
+            float pw[kTokPerGroup];
+    #pragma unroll
+            for (int u = 0; u < kTokPerGroup; ++u) {
+                pw[u] = vld[u] ? ptx::ex2(x[u] - m) : 0.f;
+                l += pw[u];
+            }
+            if constexpr (Q8) {
+                // o += (weight x V row scale) in fp16 x the row's codes as fp16 (exact), one
+                // mixed-precision FMA per element with fp32 accumulation
+                uint16_t wh[kTokPerGroup];
+    #pragma unroll
+                for (int u = 0; u < kTokPerGroup; ++u) wh[u] = __half_as_ushort(__float2half_rn(pw[u] * vsc[u]));
+    #pragma unroll
+                for (int u = 0; u < kTokPerGroup; ++u) {
+                    if (!full && !vld[u]) continue;
+    #pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch)
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint16_t vlo, vhi;
+                            ptx::split_half2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e), vlo, vhi);
+                            o[ch * 4 + e].x = ptx::fma_f16_f32(wh[u], vlo, o[ch * 4 + e].x);
+                            o[ch * 4 + e].y = ptx::fma_f16_f32(wh[u], vhi, o[ch * 4 + e].y);
+                        }
+                }
+            } else if (full) {
+    #pragma unroll
+                for (int u = 0; u < kTokPerGroup; ++u)
+    #pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch)
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e)),
+                                                       o[ch * 4 + e]);
+            } else {
+    #pragma unroll
+                for (int u = 0; u < kTokPerGroup; ++u) {
+                    if (!vld[u]) continue;
+    #pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch)
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            o[ch * 4 + e] = ptx::ffma2(make_float2(pw[u], pw[u]), ptx::half2_to_float2(pair_of<Q8, NCH>(vcw[u], vr[u], ch, e)),
+                                                       o[ch * 4 + e]);
+                }
             }
         }
         __syncwarp();
@@ -782,33 +940,52 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
 
         const bool last = (k == n - 1) || (c.t == c.nt - 1);
         if (last) {
-            // ---- merge the group states of this (s, h): the 4 groups of a warp
-            // by xor-shuffles, then the warps through shared memory
-            float mw = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-            mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
-            const float sc = mw == -INFINITY ? 0.f : ptx::ex2(m - mw);   // a warp with no row at all: 0
-            float lw = l * sc;
-            lw += __shfl_xor_sync(0xffffffffu, lw, 8);
-            lw += __shfl_xor_sync(0xffffffffu, lw, 16);
+            if constexpr (kMma) {
+                // ---- this warp's state to shared memory: l summed over lanes 4 g, output
+                // dims 16 u + 2 g, + 1 from lanes 4 g
+                float lw = l;                       // lanes 4 g hold the sums of their tokens
+                lw += __shfl_xor_sync(0xffffffffu, lw, 4);
+                lw += __shfl_xor_sync(0xffffffffu, lw, 8);
+                lw += __shfl_xor_sync(0xffffffffu, lw, 16);
+                if ((lane & 3) == 0) {
 #pragma unroll
-            for (int e = 0; e < NCH * 4; ++e) {
-                float2 v = make_float2(o[e].x * sc, o[e].y * sc);
-                v.x += __shfl_xor_sync(0xffffffffu, v.x, 8);
-                v.y += __shfl_xor_sync(0xffffffffu, v.y, 8);
-                v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
-                v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
-                o[e] = v;
-            }
-            if (lane < 8) {
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    float4 *dst = reinterpret_cast<float4 *>(sm.red_o + warp * D + chunk_elem<D, Q8>(j, ch));
-                    dst[0] = make_float4(o[ch * 4 + 0].x, o[ch * 4 + 0].y, o[ch * 4 + 1].x, o[ch * 4 + 1].y);
-                    dst[1] = make_float4(o[ch * 4 + 2].x, o[ch * 4 + 2].y, o[ch * 4 + 3].x, o[ch * 4 + 3].y);
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<float2 *>(sm.red_o + warp * D + 16 * u + 2 * (lane >> 2)) =
+                            make_float2(oacc[2 * u], oacc[2 * u + 1]);
                 }
                 if (lane == 0) {
-                    sm.red_m[warp] = mw;
+                    sm.red_m[warp] = m;
                     sm.red_l[warp] = lw;
+                }
+            } else {
+                // ---- merge the group states of this (s, h): the 4 groups of a warp
+                // by xor-shuffles, then the warps through shared memory
+                float mw = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
+                const float sc = mw == -INFINITY ? 0.f : ptx::ex2(m - mw);   // a warp with no row at all: 0
+                float lw = l * sc;
+                lw += __shfl_xor_sync(0xffffffffu, lw, 8);
+                lw += __shfl_xor_sync(0xffffffffu, lw, 16);
+    #pragma unroll
+                for (int e = 0; e < NCH * 4; ++e) {
+                    float2 v = make_float2(o[e].x * sc, o[e].y * sc);
+                    v.x += __shfl_xor_sync(0xffffffffu, v.x, 8);
+                    v.y += __shfl_xor_sync(0xffffffffu, v.y, 8);
+                    v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
+                    v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
+                    o[e] = v;
+                }
+                if (lane < 8) {
+    #pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        float4 *dst = reinterpret_cast<float4 *>(sm.red_o + warp * D + chunk_elem<D, Q8>(j, ch));
+                        dst[0] = make_float4(o[ch * 4 + 0].x, o[ch * 4 + 0].y, o[ch * 4 + 1].x, o[ch * 4 + 1].y);
+                        dst[1] = make_float4(o[ch * 4 + 2].x, o[ch * 4 + 2].y, o[ch * 4 + 3].x, o[ch * 4 + 3].y);
+                    }
+                    if (lane == 0) {
+                        sm.red_m[warp] = mw;
+                        sm.red_l[warp] = lw;
+                    }
                 }
             }
             if constexpr (!Q8) {
@@ -839,7 +1016,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             }
             const int32_t seg_lo = sm.base[c.s] + c.h * c.nt;   // (s, h) tiles: [seg_lo, seg_lo + nt)
             const int32_t seg_hi = seg_lo + c.nt - 1;
-            const int32_t ca = cta_of(total, grid, seg_lo);
+            const int32_t ca = cta_of(total, grid, seg_lo);    // the CTAs covering the (s, h)
             const int32_t cb = cta_of(total, grid, seg_hi);
             __half *dst_out = p.out + ((size_t)c.s * H + c.h) * D;
             if (ca == cb) {
@@ -851,7 +1028,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                     if (d < D) dst_out[d] = __float2half_rn(O[r] * inv);
                 }
             } else {
-                const int slot = seg_g0 == g0 ? 0 : 1;  // 0: the CTA's first (s, h); 1: its last
+                const int slot = seg_lo <= g0 ? 0 : 1;  // 0: the CTA's first (s, h); 1: its last
                 float *piece = p.pieces + ((size_t)cta * 2 + slot) * piece_stride(D);
 #pragma unroll
                 for (int r = 0; r < DPT; ++r) {
@@ -1032,11 +1209,19 @@ size_t pieces_offset(int S, int H) {
     return counters_offset() + ((size_t)S * H * sizeof(int32_t) + 255) / 256 * 256;
 }
 
-size_t workspace_bytes_for(int S, int H, int D, int num_sms) {
-    return pieces_offset(S, H) + (size_t)num_sms * kMaxCtasPerSm * 2 * piece_stride(D) * sizeof(float);
+// Workspace for a launch of `grid` CTAs: two pieces per CTA.
+size_t workspace_need(int S, int H, int D, int grid) {
+    return pieces_offset(S, H) + (size_t)grid * 2 * piece_stride(D) * sizeof(float);
 }
 
+// An upper bound for any launch on a device with num_sms SMs.
+size_t workspace_bytes_for(int S, int H, int D, int num_sms) {
+    return workspace_need(S, H, D, num_sms * kMaxCtasPerSm);
+}
+
+// swizzle128: the tile lands 128-byte swizzled (E4M3 head_dim 128: 128-byte rows).
 pkv_status encode_map(CUtensorMap *map, const void *base, int N, int B, int H, int D, int layout, bool q8) {
+    const bool swizzle128 = q8 && D == 128;
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t elem = q8 ? 1 : 2;
@@ -1054,7 +1239,8 @@ pkv_status encode_map(CUtensorMap *map, const void *base, int N, int B, int H, i
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                     const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return PKV_OK;
@@ -1156,7 +1342,7 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     size_t smem = 0;
     pkv_status st = launch_shape(dev, head_dim, q8, num_seqs, &grid, &per, &sms, &smem);
     if (st != PKV_OK) return st;
-    const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, sms);
+    const size_t need = workspace_need(num_seqs, num_heads, head_dim, grid);
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", workspace_bytes, need);
 
@@ -1179,6 +1365,7 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     prm.H = num_heads;
     prm.max_blocks = max_blocks;
     prm.B = block_size;
+    prm.lgB = __builtin_ctz((unsigned)block_size);   // a supported block size is a power of two
     prm.N = num_blocks;
     prm.layout = layout;
     const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)head_dim);
@@ -1346,11 +1533,13 @@ pkv_status pkv_decode_attention_static(const void *q, const void *k_cache, const
     if (num_seqs == 0) return PKV_OK;
     if (num_heads < 1 || !supported_head_dim(head_dim))
         return fail(PKV_ERR_INVALID_ARG, "bad num_heads or head_dim");
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return fail(PKV_ERR_CUDA, "no CUDA device");
-    const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, sms);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(PKV_ERR_CUDA, "no CUDA device");
+    int grid = 0, per = 0, sms = 0;
+    size_t smem = 0;
+    pkv_status st0 = launch_shape(dev, head_dim, false, num_seqs, &grid, &per, &sms, &smem);
+    if (st0 != PKV_OK) return st0;
+    const size_t need = workspace_need(num_seqs, num_heads, head_dim, grid);
     if (need > kStaticScratchBytes)
         return fail(PKV_ERR_INVALID_ARG,
                     "%d sequences x %d heads (head_dim %d) need %zu bytes of scratch; the static scratch holds %zu",

@@ -102,6 +102,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses of shared memory.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 4-byte asynchronous copy global -> shared (the non-bulk async copy; cached in L1).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
@@ -147,6 +153,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
@@ -199,6 +210,47 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t w) {
     __half2 h;
     memcpy(&h, &w, 4);
     return __half22float2(h);
+}
+
+// Warp-level tensor-core product D = A B + C, m16n8k16, fp16 A and B, fp32 C and D
+// (the products are exact, the sums fp32). Fragments (lane = 4 g + c): A row-major,
+// a0 = (row g, k 2c..2c+1), a1 = (row g+8, same k), a2 = (row g, k 2c+8..2c+9),
+// a3 = (row g+8, k 2c+8..); B column-major, b0 = (k 2c..2c+1, col g), b1 = (k 2c+8..,
+// col g); C/D c0 = (row g, col 2c), c1 = (row g, col 2c+1), c2/c3 = row g+8. The
+// lower half of an fp16 pair register is the element with the smaller k.
+__device__ __forceinline__ void mma_16816(float &d0, float &d1, float &d2, float &d3, uint32_t a0, uint32_t a1,
+                                          uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1, float c0, float c1,
+                                          float c2, float c3) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %12, %13};"
+        : "=f"(d0), "=f"(d1), "=f"(d2), "=f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
+
+// Four 8x8 matrices of 16-bit elements from shared memory, transposed: lanes 8i..8i+7
+// give the addresses of the 8 rows (16 bytes each) of matrix i; lane 4 g + c receives
+// in register i the elements (row 2c, col g) (low half) and (row 2c+1, col g).
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                                  uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// Byte permute: byte i of the result is byte (sel >> 4 i) & 7 of the pair {b, a} (a = bytes 0-3).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Two fp32 values -> one fp16 pair (round to nearest even), lo in the lower half.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // Programmatic dependent launch. launch_dependents lets the next kernel of the

@@ -55,5 +55,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t two_codes) {
     return out;
 }
 
+// Four E4M3 codes (byte i = element i) -> two fp16 pairs: lo = elements 0, 1 and
+// hi = elements 2, 3 (exact: every E4M3 value is an fp16 value).
+__device__ __forceinline__ void e4m3x4_to_half2x2(uint32_t four_codes, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 c0, c1;\n\tmov.b32 {c0, c1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, c0;\n\tcvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
+}
+
 }  // namespace q8
 }  // namespace pkv
