@@ -430,8 +430,11 @@ int32_t pkv_prefix_splits(int32_t num_groups, int32_t num_heads, int32_t max_pre
  * device uint32 word (required): a group outside [0, num_seqs), with more
  * than PKV_MAX_GROUP_SEQS members or a prefix not in whole blocks inside the
  * table is flagged PKV_DEV_BAD_LENGTH and writes no pieces. fp16 products,
- * fp32 accumulation, weights enter P V in fp16. The pool must be fp16, HND,
- * head_dim 128 (UNSUPPORTED otherwise). flags: 0, or PKV_ATTN_INPUTS_EARLY:
+ * fp32 accumulation, weights enter P V in fp16. The pool must be HND with
+ * head_dim 128, fp16 (the pass runs on tcgen05) or E4M3 (on the warp-level
+ * tensor cores, K and V read as code x row scale; there m is at least
+ * max_t (x_t + log2 of t's V row scale), so each weight times that scale stays
+ * within fp16) -- UNSUPPORTED otherwise. flags: 0, or PKV_ATTN_INPUTS_EARLY:
  * the groups, the block tables and the prefix's cached K/V are read -- and the
  * K/V tiles' loads issued -- before the kernel that precedes it on the stream
  * has finished; q is read and the pieces written only after. The caller
@@ -447,14 +450,13 @@ pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void 
 /* pkv_decode_append_attention and pkv_pool_decode_attention in one entry, with
  * the private half of the cascade. k_new, v_new, slot_mapping: all NULL = no
  * append (else as pkv_decode_append_attention). seq_begin, pieces: both NULL =
- * no cascade (the plain attention); the cascade needs an fp16 pool with head_dim
- * 128 (UNSUPPORTED otherwise), and its prefix pass the HND layout. Otherwise seq_begin is device int32
+ * no cascade (the plain attention); the cascade needs head_dim 128
+ * (UNSUPPORTED otherwise), and its prefix pass the HND layout. Otherwise seq_begin is device int32
  * [num_seqs]: sequence s attends here to its tokens [seq_begin[s], T_s) and,
  * when seq_begin[s] > 0, merges in the `splits` prefix pieces that
  * pkv_prefix_attention wrote for it earlier on the same stream. seq_begin[s]
  * must be a multiple of the block size in [0, T_s]; any other value is
- * flagged PKV_DEV_BAD_LENGTH and read as 0 (no prefix). fp16 pools only when
- * cascading (the prefix pass runs on fp16 tensor cores).
+ * flagged PKV_DEV_BAD_LENGTH and read as 0 (no prefix).
  * flags: 0, or PKV_ATTN_INPUTS_EARLY. With it, the kernel reads the block
  * tables, the lengths, seq_begin and the cached K/V rows -- and issues its first
  * tiles' loads -- before the kernel that precedes it on the stream has finished;

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libpkv.so")
 OBJDIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["pool.cpp", "cascade.cpp", "decode_attention.cu", "device_ops.cu", "prefill_attention.cu"]
+SOURCES = ["pool.cpp", "cascade.cpp", "decode_attention.cu", "device_ops.cu", "prefill_attention.cu",
+           "prefix_attention_q8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", f"-I{INCLUDE}", f"-I{CSRC}"]
 

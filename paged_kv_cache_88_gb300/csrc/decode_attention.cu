@@ -519,7 +519,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 // asynchronous copies of four tokens each: lanes 0-15 the K scales of tokens
                 // 4l..4l+3, lanes 16-31 the V scales. A run of four never leaves its block and
                 // every copy is 16-byte aligned, because the block size (8..256) and the tile
-                // start (a multiple of 64: an E4M3 cache takes no cascade, so beg = 0) are
+                // start (the cascade's prefix length, whole blocks, plus a multiple of 64) are
                 // multiples of 4 and the host refuses scale pools that are not 16-byte aligned.
                 // Issued before lane 0's arrival, so the stage's phase cannot complete without them.
                 static_assert(kTile == 64, "16-byte scale copies: 16 lanes x 4 tokens per pool");
@@ -1309,8 +1309,8 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     if ((seq_begin == nullptr) != (pieces == nullptr))
         return fail(PKV_ERR_INVALID_ARG, "seq_begin and pieces go together (both NULL: no cascade)");
     if (seq_begin) {
-        if (q8 || head_dim != 128)
-            return fail(PKV_ERR_UNSUPPORTED, "the cascade is built for fp16 pools with head_dim 128");
+        if (head_dim != 128)
+            return fail(PKV_ERR_UNSUPPORTED, "the cascade is built for pools with head_dim 128");
         if (splits < 1 || splits > PKV_MAX_PREFIX_SPLITS)
             return fail(PKV_ERR_INVALID_ARG, "splits %d outside 1..%d", splits, PKV_MAX_PREFIX_SPLITS);
         if ((reinterpret_cast<uintptr_t>(seq_begin) & 3u) || !aligned16(pieces))

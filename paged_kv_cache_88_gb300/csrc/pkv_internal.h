@@ -67,6 +67,13 @@ inline PoolLayer pool_layer(const pkv_pool *p, int32_t layer) {
 
 inline bool supported_head_dim(int32_t d) { return d == 64 || d == 128 || d == 256; }
 
+// The cascade's prefix pass for an E4M3 pool (HND, head_dim 128; arguments validated by
+// pkv_prefix_attention). Defined in prefix_attention_q8.cu.
+pkv_status prefix_attention_q8(const pkv_pool *pool, int32_t layer, const void *q, const pkv_prefix_group *groups,
+                               int32_t num_groups, int32_t splits, const int32_t *block_tables, int32_t max_blocks,
+                               int32_t num_seqs, float scale, void *pieces, uint32_t *status, uint32_t flags,
+                               void *stream);
+
 inline bool supported_block_size(int32_t b) {
     return b == 8 || b == 16 || b == 32 || b == 64 || b == 128 || b == 256;
 }

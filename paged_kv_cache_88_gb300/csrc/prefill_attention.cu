@@ -844,8 +844,17 @@ pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void 
                                 int32_t num_groups, int32_t splits, const int32_t *block_tables, int32_t max_blocks,
                                 int32_t num_seqs, float scale, void *pieces, size_t pieces_bytes, uint32_t *status,
                                 uint32_t flags, void *stream) {
-    pkv_status st = check_pool(pool, layer, "the prefix pass");
+    // an E4M3 pool (HND, head_dim 128) has its own prefix pass; the checks below hold for both
+    const bool q8 = pool && pool->desc.kv_dtype == PKV_KV_E4M3 && pool->desc.layout == PKV_LAYOUT_HND &&
+                    pool->desc.head_dim == kD;
+    pkv_status st = q8 ? PKV_OK : check_pool(pool, layer, "the prefix pass");
     if (st != PKV_OK) return st;
+    if (q8) {
+        if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
+        if (layer < 0 || layer >= pool->desc.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+        if (!pool->k_scale || !aligned16(pool->k_scale) || !aligned16(pool->v_scale))
+            return fail(PKV_ERR_INVALID_ARG, "an E4M3 pool needs 16-byte aligned scale pools (pkv_pool_set_scales)");
+    }
     if (flags & ~(uint32_t)PKV_ATTN_INPUTS_EARLY) return fail(PKV_ERR_INVALID_ARG, "unknown flags %#x", flags);
     if (num_groups < 0 || num_seqs < 0 || max_blocks < 1 || splits < 1 || splits > PKV_MAX_PREFIX_SPLITS)
         return fail(PKV_ERR_INVALID_ARG, "bad sizes (splits in 1..%d)", PKV_MAX_PREFIX_SPLITS);
@@ -858,6 +867,9 @@ pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void 
     const pkv_pool_desc &d = pool->desc;
     const size_t need = (size_t)num_seqs * d.num_heads * PKV_MAX_PREFIX_SPLITS * (kD + 4) * sizeof(float);
     if (pieces_bytes < need) return fail(PKV_ERR_INVALID_ARG, "pieces: %zu bytes < %zu needed", pieces_bytes, need);
+    if (q8)
+        return prefix_attention_q8(pool, layer, q, groups, num_groups, splits, block_tables, max_blocks, num_seqs,
+                                   scale, pieces, status, flags, stream);
     CUtensorMap qmap, kmap, vmap;
     st = encode_maps(pool, layer, q, num_seqs, &qmap, &kmap, &vmap);
     if (st != PKV_OK) return st;

@@ -41,8 +41,8 @@ class DecodeEngine:
         # chain for every (sequence, head) stalls the tile pipeline, and a separate
         # append launch measured up to 20 % faster per step (13B shape, batch 128)
         self.fused = (w.kv_dtype == "f16") if fused is None else bool(fused)
-        # shared-prefix cascade: only where the tensor-core prefix pass is built
-        self.cascade = bool(cascade) and w.kv_dtype == "f16" and w.layout == "HND" and w.head_dim == 128
+        # shared-prefix cascade: where a prefix pass is built (fp16 and E4M3 pools, HND, head_dim 128)
+        self.cascade = bool(cascade) and w.layout == "HND" and w.head_dim == 128
         self.device = torch.device(device)
         shape = wl.pool_shape(w)
         self.k_scale = self.v_scale = None

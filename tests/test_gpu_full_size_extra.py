@@ -88,6 +88,18 @@ def test_e4m3_long_context_full_size_sampled(free_gpu_memory):
     _e4m3_full(5, [0], n_seqs=4)
 
 
+def test_e4m3_13b_full_size_sampled(free_gpu_memory):
+    """13B shape, batch 128, block 32, pool 90 % occupied after churn, 40 layers (the tensor-core
+    E4M3 consumer at its largest batch): layers 0 and 39, sixteen sequences, every head."""
+    _e4m3_full(4, [0, 39], n_seqs=16)
+
+
+def test_e4m3_long_context_block_16_full_size_sampled(free_gpu_memory):
+    """The long-context workload at block 16 (four TMA boxes per 64-token tile, 128-entry table
+    windows refilled along 16k-token sequences): layer 0, four sequences, every head."""
+    _e4m3_full(5, [0], n_seqs=4, block_size=16)
+
+
 def _prefill_full(cfg: int, chunk: int, n_seqs: int, heads, block_size=None):
     w = wl.make_workload(cfg, decode_steps=8, block_size=block_size)
     eng = DecodeEngine(w, fill="torch")
