@@ -88,7 +88,7 @@ constexpr int kGroups = kConsumerWarps * 4;       // 8-lane groups
 constexpr int kTokPerGroup = kTile / kGroups;     // rows of a tile one group owns
 constexpr int kStagesF16 = PKV_ATTN_STAGES;
 #ifndef PKV_ATTN_STAGES_Q8
-#define PKV_ATTN_STAGES_Q8 3
+#define PKV_ATTN_STAGES_Q8 2
 #endif
 constexpr int kStagesQ8 = PKV_ATTN_STAGES_Q8;
 static_assert(kTile % kGroups == 0 && kTokPerGroup >= 1 && kTokPerGroup <= 4, "tile / group split");
@@ -161,9 +161,9 @@ __device__ __forceinline__ uint32_t pair_of(const uint32_t (&codes)[NCH * 2], co
 }
 
 // The cascade's prefix pieces of the current (s, h), staged in shared memory while its
-// tiles stream (fp16 caches only: the cascade is built for them).
+// tiles stream (the cascade is built for head_dim 128).
 template <int D, bool Q8>
-__host__ __device__ constexpr int pre_buf_floats() { return Q8 ? 0 : PKV_MAX_PREFIX_SPLITS * (D + 4); }
+__host__ __device__ constexpr int pre_buf_floats() { return D == 128 ? PKV_MAX_PREFIX_SPLITS * (D + 4) : 0; }
 
 // Shared memory: [stages][prefix pieces][reduction][seq arrays][barriers + flags]
 template <int D, bool Q8>
@@ -175,7 +175,7 @@ __host__ __device__ constexpr size_t smem_bytes_t(int S) {
 
 struct Smem {
     unsigned char *stage;  // kStages * stage bytes
-    float *pre;            // [PKV_MAX_PREFIX_SPLITS][D + 4] (fp16 caches)
+    float *pre;            // [PKV_MAX_PREFIX_SPLITS][D + 4] (head_dim 128)
     float *red_o;          // [kConsumerWarps][D]
     float *red_m;          // [kConsumerWarps]
     float *red_l;          // [kConsumerWarps]
@@ -350,6 +350,20 @@ __device__ __forceinline__ void merge_prefix(const Params &p, const float *stage
 template <int D, bool Q8>
 constexpr int min_ctas() {
     return D >= 256 ? 1 : (Stage<D, Q8>::kMma ? PKV_ATTN_MIN_CTAS_MMA : (Q8 ? PKV_ATTN_MIN_CTAS_Q8 : PKV_ATTN_MIN_CTAS));
+}
+
+// A cascade member's first tile: stage its prefix pieces with cp.async, so the combine at the
+// end of the (s, h) reads them from shared memory (the previous combine's last barrier has
+// released the buffer).
+template <int D>
+__device__ __forceinline__ void stage_prefix_pieces(const Params &p, const Smem &sm, int32_t s, int32_t h, int tid) {
+    if constexpr (D == 128) {
+        const float *src = p.pre + ((size_t)s * p.H + h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
+        const int n16 = p.pre_splits * (D + 4) / 4;
+        for (int i = tid; i < n16; i += kConsumerThreads)
+            ptx::cp_async_16_cg(ptx::smem_addr(sm.pre) + i * 16, src + i * 4);
+        ptx::cp_async_commit();
+    }
 }
 
 template <int D, bool Q8>
@@ -700,6 +714,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 for (int i = 0; i < 16; ++i) oacc[i] = 0.f;
                 m = -INFINITY;
                 l = 0.f;
+                if (sm.beg[c.s] > 0) stage_prefix_pieces<D>(p, sm, c.s, c.h, tid);
             }
             // S^T = K q^T: A rows g, g + 8 = tokens tok0 + g, tok0 + g + 8 (bytes [32 c4, 32 c4 + 32)
             // of each, 128-byte swizzled: (token & 7) == g); k step st pairs their word st (dims
@@ -802,18 +817,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 for (int e = 0; e < NCH * 4; ++e) o[e] = make_float2(0.f, 0.f);
                 m = -INFINITY;
                 l = 0.f;
-                if constexpr (!Q8) {
-                    // a cascade member: stage its prefix pieces now, so the combine at the end
-                    // of the (s, h) reads them from shared memory (the previous combine's last
-                    // barrier has released the buffer)
-                    if (sm.beg[c.s] > 0) {
-                        const float *src = p.pre + ((size_t)c.s * H + c.h) * PKV_MAX_PREFIX_SPLITS * (D + 4);
-                        const int n16 = p.pre_splits * (D + 4) / 4;
-                        for (int i = tid; i < n16; i += kConsumerThreads)
-                            ptx::cp_async_16_cg(ptx::smem_addr(sm.pre) + i * 16, src + i * 4);
-                        ptx::cp_async_commit();
-                    }
-                }
+                if (sm.beg[c.s] > 0) stage_prefix_pieces<D>(p, sm, c.s, c.h, tid);
             }
             // this group's rows of the tile: grp, grp + kGroups, ...; kr/vr hold each
             // chunk's 8 elements as four fp16 pairs (fp16 cache), kcw/vcw the row's E4M3
@@ -988,9 +992,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                     }
                 }
             }
-            if constexpr (!Q8) {
-                if (sm.beg[c.s] > 0) ptx::cp_async_wait_all();   // this thread's staged pieces (the barrier shares them)
-            }
+            if (sm.beg[c.s] > 0) ptx::cp_async_wait_all();   // this thread's staged pieces (the barrier shares them)
             ptx::named_barrier(1, kConsumerThreads);
             float M = -INFINITY;
 #pragma unroll
@@ -1020,7 +1022,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
             const int32_t cb = cta_of(total, grid, seg_hi);
             __half *dst_out = p.out + ((size_t)c.s * H + c.h) * D;
             if (ca == cb) {
-                if (sm.beg[c.s] > 0) merge_prefix<D, DPT, !Q8>(p, sm.pre, c.s, c.h, tid, M, L, O);
+                if (sm.beg[c.s] > 0) merge_prefix<D, DPT, true>(p, sm.pre, c.s, c.h, tid, M, L, O);
                 const float inv = 1.f / L;
 #pragma unroll
                 for (int r = 0; r < DPT; ++r) {
@@ -1104,7 +1106,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                             }
                         }
                     }
-                    if (sm.beg[c.s] > 0) merge_prefix<D, DPT, !Q8>(p, sm.pre, c.s, c.h, tid, Mg, Lg, Og);
+                    if (sm.beg[c.s] > 0) merge_prefix<D, DPT, true>(p, sm.pre, c.s, c.h, tid, Mg, Lg, Og);
                     const float inv = 1.f / Lg;
 #pragma unroll
                     for (int r = 0; r < DPT; ++r) {
