@@ -285,9 +285,12 @@ pkv_status pkv_scatter_blocks(const pkv_pool *pool, const int32_t *blocks, int32
  * workspace: device scratch of at least pkv_decode_workspace_bytes(...) bytes,
  *   16-byte aligned, ZERO-FILLED before its first use; each call leaves its
  *   counter area zero again, so one workspace serves every later call on the
- *   same stream (calls that overlap on the GPU must use distinct workspaces).
- *   Its first 4 bytes are the device status word of the call (PKV_DEV_* bits,
- *   sticky: clear it to reset).
+ *   same stream with at most the num_seqs and num_heads it was sized for, any
+ *   head_dim and either cache type (calls that overlap on the GPU must use
+ *   distinct workspaces). A call that ends with PKV_DEV_TIMEOUT may leave
+ *   counters set: zero the workspace again before reusing it. Its first 4
+ *   bytes are the device status word of the call (PKV_DEV_* bits, sticky:
+ *   clear it to reset).
  * Limits (every decode-attention entry point): num_seqs <= 4096 per launch (the
  *   kernel keeps three int32 per sequence in shared memory, and every CTA scans
  *   the lengths in its prologue); head_dim 64, 128 or 256 for an fp16 cache, 64

@@ -1205,20 +1205,24 @@ pkv_status launch_shape(int dev, int D, bool q8, int S, int *grid, int *per_sm, 
     return PKV_OK;
 }
 
-size_t counters_offset() { return kStatusBytes; }
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-size_t pieces_offset(int S, int H) {
-    return counters_offset() + ((size_t)S * H * sizeof(int32_t) + 255) / 256 * 256;
+// Workspace layout: [status][pieces: two per CTA][last-arriver counters: one per (s, h)].
+// The counters must be zero when a launch starts (each launch leaves those it used zero),
+// so their place may not move between calls that share a workspace: a caller's workspace
+// puts them after room for the pieces of the largest grid at the largest head_dim, so the
+// same workspace serves calls with any num_seqs, head_dim and cache type it was sized for.
+// The library's static scratch, whose counters are cleared on every call, packs the
+// pieces of the launch's own grid instead (compact).
+size_t pieces_bytes(int D, int grid) { return (size_t)grid * 2 * piece_stride(D) * sizeof(float); }
+
+size_t counters_offset(bool compact, int D, int grid, int num_sms) {
+    return kStatusBytes + round256(compact ? pieces_bytes(D, grid) : pieces_bytes(256, num_sms * kMaxCtasPerSm));
 }
 
-// Workspace for a launch of `grid` CTAs: two pieces per CTA.
-size_t workspace_need(int S, int H, int D, int grid) {
-    return pieces_offset(S, H) + (size_t)grid * 2 * piece_stride(D) * sizeof(float);
-}
-
-// An upper bound for any launch on a device with num_sms SMs.
-size_t workspace_bytes_for(int S, int H, int D, int num_sms) {
-    return workspace_need(S, H, D, num_sms * kMaxCtasPerSm);
+// Bytes of a caller's workspace for S sequences of H heads on a device with num_sms SMs.
+size_t workspace_bytes_for(int S, int H, int num_sms) {
+    return counters_offset(false, 0, 0, num_sms) + (size_t)S * H * sizeof(int32_t);
 }
 
 // swizzle128: the tile lands 128-byte swizzled (E4M3 head_dim 128: 128-byte rows).
@@ -1273,7 +1277,7 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t h
         fail(PKV_ERR_CUDA, "no CUDA device");
         return 0;
     }
-    return workspace_bytes_for(num_seqs, num_heads, head_dim, sms);
+    return workspace_bytes_for(num_seqs, num_heads, sms);
 }
 
 pkv_status pkv_decode_launch_info(int32_t num_seqs, int32_t head_dim, int32_t kv_dtype, int32_t *grid_ctas,
@@ -1306,7 +1310,8 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
                                  void *stream, const void *k_new, const void *v_new, const int64_t *slots,
                                  uint32_t *status_override = nullptr, const float *k_scale = nullptr,
                                  const float *v_scale = nullptr, const int32_t *seq_begin = nullptr,
-                                 const float *pieces = nullptr, int32_t splits = 0, uint32_t flags = 0) {
+                                 const float *pieces = nullptr, int32_t splits = 0, uint32_t flags = 0,
+                                 bool compact = false) {
     const bool q8 = k_scale != nullptr;
     if ((seq_begin == nullptr) != (pieces == nullptr))
         return fail(PKV_ERR_INVALID_ARG, "seq_begin and pieces go together (both NULL: no cascade)");
@@ -1344,7 +1349,8 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     size_t smem = 0;
     pkv_status st = launch_shape(dev, head_dim, q8, num_seqs, &grid, &per, &sms, &smem);
     if (st != PKV_OK) return st;
-    const size_t need = workspace_need(num_seqs, num_heads, head_dim, grid);
+    const size_t counters_off = counters_offset(compact, head_dim, grid, sms);
+    const size_t need = counters_off + (size_t)num_seqs * num_heads * sizeof(int32_t);
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", workspace_bytes, need);
 
@@ -1361,8 +1367,8 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     prm.lens = context_lens;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     prm.status = status_override ? status_override : reinterpret_cast<uint32_t *>(ws);
-    prm.counters = reinterpret_cast<int32_t *>(ws + counters_offset());
-    prm.pieces = reinterpret_cast<float *>(ws + pieces_offset(num_seqs, num_heads));
+    prm.pieces = reinterpret_cast<float *>(ws + kStatusBytes);
+    prm.counters = reinterpret_cast<int32_t *>(ws + counters_off);
     prm.S = num_seqs;
     prm.H = num_heads;
     prm.max_blocks = max_blocks;
@@ -1541,7 +1547,9 @@ pkv_status pkv_decode_attention_static(const void *q, const void *k_cache, const
     size_t smem = 0;
     pkv_status st0 = launch_shape(dev, head_dim, false, num_seqs, &grid, &per, &sms, &smem);
     if (st0 != PKV_OK) return st0;
-    const size_t need = workspace_need(num_seqs, num_heads, head_dim, grid);
+    const size_t counters_off = counters_offset(true, head_dim, grid, sms);
+    const size_t counters_len = (size_t)num_seqs * num_heads * sizeof(int32_t);
+    const size_t need = counters_off + counters_len;
     if (need > kStaticScratchBytes)
         return fail(PKV_ERR_INVALID_ARG,
                     "%d sequences x %d heads (head_dim %d) need %zu bytes of scratch; the static scratch holds %zu",
@@ -1551,11 +1559,14 @@ pkv_status pkv_decode_attention_static(const void *q, const void *k_cache, const
     if (st != PKV_OK) return st;
     // The array keeps the previous call's contents: the status word and the
     // last-arriver counters must start at zero, so clear them on the stream.
-    cudaError_t e = cudaMemsetAsync(scratch, 0, pieces_offset(num_seqs, num_heads), static_cast<cudaStream_t>(stream));
+    unsigned char *sc = static_cast<unsigned char *>(scratch);
+    cudaError_t e = cudaMemsetAsync(sc, 0, kStatusBytes, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaMemsetAsync(sc + counters_off, 0, counters_len, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "clearing the static scratch: %s", cudaGetErrorString(e));
     return decode_attention_impl(q, k_cache, v_cache, num_blocks, block_size, num_heads, head_dim, layout,
                                  block_tables, max_blocks, context_lens, num_seqs, scale, out, scratch,
-                                 kStaticScratchBytes, stream, nullptr, nullptr, nullptr, status);
+                                 kStaticScratchBytes, stream, nullptr, nullptr, nullptr, status, nullptr, nullptr,
+                                 nullptr, nullptr, 0, 0, true);
 }
 
 }  // extern "C"

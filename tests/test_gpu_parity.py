@@ -417,6 +417,22 @@ def test_one_long_sequence_spans_every_cta():
     assert st2 == 0 and np.array_equal(out, out2)
 
 
+def test_workspace_reused_across_batch_sizes():
+    """One workspace, sized for 48 sequences of 8 heads, serves calls with 6, then 48, then 20
+    sequences and then another head_dim. The small batch's (s, h) are split over many CTAs,
+    so its pieces fill the workspace; the counters of the larger batches must still start
+    at zero, so their place may not depend on num_seqs."""
+    H = 8
+    ws = pkv.new_workspace(48, H, 128, "cuda")
+    for S, D, seed in ((6, 128, 21), (48, 128, 22), (20, 128, 23), (48, 64, 24)):
+        rng = np.random.default_rng(seed)
+        lens = rng.integers(300, 2000, size=S).tolist()
+        q, kp, vp, tab, ln, B, N = _raw_case(lens, H=H, D=D, canary_nan=False, seed=seed, layout="HND")
+        out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N, layout="HND", ws=ws)
+        assert st == 0
+        assert_close(out, rc.decode_attention(q, kp, vp, tab, ln, B, "HND"), f"S={S} D={D}")
+
+
 def test_many_short_sequences():
     rng = np.random.default_rng(11)
     lens = rng.integers(1, 70, size=700).tolist()
