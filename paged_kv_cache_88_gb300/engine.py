@@ -11,10 +11,11 @@ One decode step over a batch (all through the C ABI):
    including it -- one ``pkv_decode_append_attention`` launch (the default for an
    fp16 cache), or ``pkv_append`` then ``pkv_pool_decode_attention`` (the default
    for an E4M3 cache). With the shared-prefix
-   cascade (fp16 HND pools, head_dim 128, on by default), the host plans groups
-   of sequences that share leading blocks (``pkv_cascade_plan``) and each
-   layer first runs ``pkv_prefix_attention`` over the groups' prefixes, then
-   ``pkv_decode_attention_ex`` over the private rest (fused append included).
+   cascade (HND pools, head_dim 128, fp16 or E4M3, on by default), the host
+   plans groups of sequences that share leading blocks (``pkv_cascade_plan``)
+   and each layer first runs ``pkv_prefix_attention`` over the groups'
+   prefixes, then ``pkv_decode_attention_ex`` over the private rest (fused
+   append included for fp16).
 
 The driver also replays a workload's set-up script (admissions, forks, dummy
 churn, multi-token writes). It holds no arithmetic of the method: slots,
