@@ -390,7 +390,8 @@ typedef struct {
 } pkv_prefix_group;
 
 #define PKV_MAX_GROUP_SEQS 128
-#define PKV_ATTN_INPUTS_EARLY 0x1u /* pkv_decode_attention_ex flag, see there */
+#define PKV_ATTN_INPUTS_EARLY 0x1u     /* pkv_decode_attention_ex flag, see there */
+#define PKV_ATTN_LAST_ROW_PENDING 0x2u /* pkv_decode_attention_ex flag, see there */
 #define PKV_MAX_PREFIX_SPLITS 8
 
 /* Host planner of the cascade for one step. block_tables: host int32
@@ -468,7 +469,11 @@ pkv_status pkv_prefix_attention(const pkv_pool *pool, int32_t layer, const void 
  * the previous layer's attention, or the prefix pass): then the load latency at
  * the start of the launch overlaps the end of the previous one. Every libpkv
  * kernel lets its successor start only after its own inputs are final, so
- * anything launched before that preceding kernel is complete. Other flag bits:
+ * anything launched before that preceding kernel is complete.
+ * PKV_ATTN_LAST_ROW_PENDING (with PKV_ATTN_INPUTS_EARLY): the preceding kernel
+ * may also write the last cached row of each sequence (it is this step's
+ * pkv_append of the layer); the tiles holding those rows are then read only
+ * after it has finished. Alone it changes nothing. Other flag bits:
  * INVALID_ARG. */
 pkv_status pkv_decode_attention_ex(const pkv_pool *pool, int32_t layer, const void *q, const void *k_new,
                                    const void *v_new, const int64_t *slot_mapping, const int32_t *block_tables,

@@ -37,6 +37,7 @@ EXPORTED = [
 
 MAX_GROUP_SEQS = 128
 ATTN_INPUTS_EARLY = 0x1
+ATTN_LAST_ROW_PENDING = 0x2
 MAX_PREFIX_SPLITS = 8
 
 
@@ -371,7 +372,8 @@ class Pool:
                             slot_mapping=None, seq_begin=None, pieces=None, splits: int = 0, scale: float = 0.0,
                             flags: int = 0, stream=None) -> None:
         """pkv_decode_attention_ex: optional fused append, optional cascade (private half + merge);
-        ``flags`` = ATTN_INPUTS_EARLY lets the launch start reading before its predecessor ends."""
+        ``flags`` = ATTN_INPUTS_EARLY lets the launch start reading before its predecessor ends
+        (| ATTN_LAST_ROW_PENDING when that predecessor is the layer's append)."""
         for t, dt, name in ((q, "float16", "q"), (out, "float16", "out"), (block_tables, "int32", "block_tables"),
                             (context_lens, "int32", "context_lens")):
             _require(t, dt, name)

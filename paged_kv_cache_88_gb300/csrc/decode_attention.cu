@@ -125,6 +125,9 @@ struct Params {
     // K/V loads issued) before the grid dependency resolves; q, k_new, v_new, the
     // workspace and out are touched only after it
     int32_t early;
+    // 1 (with early): the preceding kernel writes each sequence's last cached row (this
+    // step's append), so the tile holding it is not among the tiles loaded early
+    int32_t last_pending;
     int32_t S, H, max_blocks, B, N, layout;
     int32_t lgB;         // log2(B): B is a power of two
     float scale_log2;    // scale * log2(e)
@@ -576,12 +579,13 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         };
         int32_t k0 = 0;   // the first tile of the main loop
         if (early) {
-            // the first stages' K/V before the grid dependency resolves (not the tile the
-            // appended token goes to: it is stored first); their q rows after it
+            // the first stages' K/V before the grid dependency resolves (not a tile holding an
+            // appended token: this launch stores it first, or the preceding kernel does);
+            // their q rows after it
             Cursor pend[NS];
             bool pend_q[NS];
             for (; k0 < n && k0 < NS; ++k0) {
-                if (p.k_new != nullptr && c.t == c.nt - 1 && sm.base[c.s] + c.h * c.nt + c.nt - 1 < g1) break;
+                if ((p.k_new != nullptr || p.last_pending) && c.t == c.nt - 1) break;
                 const bool first = (k0 == 0) || (c.t == 0);
                 issue_kv(c, k0, first);
                 pend[k0] = c;
@@ -589,7 +593,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 advance(c, sm, S, H);
             }
             ptx::grid_dependency_wait();
-            ptx::launch_dependents();
+            if (!p.last_pending) ptx::launch_dependents();
             for (int32_t k = 0; k < k0; ++k)
                 if (pend_q[k]) issue_q(pend[k], k);
             __syncwarp();
@@ -662,8 +666,9 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         // successor (the next layer's append) launched at the start sits resident next
         // to these CTAs for the whole launch, and its waiting warps cost the
         // issue-bound E4M3 consumers about 4 us per layer (7B batch 32). In the early
-        // mode the trigger above, after the first stages, stays.
-        if (!early) ptx::launch_dependents();
+        // mode the trigger above, after the first stages, stays, unless this launch
+        // follows an append (last_pending), whose successor is the next layer's append.
+        if (!early || p.last_pending) ptx::launch_dependents();
         return;
     }
 
@@ -1389,6 +1394,7 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     prm.pre = pieces;
     prm.pre_splits = seq_begin ? splits : 0;
     prm.early = (flags & PKV_ATTN_INPUTS_EARLY) ? 1 : 0;
+    prm.last_pending = (flags & PKV_ATTN_LAST_ROW_PENDING) ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -1454,7 +1460,8 @@ pkv_status pkv_decode_attention_ex(const pkv_pool *pool, int32_t layer, const vo
                                    void *out, void *workspace, size_t workspace_bytes, uint32_t flags,
                                    void *stream) {
     if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
-    if (flags & ~(uint32_t)PKV_ATTN_INPUTS_EARLY) return fail(PKV_ERR_INVALID_ARG, "unknown flags %#x", flags);
+    if (flags & ~(uint32_t)(PKV_ATTN_INPUTS_EARLY | PKV_ATTN_LAST_ROW_PENDING))
+        return fail(PKV_ERR_INVALID_ARG, "unknown flags %#x", flags);
     const pkv_pool_desc &d = pool->desc;
     if (!pool->k_pool) return fail(PKV_ERR_INVALID_ARG, "pool has no device memory");
     if (layer < 0 || layer >= d.num_layers) return fail(PKV_ERR_INVALID_ARG, "layer %d out of range", layer);

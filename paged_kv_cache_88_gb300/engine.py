@@ -287,6 +287,10 @@ class DecodeEngine:
         sc = float(scale)
         fused = self.fused and n_slots == S
         early = bd.ATTN_INPUTS_EARLY if w.kv_dtype == "f16" else 0
+        # after the layer's own append launch of one token per sequence (which first waits for
+        # everything before it on the stream): the attention may start early, the tiles holding
+        # the appended rows read last
+        after_append = bd.ATTN_INPUTS_EARLY | bd.ATTN_LAST_ROW_PENDING if n_slots == S else 0
         G, splits = (self.plan_groups, self.plan_splits) if self.cascade else (0, 0)
         if G:
             gp, bp = self.groups_d.data_ptr(), self.begin_d.data_ptr()
@@ -304,11 +308,12 @@ class DecodeEngine:
                                                 bd.ATTN_INPUTS_EARLY if layer > 0 else 0, sp))
                 if not fused:
                     bd.check(L.pkv_append(h, layer, kp + off, vp + off, slp, n_slots, status, sp))
-                # after the prefix pass (which writes only pieces) the private pass may start early
+                # after the prefix pass (which writes only pieces) or the append, the private
+                # pass may start early
                 bd.check(L.pkv_decode_attention_ex(h, layer, qp + off, kp + off if fused else None,
                                                    vp + off if fused else None, slp if fused else None, tp, maxb,
                                                    lp, S, bp, pp, splits, sc, op + off, wsp, wsb,
-                                                   bd.ATTN_INPUTS_EARLY if fused else 0, sp))
+                                                   bd.ATTN_INPUTS_EARLY if fused else after_append, sp))
             elif fused:
                 # layers after the first follow the previous layer's attention, which writes
                 # none of this layer's tables, lengths or cache: start early (fp16 cache; on
@@ -318,8 +323,8 @@ class DecodeEngine:
                                                    early if layer > 0 else 0, sp))
             else:
                 bd.check(L.pkv_append(h, layer, kp + off, vp + off, slp, n_slots, status, sp))
-                bd.check(L.pkv_pool_decode_attention(h, layer, qp + off, tp, maxb, lp, S, sc, op + off, wsp, wsb,
-                                                     sp))
+                bd.check(L.pkv_decode_attention_ex(h, layer, qp + off, None, None, None, tp, maxb, lp, S,
+                                                   None, None, 0, sc, op + off, wsp, wsb, after_append, sp))
             if attn_events is not None:
                 e1.record(s)
                 attn_events.append((e0, e1))
@@ -393,7 +398,7 @@ class DecodeEngine:
                 self.plan_splits, float(scale), out.data_ptr() + off, self.workspace.data_ptr(),
                 self.workspace.numel(), bd.ATTN_INPUTS_EARLY, s.cuda_stream))
             return
-        if early and w.kv_dtype == "f16":
+        if early:
             bd.check(bd.lib().pkv_decode_attention_ex(
                 self.pool.handle, layer, q.data_ptr() + off, None, None, None, self.tables_d.data_ptr(),
                 w.max_blocks, self.lens_d.data_ptr(), w.num_seqs, None, None, 0, float(scale), out.data_ptr() + off,

@@ -681,6 +681,38 @@ def test_early_start_back_to_back_layers():
         assert_close(out[layer].cpu().numpy(), ref, f"early layer {layer}")
 
 
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3"])
+def test_early_start_behind_the_append(kv_dtype):
+    """Attention flagged to start early behind the layer's own append launch (the tiles holding
+    the appended rows read only after it) writes the same output, bit for bit, as attention
+    started after the append, and matches the oracle."""
+    w = wl.make_workload(2, num_layers=3, num_seqs=12, len_scale=0.3, decode_steps=2, kv_dtype=kv_dtype)
+    eng = DecodeEngine(w, fill="numpy", cascade=False, fused=False)
+    ora = make_oracle(w)
+    eng.run_script(values="numpy")
+    ora.run_script()
+    q, k, v = eng.step_inputs(0, "numpy")
+    n_slots, n_pairs = eng.prepare_step()
+    assert n_slots == w.num_seqs
+    if n_pairs:
+        eng.pool.copy_blocks(eng.pairs_d, n_pairs, status=eng.status)
+    ref = ora.step(*ora.step_inputs(0))
+    flags = pkv.binding.ATTN_INPUTS_EARLY | pkv.binding.ATTN_LAST_ROW_PENDING
+    outs = []
+    for f in (flags, 0):
+        out = torch.full_like(q, float("nan"))
+        for layer in range(w.num_layers):
+            eng.pool.append(layer, k[layer], v[layer], eng.slots_d[:n_slots], status=eng.status)
+            eng.pool.decode_attention_ex(layer, q[layer], eng.tables_d, eng.lens_d, out[layer], eng.workspace,
+                                         flags=f)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert eng.device_status() == 0
+    assert torch.equal(outs[0], outs[1])
+    for layer in range(w.num_layers):
+        assert_close(outs[0][layer].cpu().numpy(), ref[layer], f"{kv_dtype} layer {layer}")
+
+
 def test_attention_ex_rejects_unknown_flags():
     w = wl.make_workload(1, decode_steps=1)
     eng = DecodeEngine(w, fill="numpy", cascade=False)
@@ -688,7 +720,7 @@ def test_attention_ex_rejects_unknown_flags():
     q, _, _ = eng.step_inputs(0, "numpy")
     with pytest.raises(pkv.binding.PkvError) as e:
         eng.pool.decode_attention_ex(0, q[0], eng.tables_d, eng.lens_d, torch.empty_like(q[0]), eng.workspace,
-                                     flags=0x2)
+                                     flags=0x4)
     assert e.value.code == "INVALID_ARG"
 
 
