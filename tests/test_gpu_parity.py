@@ -134,7 +134,7 @@ def test_13b_shape_churned_pool_reduced(layout):
     run_parity(w, 2)
 
 
-@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 256])
+@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256])
 def test_long_context_block_sweep_reduced(block_size):
     w = wl.make_workload(5, num_layers=1, num_seqs=3, len_scale=0.12, decode_steps=2, block_size=block_size)
     run_parity(w, 2)
@@ -241,7 +241,7 @@ def test_e4m3_13b_shape_reduced():
     run_parity(w, 2)
 
 
-@pytest.mark.parametrize("block_size", [8, 16, 256])
+@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256])
 def test_e4m3_long_context_reduced(block_size):
     w = wl.make_workload(5, num_layers=1, num_seqs=3, len_scale=0.12, decode_steps=2, block_size=block_size,
                          kv_dtype="e4m3")
@@ -711,6 +711,44 @@ def test_early_start_behind_the_append(kv_dtype):
     assert torch.equal(outs[0], outs[1])
     for layer in range(w.num_layers):
         assert_close(outs[0][layer].cpu().numpy(), ref[layer], f"{kv_dtype} layer {layer}")
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_early_start_behind_the_append_edge_lengths(layout):
+    """Sequences of 1, 2, 15-17, 63-65 and 300 tokens: the appended row is the first row, the
+    last of a block, the first of a new one, alone in its tile or one of many. Attention
+    started early behind the append (LAST_ROW_PENDING) equals attention started after it,
+    bit for bit, and the oracle on the cache with the rows written in."""
+    lens = [1, 2, 15, 16, 17, 63, 64, 65, 300, 1]
+    H, D, B = 4, 128, 16
+    q, kp, vp, tab, ln, B, N = _raw_case(lens, H=H, D=D, B=B, layout=layout, seed=31)
+    rng = np.random.default_rng(32)
+    kn = rng.standard_normal((len(lens), H, D)).astype(np.float16)
+    vn = rng.standard_normal((len(lens), H, D)).astype(np.float16)
+    slots = np.array([tab[s, (t - 1) // B] * B + (t - 1) % B for s, t in enumerate(lens)], dtype=np.int64)
+    kp2, vp2 = kp.copy(), vp.copy()
+    for s_, sl in enumerate(slots):
+        blk, off = sl // B, sl % B
+        idx = (blk, off) if layout == "NHD" else (blk, slice(None), off)
+        kp2[idx], vp2[idx] = kn[s_], vn[s_]
+    ref = rc.decode_attention(q, kp2, vp2, tab, ln, B, layout)
+    dev = "cuda"
+    outs = []
+    for flags in (pkv.binding.ATTN_INPUTS_EARLY | pkv.binding.ATTN_LAST_ROW_PENDING, 0):
+        kd, vd = torch.from_numpy(kp[None]).to(dev), torch.from_numpy(vp[None]).to(dev)
+        pool = pkv.Pool(1, N, B, H, D, layout, k_pool=kd, v_pool=vd)
+        ws = pkv.new_workspace(len(lens), H, D, dev)
+        qd, td, ld = (torch.from_numpy(a).to(dev) for a in (q, tab, ln))
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        out = torch.full_like(qd, float("nan"))
+        pool.append(0, torch.from_numpy(kn).to(dev), torch.from_numpy(vn).to(dev), torch.from_numpy(slots).to(dev),
+                    status=st)
+        pool.decode_attention_ex(0, qd, td, ld, out, ws, flags=flags)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0 and pkv.workspace_status(ws) == 0
+        outs.append(out.cpu().numpy())
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    assert_close(outs[0], ref, f"early behind the append, {layout}")
 
 
 def test_attention_ex_rejects_unknown_flags():
