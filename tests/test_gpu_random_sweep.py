@@ -171,3 +171,61 @@ def test_random_e4m3_step(case):
     assert np.array_equal(ksd[0].cpu().numpy().view(np.uint32), ksr.view(np.uint32)), what
     assert np.array_equal(vsd[0].cpu().numpy().view(np.uint32), vsr.view(np.uint32)), what
     assert_close(out.cpu().numpy(), ref, what)
+
+
+def random_fork_spec(rng, B, max_prefix=2048):
+    """Groups of sequences forked from a root (sharing its first nsh full blocks, then
+    private tails of 0 to 5 blocks, some ending exactly at the prefix), plus unshared
+    sequences; in the (s, ...) form of the cascade tests' builders."""
+    spec = []
+    for _ in range(int(rng.integers(1, 4))):
+        nsh = int(rng.integers(1, max_prefix // B + 2))
+        root = len(spec)
+        spec.append((None, 0, nsh * B + int(rng.integers(0, 3 * B))))
+        for _ in range(int(rng.integers(1, 30))):
+            spec.append((root, nsh, nsh * B + int(rng.integers(0, 5 * B))))
+    for _ in range(int(rng.integers(0, 4))):
+        spec.append((None, 0, int(rng.integers(1, 600))))
+    return spec
+
+
+@pytest.mark.parametrize("case", CASES[:12])
+def test_random_fp16_cascade(case):
+    """The planned cascade (prefix pass, then the private pass merging its pieces) on random
+    fork structures equals the plain float64 attention."""
+    from tests.test_gpu_cascade import Case
+    rng = np.random.default_rng(9000 + case)
+    B = int(rng.choice(BLOCK_SIZES))
+    H = int(rng.choice([1, 2, 4]))
+    c = Case(random_fork_spec(rng, B), H=H, B=B, seed=9100 + case)
+    groups, begin = c.plan()
+    ref = c.oracle()
+    what = f"case {case}: S={c.S} H={H} B={B} groups={len(groups)}"
+    if len(groups):
+        splits = bd.prefix_splits(len(groups), H, int(groups[:, 2].max()))
+        c.prefix(groups, splits)
+        got = c.decode(begin, splits)
+    else:
+        got = c.decode(None, 0)
+    assert int(c.status.item()) == 0 and bd.workspace_status(c.ws) == 0, what
+    assert_close(got, ref, what)
+
+
+@pytest.mark.parametrize("case", CASES[:8])
+def test_random_e4m3_cascade(case):
+    from tests.test_gpu_cascade_e4m3 import Q8Case
+    rng = np.random.default_rng(9500 + case)
+    B = int(rng.choice(BLOCK_SIZES))
+    H = int(rng.choice([1, 2, 4]))
+    c = Q8Case(random_fork_spec(rng, B, max_prefix=768), H=H, B=B, seed=9600 + case)
+    groups, begin = c.plan()
+    ref = c.oracle()
+    what = f"case {case}: S={c.S} H={H} B={B} groups={len(groups)}"
+    if len(groups):
+        splits = bd.prefix_splits(len(groups), H, int(groups[:, 2].max()))
+        c.prefix(groups, splits)
+        got = c.decode(begin, splits)
+    else:
+        got = c.decode(None, 0)
+    assert int(c.status.item()) == 0 and bd.workspace_status(c.ws) == 0, what
+    assert_close(got, ref, what)
