@@ -229,3 +229,28 @@ def test_random_e4m3_cascade(case):
         got = c.decode(None, 0)
     assert int(c.status.item()) == 0 and bd.workspace_status(c.ws) == 0, what
     assert_close(got, ref, what)
+
+
+@pytest.mark.parametrize("case", CASES[:16])
+def test_random_prefill(case):
+    """Paged causal prefill of random chunks (the last c tokens of each context, c from 1 to
+    the whole context; chunk and context lengths on tile boundaries and between) over
+    NaN-guarded pools of every block size, against the float64 prefill definition."""
+    from oracle import ref_attn as rf
+    from tests.test_gpu_prefill import _case, _run, _check
+    rng = np.random.default_rng(9900 + case)
+    B = int(rng.choice(BLOCK_SIZES))
+    H = int(rng.choice([1, 2, 3]))
+    S = int(rng.integers(1, 9))
+    edges = [1, 2, 127, 128, 129, 255, 256, 257, 383, 384, 511, 512]
+    lens, chunks = [], []
+    for _ in range(S):
+        T = int(rng.choice(edges)) if rng.random() < 0.4 else int(rng.integers(1, 1600))
+        c = int(rng.choice([e for e in edges if e <= T] + [T])) if rng.random() < 0.5 else int(rng.integers(1, T + 1))
+        lens.append(T)
+        chunks.append(min(c, T))
+    q, qs, kp, vp, tab, ln, N = _case(lens, chunks, H, B, seed=9950 + case)
+    got, st = _run(q, qs, kp, vp, tab, ln, N, H, B, max(chunks))
+    what = f"case {case}: B={B} H={H} lens={lens} chunks={chunks}"
+    assert st == 0, what
+    _check(got, rf.prefill_attention(q, kp, vp, tab, ln, qs, B, layout="HND"), what)
