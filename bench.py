@@ -212,7 +212,8 @@ def cpu_baseline_oracle(w, k_layer, v_layer, tables, lens, seconds: float, k_sca
         passes = 0
         while True:
             s = passes % w.num_seqs
-            fp8.decode_attention(q, k_layer, v_layer, k_scale, v_scale, tables[s:s + 1], lens[s:s + 1], w.block_size)
+            fp8.decode_attention(q, k_layer, v_layer, k_scale, v_scale, tables[s:s + 1], lens[s:s + 1], w.block_size,
+                                 layout=w.layout)
             passes += 1
             el = time.perf_counter() - t0
             if el >= seconds:

@@ -63,8 +63,9 @@ enum { PKV_LAYOUT_NHD = 0, PKV_LAYOUT_HND = 1 };
  *                row, value = code * scale, scale = amax(row) / 448 (1 for an
  *                all-zero row), codes rounded to nearest even and saturated.
  *                Quantised KV halves the bytes per token (m.lqnn.cn/news/240480
- *                §6.2; hnwysp.cn/news/103996 §5.4). HND layout, head_dim 64 or 128;
- *                the scale pools are [L][N][H][B] fp32 (pkv_pool_set_scales). */
+ *                §6.2; hnwysp.cn/news/103996 §5.4). Either layout, head_dim 64 or
+ *                128; the scale pools are [L][N][H][B] fp32 in both layouts
+ *                (pkv_pool_set_scales); the cascade's prefix pass needs HND. */
 enum { PKV_KV_F16 = 0, PKV_KV_E4M3 = 1 };
 
 /* Bits of the device status word (uint32_t) that device entry points OR into. */
@@ -294,7 +295,7 @@ pkv_status pkv_scatter_blocks(const pkv_pool *pool, const int32_t *blocks, int32
  * Limits (every decode-attention entry point): num_seqs <= 4096 per launch (the
  *   kernel keeps three int32 per sequence in shared memory, and every CTA scans
  *   the lengths in its prologue); head_dim 64, 128 or 256 for an fp16 cache, 64
- *   or 128 for an E4M3 cache, which also needs the HND layout; block_size 8, 16,
+ *   or 128 for an E4M3 cache (either layout); block_size 8, 16,
  *   32, 64, 128 or 256; num_blocks * block_size * num_heads < 2^31.
  * Errors: INVALID_ARG (sizes, alignment, workspace too small), UNSUPPORTED
  *   (head_dim or block_size not built), CUDA (launch failure). */

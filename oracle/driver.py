@@ -48,7 +48,7 @@ class OracleEngine:
     def _append(self, layer, k_new, v_new, slots):
         if self.q8:
             fp8.append_kv(self.k_pool[layer], self.v_pool[layer], self.k_scale[layer], self.v_scale[layer], k_new,
-                          v_new, slots, self.w.block_size)
+                          v_new, slots, self.w.block_size, self.w.layout)
         else:
             rf.append_kv(self.k_pool[layer], self.v_pool[layer], k_new, v_new, slots, self.w.block_size,
                          self.w.layout)
@@ -141,7 +141,7 @@ class OracleEngine:
             if self.q8:
                 out[layer] = fp8.decode_attention(q[layer], self.k_pool[layer], self.v_pool[layer],
                                                   self.k_scale[layer], self.v_scale[layer], tab, self.lens,
-                                                  w.block_size, scale)
+                                                  w.block_size, scale, w.layout)
             elif impl == "c":
                 from . import ref_attn_c as rc
                 out[layer] = rc.decode_attention(q[layer], self.k_pool[layer], self.v_pool[layer], tab,

@@ -75,10 +75,17 @@ def dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return DECODE[np.asarray(codes, dtype=np.uint8)] * np.asarray(scales, dtype=np.float64)[..., None]
 
 
-# ------------------------------------------------------------------ quantised pools (HND layout)
-# codes: uint8 [N][H][B][D] per layer; scales: float32 [N][H][B] per layer.
+# ------------------------------------------------------------------ quantised pools
+# codes: uint8 per layer, [N][H][B][D] (HND) or [N][B][H][D] (NHD), the same two layouts
+# as an fp16 pool; scales: float32 [N][H][B] per layer in either case.
 
-def append_kv(k_codes, v_codes, k_scales, v_scales, k_new, v_new, slot_mapping, block_size: int) -> None:
+def _rows(codes, blk, off, layout: str):
+    """Index of the H code rows of slot (blk, off): codes[idx] has shape [H][D]."""
+    return (blk, off) if layout == "NHD" else (blk, slice(None), off)
+
+
+def append_kv(k_codes, v_codes, k_scales, v_scales, k_new, v_new, slot_mapping, block_size: int,
+              layout: str = "HND") -> None:
     """Quantise token i's K/V rows (all heads) and write codes and scales to slot_mapping[i]; slot < 0 skipped."""
     kq, ks = quantize_rows(k_new)
     vq, vs = quantize_rows(v_new)
@@ -86,8 +93,8 @@ def append_kv(k_codes, v_codes, k_scales, v_scales, k_new, v_new, slot_mapping, 
         if slot < 0:
             continue
         blk, off = divmod(slot, block_size)
-        k_codes[blk, :, off] = kq[i]
-        v_codes[blk, :, off] = vq[i]
+        k_codes[_rows(k_codes, blk, off, layout)] = kq[i]
+        v_codes[_rows(v_codes, blk, off, layout)] = vq[i]
         k_scales[blk, :, off] = ks[i]
         v_scales[blk, :, off] = vs[i]
 
@@ -100,7 +107,7 @@ def copy_blocks(k_codes, v_codes, k_scales, v_scales, pairs) -> None:
 
 
 def decode_attention(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, block_size: int,
-                     scale=None) -> np.ndarray:
+                     scale=None, layout: str = "HND") -> np.ndarray:
     """Paged decode attention over a quantised layer: the float64 definition on code * scale."""
     from . import ref_attn as rf
     S, H, D = q.shape
@@ -114,7 +121,11 @@ def decode_attention(q, k_codes, v_codes, k_scales, v_scales, block_tables, cont
         blocks = [int(block_tables[s][t // block_size]) for t in range(T)]
         offs = [t % block_size for t in range(T)]
         for h in range(H):
-            k = dequantize(k_codes[blocks, h, offs], k_scales[blocks, h, offs])
-            v = dequantize(v_codes[blocks, h, offs], v_scales[blocks, h, offs])
+            if layout == "NHD":
+                kc, vc = k_codes[blocks, offs, h], v_codes[blocks, offs, h]
+            else:
+                kc, vc = k_codes[blocks, h, offs], v_codes[blocks, h, offs]
+            k = dequantize(kc, k_scales[blocks, h, offs])
+            v = dequantize(vc, v_scales[blocks, h, offs])
             out[s, h] = rf.attend(q[s, h], k, v, scale)
     return out

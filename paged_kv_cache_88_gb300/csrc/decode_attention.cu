@@ -624,8 +624,8 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 // tile's TMA (async-proxy) read
                 if (new_slot < (int64_t)p.N * p.B) {
                     const int64_t blk = new_slot >> lgB, off = new_slot & (p.B - 1);
-                    const int64_t row = p.layout == PKV_LAYOUT_NHD ? (blk * p.B + off) * H + c.h
-                                                                   : (blk * H + c.h) * p.B + off;
+                    const int64_t srow = (blk * H + c.h) * p.B + off;   // scales: [N][H][B] in either layout
+                    const int64_t row = p.layout == PKV_LAYOUT_NHD ? (blk * p.B + off) * H + c.h : srow;
                     if constexpr (Q8) {
                         // one lane per 8 elements; the W lanes of a row reduce its amax
                         const int wi = lane;                   // NW == 1 for D <= 128
@@ -637,7 +637,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                             const uint2 codes = q8::quantize_word(nw[0], scale);
                             unsigned char *base = wi < W ? p.k_layer : p.v_layer;
                             reinterpret_cast<uint2 *>(base + row * D)[wi % W] = codes;
-                            if (wi % W == 0) (wi < W ? p.k_scale : p.v_scale)[row] = scale;
+                            if (wi % W == 0) (wi < W ? p.k_scale : p.v_scale)[srow] = scale;
                         }
                     } else {
 #pragma unroll
@@ -1333,8 +1333,8 @@ pkv_status decode_attention_impl(const void *q, const void *k_cache, const void 
     if (num_seqs == 0) return PKV_OK;
     if (!variant_built(head_dim, q8))
         return fail(PKV_ERR_UNSUPPORTED, "head_dim %d%s", head_dim, q8 ? " with an E4M3 cache" : "");
-    if (q8 && (layout != PKV_LAYOUT_HND || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
-        return fail(PKV_ERR_INVALID_ARG, "an E4M3 cache needs the HND layout and 16-byte aligned scale pools");
+    if (q8 && (!v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+        return fail(PKV_ERR_INVALID_ARG, "an E4M3 cache needs 16-byte aligned scale pools");
     if (!supported_block_size(block_size)) return fail(PKV_ERR_UNSUPPORTED, "block_size %d", block_size);
     if (layout != PKV_LAYOUT_NHD && layout != PKV_LAYOUT_HND) return fail(PKV_ERR_INVALID_ARG, "layout %d", layout);
     if (num_heads < 1 || num_blocks < 1 || max_blocks < 1) return fail(PKV_ERR_INVALID_ARG, "sizes must be >= 1");

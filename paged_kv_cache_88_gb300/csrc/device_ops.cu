@@ -56,13 +56,14 @@ append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, 
 // E4M3 cache: one warp per (token, head). Lanes 0..W-1 hold the K row's
 // 16-byte fp16 words, lanes W..2W-1 the V row's (W = D/8 <= 16); each row's
 // amax is reduced over its W lanes, then each lane stores its 8 codes and the
-// first lane of a row the row's scale.
+// first lane of a row the row's scale. The codes follow the pool's layout; the
+// scales are [N][H][B] in either.
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads)
 append_q8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, const int64_t *__restrict__ slots,
                  int32_t num_tokens, unsigned char *__restrict__ k_layer, unsigned char *__restrict__ v_layer,
                  float *__restrict__ k_scale, float *__restrict__ v_scale, int64_t num_slots, int32_t B, int32_t H,
-                 uint32_t *status) {
+                 int32_t layout, uint32_t *status) {
     constexpr int W = D / 8;
     ptx::grid_dependency_wait();
     ptx::launch_dependents();   // successors start once this grid's inputs are final
@@ -86,9 +87,10 @@ append_q8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_ne
         const float scale = q8::row_scale(m);
         if (lane < 2 * W) {
             const int64_t blk = slot / B, off = slot - blk * B;
-            const int64_t row = (blk * H + h) * B + off;
+            const int64_t srow = (blk * H + h) * B + off;   // the row's scale
+            const int64_t row = layout == PKV_LAYOUT_NHD ? (blk * B + off) * H + h : srow;
             reinterpret_cast<uint2 *>((lane < W ? k_layer : v_layer) + row * D)[lane % W] = q8::quantize_word(w, scale);
-            if (lane % W == 0) (lane < W ? k_scale : v_scale)[row] = scale;
+            if (lane % W == 0) (lane < W ? k_scale : v_scale)[srow] = scale;
         }
     }
 }
@@ -267,7 +269,7 @@ pkv_status pkv_append(const pkv_pool *pool, int32_t layer, const void *k_new, co
         e = launch_pdl(kern, dim3(grid), dim3(kAppendThreads), 0, static_cast<cudaStream_t>(stream),
                        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
                        reinterpret_cast<unsigned char *>(pl.k), reinterpret_cast<unsigned char *>(pl.v), pl.k_scale,
-                       pl.v_scale, nslots, d.block_size, d.num_heads, status);
+                       pl.v_scale, nslots, d.block_size, d.num_heads, d.layout, status);
     } else {
         const int64_t total = (int64_t)num_tokens * d.num_heads * wpr;
         const int64_t want = (total + kAppendThreads - 1) / kAppendThreads;

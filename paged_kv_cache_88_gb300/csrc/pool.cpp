@@ -105,8 +105,8 @@ pkv_status check_desc(const pkv_pool_desc *d) {
         return fail(PKV_ERR_INVALID_ARG, "num_blocks * block_size * num_heads must be < 2^31");
     if (d->kv_dtype != PKV_KV_F16 && d->kv_dtype != PKV_KV_E4M3)
         return fail(PKV_ERR_INVALID_ARG, "kv_dtype %d unknown", d->kv_dtype);
-    if (d->kv_dtype == PKV_KV_E4M3 && (d->layout != PKV_LAYOUT_HND || d->head_dim > 128))
-        return fail(PKV_ERR_UNSUPPORTED, "an E4M3 cache is built for the HND layout and head_dim 64 or 128");
+    if (d->kv_dtype == PKV_KV_E4M3 && d->head_dim > 128)
+        return fail(PKV_ERR_UNSUPPORTED, "an E4M3 cache is built for head_dim 64 or 128");
     return PKV_OK;
 }
 

@@ -223,10 +223,22 @@ def test_e4m3_tiny(fused):
     run_parity(w, 3, fused=fused)
 
 
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
 @pytest.mark.parametrize("fused", [True, False])
-def test_e4m3_7b_shape_reduced(fused):
-    w = wl.make_workload(2, num_layers=2, num_seqs=8, len_scale=0.3, decode_steps=3, kv_dtype="e4m3")
+def test_e4m3_7b_shape_reduced(fused, layout):
+    w = wl.make_workload(2, num_layers=2, num_seqs=8, len_scale=0.3, decode_steps=3, kv_dtype="e4m3", layout=layout)
     run_parity(w, 3, fused=fused)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_e4m3_nhd_tiny_and_long(fused):
+    """The E4M3 cache in the NHD layout: head_dim 64 (tiny workload) and long contexts at
+    block sizes 8 and 256; codes and scales bit-exact, attention against the oracle."""
+    run_parity(wl.make_workload(1, decode_steps=3, kv_dtype="e4m3", layout="NHD"), 3, fused=fused)
+    for bs in (8, 256):
+        w = wl.make_workload(5, num_layers=1, num_seqs=3, len_scale=0.12, decode_steps=2, block_size=bs,
+                             kv_dtype="e4m3", layout="NHD")
+        run_parity(w, 2, fused=fused)
 
 
 def test_e4m3_prefix_cow_reduced():
@@ -253,8 +265,7 @@ def test_e4m3_pool_rules():
     with pytest.raises(pkv.PkvError) as e:
         pkv.Pool(1, 1, 16, 1, 256, "HND", kv_dtype="e4m3")          # head_dim 256 not built for E4M3
     assert e.value.code == "UNSUPPORTED"
-    with pytest.raises(pkv.PkvError):
-        pkv.Pool(1, 1, 16, 1, 64, "NHD", kv_dtype="e4m3")           # HND only
+    pkv.Pool(1, 1, 16, 1, 64, "NHD", kv_dtype="e4m3")                # either layout
     p = pkv.Pool(1, 1, 8, 1, 64, "HND", k_pool=torch.zeros(512, dtype=torch.uint8, device="cuda"),
                  v_pool=torch.zeros(512, dtype=torch.uint8, device="cuda"), kv_dtype="e4m3")
     kn = torch.zeros((1, 1, 64), dtype=torch.float16, device="cuda")

@@ -127,9 +127,10 @@ def test_random_e4m3_step(case):
     D = int(rng.choice([64, 128]))
     B = int(rng.choice(BLOCK_SIZES))
     flags = int(rng.choice([0, bd.ATTN_INPUTS_EARLY | bd.ATTN_LAST_ROW_PENDING]))
+    layout = str(rng.choice(["NHD", "HND"]))
     lens = draw_lengths(rng, S, B, long_max=700)
     tables, N = draw_tables(rng, lens, B)
-    kc = rng.integers(0, 256, size=(N, H, B, D), dtype=np.uint8)
+    kc = rng.integers(0, 256, size=(N, H, B, D), dtype=np.uint8)          # made HND, turned NHD below
     vc = rng.integers(0, 256, size=(N, H, B, D), dtype=np.uint8)
     for c_ in (kc, vc):
         c_[(c_ & 0x7F) == 0x7F] ^= 1                      # no NaN code inside a context
@@ -144,19 +145,21 @@ def test_random_e4m3_step(case):
     vc.transpose(0, 2, 1, 3)[dead] = 0xFF
     ks.transpose(0, 2, 1)[dead] = np.nan
     vs.transpose(0, 2, 1)[dead] = np.nan
+    if layout == "NHD":
+        kc, vc = np.ascontiguousarray(kc.transpose(0, 2, 1, 3)), np.ascontiguousarray(vc.transpose(0, 2, 1, 3))
     q = rng.standard_normal((S, H, D)).astype(np.float16)
     kn = rng.standard_normal((S, H, D)).astype(np.float16)
     vn = rng.standard_normal((S, H, D)).astype(np.float16)
     slots = slots_of(tables, lens, B)
     kcr, vcr, ksr, vsr = kc.copy(), vc.copy(), ks.copy(), vs.copy()
-    fp8.append_kv(kcr, vcr, ksr, vsr, kn, vn, slots, B)
+    fp8.append_kv(kcr, vcr, ksr, vsr, kn, vn, slots, B, layout=layout)
     ln = np.asarray(lens, dtype=np.int32)
-    ref = fp8.decode_attention(q, kcr, vcr, ksr, vsr, tables, ln, B)
+    ref = fp8.decode_attention(q, kcr, vcr, ksr, vsr, tables, ln, B, layout=layout)
 
     dev = "cuda"
     kd, vd = torch.from_numpy(kc[None]).to(dev), torch.from_numpy(vc[None]).to(dev)
     ksd, vsd = torch.from_numpy(ks[None]).to(dev), torch.from_numpy(vs[None]).to(dev)
-    pool = pkv.Pool(1, N, B, H, D, "HND", k_pool=kd, v_pool=vd, kv_dtype="e4m3", k_scale=ksd, v_scale=vsd)
+    pool = pkv.Pool(1, N, B, H, D, layout, k_pool=kd, v_pool=vd, kv_dtype="e4m3", k_scale=ksd, v_scale=vsd)
     ws = pkv.new_workspace(S, H, D, dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     qd, td, ld = (torch.from_numpy(a).to(dev) for a in (q, tables, ln))
@@ -165,7 +168,7 @@ def test_random_e4m3_step(case):
                 status=st)
     pool.decode_attention_ex(0, qd, td, ld, out, ws, flags=flags)
     torch.cuda.synchronize()
-    what = f"case {case}: S={S} H={H} D={D} B={B} flags={flags}"
+    what = f"case {case}: S={S} H={H} D={D} B={B} {layout} flags={flags}"
     assert int(st.item()) == 0 and pkv.workspace_status(ws) == 0, what
     assert np.array_equal(kd[0].cpu().numpy(), kcr) and np.array_equal(vd[0].cpu().numpy(), vcr), what
     assert np.array_equal(ksd[0].cpu().numpy().view(np.uint32), ksr.view(np.uint32)), what

@@ -96,3 +96,38 @@ def test_append_and_copy_quantised():
     assert np.count_nonzero(kc) == np.count_nonzero(q)
     fp8.copy_blocks(kc, vc, ks, vs, [(1, 3)])
     assert np.array_equal(kc[:, 3], kc[:, 1]) and np.array_equal(vs[:, 3], vs[:, 1])
+
+
+def test_nhd_layout_is_the_hnd_one_transposed():
+    """The two code layouts hold the same rows: an NHD pool that is the HND pool with its
+    head and in-block axes swapped gives the same attention bit for bit, and an append
+    writes the same codes (at the swapped place) and the same scales. The NHD indexing is
+    the one that gathers by hand below, too."""
+    rng = np.random.default_rng(8)
+    N, H, B, D = 7, 3, 8, 64
+    kc = rng.integers(0, 0x7E, size=(N, H, B, D)).astype(np.uint8) | (rng.integers(0, 2, size=(N, H, B, D)) << 7).astype(np.uint8)
+    vc = rng.integers(0, 0x7E, size=(N, H, B, D)).astype(np.uint8) | (rng.integers(0, 2, size=(N, H, B, D)) << 7).astype(np.uint8)
+    ks = rng.uniform(1e-3, 1e-2, size=(N, H, B)).astype(np.float32)
+    vs = rng.uniform(1e-3, 1e-2, size=(N, H, B)).astype(np.float32)
+    q = rng.standard_normal((3, H, D)).astype(np.float16)
+    tables = np.array([[3, 1, 4], [0, 5, 2], [6, 0, 0]], dtype=np.int32)
+    lens = np.array([19, 17, 5], dtype=np.int32)
+    kn_, vn_ = np.ascontiguousarray(kc.transpose(0, 2, 1, 3)), np.ascontiguousarray(vc.transpose(0, 2, 1, 3))
+    hnd = fp8.decode_attention(q, kc, vc, ks, vs, tables, lens, B)
+    nhd = fp8.decode_attention(q, kn_, vn_, ks, vs, tables, lens, B, layout="NHD")
+    assert np.array_equal(hnd, nhd)
+    # by hand: sequence 1, head 2 gathers rows (block, offset) through the NHD codes
+    rows = [(int(tables[1][t // B]), t % B) for t in range(int(lens[1]))]
+    k = np.stack([fp8.DECODE[kn_[b, o, 2]] * float(ks[b, 2, o]) for b, o in rows])
+    v = np.stack([fp8.DECODE[vn_[b, o, 2]] * float(vs[b, 2, o]) for b, o in rows])
+    assert np.allclose(nhd[1, 2], rf.attend(q[1, 2], k, v, 1.0 / np.sqrt(D)), rtol=1e-12, atol=1e-14)
+    # an append: the same codes at the swapped place, the same scales
+    kn = rng.standard_normal((2, H, D)).astype(np.float16)
+    vn = rng.standard_normal((2, H, D)).astype(np.float16)
+    a = [x.copy() for x in (kc, vc, ks, vs)]
+    b = [kn_.copy(), vn_.copy(), ks.copy(), vs.copy()]
+    fp8.append_kv(*a, kn, vn, [13, 50], B)
+    fp8.append_kv(*b, kn, vn, [13, 50], B, layout="NHD")
+    assert np.array_equal(a[0].transpose(0, 2, 1, 3), b[0]) and np.array_equal(a[1].transpose(0, 2, 1, 3), b[1])
+    assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])
+    assert not np.array_equal(a[0], kc)
