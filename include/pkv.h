@@ -78,7 +78,7 @@ enum { PKV_KV_F16 = 0, PKV_KV_E4M3 = 1 };
 typedef struct pkv_pool_desc {
     int32_t num_layers; /* L >= 1 */
     int32_t num_blocks; /* N >= 1 physical blocks per layer */
-    int32_t block_size; /* B tokens per block: 8, 16, 32, 64, 128 or 256 */
+    int32_t block_size; /* B tokens per block: 8, 16, 32, 64, 128, 256 or 512 */
     int32_t num_heads;  /* H KV heads (query heads = KV heads) */
     int32_t head_dim;   /* D: 64, 128 or 256 */
     int32_t layout;     /* PKV_LAYOUT_NHD or PKV_LAYOUT_HND */
@@ -296,7 +296,7 @@ pkv_status pkv_scatter_blocks(const pkv_pool *pool, const int32_t *blocks, int32
  *   kernel keeps three int32 per sequence in shared memory, and every CTA scans
  *   the lengths in its prologue); head_dim 64, 128 or 256 for an fp16 cache, 64
  *   or 128 for an E4M3 cache (either layout); block_size 8, 16,
- *   32, 64, 128 or 256; num_blocks * block_size * num_heads < 2^31.
+ *   32, 64, 128, 256 or 512; num_blocks * block_size * num_heads < 2^31.
  * Errors: INVALID_ARG (sizes, alignment, workspace too small), UNSUPPORTED
  *   (head_dim or block_size not built), CUDA (launch failure). */
 pkv_status pkv_decode_attention(const void *q, const void *k_cache, const void *v_cache,

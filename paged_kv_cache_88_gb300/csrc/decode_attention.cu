@@ -535,7 +535,7 @@ decode_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 // the tile's scales ([N][H][B]: token i of the tile is row y_i) as 16-byte
                 // asynchronous copies of four tokens each: lanes 0-15 the K scales of tokens
                 // 4l..4l+3, lanes 16-31 the V scales. A run of four never leaves its block and
-                // every copy is 16-byte aligned, because the block size (8..256) and the tile
+                // every copy is 16-byte aligned, because the block size (8..512) and the tile
                 // start (the cascade's prefix length, whole blocks, plus a multiple of 64) are
                 // multiples of 4 and the host refuses scale pools that are not 16-byte aligned.
                 // Issued before lane 0's arrival, so the stage's phase cannot complete without them.

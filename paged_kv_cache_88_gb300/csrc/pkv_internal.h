@@ -75,7 +75,7 @@ pkv_status prefix_attention_q8(const pkv_pool *pool, int32_t layer, const void *
                                void *stream);
 
 inline bool supported_block_size(int32_t b) {
-    return b == 8 || b == 16 || b == 32 || b == 64 || b == 128 || b == 256;
+    return b == 8 || b == 16 || b == 32 || b == 64 || b == 128 || b == 256 || b == 512;
 }
 
 // Launch `kernel` on `stream` with programmatic stream serialisation: its CTAs

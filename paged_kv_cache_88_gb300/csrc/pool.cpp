@@ -96,7 +96,7 @@ pkv_status check_desc(const pkv_pool_desc *d) {
     if (d->num_layers < 1 || d->num_blocks < 1 || d->num_heads < 1)
         return fail(PKV_ERR_INVALID_ARG, "num_layers, num_blocks and num_heads must be >= 1");
     if (!pkv::supported_block_size(d->block_size))
-        return fail(PKV_ERR_UNSUPPORTED, "block_size %d not supported (8..256, power of two)", d->block_size);
+        return fail(PKV_ERR_UNSUPPORTED, "block_size %d not supported (8..512, power of two)", d->block_size);
     if (!pkv::supported_head_dim(d->head_dim))
         return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", d->head_dim);
     if (d->layout != PKV_LAYOUT_NHD && d->layout != PKV_LAYOUT_HND)

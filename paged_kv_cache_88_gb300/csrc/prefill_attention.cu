@@ -347,7 +347,7 @@ prefill_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_
         // (one box per block of the table, lane i box i). Separate warps, so a K tile
         // is refilled as soon as its S MMAs are done, whatever the V side waits for.
         const bool is_k = warp == 9;
-        const int32_t rowsb = B < kKT ? B : kKT;       // rows per box; B is a power of two, 8..256
+        const int32_t rowsb = B < kKT ? B : kKT;       // rows per box; B is a power of two, 8..512
         auto issue_q = [&] {
             if (lane == 0) {
                 ptx::mbar_arrive_expect_tx(BAR(kQFull), (has_b ? 2 : 1) * kTileBytes);

@@ -178,7 +178,7 @@ def test_prefix_pieces_early_start_identical(splits):
             assert torch.equal(got, want)
 
 
-@pytest.mark.parametrize("B", [8, 16, 64, 256])
+@pytest.mark.parametrize("B", [8, 16, 64, 256, 512])
 def test_cascade_matches_oracle(B):
     """Two groups, unshared sequences, and a member whose whole context is the prefix."""
     rng = np.random.default_rng(B)

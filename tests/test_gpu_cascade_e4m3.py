@@ -149,7 +149,7 @@ def test_e4m3_prefix_pieces(splits):
                     assert_close(o / l, rf.attend(c.q[s, h], kk, vv, c.scale), f"piece {(s, h, k)}")
 
 
-@pytest.mark.parametrize("B", [8, 16, 64, 256])
+@pytest.mark.parametrize("B", [8, 16, 64, 256, 512])
 def test_e4m3_cascade_matches_oracle(B):
     """Two groups, unshared sequences, and a member whose whole context is the prefix."""
     rng = np.random.default_rng(B + 100)

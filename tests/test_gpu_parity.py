@@ -134,7 +134,7 @@ def test_13b_shape_churned_pool_reduced(layout):
     run_parity(w, 2)
 
 
-@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256, 512])
 def test_long_context_block_sweep_reduced(block_size):
     w = wl.make_workload(5, num_layers=1, num_seqs=3, len_scale=0.12, decode_steps=2, block_size=block_size)
     run_parity(w, 2)
@@ -253,7 +253,7 @@ def test_e4m3_13b_shape_reduced():
     run_parity(w, 2)
 
 
-@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256, 512])
 def test_e4m3_long_context_reduced(block_size):
     w = wl.make_workload(5, num_layers=1, num_seqs=3, len_scale=0.12, decode_steps=2, block_size=block_size,
                          kv_dtype="e4m3")

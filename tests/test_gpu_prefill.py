@@ -57,7 +57,7 @@ def _check(got, ref, what):
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside tolerance, max err {np.nanmax(err):.3e}"
 
 
-@pytest.mark.parametrize("B", [8, 16, 64, 256])
+@pytest.mark.parametrize("B", [8, 16, 64, 256, 512])
 def test_prefill_mixed_chunks(B):
     H = 2
     lens, chunks = [200, 130, 300, 5], [200, 17, 129, 5]

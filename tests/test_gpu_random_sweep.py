@@ -26,7 +26,7 @@ from oracle import fp8  # noqa: E402
 from oracle import ref_attn_c as rc  # noqa: E402
 
 ATOL, RTOL = 2e-3, 1e-2
-BLOCK_SIZES = [8, 16, 32, 64, 128, 256]
+BLOCK_SIZES = [8, 16, 32, 64, 128, 256, 512]
 
 
 def assert_close(got, ref, what):
