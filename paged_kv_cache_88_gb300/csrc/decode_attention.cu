@@ -1248,10 +1248,19 @@ pkv_status encode_map(CUtensorMap *map, const void *base, int N, int B, int H, i
     }
     const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)std::min(B, kTile)};
     const cuuint32_t estr[2] = {1, 1};
+    // L2 promotion no wider than what a box row reads contiguously: in NHD one head's row
+    // (D elements) sits between the other heads' rows, and a wider promotion would fetch
+    // a neighbour's piece with every row (an E4M3 row at head_dim 128 is 128 bytes)
+    CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+    if (layout == PKV_LAYOUT_NHD) {
+        const cuuint64_t piece = (cuuint64_t)D * elem;
+        promo = piece >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                             : (piece >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
+    }
     CUresult r = fn(map, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                     const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    promo,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return PKV_OK;
