@@ -8,14 +8,15 @@ One decode step over a batch (all through the C ABI):
    double-buffered staging (the host can prepare step k+1 while step k runs);
 3. ``pkv_copy_blocks`` once for the step, across all layers;
 4. per layer: the new token's K/V appended and attention over the cache
-   including it -- one ``pkv_decode_append_attention`` launch (the default for an
-   fp16 cache), or ``pkv_append`` then ``pkv_pool_decode_attention`` (the default
-   for an E4M3 cache). With the shared-prefix
-   cascade (HND pools, head_dim 128, fp16 or E4M3, on by default), the host
-   plans groups of sequences that share leading blocks (``pkv_cascade_plan``)
-   and each layer first runs ``pkv_prefix_attention`` over the groups'
-   prefixes, then ``pkv_decode_attention_ex`` over the private rest (fused
-   append included for fp16).
+   including it -- one launch that appends and attends (the default for an fp16
+   cache, and for an E4M3 cache whose batch gives each CTA at most four
+   (sequence, head) pairs), or ``pkv_append`` then the attention started early
+   behind it (an E4M3 cache with more). With the shared-prefix cascade (HND
+   pools, head_dim 128, fp16 or E4M3, on by default), the host plans groups of
+   sequences that share leading blocks (``pkv_cascade_plan``) and each layer
+   first runs ``pkv_prefix_attention`` over the groups' prefixes, then
+   ``pkv_decode_attention_ex`` over the private rest (with the append when
+   fused).
 
 The driver also replays a workload's set-up script (admissions, forks, dummy
 churn, multi-token writes). It holds no arithmetic of the method: slots,
@@ -33,15 +34,27 @@ import workloads as wl
 from . import binding as bd
 
 
+# E4M3 cache: the attention launch appends the step's rows itself while each of its CTAs
+# ends at most this many (sequence, head) pairs on average, else a separate append launch
+FUSED_E4M3_UNITS_PER_CTA = 4
+
+
 class DecodeEngine:
     def __init__(self, w: wl.Workload, device: str = "cuda", fill: str = "torch", max_new_per_step: int = 1,
                  fused: Optional[bool] = None, cascade: bool = True):
         self.w = w
         # append inside the attention launch (pkv_decode_append_attention). By default
-        # on an fp16 cache only: on an E4M3 cache the producer warp's quantise-store-fence
-        # chain for every (sequence, head) stalls the tile pipeline, and a separate
-        # append launch measured up to 20 % faster per step (13B shape, batch 128)
-        self.fused = (w.kv_dtype == "f16") if fused is None else bool(fused)
+        # always on an fp16 cache; on an E4M3 cache only while each CTA of the attention
+        # launch ends few (sequence, head) pairs: the quantise-store-fence chain of each
+        # stalls its producer warp, and past about four a CTA the separate append launch
+        # wins (7B batch 32: 1.7 a CTA, fused +3.6 % per step; 13B batch 128: 8.4, fused
+        # -10 %)
+        if fused is None:
+            fused = True
+            if w.kv_dtype != "f16":
+                grid = bd.decode_launch_info(w.num_seqs, w.head_dim, w.kv_dtype)["grid_ctas"]
+                fused = w.num_seqs * w.num_heads <= FUSED_E4M3_UNITS_PER_CTA * grid
+        self.fused = bool(fused)
         # shared-prefix cascade: where a prefix pass is built (fp16 and E4M3 pools, HND, head_dim 128)
         self.cascade = bool(cascade) and w.layout == "HND" and w.head_dim == 128
         self.device = torch.device(device)
@@ -286,7 +299,7 @@ class DecodeEngine:
         maxb, S = w.max_blocks, w.num_seqs
         sc = float(scale)
         fused = self.fused and n_slots == S
-        early = bd.ATTN_INPUTS_EARLY if w.kv_dtype == "f16" else 0
+        early = bd.ATTN_INPUTS_EARLY
         # after the layer's own append launch of one token per sequence (which first waits for
         # everything before it on the stream): the attention may start early, the tiles holding
         # the appended rows read last
@@ -316,8 +329,7 @@ class DecodeEngine:
                                                    bd.ATTN_INPUTS_EARLY if fused else after_append, sp))
             elif fused:
                 # layers after the first follow the previous layer's attention, which writes
-                # none of this layer's tables, lengths or cache: start early (fp16 cache; on
-                # an E4M3 cache the early start measured 1-4 % slower)
+                # none of this layer's tables, lengths or cache: start early
                 bd.check(L.pkv_decode_attention_ex(h, layer, qp + off, kp + off, vp + off, slp, tp, maxb, lp, S,
                                                    None, None, 0, sc, op + off, wsp, wsb,
                                                    early if layer > 0 else 0, sp))
