@@ -540,6 +540,47 @@ def test_fused_append_skip_and_bad_slot():
     assert_close(out[0].cpu().numpy(), ref, "fused skip / bad slot")
 
 
+@pytest.mark.parametrize("shape", ["tiny", "7b"])
+def test_fused_append_skip_and_bad_slot_e4m3(shape):
+    """E4M3 cache, append inside the attention launch: slot -1 stores nothing and the pool
+    row (codes and scale) is read as it is; slot >= N*B is flagged and not stored (head_dim
+    64 on the CUDA-core consumers, head_dim 128 on the tensor-core ones)."""
+    from oracle import fp8
+    if shape == "tiny":
+        w = wl.make_workload(1, decode_steps=2, kv_dtype="e4m3")
+    else:
+        w = wl.make_workload(2, num_layers=1, num_seqs=6, len_scale=0.2, decode_steps=2, kv_dtype="e4m3")
+    eng = DecodeEngine(w, fill="numpy", fused=True)
+    ora = make_oracle(w)
+    eng.run_script(values="numpy")
+    ora.run_script()
+    q, k, v = ora.step_inputs(0)
+    qd, kd, vd = eng.step_inputs(0, "numpy")
+    n_slots, n_pairs = eng.prepare_step()
+    slots = eng.slots_d.clone()
+    eng.slots_d[1] = -1
+    eng.slots_d[2] = w.num_blocks * w.block_size + 3
+    out = torch.empty_like(qd)
+    eng.device_step(qd, kd, vd, out, n_slots, n_pairs)
+    torch.cuda.synchronize()
+    assert pkv.workspace_status(eng.workspace) & pkv.DEV_BAD_SLOT
+    eng.workspace.zero_()
+    slots_o, pairs_o = ora.pool.prepare_append(ora.tables, ora.lens, [1] * w.num_seqs, w.block_size, w.max_blocks)
+    assert slots_o == slots.tolist()
+    ora._copy(pairs_o)
+    slots_o[1] = -1
+    slots_o[2] = -1
+    fp8.append_kv(ora.k_pool[0], ora.v_pool[0], ora.k_scale[0], ora.v_scale[0], k[0], v[0], slots_o,
+                  w.block_size, w.layout)
+    ref = fp8.decode_attention(q[0], ora.k_pool[0], ora.v_pool[0], ora.k_scale[0], ora.v_scale[0],
+                               ora.tables_array(), ora.lens, w.block_size, layout=w.layout)
+    assert np.array_equal(bits(eng.k_pool)[0], ora.k_pool[0].view(np.uint8))
+    assert np.array_equal(bits(eng.v_pool)[0], ora.v_pool[0].view(np.uint8))
+    assert np.array_equal(bits(eng.k_scale)[0], ora.k_scale[0].view(np.uint32))
+    assert np.array_equal(bits(eng.v_scale)[0], ora.v_scale[0].view(np.uint32))
+    assert_close(out[0].cpu().numpy(), ref, f"E4M3 fused skip / bad slot ({shape})")
+
+
 def test_host_argument_errors():
     dev = "cuda"
     q = torch.zeros((2, 2, 96), dtype=torch.float16, device=dev)
