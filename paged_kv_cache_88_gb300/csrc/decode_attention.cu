@@ -7,7 +7,7 @@
 // [page, slot, head, dim] through the page table; icman.com.cn/news/78786 §2.4
 // walks the block table and loads each block's K/V). Single-query decode is a
 // GEMV over the cache: about 0.5 FMA per byte, so the kernel is bound by HBM
-// bandwidth and uses no tensor cores.
+// bandwidth, not by arithmetic.
 //
 // Design (GB300-first; the pages' A100 kernel advice -- table in shared memory,
 // vectorised loads, many heads per launch -- is prior art, not the blueprint):
@@ -19,23 +19,36 @@
 //   number of tiles (+-1).
 // * A producer warp walks the CTA's range and issues TMA tensor loads of each
 //   tile's K and V rows (one box per block, or a 64-row box inside a large
-//   block) into a multi-stage shared-memory ring guarded by mbarriers; it keeps a
-//   window of 32 block-table entries of the current sequence in registers (one
-//   coalesced load serves every head of the sequence). The query row of a new
-//   (s, h) rides along in the same stage as a 1-D bulk copy.
-// * Four consumer warps split each tile into 16 groups of 8 lanes; a group owns
-//   four rows (tokens) of the tile, a lane 8 x (D / 64) elements of the head dim.
-//   Rows are read from shared memory as 16-byte words, a group covering 128
-//   contiguous bytes per load (no bank conflicts). q.K accumulates fp16 x fp16
-//   products in fp32 (mixed-precision FMA; the products are exact) and finishes
-//   with three xor-shuffles; p.V runs as packed fp32 pair FMAs. Each group keeps
-//   its own online-softmax state (running max m, sum l, unnormalised o), so no
-//   block-wide synchronisation happens per tile.
-// * When an (s, h) ends inside the CTA, the 16 group states are merged through
+//   block; lane i issues box i) into a 2-stage shared-memory ring guarded by
+//   mbarriers; it keeps a window of 128 block-table entries of the current
+//   sequence in registers (one coalesced load serves every head of the
+//   sequence). The query row of a new (s, h) rides along in the same stage as a
+//   1-D bulk copy; an FP8 E4M3 cache's per-row scales as 16-byte cp.async copies.
+// * Consumers, fp16 cache (and E4M3 at head_dim 64): four warps split each tile
+//   into 16 groups of 8 lanes; a group owns four rows (tokens) of the tile, a
+//   lane 8 x (D / 64) elements of the head dim. Rows are read from shared memory
+//   as 16-byte words, a group covering 128 contiguous bytes per load (no bank
+//   conflicts). q.K accumulates fp16 x fp16 products in fp32 (mixed-precision
+//   FMA; the products are exact) and finishes with three xor-shuffles; p.V runs
+//   as packed fp32 pair FMAs. Each group keeps its own online-softmax state
+//   (running max m, sum l, unnormalised o), so no block-wide synchronisation
+//   happens per tile.
+// * Consumers, E4M3 cache at head_dim 128: the tiles land 128-byte swizzled and
+//   each warp runs q.K and p.V for 16 tokens of a tile on the warp-level tensor
+//   cores (mma.sync m16n8k16, codes converted to fp16 operands, fp32 sums); the
+//   softmax reference covers x + log2(V row scale), so the weights x scale enter
+//   p.V as fp16 <= 1.
+// * When an (s, h) ends inside the CTA, the per-warp states are merged through
 //   shared memory. A (s, h) that lies wholly in the CTA is written straight to
 //   out; one split across CTAs writes its piece (m, l, o) to the workspace and
 //   the last CTA to arrive (an atomic counter, no waiting) merges the pieces and
-//   writes out -- split-KV with the combine fused into the same launch.
+//   writes out -- split-KV with the combine fused into the same launch. A
+//   cascade member also merges the prefix pass's pieces of its shared prefix.
+// * Optional in the same launch: the step's append (the producer stores each
+//   sequence's new K/V row -- quantised for an E4M3 cache -- before the tile
+//   that holds it), and an early start behind the previous kernel on the stream
+//   (tables, lengths and the first tiles' K/V read before the grid dependency
+//   resolves).
 // * Every mbarrier wait has a time limit; on expiry the CTA flags
 //   PKV_DEV_TIMEOUT, stops waiting and runs to the end (no trap, no hang).
 #include <cuda.h>
