@@ -51,14 +51,17 @@ def _sample(lens: np.ndarray, n: int) -> list:
     return sorted(pick)
 
 
-def _e4m3_full(cfg: int, check_layers, n_seqs=None, fused=None, **kw):
+def _e4m3_full(cfg: int, check_layers, n_seqs=None, fused=None, pairs=0, groups=0, cow=0, **kw):
     """The benchmark's E4M3 step (the engine's default: the append inside the attention
     launch while each CTA ends at most four (sequence, head) pairs, else a separate launch),
-    checked on sampled outputs; ``fused`` is the choice the engine must make here."""
+    checked on sampled outputs; ``fused`` is the choice the engine must make here, ``pairs``
+    the copy-on-write copies the step makes (applied to the oracle's pools before its append),
+    ``cow`` the pool's copies after the set-up, ``groups`` the cascade's groups."""
     w = wl.make_workload(cfg, kv_dtype="e4m3", **kw)
     eng = DecodeEngine(w, fill="torch")
     assert eng.fused == fused
     eng.run_script(values="torch")
+    assert eng.pool.stats()["cow_copies"] == cow
     qd, kd, vd = eng.step_inputs(0, "torch")
     before = {l: [t[l].cpu().numpy() for t in (eng.k_pool, eng.v_pool, eng.k_scale, eng.v_scale)]
               for l in check_layers}
@@ -66,11 +69,13 @@ def _e4m3_full(cfg: int, check_layers, n_seqs=None, fused=None, **kw):
     eng.step(qd, kd, vd, out)
     torch.cuda.synchronize()
     assert eng.device_status() == 0
-    assert len(eng.last_pairs) == 0
+    assert len(eng.last_pairs) == pairs
+    assert eng.plan_groups == groups
     tab, lens = eng.tables.copy(), eng.lens.copy()
     seqs = list(range(w.num_seqs)) if n_seqs is None else _sample(lens, n_seqs)
     for l in check_layers:
         kc, vc, ks, vs = before[l]
+        fp8.copy_blocks(kc[None], vc[None], ks[None], vs[None], [tuple(p) for p in eng.last_pairs.tolist()])
         fp8.append_kv(kc, vc, ks, vs, kd[l].cpu().numpy(), vd[l].cpu().numpy(), eng.last_slots, w.block_size)
         assert np.array_equal(kc, eng.k_pool[l].cpu().numpy()), f"K codes layer {l}"
         assert np.array_equal(vc, eng.v_pool[l].cpu().numpy()), f"V codes layer {l}"
@@ -89,6 +94,14 @@ def test_e4m3_7b_full_size_sampled(free_gpu_memory):
 def test_e4m3_long_context_full_size_sampled(free_gpu_memory):
     """16 sequences of 4k-16k tokens, block 256: layer 0, four sequences, every head."""
     _e4m3_full(5, [0], n_seqs=4, fused=True)
+
+
+def test_e4m3_prefix_cow_cascade_full_size_sampled(free_gpu_memory):
+    """Forked prompt at full size with an E4M3 cache (64 sequences on one 520-token prompt,
+    32 layers, codes and scales copied on write for 63 of them in the set-up): the cascade's
+    prefix pass over the shared 512 tokens and the private pass with the append inside;
+    layers 0 and 31, eight sequences, every head."""
+    _e4m3_full(3, [0, 31], n_seqs=8, fused=True, groups=1, cow=63)
 
 
 def test_e4m3_13b_full_size_sampled(free_gpu_memory):
