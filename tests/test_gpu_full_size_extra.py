@@ -76,13 +76,14 @@ def _e4m3_full(cfg: int, check_layers, n_seqs=None, fused=None, pairs=0, groups=
     for l in check_layers:
         kc, vc, ks, vs = before[l]
         fp8.copy_blocks(kc[None], vc[None], ks[None], vs[None], [tuple(p) for p in eng.last_pairs.tolist()])
-        fp8.append_kv(kc, vc, ks, vs, kd[l].cpu().numpy(), vd[l].cpu().numpy(), eng.last_slots, w.block_size)
+        fp8.append_kv(kc, vc, ks, vs, kd[l].cpu().numpy(), vd[l].cpu().numpy(), eng.last_slots, w.block_size,
+                      w.layout)
         assert np.array_equal(kc, eng.k_pool[l].cpu().numpy()), f"K codes layer {l}"
         assert np.array_equal(vc, eng.v_pool[l].cpu().numpy()), f"V codes layer {l}"
         assert np.array_equal(ks.view(np.uint32), eng.k_scale[l].cpu().numpy().view(np.uint32)), f"K scales {l}"
         assert np.array_equal(vs.view(np.uint32), eng.v_scale[l].cpu().numpy().view(np.uint32)), f"V scales {l}"
         q = qd[l].cpu().numpy()[seqs]
-        ref = fp8.decode_attention(q, kc, vc, ks, vs, tab[seqs], lens[seqs], w.block_size)
+        ref = fp8.decode_attention(q, kc, vc, ks, vs, tab[seqs], lens[seqs], w.block_size, layout=w.layout)
         assert_close(out[l].cpu().numpy()[seqs], ref, f"E4M3 cfg {cfg} layer {l}")
 
 
@@ -102,6 +103,14 @@ def test_e4m3_prefix_cow_cascade_full_size_sampled(free_gpu_memory):
     prefix pass over the shared 512 tokens and the private pass with the append inside;
     layers 0 and 31, eight sequences, every head."""
     _e4m3_full(3, [0, 31], n_seqs=8, fused=True, groups=1, cow=63)
+
+
+def test_e4m3_nhd_full_size_sampled(free_gpu_memory):
+    """E4M3 codes in NHD pools (a head's 128-byte row every H*D bytes; scales [N][H][B] as in
+    HND), as `bench.py --kv-dtype e4m3 --layout NHD` runs them: the 7B workload (layers 0 and
+    31, every sequence and head) and the long one (layer 0, four sequences)."""
+    _e4m3_full(2, [0, 31], fused=True, layout="NHD")
+    _e4m3_full(5, [0], n_seqs=4, fused=True, layout="NHD")
 
 
 def test_e4m3_13b_full_size_sampled(free_gpu_memory):

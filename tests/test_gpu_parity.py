@@ -607,14 +607,16 @@ def free_gpu_memory():
     torch.cuda.empty_cache()
 
 
-def test_7b_full_size_bench_launch_sampled(free_gpu_memory):
-    """The 7B-shape batch-32 workload at full size, 32 layers, in the benchmark's launch configuration.
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+def test_7b_full_size_bench_launch_sampled(layout, free_gpu_memory):
+    """The 7B-shape batch-32 workload at full size, 32 layers, in the benchmark's launch configuration
+    (the default HND pools, and NHD as `bench.py --layout NHD` runs it).
 
     The oracle allocator replays the same script (tables bit-exact); for two
     layers the pre-step pools are read back and the float64 C oracle computes
     every (sequence, head) of the step.
     """
-    w = wl.make_workload(2)
+    w = wl.make_workload(2, layout=layout)
     eng = DecodeEngine(w, fill="torch")
     eng.run_script()
     from oracle import ref_alloc as ra
@@ -706,10 +708,17 @@ def test_13b_full_size_sampled(free_gpu_memory):
 def test_long_context_full_size_sampled(block_size, free_gpu_memory):
     """16 sequences of 4k-16k tokens, full size (32 layers): in 4 MiB pages (block 256), and the
     block-size sweep's ends with the same token data -- block 8 gives tables of up to 2049 entries
-    (the producer's 32-entry table window is refilled 64 times per (sequence, head)), block 64
+    (the producer's 128-entry table window is refilled 16 times per (sequence, head)), block 64
     one TMA box per 64-token tile."""
     w = wl.make_workload(5, decode_steps=4, block_size=block_size)
     _full_size(w, [0, w.num_layers - 1], steps=2)
+
+
+def test_long_context_nhd_full_size_sampled(free_gpu_memory):
+    """The long-context workload at full size in NHD pools (block 256: a head's 256-byte row
+    every H*D elements), as `bench.py --layout NHD --config 5` runs it; layer 0."""
+    w = wl.make_workload(5, decode_steps=4, layout="NHD")
+    _full_size(w, [0], steps=1)
 
 
 def test_early_start_back_to_back_layers():
