@@ -125,6 +125,13 @@ def test_e4m3_long_context_block_16_full_size_sampled(free_gpu_memory):
     _e4m3_full(5, [0], n_seqs=4, block_size=16, fused=True)
 
 
+@pytest.mark.parametrize("block_size", [64, 512])
+def test_e4m3_long_context_block_sweep_full_size_sampled(block_size, free_gpu_memory):
+    """The long-context E4M3 rows of the block-size sweep at full size (block 64: one TMA box
+    a tile; block 512: the quantised cache's 512-token pages): layer 0, two sequences."""
+    _e4m3_full(5, [0], n_seqs=2, block_size=block_size, fused=True)
+
+
 def _prefill_full(cfg: int, chunk: int, n_seqs: int, heads, block_size=None):
     w = wl.make_workload(cfg, decode_steps=8, block_size=block_size)
     eng = DecodeEngine(w, fill="torch")
@@ -160,6 +167,19 @@ def test_prefill_whole_prompts_7b_full_size_sampled(free_gpu_memory):
     """The benchmark's whole-prompt prefill (chunks of up to 2048) on the 7B workload:
     four sequences, heads 0 and 31, every row."""
     _prefill_full(2, 2048, 4, [0, 31])
+
+
+def test_prefill_chunks_of_512_7b_full_size_sampled(free_gpu_memory):
+    """The benchmark's 7B prefill in chunks of 512 (each sequence's last 512 tokens over the
+    rest of its context): four sequences, heads 0 and 31, every row."""
+    _prefill_full(2, 512, 4, [0, 31])
+
+
+@pytest.mark.parametrize("block_size", [16, 512])
+def test_prefill_long_chunks_other_blocks_full_size_sampled(block_size, free_gpu_memory):
+    """The 4096-token chunks over the long contexts at blocks 16 and 512 (the prefill rows of
+    the block-size sweep): the longest and the shortest sequence, head 0, every row."""
+    _prefill_full(5, 4096, 2, [0], block_size=block_size)
 
 
 def test_prefill_long_chunks_full_size_sampled(free_gpu_memory):

@@ -704,7 +704,7 @@ def test_13b_full_size_sampled(free_gpu_memory):
     _full_size(w, [0, w.num_layers - 1], steps=2)
 
 
-@pytest.mark.parametrize("block_size", [256, 8, 64])
+@pytest.mark.parametrize("block_size", [256, 8, 64, 512])
 def test_long_context_full_size_sampled(block_size, free_gpu_memory):
     """16 sequences of 4k-16k tokens, full size (32 layers): in 4 MiB pages (block 256), and the
     block-size sweep's ends with the same token data -- block 8 gives tables of up to 2049 entries
