@@ -28,7 +28,9 @@
  *     flagged in the status word; every wait in a kernel has a time limit.
  *   - A pool handle is not thread-safe: the caller serialises calls that
  *     mutate it. Distinct pools are independent.
- *   - Element type: IEEE binary16 (fp16) for K, V, q and out.
+ *   - Element types: IEEE binary16 (fp16) for q, out and the new tokens' K/V rows;
+ *     the K/V pools hold fp16 or FP8 E4M3 codes with per-row fp32 scales
+ *     (PKV_KV_F16 / PKV_KV_E4M3 below).
  */
 #ifndef PKV_H
 #define PKV_H
