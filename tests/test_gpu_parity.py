@@ -428,6 +428,17 @@ def test_one_long_sequence_spans_every_cta():
     assert st2 == 0 and np.array_equal(out, out2)
 
 
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+def test_very_long_sequence_small_blocks(layout):
+    """One 65,536-token sequence in 8-token blocks beside a short one: an 8,192-entry block
+    table (the producer's 128-entry window refilled 64 times per (sequence, head)), blocks
+    scattered over the pool, every CTA of the launch on the long sequence's pieces."""
+    q, kp, vp, tab, ln, B, N = _raw_case([65536, 100], H=2, B=8, canary_nan=True, seed=9, layout=layout)
+    out, st, _ = _gpu_attn(q, kp, vp, tab, ln, B, N, layout)
+    assert st == 0
+    assert_close(out, rc.decode_attention(q, kp, vp, tab, ln, B, layout), f"65536 tokens B=8 {layout}")
+
+
 def test_workspace_reused_across_batch_sizes():
     """One workspace, sized for 48 sequences of 8 heads, serves calls with 6, then 48, then 20
     sequences and then another head_dim. The small batch's (s, h) are split over many CTAs,
