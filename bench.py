@@ -360,11 +360,11 @@ def run_ours(args):
     import torch
 
     rank, world, local = dist_env()
+    torch.cuda.set_device(local)      # before the process group, so NCCL binds this rank's GPU
+    dev = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
 
     from paged_kv_cache_88_gb300.engine import DecodeEngine
     import paged_kv_cache_88_gb300 as pkv
