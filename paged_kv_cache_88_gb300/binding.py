@@ -168,9 +168,10 @@ def _require(t, dtype_name: str, what: str):
 class Pool:
     """A block pool (host metadata in libpkv) over caller-owned K/V pool tensors.
 
-    ``k_pool``/``v_pool``: CUDA fp16 tensors of L*N*B*H*D elements laid out as
-    [L, N, H, B, D] (HND, the default) or [L, N, B, H, D] (NHD), or None for a
-    host-only pool.
+    ``k_pool``/``v_pool``: CUDA tensors of L*N*B*H*D elements (fp16, or uint8 E4M3
+    codes for ``kv_dtype="e4m3"``) laid out as [L, N, H, B, D] (HND, the default) or
+    [L, N, B, H, D] (NHD), or None for a host-only pool. ``k_scale``/``v_scale``
+    (E4M3): fp32 tensors of L*N*H*B row scales, [L, N, H, B] in either layout.
     """
 
     def __init__(self, num_layers: int, num_blocks: int, block_size: int, num_heads: int, head_dim: int,

@@ -267,6 +267,15 @@ def test_cascade_argument_errors():
         small.prefix_attention(0, torch.zeros((3, 2, 64), dtype=torch.float16, device="cuda"), gd, 1, 1, c.tab_d,
                                c.pieces, c.status)
     assert e.value.code == "UNSUPPORTED"
+    # nor has an NHD pool, fp16 or E4M3 (a head's rows are not contiguous there)
+    for kv in ("f16", "e4m3"):
+        dt = torch.float16 if kv == "f16" else torch.uint8
+        nhd = pkv.Pool(1, 8, 16, 2, 128, "NHD", kv_dtype=kv, k_pool=torch.zeros((8, 16, 2, 128), dtype=dt, device="cuda"),
+                       v_pool=torch.zeros((8, 16, 2, 128), dtype=dt, device="cuda"))
+        with pytest.raises(bd.PkvError) as e:
+            nhd.prefix_attention(0, torch.zeros((3, 2, 128), dtype=torch.float16, device="cuda"), gd, 1, 1, c.tab_d,
+                                 c.pieces, c.status)
+        assert e.value.code == "UNSUPPORTED"
     torch.cuda.synchronize()
 
 
