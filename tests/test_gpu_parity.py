@@ -592,6 +592,32 @@ def test_fused_append_skip_and_bad_slot_e4m3(shape):
     assert_close(out[0].cpu().numpy(), ref, f"E4M3 fused skip / bad slot ({shape})")
 
 
+def test_empty_batches_are_no_ops():
+    """Zero sequences, tokens, pairs or chunks: each device entry point returns without a
+    launch and leaves the pools and the status words as they were."""
+    dev = "cuda"
+    H, D, B, N = 2, 128, 16, 4
+    kp = torch.randn((1, N, H, B, D), device=dev).half()
+    vp = torch.randn((1, N, H, B, D), device=dev).half()
+    k0, v0 = kp.clone(), vp.clone()
+    pool = pkv.Pool(1, N, B, H, D, "HND", k_pool=kp, v_pool=vp)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = pkv.new_workspace(1, H, D)
+    q = torch.zeros((0, H, D), dtype=torch.float16, device=dev)
+    out = torch.zeros_like(q)
+    tab = torch.zeros((0, 1), dtype=torch.int32, device=dev)
+    lens = torch.zeros(0, dtype=torch.int32, device=dev)
+    slots = torch.zeros(0, dtype=torch.int64, device=dev)
+    pool.decode_attention(0, q, tab, lens, out, ws)
+    pool.decode_append_attention(0, q, q, q, slots, tab, lens, out, ws)
+    pool.append(0, q, q, slots, status=status)
+    pool.copy_blocks(torch.zeros((0, 2), dtype=torch.int32, device=dev), status=status)
+    pool.prefill_attention(0, q, torch.zeros(1, dtype=torch.int32, device=dev), 0, tab, lens, out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and pkv.workspace_status(ws) == 0
+    assert torch.equal(kp, k0) and torch.equal(vp, v0)
+
+
 def test_host_argument_errors():
     dev = "cuda"
     q = torch.zeros((2, 2, 96), dtype=torch.float16, device=dev)
