@@ -1,10 +1,11 @@
 """Full-size GPU parity of the E4M3 decode step and of the tensor-core prefill, each in the
 launch configuration bench.py times, checked against the oracle on sampled outputs.
 
-* E4M3: the engine's default step (separate quantising append, then attention) on the
-  full 7B and long-context workloads; the appended codes and scales of the checked
-  layers are compared bit for bit with the oracle quantiser, and the attention of the
-  sampled sequences (every head) with the float64 definition on code x scale.
+* E4M3: the engine's default step on the full 7B, forked-prompt, 13B and long-context
+  workloads (both layouts for 7B and long); the oracle replays the set-up and the step
+  with its own allocator and quantiser from the pools as filled, the codes and scales of
+  the checked layers are compared bit for bit, and the attention of the sampled
+  sequences (every head) with the float64 definition on code x scale.
 * Prefill: the benchmark's causal prefill (whole prompts of the 7B workload; chunks of
   4096 over the long contexts), every row of the sampled (sequence, head) pairs against
   the float64 causal definition, computed on just that sequence's blocks.
@@ -51,39 +52,66 @@ def _sample(lens: np.ndarray, n: int) -> list:
     return sorted(pick)
 
 
-def _e4m3_full(cfg: int, check_layers, n_seqs=None, fused=None, pairs=0, groups=0, cow=0, **kw):
+def _e4m3_full(cfg: int, check_layers, n_seqs=None, fused=None, groups=0, cow=0, **kw):
     """The benchmark's E4M3 step (the engine's default: the append inside the attention
-    launch while each CTA ends at most four (sequence, head) pairs, else a separate launch),
-    checked on sampled outputs; ``fused`` is the choice the engine must make here, ``pairs``
-    the copy-on-write copies the step makes (applied to the oracle's pools before its append),
-    ``cow`` the pool's copies after the set-up, ``groups`` the cascade's groups."""
+    launch while each CTA ends at most four (sequence, head) pairs, else a separate launch)
+    at full size, against the oracle on the listed layers: the oracle starts from the pools
+    as filled before any write, replays the set-up with its own allocator and quantiser
+    (tables, codes and scales bit-exact after it), then takes the step's slots and copies
+    from its own allocator, appends with its own quantiser (codes and scales bit-exact
+    again) and computes the attention of the sampled sequences (every head). ``fused`` is
+    the choice the engine must make here, ``cow`` the set-up's copies, ``groups`` the
+    cascade's groups."""
+    import dataclasses
+    from oracle.driver import OracleEngine
     w = wl.make_workload(cfg, kv_dtype="e4m3", **kw)
     eng = DecodeEngine(w, fill="torch")
     assert eng.fused == fused
+    snap = [np.stack([t[l].cpu().numpy() for l in check_layers])
+            for t in (eng.k_pool, eng.v_pool, eng.k_scale, eng.v_scale)]
     eng.run_script(values="torch")
     assert eng.pool.stats()["cow_copies"] == cow
+    ora = OracleEngine(dataclasses.replace(w, num_layers=len(check_layers)), *snap)
+    del snap
+
+    def values(op_index, i, which, n):
+        return wl.torch_normal_fp16(w.seed, (400 + which, op_index, check_layers[i]), (n, w.num_heads, w.head_dim),
+                                    "cuda").cpu().numpy()
+
+    ora.run_script(values)
+    torch.cuda.synchronize()
+    assert eng.tables.tolist() == ora.tables and eng.lens.tolist() == ora.lens
+
+    def same_pools(what):
+        for i, l in enumerate(check_layers):
+            assert np.array_equal(eng.k_pool[l].cpu().numpy(), ora.k_pool[i]), f"K codes layer {l} {what}"
+            assert np.array_equal(eng.v_pool[l].cpu().numpy(), ora.v_pool[i]), f"V codes layer {l} {what}"
+            assert np.array_equal(eng.k_scale[l].cpu().numpy().view(np.uint32), ora.k_scale[i].view(np.uint32)), \
+                f"K scales layer {l} {what}"
+            assert np.array_equal(eng.v_scale[l].cpu().numpy().view(np.uint32), ora.v_scale[i].view(np.uint32)), \
+                f"V scales layer {l} {what}"
+
+    same_pools("after set-up")
     qd, kd, vd = eng.step_inputs(0, "torch")
-    before = {l: [t[l].cpu().numpy() for t in (eng.k_pool, eng.v_pool, eng.k_scale, eng.v_scale)]
-              for l in check_layers}
     out = torch.empty_like(qd)
     eng.step(qd, kd, vd, out)
     torch.cuda.synchronize()
     assert eng.device_status() == 0
-    assert len(eng.last_pairs) == pairs
     assert eng.plan_groups == groups
-    tab, lens = eng.tables.copy(), eng.lens.copy()
+    slots, pairs = ora.pool.prepare_append(ora.tables, ora.lens, [1] * w.num_seqs, w.block_size, w.max_blocks)
+    assert eng.last_slots.tolist() == slots and [tuple(p) for p in eng.last_pairs.tolist()] == pairs
+    assert eng.tables.tolist() == ora.tables
+    ora._copy(pairs)
+    for i, l in enumerate(check_layers):
+        fp8.append_kv(ora.k_pool[i], ora.v_pool[i], ora.k_scale[i], ora.v_scale[i], kd[l].cpu().numpy(),
+                      vd[l].cpu().numpy(), slots, w.block_size, w.layout)
+    same_pools("after the step's append")
+    tab, lens = ora.tables_array(), np.asarray(ora.lens, dtype=np.int32)
     seqs = list(range(w.num_seqs)) if n_seqs is None else _sample(lens, n_seqs)
-    for l in check_layers:
-        kc, vc, ks, vs = before[l]
-        fp8.copy_blocks(kc[None], vc[None], ks[None], vs[None], [tuple(p) for p in eng.last_pairs.tolist()])
-        fp8.append_kv(kc, vc, ks, vs, kd[l].cpu().numpy(), vd[l].cpu().numpy(), eng.last_slots, w.block_size,
-                      w.layout)
-        assert np.array_equal(kc, eng.k_pool[l].cpu().numpy()), f"K codes layer {l}"
-        assert np.array_equal(vc, eng.v_pool[l].cpu().numpy()), f"V codes layer {l}"
-        assert np.array_equal(ks.view(np.uint32), eng.k_scale[l].cpu().numpy().view(np.uint32)), f"K scales {l}"
-        assert np.array_equal(vs.view(np.uint32), eng.v_scale[l].cpu().numpy().view(np.uint32)), f"V scales {l}"
+    for i, l in enumerate(check_layers):
         q = qd[l].cpu().numpy()[seqs]
-        ref = fp8.decode_attention(q, kc, vc, ks, vs, tab[seqs], lens[seqs], w.block_size, layout=w.layout)
+        ref = fp8.decode_attention(q, ora.k_pool[i], ora.v_pool[i], ora.k_scale[i], ora.v_scale[i], tab[seqs],
+                                   lens[seqs], w.block_size, layout=w.layout)
         assert_close(out[l].cpu().numpy()[seqs], ref, f"E4M3 cfg {cfg} layer {l}")
 
 
