@@ -165,7 +165,13 @@ def _prefill_full(cfg: int, chunk: int, n_seqs: int, heads, block_size=None):
     eng = DecodeEngine(w, fill="torch")
     eng.run_script(values="torch")
     H, D, B = w.num_heads, w.head_dim, w.block_size
-    lens = eng.lens.copy()
+    # the set-up only admits sequences (the pools keep their generated values): the oracle
+    # allocator's tables for the same admissions, equal to the library's
+    from oracle import ref_alloc as ra
+    op = ra.RefPool(w.num_blocks, [int(x) for x in w.free_order])
+    tabs = np.asarray([ra.admit(op, int(t), B, w.max_blocks) for t in w.context_lens], dtype=np.int64)
+    lens = np.asarray(w.context_lens, dtype=np.int64)
+    assert eng.tables.tolist() == tabs.tolist() and eng.lens.tolist() == lens.tolist()
     chunks = np.minimum(lens, chunk).astype(np.int64)
     q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
     g = torch.Generator(device="cuda")
@@ -180,7 +186,7 @@ def _prefill_full(cfg: int, chunk: int, n_seqs: int, heads, block_size=None):
     for s in _sample(lens, n_seqs):
         T, C = int(lens[s]), int(chunks[s])
         nb = -(-T // B)
-        blocks = torch.from_numpy(eng.tables[s, :nb].astype(np.int64)).cuda()
+        blocks = torch.from_numpy(tabs[s, :nb]).cuda()
         tab = np.arange(nb, dtype=np.int32)[None]
         r0, r1 = int(q_start[s]), int(q_start[s + 1])
         for h in heads:

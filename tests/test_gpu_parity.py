@@ -773,9 +773,13 @@ def test_early_start_back_to_back_layers():
     torch.cuda.synchronize()
     assert eng.device_status() == 0
     kp, vp = wl.pool_values(w, 0), wl.pool_values(w, 1)
+    from oracle import ref_alloc as ra       # the set-up only admits: the oracle allocator's tables
+    op = ra.RefPool(w.num_blocks, [int(x) for x in w.free_order])
+    tabs = np.asarray([ra.admit(op, int(t), w.block_size, w.max_blocks) for t in w.context_lens], dtype=np.int32)
+    lens = np.asarray(w.context_lens, dtype=np.int32)
+    assert eng.tables.tolist() == tabs.tolist() and eng.lens.tolist() == lens.tolist()
     for layer in range(w.num_layers):
-        ref = rf.decode_attention(q[layer].cpu().numpy(), kp[layer], vp[layer], eng.tables, eng.lens,
-                                  w.block_size, w.layout)
+        ref = rf.decode_attention(q[layer].cpu().numpy(), kp[layer], vp[layer], tabs, lens, w.block_size, w.layout)
         assert_close(out[layer].cpu().numpy(), ref, f"early layer {layer}")
 
 
