@@ -45,10 +45,11 @@ class DecodeEngine:
         self.w = w
         # append inside the attention launch (pkv_decode_append_attention). By default
         # always on an fp16 cache; on an E4M3 cache only while each CTA of the attention
-        # launch ends few (sequence, head) pairs: the quantise-store-fence chain of each
-        # stalls its producer warp, and past about four a CTA the separate append launch
-        # wins (7B batch 32: 1.7 a CTA, fused +3.6 % per step; 13B batch 128: 8.4, fused
-        # -10 %)
+        # launch ends few (sequence, head) pairs: each costs its producer warp a load-
+        # quantise-store-fence chain, paid one after another by a CTA whose range holds
+        # many short sequences, and past about four a CTA on average the separate append
+        # launch wins (7B batch 32: 1.7 a CTA, fused +4 % per step; 13B batch 128: 8.4,
+        # fused -9 %)
         if fused is None:
             fused = True
             if w.kv_dtype != "f16":
