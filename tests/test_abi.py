@@ -342,3 +342,20 @@ def test_prefix_cache_matches_oracle(seed):
                        lambda: o.prepare_append(tables_o, lens_o, [n], B, maxb))
         assert tables_c.tolist() == tables_o and lens_c.tolist() == lens_o
         _same_prefix_state(c, o)
+
+
+def test_package_import_fails_loudly_without_the_library(tmp_path):
+    """A copy of the package with no libpkv.so next to it refuses to import (there is no CPU or
+    library fallback)."""
+    import shutil
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(root, "paged_kv_cache_88_gb300")
+    dst = tmp_path / "paged_kv_cache_88_gb300"
+    shutil.copytree(pkg, dst, ignore=shutil.ignore_patterns("*.so", "__pycache__", "csrc"))
+    shutil.copytree(os.path.join(root, "workloads"), tmp_path / "workloads")
+    r = subprocess.run([sys.executable, "-c", "import paged_kv_cache_88_gb300"], capture_output=True, text=True,
+                       cwd=str(tmp_path), timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libpkv.so" in r.stderr
