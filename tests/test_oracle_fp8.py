@@ -131,3 +131,97 @@ def test_nhd_layout_is_the_hnd_one_transposed():
     assert np.array_equal(a[0].transpose(0, 2, 1, 3), b[0]) and np.array_equal(a[1].transpose(0, 2, 1, 3), b[1])
     assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])
     assert not np.array_equal(a[0], kc)
+
+
+# --------------------------------------------------------------------------- planted mistakes
+# The pins above, as checks of a given encoder / quantiser, and copies of the oracle's
+# quantiser with one plausible slip each: every slip makes at least one check fail.
+
+def _check_round_trip(encode):
+    codes = [c for c in range(256) if not np.isnan(fp8.DECODE[c])]
+    return all(int(encode(np.array([fp8.DECODE[c]]))[0]) == c for c in codes)
+
+
+def _check_ties_and_saturation(encode):
+    return (int(encode(np.array([1.0625]))[0]) == 0x38 and int(encode(np.array([1.1875]))[0]) == 0x3A
+            and encode(np.array([1000.0, -1000.0])).tolist() == [0x7E, 0xFE]
+            and int(encode(np.array([2.0 ** -10]))[0]) == 0x00)
+
+
+def _check_torch(encode):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    for sc in (1e-3, 1.0, 300.0):
+        x = np.clip(rng.standard_normal(20000).astype(np.float32) * sc, -448, 448)
+        t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        if not np.array_equal(encode(x), t):
+            return False
+    return True
+
+
+def _check_rows(quantize):
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((50, 3, 128)).astype(np.float16)
+    codes, scales = quantize(x)
+    if scales.shape != (50, 3) or not np.all(np.max(np.abs(fp8.DECODE[codes]), axis=-1) == 448.0):
+        return False
+    deq = fp8.dequantize(codes, scales)
+    xf = x.astype(np.float64)
+    big = np.abs(xf) >= scales[..., None].astype(np.float64) * 2.0 ** -6
+    return bool(np.all(np.abs(deq - xf)[big] <= 2.0 ** -4 * np.abs(xf)[big] + 1e-12))
+
+
+def _mutant_encode(kind):
+    vals = fp8.DECODE[:0x7F]
+
+    def encode(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.abs(x) if kind == "no_saturation" else np.minimum(np.abs(x), 448.0)
+        lo = np.clip(np.searchsorted(vals, a, side="right") - 1, 0, 0x7E)
+        hi = np.minimum(lo + 1, 0x7E)
+        below, above = a - vals[lo], vals[hi] - a
+        if kind == "ties_away":
+            pick_hi = (above < below) | ((above == below) & (hi != lo))
+        elif kind == "truncate":
+            pick_hi = np.zeros(a.shape, dtype=bool)
+        else:
+            pick_hi = (above < below) | ((above == below) & (hi != lo) & ((hi & 1) == 0))
+        code = np.where(pick_hi, hi, lo).astype(np.int64)
+        if kind == "no_saturation":
+            code = np.where(a > 448.0, 0x7F, code)
+        sign = np.signbit(x).astype(np.int64) << 7
+        if kind == "sign_lost_at_zero":
+            sign = np.where(code == 0, 0, sign)
+        return (code | sign).astype(np.uint8)
+    return encode
+
+
+def _mutant_quantize(kind):
+    def quantize(x16):
+        x = np.asarray(x16, dtype=np.float16).astype(np.float32)
+        if kind == "amax_over_heads":
+            amax = np.broadcast_to(np.max(np.abs(x), axis=(-2, -1))[..., None], x.shape[:-1])
+        else:
+            amax = np.max(np.abs(x), axis=-1)
+        div = np.float32(256.0) if kind == "scale_256" else np.float32(448.0)
+        scale = np.where(amax > 0, amax / div, np.float32(1.0)).astype(np.float32)
+        y = (x / scale[..., None]).astype(np.float32)
+        return fp8.e4m3_encode(y), scale
+    return quantize
+
+
+@pytest.mark.parametrize("kind", ["ties_away", "truncate", "no_saturation", "sign_lost_at_zero"])
+def test_planted_encoder_mistake_is_caught(kind):
+    enc = _mutant_encode(kind)
+    assert not (_check_round_trip(enc) and _check_ties_and_saturation(enc) and _check_torch(enc)), kind
+
+
+@pytest.mark.parametrize("kind", ["scale_256", "amax_over_heads"])
+def test_planted_quantiser_mistake_is_caught(kind):
+    assert not _check_rows(_mutant_quantize(kind)), kind
+
+
+def test_unmutated_quantiser_copies_pass():
+    enc = _mutant_encode("none")
+    assert _check_round_trip(enc) and _check_ties_and_saturation(enc) and _check_torch(enc)
+    assert _check_rows(_mutant_quantize("none"))
