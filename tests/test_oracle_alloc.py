@@ -255,3 +255,142 @@ def test_config_free_orders_are_permutations():
         w = workloads.make_workload(i)
         assert sorted(w.free_order.tolist()) == list(range(w.num_blocks))
         assert np.any(w.free_order != np.arange(w.num_blocks))
+
+
+# --------------------------------------------------------------------------- planted mistakes
+# The worked examples above as checks of a given pool class, and copies of the oracle's
+# pool with one plausible slip each: every slip makes at least one check fail.
+
+def _ok(fn):
+    try:
+        return bool(fn())
+    except Exception:
+        return False
+
+
+def _check_fifo(P):
+    p = P(4, [2, 0, 3, 1])
+    if p.alloc(2) != [2, 0]:
+        return False
+    p.incref([0])
+    p.free([2])
+    p.free([0])
+    if list(p.free_queue) != [3, 1, 2] or p.alloc(3) != [3, 1, 2]:
+        return False
+    try:
+        p.alloc(1)
+        return False
+    except ra.PoolError:
+        pass
+    p.free([0, 3])
+    return list(p.free_queue) == [0, 3] and p.refcount == [0, 1, 1, 0]
+
+
+def _check_cow(P):
+    B, p = 4, P(8)
+    t0 = ra.admit(p, 5, B, 4)
+    t1 = ra.fork(p, t0, 5, B)
+    tables, lens = [t0, t1], [5, 5]
+    slots, pairs = p.prepare_append(tables, lens, [1, 1], B, 4)
+    return (pairs == [(1, 2)] and slots == [9, 5] and tables == [[0, 2, -1, -1], [0, 1, -1, -1]]
+            and p.refcount[:3] == [2, 1, 1] and p.cow_copies == 1)
+
+
+def _check_rollback(P):
+    B, p = 2, P(3)
+    t0 = ra.admit(p, 2, B, 3)
+    t1 = ra.fork(p, t0, 2, B)
+    tables, lens = [t0, t1], [2, 2]
+    before = (list(map(list, tables)), list(lens), list(p.free_queue), list(p.refcount))
+    try:
+        p.prepare_append(tables, lens, [3, 3], B, 3)
+        return False
+    except ra.PoolError:
+        pass
+    return (tables, lens, list(p.free_queue), list(p.refcount)) == before
+
+
+def _check_tiny_slots(P):
+    w = workloads.make_workload(1)
+    perm = [int(x) for x in w.free_order]
+    p = P(w.num_blocks, perm)
+    tables = [ra.admit(p, t, w.block_size, w.max_blocks) for t in w.context_lens]
+    lens = [int(x) for x in w.context_lens]
+    slots, pairs = p.prepare_append(tables, lens, [1, 1, 1, 1], w.block_size, w.max_blocks)
+    return pairs == [] and slots == [perm[1] * 16 + 1, perm[4] * 16 + 1, perm[8] * 16 + 2, perm[13] * 16 + 0]
+
+
+def _check_alloc_all_or_nothing(P):
+    p = P(3)
+    p.alloc(2)
+    try:
+        p.alloc(2)
+        return False
+    except ra.PoolError:
+        return list(p.free_queue) == [2] and p.refcount == [1, 1, 0]
+
+
+class _LifoFree(ra.RefPool):
+    def free(self, ids):
+        for b in [int(x) for x in ids]:
+            if self.refcount[b] < 1:
+                raise ra.PoolError(ra.REFCOUNT, "free block")
+            self.refcount[b] -= 1
+            if self.refcount[b] == 0:
+                self.free_queue.appendleft(b)
+
+
+class _PartialAlloc(ra.RefPool):
+    def alloc(self, n):
+        ids = []
+        for _ in range(n):
+            if not self.free_queue:
+                raise ra.PoolError(ra.OUT_OF_BLOCKS, "empty")
+            b = self._take()
+            self.refcount[b] = 1
+            ids.append(b)
+        return ids
+
+
+def _append_mutant(kind):
+    class _P(ra.RefPool):
+        def prepare_append(self, tables, lens, num_new, block_size, max_blocks):
+            slots, pairs = [], []
+            for s in range(len(lens)):
+                for _ in range(int(num_new[s])):
+                    p = lens[s]
+                    logical, offset = divmod(p, block_size)
+                    if logical >= max_blocks:
+                        raise ra.PoolError(ra.INVALID_ARG, "table too short")
+                    if offset == 0:
+                        tables[s][logical] = self.alloc(1)[0]
+                    else:
+                        cur = tables[s][logical]
+                        if self.refcount[cur] > 1 and kind != "no_cow":
+                            dst = self.alloc(1)[0]
+                            pairs.append((cur, dst))
+                            if kind != "cow_no_decref":
+                                self.refcount[cur] -= 1
+                            self.cow_copies += 1
+                            tables[s][logical] = dst
+                    blk = logical if kind == "logical_slot" else tables[s][logical]
+                    slots.append(blk * block_size + offset)
+                    lens[s] = p + 1
+            return slots, pairs       # kind "no_rollback" too: nothing restored on failure
+    return _P
+
+
+_MUTANTS = {"lifo_free": _LifoFree, "partial_alloc": _PartialAlloc, "no_cow": _append_mutant("no_cow"),
+            "cow_no_decref": _append_mutant("cow_no_decref"), "logical_slot": _append_mutant("logical_slot"),
+            "no_rollback": _append_mutant("no_rollback")}
+_CHECKS = (_check_fifo, _check_cow, _check_rollback, _check_tiny_slots, _check_alloc_all_or_nothing)
+
+
+@pytest.mark.parametrize("kind", sorted(_MUTANTS))
+def test_planted_allocator_mistake_is_caught(kind):
+    P = _MUTANTS[kind]
+    assert not all(_ok(lambda c=c: c(P)) for c in _CHECKS), kind
+
+
+def test_oracle_pool_passes_the_checks():
+    assert all(_ok(lambda c=c: c(ra.RefPool)) for c in _CHECKS)
