@@ -114,3 +114,104 @@ def test_prefix_invariants_random(seed):
     for k in list(live):
         p.free(live.pop(k))
     assert all(r == 0 for r in p.refcount) and sorted(p.free_queue) == list(range(N))
+
+
+# --------------------------------------------------------------------------- planted mistakes
+# The pins above as checks of a given (hash functions, pool class) and copies with one
+# plausible slip each: every slip makes at least one check fail.
+
+class _Impl:
+    """The oracle's prefix-cache functions, with one slip when kind names one."""
+
+    def __init__(self, kind):
+        self.kind = kind
+        impl = self
+
+        class Pool(ra.RefPool):
+            def prefix_lookup(self, hashes):
+                ids = []
+                for h in hashes:
+                    b = self.by_hash.get(int(h))
+                    if b is None:
+                        if impl.kind == "lookup_past_miss":
+                            continue
+                        break
+                    if self.refcount[b] == 0 and impl.kind != "revive_stays_queued":
+                        self.free_queue.remove(b)
+                    self.refcount[b] += 1
+                    ids.append(b)
+                self.prefix_hits += len(ids)
+                self.prefix_misses += len(hashes) - len(ids)
+                return ids
+        self.Pool = Pool
+
+    def fnv(self, data):
+        h = ra.FNV64_OFFSET
+        for byte in data:
+            h = ((h * ra.FNV64_PRIME) ^ byte) & ra.MASK64 if self.kind == "fnv1_order" else \
+                ((h ^ byte) * ra.FNV64_PRIME) & ra.MASK64
+        return h
+
+    def block_hash(self, parent, toks):
+        if self.kind == "unchained":
+            parent = 0
+        return self.fnv(int(parent).to_bytes(8, "little") +
+                        b"".join(int(t).to_bytes(4, "little", signed=True) for t in toks))
+
+    def prompt_hashes(self, toks, B):
+        out, parent = [], 0
+        n = -(-len(toks) // B) if self.kind == "partial_block_hashed" else len(toks) // B
+        for i in range(n):
+            parent = self.block_hash(parent, toks[i * B:(i + 1) * B])
+            out.append(parent)
+        return out
+
+
+def _check_vectors(m):
+    return all(m.fnv(v["input_ascii"].encode()) == int(v["hash"], 16) for v in GOLD["vectors"])
+
+
+def _check_chaining(m):
+    rng = random.Random(0)
+    toks = [rng.randrange(32000) for _ in range(64)]
+    h = m.prompt_hashes(toks, 16)
+    other = list(toks)
+    other[3] += 1
+    h2 = m.prompt_hashes(other, 16)
+    return (len(h) == 4 and m.prompt_hashes(toks + [5, 6, 7], 16) == h and all(a != b for a, b in zip(h, h2)))
+
+
+def _check_scenario(m):
+    B, p = 2, m.Pool(6)
+    hA = m.prompt_hashes([1, 2, 3, 4, 5], B)
+    a_ids = p.alloc(3)
+    p.prefix_register(hA, a_ids[:2])
+    hB = m.prompt_hashes([1, 2, 3, 4, 9, 9], B)
+    if p.prefix_lookup(hB) != [0, 1]:
+        return False
+    b_ids = [0, 1] + p.alloc(1)
+    p.prefix_register(hB[2:], b_ids[2:])
+    p.free(a_ids)
+    p.free(b_ids)
+    if p.prefix_lookup([hA[0], 12345, hA[1]]) != [0]:    # stops at the first miss
+        return False
+    p.validate()
+    return list(p.free_queue) == [4, 5, 2, 1, 3]
+
+
+@pytest.mark.parametrize("kind", ["fnv1_order", "unchained", "partial_block_hashed", "lookup_past_miss",
+                                  "revive_stays_queued"])
+def test_planted_prefix_cache_mistake_is_caught(kind):
+    m = _Impl(kind)
+    results = []
+    for check in (_check_vectors, _check_chaining, _check_scenario):
+        try:
+            results.append(check(m))
+        except Exception:
+            results.append(False)
+    assert not all(results), kind
+
+
+def test_unmutated_prefix_cache_copy_passes():
+    m = _Impl("none")
+    assert _check_vectors(m) and _check_chaining(m) and _check_scenario(m)
