@@ -1165,6 +1165,7 @@ struct DeviceInfo {
     int num_sms = 0;
     int ctas_per_sm[6] = {0, 0, 0, 0, 0, 0};  // per (head_dim 64/128/256, fp16/E4M3), at the smem size last queried
     size_t smem_for[6] = {0, 0, 0, 0, 0, 0};
+    size_t smem_attr[6] = {0, 0, 0, 0, 0, 0};  // the kernel's dynamic shared memory limit as set (only grows)
 };
 
 constexpr int kMaxDevices = 64;
@@ -1206,11 +1207,16 @@ pkv_status launch_shape(int dev, int D, bool q8, int S, int *grid, int *per_sm, 
     }
     const int vi = variant_index(D, q8);
     if (di.smem_for[vi] != bytes) {
-        cudaError_t e = cudaFuncSetAttribute(kernel_for(D, q8), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)std::max<size_t>(bytes, 48 * 1024));
-        if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        // the limit only grows, so a launch sized for more sequences on another host thread
+        // never meets a limit lowered after its own query
+        if (bytes > di.smem_attr[vi]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel_for(D, q8), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)std::max<size_t>(bytes, 48 * 1024));
+            if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            di.smem_attr[vi] = bytes;
+        }
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel_for(D, q8), kThreads, bytes);
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel_for(D, q8), kThreads, bytes);
         if (e != cudaSuccess || occ < 1)
             return fail(PKV_ERR_CUDA, "occupancy query failed (%s, %d)", cudaGetErrorString(e), occ);
         di.ctas_per_sm[vi] = std::min(occ, kMaxCtasPerSm);
