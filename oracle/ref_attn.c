@@ -46,8 +46,8 @@ static int64_t kv_row(int layout, int64_t block, int64_t slot, int64_t head, int
 /*
  * q: [S][H][D] binary16; k_pool, v_pool: one layer, N blocks; tables: [S][max_blocks];
  * lens: [S]; out: [S][H][D] double. pairs (nullable): num_pairs (s, h) pairs to compute,
- * the rest of out is left untouched. Returns 0, or -1 on a bad argument (a block id
- * outside [0, N) or a length beyond the table).
+ * the rest of out is left untouched. Returns 0, -1 on a bad argument (a block id
+ * outside [0, N) or a length beyond the table), or -2 if scratch memory ran out.
  */
 int oracle_decode_attention(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
                             int layout, int64_t N, int B, int H, int D,
@@ -63,6 +63,7 @@ int oracle_decode_attention(const uint16_t *q, const uint16_t *k_pool, const uin
             if (tables[(int64_t)s * max_blocks + i] < 0 || tables[(int64_t)s * max_blocks + i] >= N) bad = 1;
     }
     if (bad) return -1;
+    int oom = 0;
 #ifdef _OPENMP
     if (num_threads > 0) omp_set_num_threads(num_threads);
 #endif
@@ -82,6 +83,12 @@ int oracle_decode_attention(const uint16_t *q, const uint16_t *k_pool, const uin
                 free(x);
                 cap = T;
                 x = (double *)malloc(sizeof(double) * (size_t)cap);
+                if (!x) {
+                    cap = 0;
+#pragma omp atomic write
+                    oom = 1;
+                    continue;
+                }
             }
             const uint16_t *qv = q + ((int64_t)s * H + h) * D;
             double mx = -INFINITY;
@@ -107,7 +114,7 @@ int oracle_decode_attention(const uint16_t *q, const uint16_t *k_pool, const uin
         }
         free(x);
     }
-    return 0;
+    return oom ? -2 : 0;
 }
 
 int oracle_max_threads(void) {

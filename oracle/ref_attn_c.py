@@ -62,6 +62,8 @@ def decode_attention(q: np.ndarray, k_pool_layer: np.ndarray, v_pool_layer: np.n
         q16.ctypes.data, k16.ctypes.data, v16.ctypes.data, 0 if layout == "NHD" else 1, N, B, H, D,
         tables.ctypes.data, tables.shape[1], lens.ctypes.data, S, float(scale), out.ctypes.data,
         pptr, npairs, num_threads)
+    if rc == -2:
+        raise MemoryError("C oracle ran out of scratch memory")
     if rc != 0:
         raise ValueError("C oracle rejected its arguments (block id or length out of range)")
     return out
